@@ -1,0 +1,169 @@
+"""fp64 CPU oracle for frozen-prefix chunk attention (ctypes glue).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg use it; the library under
+``frozen_prefix_chunk_gb300`` never imports it, and this module never imports
+that package.  The arithmetic lives in ``cfa_oracle.c`` (plain loops, fp64);
+this file only builds it, slices the packed inputs per (window, KV head) and
+converts bf16 to fp64 (exact).
+
+Parity is pinned by the CPU tests in ``tests/test_oracle_pins.py``: central
+finite differences, full-window attention with the prefix detached (torch
+fp64 autograd), Lp = 0 against causal SDPA, closed forms, and hand-worked q8_0
+dequant values in ``tests/golden``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "cfa_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libcfa_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+_dp = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O3, OpenMP).  Returns the .so path."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O3", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                           "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = ctypes.CDLL(build())
+            _lib.cfa_oracle_group.restype = ctypes.c_int
+            _lib.cfa_oracle_group.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                _dp, _dp, _dp, _dp, _dp, _dp,
+                _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
+            _lib.cfa_oracle_dequant_q8_0.restype = None
+            _lib.cfa_oracle_dequant_q8_0.argtypes = [
+                ctypes.c_void_p, ctypes.c_long, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_int]
+            _lib.cfa_oracle_threads.restype = ctypes.c_int
+    return _lib
+
+
+def threads() -> int:
+    return lib().cfa_oracle_threads()
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_dp) if a is not None else None
+
+
+def dequant_q8_0(blocks, mutation: int = 0):
+    """q8_0 bytes (any shape, last dim a multiple of 34) -> (f64, f32, bf16 bits).
+    Each output has the shape of ``blocks`` with the last dim replaced by the
+    number of values (32 per block)."""
+    b = np.ascontiguousarray(np.asarray(blocks, dtype=np.uint8))
+    assert b.shape[-1] % 34 == 0
+    nb = b.size // 34
+    shape = b.shape[:-1] + (b.shape[-1] // 34 * 32,)
+    f64 = np.empty(shape, dtype=np.float64)
+    f32 = np.empty(shape, dtype=np.float32)
+    bf = np.empty(shape, dtype=np.uint16)
+    lib().cfa_oracle_dequant_q8_0(b.ctypes.data, nb, f64.ctypes.data, f32.ctypes.data,
+                                  bf.ctypes.data, mutation)
+    return f64, f32, bf
+
+
+def _f64(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        return np.ascontiguousarray(x.to(torch.float64).numpy())
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def group(lp, lc, g, d, scale, q, kp, vp, kc, vc, dout, mutation=0, backward=True):
+    """Run the oracle on one (window, KV head) group given fp64 arrays:
+    q, dout [lc, g, d]; kp, vp [lp, d]; kc, vc [lc, d].
+    Returns dict o, lse [g, lc], delta [g, lc], dq, dk, dv."""
+    q, kp, vp, kc, vc, dout = (_f64(a) for a in (q, kp, vp, kc, vc, dout))
+    o = np.zeros((lc, g, d))
+    lse = np.zeros((g, lc))
+    delta = np.zeros((g, lc))
+    dq = np.zeros((lc, g, d)) if backward else None
+    dk = np.zeros((lc, d)) if backward else None
+    dv = np.zeros((lc, d)) if backward else None
+    # empty arrays still need a valid pointer
+    kp = kp if kp.size else np.zeros(1)
+    vp = vp if vp.size else np.zeros(1)
+    rc = lib().cfa_oracle_group(lp, lc, g, d, float(scale), _ptr(q), _ptr(kp), _ptr(vp),
+                                _ptr(kc), _ptr(vc), _ptr(dout), _ptr(o), _ptr(lse),
+                                _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), mutation)
+    if rc != 0:
+        raise MemoryError("oracle allocation failed")
+    return dict(o=o, lse=lse, delta=delta, dq=dq, dk=dk, dv=dv)
+
+
+def _prefix_rows(x: torch.Tensor, p0: int, p1: int, hk: int, d: int, q8: bool,
+                 mutation: int) -> np.ndarray:
+    if q8:
+        blocks = x[p0:p1, hk].numpy()                        # [lp, d/32*34]
+        f64, _, _ = dequant_q8_0(blocks, mutation if mutation in (11, 12) else 0)
+        return f64.reshape(p1 - p0, d)
+    return _f64(x[p0:p1, hk])
+
+
+def run(inputs: dict, groups=None, mutation: int = 0, head_map=None, backward=True) -> dict:
+    """Oracle outputs for packed inputs from ``synth.make_inputs``.
+
+    ``groups``: iterable of (window, kv_head) pairs to compute (default: all).
+    Entries of the outputs outside those groups are NaN.
+    ``head_map``: planted-mistake hook for the pin tests -- maps (kv_head, g,
+    hkv) to the list of query heads read; default is the contiguous grouping
+    h // g == kv_head.
+    Returns O [tc, hq, d], LSE [hq, tc], delta [hq, tc], dQ [tc, hq, d],
+    dK_c / dV_c [tc, hkv, d] (float64 numpy).
+    """
+    w = inputs["workload"]
+    hq, hkv, d = w.hq, w.hkv, w.head_dim
+    g = hq // hkv
+    cu_p = inputs["cu_seqlens_prefix"].tolist()
+    cu_c = inputs["cu_seqlens_chunk"].tolist()
+    tc = cu_c[-1]
+    q8 = w.prefix_dtype == 1
+    out = dict(o=np.full((tc, hq, d), np.nan), lse=np.full((hq, tc), np.nan),
+               delta=np.full((hq, tc), np.nan), dq=np.full((tc, hq, d), np.nan),
+               dk=np.full((tc, hkv, d), np.nan), dv=np.full((tc, hkv, d), np.nan))
+    if groups is None:
+        groups = [(b, hk) for b in range(w.batch) for hk in range(hkv)]
+    for b, hk in groups:
+        p0, p1, c0, c1 = cu_p[b], cu_p[b + 1], cu_c[b], cu_c[b + 1]
+        lp, lc = p1 - p0, c1 - c0
+        if lc == 0:
+            continue
+        heads = head_map(hk, g, hkv) if head_map else list(range(hk * g, (hk + 1) * g))
+        qg = inputs["q"][c0:c1, heads]
+        dog = inputs["dout"][c0:c1, heads]
+        kp = _prefix_rows(inputs["k_prefix"], p0, p1, hk, d, q8, mutation)
+        vp = _prefix_rows(inputs["v_prefix"], p0, p1, hk, d, q8, mutation)
+        r = group(lp, lc, g, d, w.softmax_scale, qg, kp, vp, inputs["k_chunk"][c0:c1, hk],
+                  inputs["v_chunk"][c0:c1, hk], dog, mutation=mutation, backward=backward)
+        out["o"][c0:c1, heads] = r["o"]
+        out["lse"][heads, c0:c1] = r["lse"]
+        out["delta"][heads, c0:c1] = r["delta"]
+        if backward:
+            out["dq"][c0:c1, heads] = r["dq"]
+            out["dk"][c0:c1, hk] = r["dk"]
+            out["dv"][c0:c1, hk] = r["dv"]
+    return out

@@ -1,0 +1,247 @@
+/*
+ * fp64 CPU oracle for frozen-prefix chunk attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file: only the tests, the package's smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header or table with the CUDA
+ * library.
+ *
+ * What it computes (one window, one KV head and the g query heads that read
+ * it), written out as the plain definition, with no tiling or online softmax:
+ *
+ *   The chunk's queries attend to the frozen prefix, which the walk reads as
+ *   constants ("train: walk the window", "What it is"), plus the chunk's own
+ *   causal keys.  Chunk row t sits at absolute position Lp + t, so it sees
+ *   every prefix key and chunk keys j <= t (bottom-right causal mask).
+ *
+ *     S_tj   = scale * q_t . k_j                     j visible to t
+ *     LSE_t  = ln sum_j exp(S_tj)
+ *     P_tj   = exp(S_tj - LSE_t)
+ *     O_t    = sum_j P_tj v_j
+ *
+ *   Backward for the loss L = sum <O, dO>, gradients stopped at the prefix
+ *   ("Context-Frozen Training", "Phase 2"; "train: walk the window", "Why it's
+ *   a draft": cached prefixes are stop-gradient constants), i.e. the
+ *   query-split attention backward that the prime-rl POC lists under "Known
+ *   gaps":
+ *
+ *     delta_t = dO_t . O_t
+ *     dP_tj   = dO_t . v_j
+ *     dS_tj   = P_tj (dP_tj - delta_t)
+ *     dQ_t    = scale * sum_{j visible} dS_tj k_j          (prefix and chunk keys)
+ *     dK_c,j  = scale * sum_{h in group} sum_{t >= j} dS_tj q_t   (chunk keys only)
+ *     dV_c,j  =         sum_{h in group} sum_{t >= j} P_tj dO_t    (chunk keys only)
+ *
+ *   The prefix gets no gradient: none is computed or returned.
+ *
+ * q8_0 (the llama.cpp cache type named in "train: walk the window"): a block
+ * is a little-endian IEEE binary16 scale d followed by 32 signed 8-bit codes;
+ * value i is d * q_i.  The fp32 value fp32(d)*q_i is exact (11 x 8 significant
+ * bits); the bf16 that a kernel multiplies with is that value rounded to
+ * nearest, ties to even.  The attention itself uses the exact values.
+ *
+ * `mutation` plants one deliberate mistake (0 = none).  Only the tests that
+ * check that the pins catch such mistakes pass a non-zero value.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- number formats, from their definitions ---------------------------- */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double half_bits_to_double(uint16_t h, int mutation)
+{
+    if (mutation == 11) {            /* planted: read the scale as bf16 bits */
+        uint32_t u = (uint32_t)h << 16;
+        float f;
+        memcpy(&f, &u, 4);
+        return (double)f;
+    }
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                    /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);        /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* Round a finite fp32 value to bf16 (keep the top 16 bits), nearest, ties to
+ * even.  Operates on the bit pattern: add 0x7fff plus the lowest kept bit,
+ * then truncate.  Used only on finite values. */
+static uint16_t float_to_bf16_rne(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/*
+ * Dequantise n_blocks q8_0 blocks (34 bytes each, contiguous).
+ * out_f64 / out_f32 / out_bf16 may each be NULL; each receives 32 values per
+ * block in order.
+ */
+void cfa_oracle_dequant_q8_0(const uint8_t *blocks, long n_blocks, double *out_f64,
+                             float *out_f32, uint16_t *out_bf16, int mutation)
+{
+    for (long b = 0; b < n_blocks; ++b) {
+        const uint8_t *blk = blocks + 34 * b;
+        uint16_t hbits = (uint16_t)(blk[0] | (blk[1] << 8));
+        double d = half_bits_to_double(hbits, mutation);
+        for (int i = 0; i < 32; ++i) {
+            int qi = (mutation == 12) ? (int)blk[2 + i] : (int)(int8_t)blk[2 + i];
+            double v = d * (double)qi;                 /* exact in double */
+            long k = 32 * b + i;
+            if (out_f64) out_f64[k] = v;
+            if (out_f32) out_f32[k] = (float)v;         /* exact: v fits fp32 */
+            if (out_bf16) out_bf16[k] = float_to_bf16_rne((float)v);
+        }
+    }
+}
+
+/* ---- attention ---------------------------------------------------------- */
+
+static double dot(const double *a, const double *b, int n)
+{
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s += a[i] * b[i];
+    return s;
+}
+
+/*
+ * One window, one KV head, its g query heads.
+ *   q, dout : [lc][g][d]      kp, vp : [lp][d]      kc, vc : [lc][d]
+ *   o, dq   : [lc][g][d]      lse, delta : [g][lc]  dkc, dvc : [lc][d]
+ * Any output pointer may be NULL except that the backward needs o/lse/delta
+ * internally (allocated here when NULL).  Returns 0, or -1 on allocation
+ * failure.
+ */
+int cfa_oracle_group(int lp, int lc, int g, int d, double scale,
+                     const double *q, const double *kp, const double *vp,
+                     const double *kc, const double *vc, const double *dout,
+                     double *o, double *lse, double *delta,
+                     double *dq, double *dkc, double *dvc, int mutation)
+{
+    const int nrow = lc * g;
+    double *o_own = NULL, *lse_own = NULL, *delta_own = NULL;
+    if (!o) o = o_own = (double *)malloc(sizeof(double) * (size_t)nrow * d + 8);
+    if (!lse) lse = lse_own = (double *)malloc(sizeof(double) * (size_t)nrow + 8);
+    if (!delta) delta = delta_own = (double *)malloc(sizeof(double) * (size_t)nrow + 8);
+    if (!o || !lse || !delta) {
+        free(o_own); free(lse_own); free(delta_own);
+        return -1;
+    }
+    int fail = 0;
+
+    /* Pass 1, one query row at a time: S, LSE, P, O, delta and dQ. */
+#pragma omp parallel
+    {
+        double *S = (double *)malloc(sizeof(double) * ((size_t)lp + lc + 1));
+        double *P = (double *)malloc(sizeof(double) * ((size_t)lp + lc + 1));
+        if (!S || !P) {
+#pragma omp atomic write
+            fail = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int r = 0; r < nrow; ++r) {
+            if (!S || !P) continue;
+            const int t = r / g, hh = r % g;
+            const double *qt = q + (size_t)r * d;
+            const double *dot_ = dout + (size_t)r * d;
+            /* visible chunk keys: j <= t (planted mistake 1: one future key) */
+            int nc = t + 1;
+            if (mutation == 1 && nc < lc) nc = t + 2;
+            const int n = lp + nc;
+            for (int j = 0; j < lp; ++j) S[j] = scale * dot(qt, kp + (size_t)j * d, d);
+            for (int j = 0; j < nc; ++j) S[lp + j] = scale * dot(qt, kc + (size_t)j * d, d);
+            double m = -INFINITY;
+            for (int j = 0; j < n; ++j) m = S[j] > m ? S[j] : m;
+            double sum = 0.0;
+            int j0 = (mutation == 9) ? lp : 0;       /* planted: drop prefix from the sum */
+            for (int j = j0; j < n; ++j) sum += exp(S[j] - m);
+            double L = (mutation == 7) ? m + log2(sum) : m + log(sum);
+            lse[(size_t)hh * lc + t] = L;
+            for (int j = 0; j < n; ++j) P[j] = exp(S[j] - L);
+            double *ot = o + (size_t)r * d;
+            for (int c = 0; c < d; ++c) ot[c] = 0.0;
+            for (int j = 0; j < n; ++j) {
+                const double *vj = (mutation == 8)
+                    ? (j < lp ? kp + (size_t)j * d : kc + (size_t)(j - lp) * d)
+                    : (j < lp ? vp + (size_t)j * d : vc + (size_t)(j - lp) * d);
+                for (int c = 0; c < d; ++c) ot[c] += P[j] * vj[c];
+            }
+            double dl = dot(dot_, ot, d);
+            delta[(size_t)hh * lc + t] = dl;
+            if (dq) {
+                double *dqt = dq + (size_t)r * d;
+                for (int c = 0; c < d; ++c) dqt[c] = 0.0;
+                for (int j = 0; j < n; ++j) {
+                    const double *vj = j < lp ? vp + (size_t)j * d : vc + (size_t)(j - lp) * d;
+                    const double *kj = j < lp ? kp + (size_t)j * d : kc + (size_t)(j - lp) * d;
+                    if (mutation == 6) kj = vj;               /* planted: transposed operand */
+                    double dpj = dot(dot_, vj, d);
+                    double dsj = (mutation == 3) ? P[j] * (dpj + dl) : P[j] * (dpj - dl);
+                    double f = (mutation == 2) ? dsj : scale * dsj;
+                    for (int c = 0; c < d; ++c) dqt[c] += f * kj[c];
+                }
+            }
+        }
+        free(S);
+        free(P);
+    }
+
+    /* Pass 2, one chunk key at a time: dK_c and dV_c, summed over the group. */
+    if (!fail && (dkc || dvc)) {
+#pragma omp parallel for schedule(dynamic, 4)
+        for (int j = 0; j < lc; ++j) {
+            const double *kj = kc + (size_t)j * d, *vj = vc + (size_t)j * d;
+            double *dk = dkc ? dkc + (size_t)j * d : NULL;
+            double *dv = dvc ? dvc + (size_t)j * d : NULL;
+            if (dk) for (int c = 0; c < d; ++c) dk[c] = 0.0;
+            if (dv) for (int c = 0; c < d; ++c) dv[c] = 0.0;
+            for (int t = j; t < lc; ++t) {
+                for (int hh = 0; hh < g; ++hh) {
+                    if (mutation == 10 && hh > 0) continue;   /* planted: drop the group sum */
+                    const int r = t * g + hh;
+                    const double *qt = q + (size_t)r * d;
+                    const double *dot_ = dout + (size_t)r * d;
+                    double s = scale * dot(qt, kj, d);
+                    double p = exp(s - lse[(size_t)hh * lc + t]);
+                    double dp = dot(dot_, vj, d);
+                    double ds = p * (dp - delta[(size_t)hh * lc + t]);
+                    if (mutation == 3) ds = p * (dp + delta[(size_t)hh * lc + t]);
+                    double fk = (mutation == 5) ? ds : scale * ds;
+                    double fv = (mutation == 4) ? ds : p;
+                    if (dk) for (int c = 0; c < d; ++c) dk[c] += fk * qt[c];
+                    if (dv) for (int c = 0; c < d; ++c) dv[c] += fv * dot_[c];
+                }
+            }
+        }
+    }
+
+    free(o_own);
+    free(lse_own);
+    free(delta_own);
+    return fail ? -1 : 0;
+}
+
+/* Number of threads the parallel regions above use. */
+int cfa_oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
