@@ -1,0 +1,332 @@
+// C-ABI boundary of the cfa library: argument validation, work planning,
+// workspace carve-up, TMA descriptor encoding and kernel launches.  Nothing
+// here allocates device memory or synchronises (except cfa_read_status).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "cfa.h"
+#include "cfa_kernels.cuh"
+
+using namespace cfa;
+
+namespace {
+
+constexpr int kMinTilesPerSplit = 4;   // key tiles per split, at least
+constexpr int kWavesTarget = 4;        // CTAs per SM the split count aims for
+constexpr size_t kWsHeader = 256;      // status word + padding
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// bf16 tensor [rows, heads, d] -> 3-D map with boxes of 64 columns x box_h
+// heads x box_t rows, 128-byte swizzle (the UMMA K-major / MN-major canonical
+// layout).  Rows beyond the tensor read as zero.
+int make_map_bf16(CUtensorMap* m, const void* ptr, int d, int heads, long long rows, int box_h,
+                  int box_t) {
+  std::memset(m, 0, sizeof(*m));
+  if (rows <= 0) return CFA_OK;  // never dereferenced
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return CFA_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_h, (cuuint32_t)box_t};
+  cuuint32_t es[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CFA_OK : CFA_ERR_INVALID_ARG;
+}
+
+int validate(const cfa_args* a) {
+  if (!a) return CFA_ERR_INVALID_ARG;
+  if (a->batch < 1 || a->batch > 65535) return CFA_ERR_INVALID_ARG;
+  if (a->hq < 1 || a->hkv < 1 || a->hkv > 65535 || a->hq % a->hkv != 0) return CFA_ERR_INVALID_ARG;
+  if (a->hq / a->hkv > 128) return CFA_ERR_UNSUPPORTED;
+  if (a->head_dim != 64 && a->head_dim != 128) return CFA_ERR_UNSUPPORTED;
+  if (a->prefix_dtype != CFA_PREFIX_BF16 && a->prefix_dtype != CFA_PREFIX_Q8_0)
+    return CFA_ERR_INVALID_ARG;
+  if (a->max_lp < 0 || a->max_lc < 0 || a->total_lp < 0 || a->total_lc < 0)
+    return CFA_ERR_INVALID_ARG;
+  if (a->max_lp > a->total_lp || a->max_lc > a->total_lc) return CFA_ERR_INVALID_ARG;
+  if (!(a->softmax_scale > 0.f) || !std::isfinite(a->softmax_scale)) return CFA_ERR_INVALID_ARG;
+  if (!a->cu_seqlens_prefix || !a->cu_seqlens_chunk) return CFA_ERR_INVALID_ARG;
+  if (a->total_lc > 0 && (!a->q || !a->k_chunk || !a->v_chunk)) return CFA_ERR_INVALID_ARG;
+  if (a->total_lp > 0 && (!a->k_prefix || !a->v_prefix)) return CFA_ERR_INVALID_ARG;
+  if (!aligned16(a->q) || !aligned16(a->k_chunk) || !aligned16(a->v_chunk) ||
+      !aligned16(a->k_prefix) || !aligned16(a->v_prefix))
+    return CFA_ERR_INVALID_ARG;
+  if ((long long)a->total_lc * a->hq * a->head_dim >= (1ll << 40)) return CFA_ERR_UNSUPPORTED;
+  if (a->prefix_dtype == CFA_PREFIX_Q8_0) return CFA_ERR_UNSUPPORTED;
+  return CFA_OK;
+}
+
+struct Plan {
+  Tiling fwd, dq;
+  int n_kc_max;        // 128-key chunk tiles per window, upper bound
+  size_t off_opart, off_lsepart, ws_fwd;
+  size_t off_dqpart, ws_bwd;
+};
+
+int sm_count(int* n) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CFA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return CFA_ERR_CUDA;
+  return CFA_OK;
+}
+
+Tiling make_tiling(const cfa_args* a, int q_per_cta, int sms) {
+  Tiling t;
+  t.g = a->hq / a->hkv;
+  t.tpt = kTileM / t.g;
+  t.rows = t.tpt * t.g;
+  t.q_per_cta = q_per_cta;
+  const int tok_blk = q_per_cta * t.tpt;
+  t.n_qblk_max = ceil_div(a->max_lc > 0 ? a->max_lc : 1, tok_blk);
+  const int n_kt_max = ceil_div(a->max_lp, kTileN) + ceil_div(a->max_lc > 0 ? a->max_lc : 1, kTileN);
+  const long long base = (long long)a->batch * a->hkv * t.n_qblk_max;
+  const long long target = (long long)kWavesTarget * sms;
+  const int want = (int)(base >= target ? 1 : (target + base - 1) / base);
+  int tps = ceil_div(n_kt_max, want);
+  if (tps < kMinTilesPerSplit) tps = kMinTilesPerSplit;
+  t.tiles_per_split = tps;
+  t.n_split_max = ceil_div(n_kt_max, tps);
+  return t;
+}
+
+int make_plan(const cfa_args* a, Plan* p) {
+  int sms = 0;
+  int st = sm_count(&sms);
+  if (st) return st;
+  p->fwd = make_tiling(a, 2, sms);
+  p->dq = make_tiling(a, 1, sms);
+  p->n_kc_max = ceil_div(a->max_lc > 0 ? a->max_lc : 1, kTileN);
+  const size_t rows = (size_t)a->total_lc * a->hq;
+  size_t off = kWsHeader;
+  p->off_opart = p->off_lsepart = 0;
+  if (p->fwd.n_split_max > 1) {
+    p->off_opart = off;
+    off = align256(off + (size_t)p->fwd.n_split_max * rows * a->head_dim * 4);
+    p->off_lsepart = off;
+    off = align256(off + (size_t)p->fwd.n_split_max * rows * 4);
+  }
+  p->ws_fwd = off;
+  off = kWsHeader;
+  p->off_dqpart = 0;
+  if (p->dq.n_split_max > 1) {
+    p->off_dqpart = off;
+    off = align256(off + (size_t)p->dq.n_split_max * rows * a->head_dim * 4);
+  }
+  p->ws_bwd = off;
+  return CFA_OK;
+}
+
+unsigned long long wait_limit_ns() {
+  const char* e = std::getenv("CFA_WAIT_LIMIT_NS");
+  if (!e || !*e) return kDefaultWaitNs;
+  char* end = nullptr;
+  unsigned long long v = std::strtoull(e, &end, 10);
+  return (end && *end == 0) ? v : kDefaultWaitNs;
+}
+
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < need)
+    return CFA_ERR_WORKSPACE;
+  return CFA_OK;
+}
+
+int encode_kv_maps(const cfa_args* a, Maps* m) {
+  const int d = a->head_dim;
+  int st = make_map_bf16(&m->kc, a->k_chunk, d, a->hkv, a->total_lc, 1, kTileN);
+  if (!st) st = make_map_bf16(&m->vc, a->v_chunk, d, a->hkv, a->total_lc, 1, kTileN);
+  if (!st) st = make_map_bf16(&m->kp, a->k_prefix, d, a->hkv, a->total_lp, 1, kTileN);
+  if (!st) st = make_map_bf16(&m->vp, a->v_prefix, d, a->hkv, a->total_lp, 1, kTileN);
+  return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cfa_version(void) { return (1 << 16) | 0; }
+
+const char* cfa_status_string(int s) {
+  switch (s) {
+    case CFA_OK: return "ok";
+    case CFA_ERR_INVALID_ARG: return "invalid argument";
+    case CFA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CFA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case CFA_ERR_LAUNCH: return "kernel launch failed";
+    case CFA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case CFA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+size_t cfa_workspace_size(const cfa_args* a, int which) {
+  if (validate(a) != CFA_OK) return 0;
+  Plan p;
+  if (make_plan(a, &p) != CFA_OK) return 0;
+  if (which == CFA_WS_FORWARD) return p.ws_fwd;
+  if (which == CFA_WS_BACKWARD) return p.ws_bwd;
+  return 0;
+}
+
+int cfa_forward(const cfa_args* a, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  int st = validate(a);
+  if (st) return st;
+  if (a->total_lc > 0 && (!o || !lse || !aligned16(o))) return CFA_ERR_INVALID_ARG;
+  Plan p;
+  if ((st = make_plan(a, &p))) return st;
+  if ((st = check_ws(ws, ws_bytes, p.ws_fwd))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  if (a->total_lc == 0 || a->max_lc == 0) return CFA_OK;
+
+  Maps m;
+  std::memset(&m, 0, sizeof(m));
+  const Tiling& tl = p.fwd;
+  if ((st = make_map_bf16(&m.q, a->q, a->head_dim, a->hq, a->total_lc, tl.g, tl.tpt))) return st;
+  if ((st = encode_kv_maps(a, &m))) return st;
+
+  FwdArgs fa;
+  fa.cu_p = a->cu_seqlens_prefix;
+  fa.cu_c = a->cu_seqlens_chunk;
+  fa.hq = a->hq;
+  fa.hkv = a->hkv;
+  fa.total_lc = a->total_lc;
+  fa.tl = tl;
+  fa.scale_log2 = a->softmax_scale * kLog2e;
+  fa.o = static_cast<__nv_bfloat16*>(o);
+  fa.lse = lse;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  fa.o_part = p.off_opart ? reinterpret_cast<float*>(w + p.off_opart) : nullptr;
+  fa.lse_part = p.off_lsepart ? reinterpret_cast<float*>(w + p.off_lsepart) : nullptr;
+  fa.status = reinterpret_cast<int*>(w);
+  fa.limit_ns = wait_limit_ns();
+
+  dim3 grid((unsigned)(tl.n_qblk_max * tl.n_split_max), (unsigned)a->hkv, (unsigned)a->batch);
+  if (launch_fwd(m, fa, a->head_dim, 0, grid, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  if (tl.n_split_max > 1 &&
+      launch_fwd_combine(fa, a->head_dim, a->batch, a->max_lc, s) != cudaSuccess)
+    return CFA_ERR_LAUNCH;
+  return CFA_OK;
+}
+
+int cfa_backward_preprocess(const cfa_args* a, const void* o, const void* dout, float* delta,
+                            void* stream) {
+  int st = validate(a);
+  if (st) return st;
+  if (a->total_lc == 0) return CFA_OK;
+  if (!o || !dout || !delta || !aligned16(o) || !aligned16(dout)) return CFA_ERR_INVALID_ARG;
+  if (launch_delta(static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout),
+                   delta, a->total_lc, a->hq, a->head_dim,
+                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CFA_ERR_LAUNCH;
+  return CFA_OK;
+}
+
+int cfa_backward(const cfa_args* a, const void* dout, const float* lse, const float* delta,
+                 void* dq, void* dk_chunk, void* dv_chunk, void* ws, size_t ws_bytes,
+                 void* stream) {
+  int st = validate(a);
+  if (st) return st;
+  if (a->total_lc > 0 && (!dout || !lse || !delta || !dq || !dk_chunk || !dv_chunk ||
+                          !aligned16(dout) || !aligned16(dq) || !aligned16(dk_chunk) ||
+                          !aligned16(dv_chunk)))
+    return CFA_ERR_INVALID_ARG;
+  Plan p;
+  if ((st = make_plan(a, &p))) return st;
+  if ((st = check_ws(ws, ws_bytes, p.ws_bwd))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  if (a->total_lc == 0 || a->max_lc == 0) return CFA_OK;
+
+  Maps m;
+  std::memset(&m, 0, sizeof(m));
+  const Tiling& tl = p.dq;
+  if ((st = make_map_bf16(&m.q, a->q, a->head_dim, a->hq, a->total_lc, tl.g, tl.tpt))) return st;
+  if ((st = make_map_bf16(&m.dout, dout, a->head_dim, a->hq, a->total_lc, tl.g, tl.tpt)))
+    return st;
+  if ((st = encode_kv_maps(a, &m))) return st;
+
+  BwdArgs ba;
+  ba.cu_p = a->cu_seqlens_prefix;
+  ba.cu_c = a->cu_seqlens_chunk;
+  ba.hq = a->hq;
+  ba.hkv = a->hkv;
+  ba.total_lc = a->total_lc;
+  ba.tl = tl;
+  ba.scale_log2 = a->softmax_scale * kLog2e;
+  ba.scale = a->softmax_scale;
+  ba.lse = lse;
+  ba.delta = delta;
+  ba.dq = static_cast<__nv_bfloat16*>(dq);
+  ba.dk = static_cast<__nv_bfloat16*>(dk_chunk);
+  ba.dv = static_cast<__nv_bfloat16*>(dv_chunk);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  ba.dq_part = p.off_dqpart ? reinterpret_cast<float*>(w + p.off_dqpart) : nullptr;
+  ba.status = reinterpret_cast<int*>(w);
+  ba.limit_ns = wait_limit_ns();
+
+  dim3 grid_dq((unsigned)(tl.n_qblk_max * tl.n_split_max), (unsigned)a->hkv, (unsigned)a->batch);
+  if (launch_bwd_dq(m, ba, a->head_dim, 0, grid_dq, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  dim3 grid_kv((unsigned)p.n_kc_max, (unsigned)a->hkv, (unsigned)a->batch);
+  if (launch_bwd_dkdv(m, ba, a->head_dim, grid_kv, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  if (tl.n_split_max > 1 &&
+      launch_bwd_dq_reduce(ba, a->head_dim, a->batch, a->max_lc, s) != cudaSuccess)
+    return CFA_ERR_LAUNCH;
+  return CFA_OK;
+}
+
+int cfa_dequant_q8_0(const void* blocks, long long n_blocks, float* out_f32, void* out_bf16,
+                     void* stream) {
+  if (n_blocks < 0) return CFA_ERR_INVALID_ARG;
+  if (n_blocks == 0) return CFA_OK;
+  if (!blocks || (!out_f32 && !out_bf16)) return CFA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(blocks) & 1u) || (reinterpret_cast<uintptr_t>(out_f32) & 3u) ||
+      (reinterpret_cast<uintptr_t>(out_bf16) & 1u))
+    return CFA_ERR_INVALID_ARG;
+  if (launch_dequant_q8_0(static_cast<const uint8_t*>(blocks), n_blocks, out_f32,
+                          static_cast<__nv_bfloat16*>(out_bf16),
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CFA_ERR_LAUNCH;
+  return CFA_OK;
+}
+
+int cfa_read_status(const void* ws, void* stream) {
+  if (!ws) return CFA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CFA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CFA_ERR_CUDA;
+  return v;
+}
+
+}  // extern "C"

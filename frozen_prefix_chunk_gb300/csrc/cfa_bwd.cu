@@ -1,0 +1,696 @@
+// Query-split backward of frozen-prefix chunk attention on sm_103a.
+//
+// The prefix is a stop-gradient constant, so the backward needs
+//   dQ_t  = s * sum_{visible j} dS_tj k_j        over prefix AND chunk keys
+//   dK_j, dV_j                                    over the chunk's keys only
+// with P_tj = exp(s q_t.k_j - LSE_t), dS_tj = P_tj (dO_t.v_j - delta_t).
+//
+// Two kernels split the work so that neither needs atomics:
+//
+// * bwd_dq_kernel -- query-major.  A CTA owns one 128-row query tile and one
+//   split of its key-tile list (prefix tiles, then visible chunk tiles) and
+//   streams K/V through three MMAs per tile: S = Q K^T, dP = dO V^T,
+//   dQ += dS K.  Prefix tiles never produce dK/dV.  Split partials of dQ go
+//   to the workspace and bwd_dq_reduce_kernel sums them in split order.
+//     warps 0-7  elementwise (two warps per TMEM lane quadrant, each owning
+//                64 of the 128 key columns): P, dS, bf16 dS into TMEM
+//     warp  8    TMA producer      warp 9  TMEM owner + MMA issuer
+//   TMEM: S0 [0,128) S1 [128,256) dP [256,384) dQ [384,384+D); dS overwrites
+//   the S columns its own warp has read (keys 0-63 -> cols 0-31, keys
+//   64-127 -> cols 64-95) and is the A operand of the dQ MMA.
+//
+// * bwd_dkdv_kernel -- key-major over the chunk keys.  A CTA owns one
+//   128-key chunk tile and walks the query tiles that can see it:
+//   S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q, with P^T and dS^T
+//   staged bf16 in TMEM.  TMEM: S^T [0,128) dP^T [128,256) dV, dK.
+#include "cfa_kernels.cuh"
+#include "cfa_ptx.cuh"
+
+namespace cfa {
+namespace {
+
+constexpr int kBoxBytes = 128 * 128;
+
+// Column of the k-th 16-key slice of a bf16 operand staged in TMEM by the two
+// half-warps (keys 0-63 at columns 0-31, keys 64-127 at columns 64-95).
+__device__ __forceinline__ uint32_t staged_col(int k) {
+  return (k < 4) ? (uint32_t)(k * 8) : (uint32_t)(64 + (k - 4) * 8);
+}
+
+// D = A B^T with A, B K-major 128B-swizzled tiles of 128 rows x D columns.
+template <int D>
+__device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    const uint32_t off = (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
+    mma_bf16_ss(d_tmem, smem_desc_sw128(a_addr + off, 16, 1024),
+                smem_desc_sw128(b_addr + off, 16, 1024), idesc, k > 0 ? 1u : 0u);
+  }
+}
+
+// D (+)= A[tmem, staged] B with B a 128-row x D tile read MN-major.
+template <int D>
+__device__ __forceinline__ void issue_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_addr,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    mma_bf16_ts(d_tmem, a_tmem + staged_col(k),
+                smem_desc_sw128(b_addr + (uint32_t)k * 2048u, kBoxBytes, 1024), idesc,
+                (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+struct DqCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kQOff = 0;
+  static constexpr int kDOOff = kTileBytes;
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q,
+                  const __grid_constant__ CUtensorMap map_do,
+                  const __grid_constant__ CUtensorMap map_kp,
+                  const __grid_constant__ CUtensorMap map_vp,
+                  const __grid_constant__ CUtensorMap map_kc,
+                  const __grid_constant__ CUtensorMap map_vc, const BwdArgs a) {
+  using C = DqCfg<D>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_addr(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw_base);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Tiling tl = a.tl;
+  const int b = blockIdx.z, hk = blockIdx.y;
+  const int qblk = blockIdx.x / tl.n_split_max, split = blockIdx.x % tl.n_split_max;
+  const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
+  const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
+  const int t0 = qblk * tl.tpt;
+  if (t0 >= lc) return;
+  const int np_t = ceil_div(lp, kTileN);
+  const int n_kt = block_key_tiles(lp, lc, t0, tl.tpt);
+  const int n_split = ceil_div(n_kt, tl.tiles_per_split);
+  if (split >= n_split) return;
+  const int kt0 = split * tl.tiles_per_split;
+  const int n = min(tl.tiles_per_split, n_kt - kt0);
+
+  const uint32_t bars = base + C::kBarOff;
+  const uint32_t bar_qdo = bars;
+  const uint32_t bar_kfull = bars + 8;
+  const uint32_t bar_vfull = bars + 8 * (1 + S);
+  const uint32_t bar_kvempty = bars + 8 * (1 + 2 * S);
+  const uint32_t bar_sfull = bars + 8 * (1 + 3 * S);  // [2]
+  const uint32_t bar_dpfull = bar_sfull + 16;
+  const uint32_t bar_dpfree = bar_dpfull + 8;
+  const uint32_t bar_dsfull = bar_dpfree + 8;
+  const uint32_t bar_dqfull = bar_dsfull + 8;
+  const uint32_t bar_drain = bar_dqfull + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_qdo, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_kfull + 8 * s, 1);
+      mbar_init(bar_vfull + 8 * s, 1);
+      mbar_init(bar_kvempty + 8 * s, 1);
+    }
+    mbar_init(bar_sfull, 1);
+    mbar_init(bar_sfull + 8, 1);
+    mbar_init(bar_dpfull, 1);
+    mbar_init(bar_dpfree, 8);
+    mbar_init(bar_dsfull, 8);
+    mbar_init(bar_dqfull, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter W{a.limit_ns, abort_flag, a.status};
+
+  if (warp == 8) {
+    if (lane == 0) {
+      const uint32_t qbytes = (uint32_t)(C::kBoxes * 128 * tl.rows);
+      mbar_arrive_expect_tx(bar_qdo, 2 * qbytes);
+      for (int kb = 0; kb < C::kBoxes; ++kb) {
+        tma_load_3d(base + C::kQOff + kb * kBoxBytes, &map_q, bar_qdo, kb * 64, hk * tl.g, c0 + t0);
+        tma_load_3d(base + C::kDOOff + kb * kBoxBytes, &map_do, bar_qdo, kb * 64, hk * tl.g,
+                    c0 + t0);
+      }
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(W, bar_kvempty + 8 * s, ((uint32_t)(i / S) & 1u) ^ 1u)) break;
+        const int kt = kt0 + i;
+        const CUtensorMap* mk = &map_kc;
+        const CUtensorMap* mv = &map_vc;
+        int row0 = c0 + (kt - np_t) * kTileN;
+        if (kt < np_t) {
+          mk = &map_kp;
+          mv = &map_vp;
+          row0 = p0 + kt * kTileN;
+        }
+        mbar_arrive_expect_tx(bar_kfull + 8 * s, C::kTileBytes);
+        for (int kb = 0; kb < C::kBoxes; ++kb)
+          tma_load_3d(base + C::kKOff + s * C::kTileBytes + kb * kBoxBytes, mk, bar_kfull + 8 * s,
+                      kb * 64, hk, row0);
+        mbar_arrive_expect_tx(bar_vfull + 8 * s, C::kTileBytes);
+        for (int kb = 0; kb < C::kBoxes; ++kb)
+          tma_load_3d(base + C::kVOff + s * C::kTileBytes + kb * kBoxBytes, mv, bar_vfull + 8 * s,
+                      kb * 64, hk, row0);
+        issued = i + 1;
+      }
+      mbar_wait_bounded(bar_qdo, 0, kDrainLimitNs);
+      for (int i = (issued > S ? issued - S : 0); i < issued; ++i) {
+        const uint32_t ph = (uint32_t)(i / S) & 1u;
+        mbar_wait_bounded(bar_kfull + 8 * (i % S), ph, kDrainLimitNs);
+        mbar_wait_bounded(bar_vfull + 8 * (i % S), ph, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {
+      bool ok = mbar_wait(W, bar_qdo, 0);
+      tc_fence_after_sync();
+      const uint32_t t_dq = tmem + 384;
+      for (int i = 0; ok && i < n; ++i) {
+        const int s = i % S;
+        const uint32_t ph = (uint32_t)(i / S) & 1u;
+        if (!(ok = mbar_wait(W, bar_kfull + 8 * s, ph))) break;
+        tc_fence_after_sync();
+        issue_nt<D>(tmem + (uint32_t)(i & 1) * 128u, base + C::kQOff,
+                    base + C::kKOff + s * C::kTileBytes);
+        tc_commit(bar_sfull + 8 * (i & 1));
+        if (i > 0) {
+          const int sp = (i - 1) % S;
+          if (!(ok = mbar_wait(W, bar_dsfull, (uint32_t)(i - 1) & 1u))) break;
+          tc_fence_after_sync();
+          issue_tn<D>(t_dq, tmem + (uint32_t)((i - 1) & 1) * 128u,
+                      base + C::kKOff + sp * C::kTileBytes, i - 1 > 0);
+          tc_commit(bar_kvempty + 8 * sp);
+          if (!(ok = mbar_wait(W, bar_dpfree, (uint32_t)(i - 1) & 1u))) break;
+          tc_fence_after_sync();
+        }
+        if (!(ok = mbar_wait(W, bar_vfull + 8 * s, ph))) break;
+        tc_fence_after_sync();
+        issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + s * C::kTileBytes);
+        tc_commit(bar_dpfull);
+      }
+      if (ok) {
+        const int i = n - 1, s = i % S;
+        if (mbar_wait(W, bar_dsfull, (uint32_t)i & 1u)) {
+          tc_fence_after_sync();
+          issue_tn<D>(t_dq, tmem + (uint32_t)(i & 1) * 128u, base + C::kKOff + s * C::kTileBytes,
+                      i > 0);
+          tc_commit(bar_dqfull);
+        }
+      }
+      tc_commit(bar_drain);
+      mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
+    }
+  } else {
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    const int token = t0 + row / tl.g;
+    const int head = hk * tl.g + row % tl.g;
+    const bool row_valid = row < tl.rows && token < lc;
+    const size_t grow = (size_t)(c0 + (row_valid ? token : 0));
+    const float lse2 = row_valid ? a.lse[(size_t)head * a.total_lc + grow] * kLog2e : 0.f;
+    const float dl = row_valid ? a.delta[(size_t)head * a.total_lc + grow] : 0.f;
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const uint32_t sb = (uint32_t)(i & 1) * 128u + (uint32_t)half * 64u;
+      if (!(ok = warp_wait(W, bar_sfull + 8 * (i & 1), (uint32_t)(i >> 1) & 1u))) break;
+      tc_fence_after_sync();
+      const int kt = kt0 + i;
+      int lim = (kt < np_t) ? (lp - kt * kTileN) : (token - (kt - np_t) * kTileN + 1);
+      if (!row_valid) lim = 0;
+      lim -= half * 64;  // visible columns [0, lim) of this warp's 64
+      float p[64];
+      {
+        uint32_t r[64];
+        tmem_ld_x64(t_lane + sb, r);
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          p[j] = (j < lim) ? ex2_approx(fmaf(__uint_as_float(r[j]), sl2, -lse2)) : 0.f;
+      }
+      if (!(ok = warp_wait(W, bar_dpfull, (uint32_t)i & 1u))) break;
+      tc_fence_after_sync();
+      uint32_t pk[32];
+      {
+        uint32_t r[64];
+        tmem_ld_x64(t_lane + 256 + half * 64, r);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_dpfree);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          pk[j] = pack_bf16x2(p[2 * j] * (__uint_as_float(r[2 * j]) - dl),
+                              p[2 * j + 1] * (__uint_as_float(r[2 * j + 1]) - dl));
+      }
+      tmem_st_x32(t_lane + sb, pk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dsfull);
+    }
+    if (ok) ok = warp_wait(W, bar_dqfull, 0);
+    if (ok) {
+      tc_fence_after_sync();
+      const bool single = (n_split == 1);
+#pragma unroll
+      for (int cb = half * (D / 2); cb < (half + 1) * (D / 2); cb += 32) {
+        uint32_t r[32];
+        tmem_ld_x32(t_lane + 384 + cb, r);
+        if (row_valid) {
+          if (single) {
+            uint4* dst = reinterpret_cast<uint4*>(a.dq + (grow * a.hq + head) * D + cb);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * a.scale,
+                                __uint_as_float(r[8 * v + 1]) * a.scale);
+              u.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * a.scale,
+                                __uint_as_float(r[8 * v + 3]) * a.scale);
+              u.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * a.scale,
+                                __uint_as_float(r[8 * v + 5]) * a.scale);
+              u.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * a.scale,
+                                __uint_as_float(r[8 * v + 7]) * a.scale);
+              dst[v] = u;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(
+                a.dq_part + (((size_t)split * a.total_lc + grow) * a.hq + head) * D + cb);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(r[4 * v + 0]) * a.scale,
+                                   __uint_as_float(r[4 * v + 1]) * a.scale,
+                                   __uint_as_float(r[4 * v + 2]) * a.scale,
+                                   __uint_as_float(r[4 * v + 3]) * a.scale);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+struct DkvCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQOff = 2 * kTileBytes;           // stage s: Q at +2s*T, dO at +(2s+1)*T
+  static constexpr int kRowOff = kQOff + 2 * kStages * kTileBytes;  // per-warp LSE/delta
+  static constexpr int kBarOff = kRowOff + 8 * 128 * 4;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q,
+                    const __grid_constant__ CUtensorMap map_do,
+                    const __grid_constant__ CUtensorMap map_kc,
+                    const __grid_constant__ CUtensorMap map_vc, const BwdArgs a) {
+  using C = DkvCfg<D>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_addr(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw_base);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Tiling tl = a.tl;
+  const int b = blockIdx.z, hk = blockIdx.y;
+  const int key0 = blockIdx.x * kTileN;
+  const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
+  if (key0 >= lc) return;
+  const int qi_lo = key0 / tl.tpt;
+  const int n = ceil_div(lc, tl.tpt) - qi_lo;
+
+  const uint32_t bars = base + C::kBarOff;
+  const uint32_t bar_kv = bars;
+  const uint32_t bar_qfull = bars + 8;               // [S]
+  const uint32_t bar_qempty = bars + 8 * (1 + S);    // [S]
+  const uint32_t bar_stfull = bars + 8 * (1 + 2 * S);
+  const uint32_t bar_dptfull = bar_stfull + 8;
+  const uint32_t bar_pdsfull = bar_dptfull + 8;
+  const uint32_t bar_dkvfull = bar_pdsfull + 8;
+  const uint32_t bar_drain = bar_dkvfull + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_qfull + 8 * s, 1);
+      mbar_init(bar_qempty + 8 * s, 1);
+    }
+    mbar_init(bar_stfull, 1);
+    mbar_init(bar_dptfull, 1);
+    mbar_init(bar_pdsfull, 8);
+    mbar_init(bar_dkvfull, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter W{a.limit_ns, abort_flag, a.status};
+  const uint32_t t_dv = tmem + 256, t_dk = tmem + 256 + D;
+
+  if (warp == 8) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
+      for (int kb = 0; kb < C::kBoxes; ++kb) {
+        tma_load_3d(base + C::kKOff + kb * kBoxBytes, &map_kc, bar_kv, kb * 64, hk, c0 + key0);
+        tma_load_3d(base + C::kVOff + kb * kBoxBytes, &map_vc, bar_kv, kb * 64, hk, c0 + key0);
+      }
+      const uint32_t qbytes = (uint32_t)(C::kBoxes * 128 * tl.rows);
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(W, bar_qempty + 8 * s, ((uint32_t)(i / S) & 1u) ^ 1u)) break;
+        const int tok = c0 + (qi_lo + i) * tl.tpt;
+        mbar_arrive_expect_tx(bar_qfull + 8 * s, 2 * qbytes);
+        for (int kb = 0; kb < C::kBoxes; ++kb) {
+          tma_load_3d(base + C::kQOff + (2 * s) * C::kTileBytes + kb * kBoxBytes, &map_q,
+                      bar_qfull + 8 * s, kb * 64, hk * tl.g, tok);
+          tma_load_3d(base + C::kQOff + (2 * s + 1) * C::kTileBytes + kb * kBoxBytes, &map_do,
+                      bar_qfull + 8 * s, kb * 64, hk * tl.g, tok);
+        }
+        issued = i + 1;
+      }
+      mbar_wait_bounded(bar_kv, 0, kDrainLimitNs);
+      for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
+        mbar_wait_bounded(bar_qfull + 8 * (i % S), (uint32_t)(i / S) & 1u, kDrainLimitNs);
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {
+      bool ok = mbar_wait(W, bar_kv, 0);
+      tc_fence_after_sync();
+      for (int i = 0; ok && i < n; ++i) {
+        const int s = i % S;
+        if (!(ok = mbar_wait(W, bar_qfull + 8 * s, (uint32_t)(i / S) & 1u))) break;
+        tc_fence_after_sync();
+        const uint32_t q_addr = base + C::kQOff + (2 * s) * C::kTileBytes;
+        const uint32_t do_addr = q_addr + C::kTileBytes;
+        issue_nt<D>(tmem, base + C::kKOff, q_addr);            // S^T = K Q^T
+        tc_commit(bar_stfull);
+        issue_nt<D>(tmem + 128, base + C::kVOff, do_addr);     // dP^T = V dO^T
+        tc_commit(bar_dptfull);
+        if (!(ok = mbar_wait(W, bar_pdsfull, (uint32_t)i & 1u))) break;
+        tc_fence_after_sync();
+        issue_tn<D>(t_dv, tmem, do_addr, i > 0);                // dV += P^T dO
+        issue_tn<D>(t_dk, tmem + 128, q_addr, i > 0);           // dK += dS^T Q
+        tc_commit(bar_qempty + 8 * s);
+      }
+      if (ok) tc_commit(bar_dkvfull);
+      tc_commit(bar_drain);
+      mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
+    }
+  } else {
+    const int quad = warp & 3, half = warp >> 2;
+    const int krow = quad * 32 + lane;
+    const int key = key0 + krow;
+    const bool key_valid = key < lc;
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    float* my_lse = reinterpret_cast<float*>(gbase + C::kRowOff) + warp * 128;
+    float* my_dl = my_lse + 64;
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int tok0 = (qi_lo + i) * tl.tpt;
+      // columns r of this warp are half*64 + j; row r is (token tok0 + r / g, head r % g)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int r = half * 64 + u * 32 + lane;
+        const int tok = tok0 + r / tl.g;
+        const bool v = r < tl.rows && tok < lc;
+        const size_t idx = (size_t)(hk * tl.g + r % tl.g) * a.total_lc + (size_t)(c0 + tok);
+        my_lse[u * 32 + lane] = v ? a.lse[idx] * kLog2e : 0.f;
+        my_dl[u * 32 + lane] = v ? a.delta[idx] : 0.f;
+      }
+      __syncwarp();
+      // visible columns: r_min <= r < r_max (key <= token, token < Lc, r < rows)
+      int r_lo = (key - tok0) * tl.g;
+      r_lo = r_lo < 0 ? 0 : r_lo;
+      int r_hi = (lc - tok0) * tl.g;
+      r_hi = r_hi < tl.rows ? r_hi : tl.rows;
+      if (!key_valid) r_hi = 0;
+      r_lo -= half * 64;
+      r_hi -= half * 64;
+      if (!(ok = warp_wait(W, bar_stfull, (uint32_t)i & 1u))) break;
+      tc_fence_after_sync();
+      float p[64];
+      {
+        uint32_t r[64];
+        tmem_ld_x64(t_lane + half * 64, r);
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          p[j] = (j >= r_lo && j < r_hi) ? ex2_approx(fmaf(__uint_as_float(r[j]), sl2, -my_lse[j]))
+                                         : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
+        tmem_st_x32(t_lane + half * 64, pk);
+      }
+      if (!(ok = warp_wait(W, bar_dptfull, (uint32_t)i & 1u))) break;
+      tc_fence_after_sync();
+      {
+        uint32_t r[64];
+        tmem_ld_x64(t_lane + 128 + half * 64, r);
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          pk[j] = pack_bf16x2(p[2 * j] * (__uint_as_float(r[2 * j]) - my_dl[2 * j]),
+                              p[2 * j + 1] * (__uint_as_float(r[2 * j + 1]) - my_dl[2 * j + 1]));
+        tmem_st_x32(t_lane + 128 + half * 64, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pdsfull);
+    }
+    if (ok) ok = warp_wait(W, bar_dkvfull, 0);
+    if (ok) {
+      tc_fence_after_sync();
+      const size_t grow = (size_t)(c0 + key) * a.hkv + hk;
+#pragma unroll
+      for (int cb = half * (D / 2); cb < (half + 1) * (D / 2); cb += 32) {
+        uint32_t rv[32], rk[32];
+        tmem_ld_x32(t_dv + ((uint32_t)(quad * 32) << 16) + cb, rv);
+        tmem_ld_x32(t_dk + ((uint32_t)(quad * 32) << 16) + cb, rk);
+        if (key_valid) {
+          uint4* dv = reinterpret_cast<uint4*>(a.dv + grow * D + cb);
+          uint4* dk = reinterpret_cast<uint4*>(a.dk + grow * D + cb);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 u, w;
+            u.x = pack_bf16x2(__uint_as_float(rv[8 * v + 0]), __uint_as_float(rv[8 * v + 1]));
+            u.y = pack_bf16x2(__uint_as_float(rv[8 * v + 2]), __uint_as_float(rv[8 * v + 3]));
+            u.z = pack_bf16x2(__uint_as_float(rv[8 * v + 4]), __uint_as_float(rv[8 * v + 5]));
+            u.w = pack_bf16x2(__uint_as_float(rv[8 * v + 6]), __uint_as_float(rv[8 * v + 7]));
+            w.x = pack_bf16x2(__uint_as_float(rk[8 * v + 0]) * a.scale,
+                              __uint_as_float(rk[8 * v + 1]) * a.scale);
+            w.y = pack_bf16x2(__uint_as_float(rk[8 * v + 2]) * a.scale,
+                              __uint_as_float(rk[8 * v + 3]) * a.scale);
+            w.z = pack_bf16x2(__uint_as_float(rk[8 * v + 4]) * a.scale,
+                              __uint_as_float(rk[8 * v + 5]) * a.scale);
+            w.w = pack_bf16x2(__uint_as_float(rk[8 * v + 6]) * a.scale,
+                              __uint_as_float(rk[8 * v + 7]) * a.scale);
+            dv[v] = u;
+            dk[v] = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Sum the dQ split partials in split order (deterministic) and round to bf16.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
+  constexpr int E = D / 32;
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rid = blockIdx.x * 8 + warp;
+  const int t = rid / a.hq, h = rid % a.hq;
+  const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
+  const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
+  if (t >= lc) return;
+  const int ns = block_splits(a.tl, lp, lc, t / a.tl.tpt);
+  if (ns <= 1) return;
+  const size_t grow = (size_t)(c0 + t);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float* src = a.dq_part + (((size_t)s * a.total_lc + grow) * a.hq + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] += src[e];
+  }
+  __nv_bfloat16* dst = a.dq + (grow * a.hq + h) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e], acc[e + 1]);
+}
+
+// delta[h, t] = sum_c dO[t, h, c] * O[t, h, c]; one warp per (t, h) row.
+template <int D>
+__global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                    const __nv_bfloat16* __restrict__ dout,
+                                                    float* __restrict__ delta, int total_lc,
+                                                    int hq) {
+  constexpr int E = D / 32;
+  const long long rid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (rid >= (long long)total_lc * hq) return;
+  const __nv_bfloat16* po = o + rid * D + lane * E;
+  const __nv_bfloat16* pd = dout + rid * D + lane * E;
+  float sum = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(po + e);
+    const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(pd + e);
+    const float2 fx = __bfloat1622float2(x), fy = __bfloat1622float2(y);
+    sum = fmaf(fx.x, fy.x, sum);
+    sum = fmaf(fx.y, fy.y, sum);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane == 0) {
+    const long long t = rid / hq, h = rid % hq;
+    delta[h * total_lc + t] = sum;
+  }
+}
+
+// q8_0 -> fp32 (exact) and bf16 (round to nearest even), one thread per value.
+__global__ void dequant_q8_0_kernel(const uint8_t* __restrict__ blocks, long long n_values,
+                                    float* __restrict__ out_f32,
+                                    __nv_bfloat16* __restrict__ out_bf16) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_values) return;
+  const uint8_t* blk = blocks + (idx >> 5) * 34;
+  const uint16_t hbits = (uint16_t)blk[0] | ((uint16_t)blk[1] << 8);
+  const float d = __half2float(__ushort_as_half(hbits));
+  const float v = d * (float)(int8_t)blk[2 + (idx & 31)];
+  if (out_f32) out_f32[idx] = v;
+  if (out_bf16) out_bf16[idx] = __float2bfloat16_rn(v);
+}
+
+}  // namespace
+
+int bwd_dq_smem_bytes(int d, int q8) {
+  (void)q8;
+  return d == 128 ? DqCfg<128>::kSmemBytes : DqCfg<64>::kSmemBytes;
+}
+int bwd_dkdv_smem_bytes(int d) {
+  return d == 128 ? DkvCfg<128>::kSmemBytes : DkvCfg<64>::kSmemBytes;
+}
+
+cudaError_t launch_bwd_dq(const Maps& m, const BwdArgs& a, int d, int q8, dim3 grid,
+                          cudaStream_t st) {
+  (void)q8;
+  if (d == 128) {
+    auto k = bwd_dq_kernel<128>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DqCfg<128>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k<<<grid, 320, DqCfg<128>::kSmemBytes, st>>>(m.q, m.dout, m.kp, m.vp, m.kc, m.vc, a);
+  } else {
+    auto k = bwd_dq_kernel<64>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DqCfg<64>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k<<<grid, 320, DqCfg<64>::kSmemBytes, st>>>(m.q, m.dout, m.kp, m.vp, m.kc, m.vc, a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, dim3 grid, cudaStream_t st) {
+  if (d == 128) {
+    auto k = bwd_dkdv_kernel<128>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DkvCfg<128>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k<<<grid, 320, DkvCfg<128>::kSmemBytes, st>>>(m.q, m.dout, m.kc, m.vc, a);
+  } else {
+    auto k = bwd_dkdv_kernel<64>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DkvCfg<64>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k<<<grid, 320, DkvCfg<64>::kSmemBytes, st>>>(m.q, m.dout, m.kc, m.vc, a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_reduce(const BwdArgs& a, int d, int batch, int max_lc, cudaStream_t st) {
+  const long long rows = (long long)max_lc * a.hq;
+  dim3 grid((unsigned)((rows + 7) / 8), (unsigned)batch);
+  if (d == 128)
+    bwd_dq_reduce_kernel<128><<<grid, 256, 0, st>>>(a);
+  else
+    bwd_dq_reduce_kernel<64><<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta,
+                         int total_lc, int hq, int d, cudaStream_t st) {
+  const long long threads = (long long)total_lc * hq * 32;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (d == 128)
+    delta_kernel<128><<<blocks, 256, 0, st>>>(o, dout, delta, total_lc, hq);
+  else
+    delta_kernel<64><<<blocks, 256, 0, st>>>(o, dout, delta, total_lc, hq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_q8_0(const uint8_t* blocks, long long n_blocks, float* out_f32,
+                                __nv_bfloat16* out_bf16, cudaStream_t st) {
+  const long long nv = n_blocks * 32;
+  const unsigned grid = (unsigned)((nv + 255) / 256);
+  dequant_q8_0_kernel<<<grid, 256, 0, st>>>(blocks, nv, out_f32, out_bf16);
+  return cudaGetLastError();
+}
+
+}  // namespace cfa

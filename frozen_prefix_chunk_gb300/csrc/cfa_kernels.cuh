@@ -1,0 +1,76 @@
+// Kernel argument blocks and launchers shared between the host layer
+// (cfa_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "cfa_sched.cuh"
+
+namespace cfa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Wall-clock limit of the bounded waits that unwind a CTA after it has
+// already given up (draining copies and MMAs still in flight).
+constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s
+
+struct FwdArgs {
+  const int32_t* cu_p;
+  const int32_t* cu_c;
+  int hq, hkv, total_lc;
+  Tiling tl;
+  float scale_log2;      // softmax_scale * log2(e)
+  __nv_bfloat16* o;      // [total_lc, hq, D]
+  float* lse;            // [hq, total_lc]
+  float* o_part;         // [n_split_max, total_lc, hq, D]   (split partials)
+  float* lse_part;       // [n_split_max, hq, total_lc]
+  int* status;           // workspace status word
+  unsigned long long limit_ns;
+};
+
+struct BwdArgs {
+  const int32_t* cu_p;
+  const int32_t* cu_c;
+  int hq, hkv, total_lc;
+  Tiling tl;             // dQ tiling (one query tile per CTA)
+  float scale_log2;
+  float scale;
+  const float* lse;      // [hq, total_lc]
+  const float* delta;    // [hq, total_lc]
+  __nv_bfloat16* dq;     // [total_lc, hq, D]
+  __nv_bfloat16* dk;     // [total_lc, hkv, D]
+  __nv_bfloat16* dv;     // [total_lc, hkv, D]
+  float* dq_part;        // [n_split_max, total_lc, hq, D]
+  int* status;
+  unsigned long long limit_ns;
+};
+
+// The five TMA descriptors of one call.  Prefix maps describe bf16 K/V
+// [total_lp, hkv, D] in 64-column boxes of 128 rows, or, for q8_0, the raw
+// block bytes.
+struct Maps {
+  CUtensorMap q, dout, kp, vp, kc, vc;
+};
+
+// Launchers (return a cudaError_t of the launch).
+int fwd_smem_bytes(int d, int q8);
+cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, int q8, dim3 grid,
+                       cudaStream_t st);
+cudaError_t launch_fwd_combine(const FwdArgs& a, int d, int batch, int max_lc, cudaStream_t st);
+
+int bwd_dq_smem_bytes(int d, int q8);
+int bwd_dkdv_smem_bytes(int d);
+cudaError_t launch_bwd_dq(const Maps& m, const BwdArgs& a, int d, int q8, dim3 grid,
+                          cudaStream_t st);
+cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, dim3 grid, cudaStream_t st);
+cudaError_t launch_bwd_dq_reduce(const BwdArgs& a, int d, int batch, int max_lc, cudaStream_t st);
+cudaError_t launch_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta,
+                         int total_lc, int hq, int d, cudaStream_t st);
+cudaError_t launch_dequant_q8_0(const uint8_t* blocks, long long n_blocks, float* out_f32,
+                                __nv_bfloat16* out_bf16, cudaStream_t st);
+
+}  // namespace cfa

@@ -1,0 +1,151 @@
+/*
+ * cfa -- frozen-prefix chunk attention for GB300 (sm_103a), C ABI.
+ *
+ * One trainable reply chunk of Lc query rows attends to a frozen KV prefix of
+ * Lp cached rows plus its own causal keys.  The prefix is a constant: the
+ * training walk of "train: walk the window" (llama.cpp fork PR #40, "What it
+ * is") reads the cached prefix as constants, and its "Why it's a draft"
+ * section states that cached prefixes are stop-gradient constants; the
+ * two-phase step of "Context-Frozen Training" ("The Solution", Phase 2) runs
+ * the decision tokens with gradients against the no-grad cache.  The backward
+ * is the "query-split attention (grad for kept queries only)" that the
+ * prime-rl POC "stop-gradient through context tokens" lists under "Known
+ * gaps": it returns dQ for the chunk rows over all Lp + Lc keys and dK/dV for
+ * the chunk's own keys, and never computes or writes a prefix gradient.
+ *
+ * Definitions (per window b, query head h, kv head h / (Hq/Hkv), chunk row t
+ * at absolute position Lp + t, scale s):
+ *   visible keys J_t = all Lp prefix keys and chunk keys j <= t
+ *   S_tj = s * q_t . k_j,  LSE_t = ln sum_{J_t} exp S_tj,  P_tj = exp(S_tj - LSE_t)
+ *   O_t = sum_{J_t} P_tj v_j
+ *   for dO: delta_t = dO_t . O_t,  dS_tj = P_tj (dO_t . v_j - delta_t)
+ *   dQ_t = s sum_{J_t} dS_tj k_j
+ *   dK_chunk,j = s sum_{heads of the group} sum_{t >= j} dS_tj q_t
+ *   dV_chunk,j =   sum_{heads of the group} sum_{t >= j} P_tj dO_t
+ *
+ * Layouts (packed varlen, "THD", head_dim innermost, row-major, contiguous):
+ *   q, o, dout, dq            [total_lc, hq,  d]      bf16
+ *   k_chunk, v_chunk, dk, dv  [total_lc, hkv, d]      bf16
+ *   k_prefix, v_prefix        [total_lp, hkv, d]      bf16, or
+ *                             [total_lp, hkv, d/32] q8_0 blocks of 34 bytes:
+ *                             little-endian fp16 scale then 32 int8 codes
+ *                             (the llama.cpp q8_0 cache type; V untransposed)
+ *   lse, delta                [hq, total_lc]          fp32 (natural log)
+ *   cu_seqlens_prefix/chunk   [batch + 1]             int32, device memory,
+ *                             non-decreasing, starting at 0
+ * Window b owns prefix rows [cu_p[b], cu_p[b+1]) and chunk rows
+ * [cu_c[b], cu_c[b+1]).  Empty windows and Lp = 0 are allowed.
+ *
+ * Ownership: every pointer is caller-owned device memory (the prefix may be an
+ * imported cache); the library allocates nothing and keeps no state between
+ * calls.  `ws` is caller-provided scratch of at least cfa_workspace_size()
+ * bytes, 256-byte aligned.
+ *
+ * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream).  Nothing synchronises the host or copies device
+ * data to the host, except cfa_read_status().  Host-side sizes (batch,
+ * max_*, total_*) must agree with the device cu_seqlens; they size the grids
+ * and the TMA descriptors, so no device-to-host read is needed.
+ *
+ * Errors: every entry point returns CFA_OK (0) or a negative cfa_status and
+ * never aborts.  Argument errors are found on the host before anything is
+ * enqueued.  A device-side wait that does not finish in time (default 2 s;
+ * the environment variable CFA_WAIT_LIMIT_NS overrides it) ends its kernel
+ * early and records CFA_ERR_DEVICE_TIMEOUT in the status word at the start of
+ * the workspace, readable with cfa_read_status().
+ *
+ * Determinism: the same inputs give bitwise-identical outputs (fixed-order
+ * reductions, no atomics on data); the forward does not depend on whether a
+ * backward follows.
+ */
+#ifndef CFA_H
+#define CFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cfa_status {
+  CFA_OK = 0,
+  CFA_ERR_INVALID_ARG = -1,     /* null/misaligned pointer, bad size or layout */
+  CFA_ERR_UNSUPPORTED = -2,     /* valid but not implemented (e.g. head_dim not 64/128) */
+  CFA_ERR_WORKSPACE = -3,       /* workspace missing, misaligned or too small */
+  CFA_ERR_LAUNCH = -4,          /* a kernel launch or stream operation failed */
+  CFA_ERR_DEVICE_TIMEOUT = -5,  /* a device-side wait ran out (see cfa_read_status) */
+  CFA_ERR_CUDA = -6             /* other CUDA runtime/driver error */
+} cfa_status;
+
+enum { CFA_PREFIX_BF16 = 0, CFA_PREFIX_Q8_0 = 1 };
+enum { CFA_WS_FORWARD = 0, CFA_WS_BACKWARD = 1 };
+
+typedef struct cfa_args {
+  const void* q;                     /* [total_lc, hq, d] bf16 */
+  const void* k_prefix;              /* see layouts; may be NULL iff total_lp == 0 */
+  const void* v_prefix;
+  const void* k_chunk;               /* [total_lc, hkv, d] bf16 */
+  const void* v_chunk;
+  const int32_t* cu_seqlens_prefix;  /* device [batch + 1] */
+  const int32_t* cu_seqlens_chunk;   /* device [batch + 1] */
+  int32_t batch;                     /* windows, >= 1 */
+  int32_t max_lp;                    /* max over windows of Lp (host copy) */
+  int32_t max_lc;                    /* max over windows of Lc (host copy) */
+  int32_t total_lp;                  /* cu_seqlens_prefix[batch] (host copy) */
+  int32_t total_lc;                  /* cu_seqlens_chunk[batch]  (host copy) */
+  int32_t hq;                        /* query heads */
+  int32_t hkv;                       /* kv heads; hq % hkv == 0, hq / hkv <= 128 */
+  int32_t head_dim;                  /* 64 or 128 */
+  int32_t prefix_dtype;              /* CFA_PREFIX_BF16 or CFA_PREFIX_Q8_0 */
+  float softmax_scale;               /* s > 0, applied to the fp32 logits */
+} cfa_args;
+
+/* Bytes of scratch that cfa_forward (which = CFA_WS_FORWARD) or cfa_backward
+ * (which = CFA_WS_BACKWARD) needs for these arguments on the current device.
+ * Returns 0 for invalid arguments. */
+size_t cfa_workspace_size(const cfa_args* a, int which);
+
+/* Forward: O (bf16, [total_lc, hq, d]) and LSE (fp32, [hq, total_lc]).
+ * Attention over prefix + causal chunk keys with an online softmax (q8_0
+ * prefixes are dequantised on the fly), split across CTAs along the keys
+ * when there are few query tiles, then a combine of the split partials. */
+int cfa_forward(const cfa_args* a, void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward preprocess: delta[h, t] = sum_c dO[t, h, c] * O[t, h, c] (fp32
+ * accumulate of the bf16 inputs), the row term of dS. */
+int cfa_backward_preprocess(const cfa_args* a, const void* o, const void* dout, float* delta,
+                            void* stream);
+
+/* Query-split backward: dq ([total_lc, hq, d]) over all prefix and causal
+ * chunk keys; dk_chunk, dv_chunk ([total_lc, hkv, d]) for the chunk keys only,
+ * summed over the query heads of each group.  No prefix gradient exists in
+ * this interface.  Needs lse from cfa_forward and delta from
+ * cfa_backward_preprocess. */
+int cfa_backward(const cfa_args* a, const void* dout, const float* lse, const float* delta,
+                 void* dq, void* dk_chunk, void* dv_chunk, void* ws, size_t ws_bytes,
+                 void* stream);
+
+/* q8_0 dequantisation of n_blocks contiguous 34-byte blocks into 32*n_blocks
+ * values: out_f32 = fp32(d) * q (exact), out_bf16 = that value rounded to
+ * nearest-even bf16 -- the operand the attention kernels multiply with.
+ * Either output may be NULL.  Device pointers; blocks need 2-byte alignment. */
+int cfa_dequant_q8_0(const void* blocks, long long n_blocks, float* out_f32, void* out_bf16,
+                     void* stream);
+
+/* Waits for `stream`, then returns the status word that the kernels of the
+ * last cfa_forward / cfa_backward on this workspace left (CFA_OK or
+ * CFA_ERR_DEVICE_TIMEOUT), or a CUDA error. */
+int cfa_read_status(const void* ws, void* stream);
+
+/* Short description of a status code (static string). */
+const char* cfa_status_string(int status);
+
+/* ABI version: (major << 16) | minor. */
+int cfa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CFA_H */

@@ -1,0 +1,87 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Small workloads are compared on every output; the full-size layer workloads
+on the complete outputs of a sample of (window, KV head) groups, computed in
+the same launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(inp, groups=None):
+    gpu = gu.run_cuda(inp)
+    ref = oracle.run(inp, groups=groups)
+    err = gu.errors(gpu, ref, inp, groups)
+    print(inp["workload"].name, err)
+    gu.assert_within(err)
+    return gpu
+
+
+def test_tiny_workload():
+    _check(synth.make_inputs(synth.workload("tiny")))
+
+
+def test_qwen3_1p7b_layer_full():
+    _check(synth.make_inputs(synth.workload("qwen3_1p7b")))
+
+
+EDGE = [
+    # hq, hkv, d, lp, lc
+    dict(hq=2, hkv=1, head_dim=64, lp=[0], lc=[64]),          # no prefix: plain causal
+    dict(hq=4, hkv=2, head_dim=128, lp=[300], lc=[1]),        # single chunk row
+    dict(hq=4, hkv=4, head_dim=128, lp=[129], lc=[130]),      # g = 1, ragged tiles
+    dict(hq=6, hkv=2, head_dim=64, lp=[257], lc=[77]),        # g = 3: 126-row tiles
+    dict(hq=8, hkv=1, head_dim=128, lp=[1000], lc=[200]),     # g = 8
+    dict(hq=4, hkv=2, head_dim=128, lp=[5, 0, 700, 128], lc=[37, 100, 0, 256]),  # varlen + empty
+    dict(hq=2, hkv=2, head_dim=64, lp=[4096], lc=[3]),        # long prefix, many splits
+]
+
+
+@pytest.mark.parametrize("cfg", EDGE, ids=[str(i) for i in range(len(EDGE))])
+def test_edge_shapes(cfg):
+    w = synth.custom(**cfg, seed=11, dout_std=1.0)
+    _check(synth.make_inputs(w))
+
+
+def test_qwen3_8b_layer_sampled_groups():
+    inp = synth.make_inputs(synth.workload("qwen3_8b"))
+    _check(inp, groups=[(0, 0), (0, 5)])
+
+
+def test_varlen8_sampled_groups():
+    inp = synth.make_inputs(synth.workload("varlen8"))
+    _check(inp, groups=[(2, 1), (3, 7), (5, 0)])
+
+
+def test_deterministic_and_forward_independent_of_backward():
+    inp = synth.make_inputs(synth.custom(hq=8, hkv=2, head_dim=128, lp=[2000, 300],
+                                         lc=[200, 129], seed=3))
+    a = gu.run_cuda(inp)
+    b = gu.run_cuda(inp)
+    c = gu.run_cuda(inp, backward=False)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    assert torch.equal(a["o"], c["o"]) and torch.equal(a["lse"], c["lse"])
+
+
+def test_dequant_q8_0_bit_exact():
+    import frozen_prefix_chunk_gb300 as cfa
+    x = torch.randn(4096, 128, generator=torch.Generator().manual_seed(9)) * 3
+    blocks = synth.encode_q8_0(x)
+    # also the corner codes the encoder never emits
+    raw = blocks.clone().view(-1, 34)
+    raw[0, 2] = 0x80       # code -128
+    raw[1, 0:2] = torch.tensor([0x01, 0x00], dtype=torch.uint8)   # subnormal scale
+    raw[2, 0:2] = torch.tensor([0x00, 0x80], dtype=torch.uint8)   # -0 scale
+    blocks = raw.view_as(blocks)
+    f32, bf = cfa.dequant_q8_0(blocks.cuda())
+    rf64, rf32, rbf = oracle.dequant_q8_0(blocks.numpy())
+    assert np.array_equal(f32.cpu().numpy().view(np.uint32), rf32.view(np.uint32))
+    assert np.array_equal(bf.cpu().view(torch.int16).numpy().view(np.uint16), rbf)
