@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark: frozen-prefix chunk attention fwd+bwd on GB300.
+
+One step = cfa_forward + cfa_backward_preprocess + cfa_backward (as its two
+halves, cfa_backward_dq and cfa_backward_dkdv) over one batch of synthetic
+input resident in HBM.  Prints ONE JSON line (rank 0).
+
+Metric: useful TFLOP/s of fwd+bwd.  Useful FLOPs per query head, with
+Np = sum Lc*Lp and Nc = sum Lc(Lc+1)/2 (masked halves and the prefix dK/dV
+the method never computes are not counted):
+    forward  4 d (Np + Nc)          backward  6 d Np + 10 d Nc
+Roofline of the step: t_roof = max(F / bf16 peak, algorithmic bytes / HBM
+bandwidth), fraction = t_roof / t_measured.
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
+launching stream; L2 is flushed (256 MiB write) before every timed step,
+outside the events.  Under torchrun every rank runs its own replica of the
+workload (weak scaling, no collective on the data path); value = all ranks'
+FLOPs / max over ranks of the time.
+
+--impl reference times the fp64 CPU oracle instead (the deliberately slow
+baseline arm), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "frozen-prefix chunk attention fwd+bwd TFLOP/s and % of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------- accounting --
+
+def useful_flops(w) -> dict:
+    np_pairs = sum(c * p for c, p in zip(w.lc, w.lp))
+    nc_pairs = sum(c * (c + 1) // 2 for c in w.lc)
+    d, h = w.head_dim, w.hq
+    fwd = 4 * d * (np_pairs + nc_pairs) * h
+    bwd = (6 * d * np_pairs + 10 * d * nc_pairs) * h
+    # the dQ kernel's own contraction work: S, dP and dQ over every visible pair
+    dq_kernel = 6 * d * (np_pairs + nc_pairs) * h
+    return dict(fwd=fwd, bwd=bwd, total=fwd + bwd, dq_kernel=dq_kernel)
+
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes each pass must move at least once (split partials excluded)."""
+    d, tp, tc = w.head_dim, sum(w.lp), sum(w.lc)
+    pref = 34 / 32 if w.prefix_dtype == synth.PREFIX_Q8_0 else 2.0
+    qb = tc * w.hq * d * 2
+    kvp = 2 * tp * w.hkv * d * pref
+    kvc = 2 * tc * w.hkv * d * 2
+    lse = tc * w.hq * 4
+    fwd = qb + kvp + kvc + qb + lse                  # read q, k, v; write O, LSE
+    pre = 2 * qb + lse                                # read O, dO; write delta
+    dq_kernel = 2 * qb + 2 * lse + kvp + kvc + qb     # read q, dO, lse, delta, k, v; write dQ
+    bwd = dq_kernel + 2 * qb + 2 * lse + kvc + kvc    # + dK/dV half: q, dO, lse, delta, kc/vc, dK/dV
+    return dict(fwd=fwd, pre=pre, bwd=bwd, dq_kernel=dq_kernel, total=fwd + pre + bwd)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "frozen_prefix_chunk_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dQ kernel from the committed ncu summary,
+    or None when the kernels changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    rec = d.get(workload)
+    if not rec or rec.get("csrc_sha") != kernel_source_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(device_index), "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- oracle arm --
+
+def _group_inputs(inp, b, hk, lc_sub):
+    """The first lc_sub chunk rows of window b, KV head hk, as a one-window
+    one-head-group workload (rows before lc_sub see exactly the same keys)."""
+    w = inp["workload"]
+    g = w.hq // w.hkv
+    cu_p = inp["cu_seqlens_prefix"].tolist()
+    cu_c = inp["cu_seqlens_chunk"].tolist()
+    c0, p0, p1 = cu_c[b], cu_p[b], cu_p[b + 1]
+    sub = synth.custom(hq=g, hkv=1, head_dim=w.head_dim, lp=[p1 - p0], lc=[lc_sub],
+                       prefix_dtype=w.prefix_dtype, softmax_scale=w.softmax_scale,
+                       name=w.name)
+    heads = slice(hk * g, (hk + 1) * g)
+    rows = slice(c0, c0 + lc_sub)
+    return dict(q=inp["q"][rows, heads].contiguous(),
+                k_prefix=inp["k_prefix"][p0:p1, hk:hk + 1].contiguous(),
+                v_prefix=inp["v_prefix"][p0:p1, hk:hk + 1].contiguous(),
+                k_chunk=inp["k_chunk"][rows, hk:hk + 1].contiguous(),
+                v_chunk=inp["v_chunk"][rows, hk:hk + 1].contiguous(),
+                dout=inp["dout"][rows, heads].contiguous(),
+                cu_seqlens_prefix=synth.cu_seqlens([p1 - p0]),
+                cu_seqlens_chunk=synth.cu_seqlens([lc_sub]), workload=sub)
+
+
+def oracle_sample(inp, budget_s, group=(0, 0)):
+    """Time the oracle, as it stands, on a bounded sample: the first rows of
+    one (window, KV head) group, as many as fit in about budget_s (calibrated
+    on two rows).  Returns (seconds, useful FLOPs of the sample, text)."""
+    import oracle
+
+    oracle.build()
+    w = inp["workload"]
+    b, hk = group
+    lc = w.lc[b]
+    probe = _group_inputs(inp, b, hk, min(lc, 2))
+    t0 = time.perf_counter()
+    oracle.run(probe)
+    per_row = (time.perf_counter() - t0) / min(lc, 2)
+    lc_sub = max(1, min(lc, int(budget_s / max(per_row, 1e-9))))
+    sub = _group_inputs(inp, b, hk, lc_sub)
+    t0 = time.perf_counter()
+    oracle.run(sub)
+    dt = time.perf_counter() - t0
+    f = useful_flops(sub["workload"])["total"]
+    desc = (f"oracle fwd+bwd of chunk rows 0..{lc_sub - 1} of window {b}, kv head {hk} of "
+            f"{w.name} ({w.hq // w.hkv} query heads, Lp={w.lp[b]}, Lc={lc_sub} of {lc})")
+    return dt, f, desc
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    import oracle
+
+    inp = synth.make_inputs(w)
+    oracle.build()
+    budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))
+    times, f, desc = [], 0, ""
+    for i in range(args.warmup + args.steps):
+        dt, f, desc = oracle_sample(inp, budget, group=(i % w.batch, i % w.hkv))
+        if i >= args.warmup:
+            times.append((dt, f))
+    sec = sum(t for t, _ in times)
+    value = sum(x for _, x in times) / sec / 1e12
+    ms = sec / len(times) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, "n/a (CPU)"),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
+                             "kind": "oracle", "sample": desc + " (one group per step)"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, l2):
+    return {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv,
+            "head_dim": w.head_dim, "lp": w.lp, "lc": w.lc,
+            "prefix": "q8_0" if w.prefix_dtype == synth.PREFIX_Q8_0 else "bf16",
+            "softmax_scale": w.softmax_scale, "l2": l2, "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------- GPU arm --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="cfa", choices=["cfa", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b", choices=list(synth.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = synth.workload(args.workload, seed=0)
+
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+
+    import torch.distributed as dist
+    import frozen_prefix_chunk_gb300 as cfa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    cfa.lib(build_if_missing=True)
+
+    # every rank has its own replica of the workload
+    w = synth.workload(args.workload, seed=rank)
+    host = synth.make_inputs(w)
+    names = ("q", "k_prefix", "v_prefix", "k_chunk", "v_chunk", "dout",
+             "cu_seqlens_prefix", "cu_seqlens_chunk")
+    d = {k: host[k].to(dev) for k in names}
+    a = cfa.make_args(d["q"], d["k_prefix"], d["v_prefix"], d["k_chunk"], d["v_chunk"],
+                      d["cu_seqlens_prefix"], d["cu_seqlens_chunk"], max(w.lp), max(w.lc),
+                      w.softmax_scale, w.prefix_dtype, hkv=w.hkv, total_lp=sum(w.lp))
+    tc = sum(w.lc)
+    o = torch.empty_like(d["q"])
+    lse = torch.empty(w.hq, tc, dtype=torch.float32, device=dev)
+    delta = torch.empty_like(lse)
+    dq = torch.empty_like(d["q"])
+    dk = torch.empty(tc, w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
+    dv = torch.empty_like(dk)
+    ws_f = torch.empty(cfa.workspace_size(a, cfa.WS_FORWARD), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(cfa.workspace_size(a, cfa.WS_BACKWARD), dtype=torch.uint8, device=dev)
+    ws_kv = torch.empty(256, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    # kernels launched per step: forward (+ split combine), delta, dQ (+ split
+    # reduce), dK/dV; a workspace beyond its 256-byte header holds partials
+    launches_per_step = (1 + (ws_f.numel() > 256)) + 1 + (1 + (ws_b.numel() > 256)) + 1
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        cfa.forward(a, d["q"], o, lse, ws_f)
+        if ev:
+            ev[1].record(stream)
+        cfa.backward_preprocess(a, o, d["dout"], delta)
+        if ev:
+            ev[2].record(stream)
+        cfa.backward_dq(a, d["dout"], lse, delta, dq, ws_b)
+        if ev:
+            ev[3].record(stream)
+        cfa.backward_dkdv(a, d["dout"], lse, delta, dk, dv, ws_kv)
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    for ws in (ws_f, ws_b, ws_kv):
+        st = cfa.read_status(ws)
+        assert st == 0, f"device status {st}"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        step(evs[k])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    for ws in (ws_f, ws_b, ws_kv):
+        assert cfa.read_status(ws) == 0
+
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dq_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    dkdv_ms = [e[3].elapsed_time(e[4]) for e in evs]
+    tot_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms_per_step = tot_ms / args.steps
+
+    flops = useful_flops(w)
+    byts = algorithmic_bytes(w)
+    value = world * flops["total"] / (ms_per_step * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    bf16_peak = peaks["bf16_tflops"]
+    hbm_peak = peaks["hbm_gbs"]
+    dq_mean = statistics.mean(dq_ms)
+    achieved = flops["dq_kernel"] / (dq_mean * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": achieved / bf16_peak, "traffic": recorded_traffic(w.name),
+                "kernel": "bwd_dq_kernel + split reduce (cfa_backward_dq)",
+                "peak_source": f"bf16_tflops burst, {peak_src}",
+                "algorithmic_flops_per_launch": flops["dq_kernel"], "ms_per_launch": dq_mean}
+    t_roof = max(flops["total"] / (bf16_peak * 1e12), byts["total"] / (hbm_peak * 1e9))
+    step_roof = {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_per_step * 1e-3),
+                 "fwd_ms": statistics.mean(fwd_ms), "dq_ms": dq_mean,
+                 "dkdv_ms": statistics.mean(dkdv_ms),
+                 "fwd_tflops": flops["fwd"] / (statistics.mean(fwd_ms) * 1e-3) / 1e12,
+                 "useful_gflop": flops["total"] / 1e9, "algorithmic_mb": byts["total"] / 1e6,
+                 "peaks": f"bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s ({peak_src})"}
+
+    # ---- end to end through the public API, host buffers, copies timed
+    pin = {k: host[k].pin_memory() for k in names}
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    e2e_ms = []
+    for k in range(args.e2e_steps + 2):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for n in names:
+            d[n].copy_(pin[n], non_blocking=True)
+        step()
+        for src, dst in zip((o, lse, dq, dk, dv), outs_h):
+            dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if k >= 2:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_val = world * flops["total"] / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        dt, f, desc = oracle_sample(host, 15.0, (0, 0))
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+               "kind": "oracle", "sample": desc, "seconds": dt}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v, N(0,0.1) dO)",
+                "config": config_of(w, "flushed before every timed step (256 MiB write)"),
+                "roofline": roofline, "step_roofline": step_roof,
+                "cpu_baseline": cpu,
+                "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+                "gpu_launches": launches_per_step * args.steps,
+                "clocks": clocks, "wall_s_timed": t_wall}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -22,7 +22,7 @@ import torch
 from . import build as _build
 
 __all__ = ["CfaError", "Args", "lib", "workspace_size", "forward", "backward_preprocess",
-           "backward", "dequant_q8_0", "read_status", "PREFIX_BF16", "PREFIX_Q8_0"]
+           "backward", "backward_dq", "backward_dkdv", "dequant_q8_0", "read_status", "PREFIX_BF16", "PREFIX_Q8_0"]
 
 PREFIX_BF16 = 0
 PREFIX_Q8_0 = 1
@@ -69,11 +69,14 @@ def lib(build_if_missing: bool = False):
             L.cfa_forward.argtypes = [ap, vp, vp, vp, sz, vp]
             L.cfa_backward_preprocess.argtypes = [ap, vp, vp, vp, vp]
             L.cfa_backward.argtypes = [ap, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.cfa_backward_dq.argtypes = [ap, vp, vp, vp, vp, vp, sz, vp]
+            L.cfa_backward_dkdv.argtypes = [ap, vp, vp, vp, vp, vp, vp, sz, vp]
             L.cfa_dequant_q8_0.argtypes = [vp, ctypes.c_longlong, vp, vp, vp]
             L.cfa_read_status.argtypes = [vp, vp]
             L.cfa_status_string.argtypes = [ctypes.c_int]
             L.cfa_status_string.restype = ctypes.c_char_p
             for f in ("cfa_forward", "cfa_backward_preprocess", "cfa_backward",
+                      "cfa_backward_dq", "cfa_backward_dkdv",
                       "cfa_dequant_q8_0", "cfa_read_status", "cfa_version"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
@@ -171,6 +174,22 @@ def backward(args: Args, dout, lse, delta, dq=None, dk=None, dv=None, ws=None, s
                               _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)),
            "cfa_backward")
     return dq, dk, dv, ws
+
+
+def backward_dq(args: Args, dout, lse, delta, dq, ws, stream=None):
+    """cfa_backward_dq: the dQ half of the backward (dq preallocated)."""
+    _check(lib().cfa_backward_dq(ctypes.byref(args), _ptr(dout), _ptr(lse), _ptr(delta),
+                                 _ptr(dq), _ptr(ws), ws.numel(), _stream(stream)),
+           "cfa_backward_dq")
+    return dq
+
+
+def backward_dkdv(args: Args, dout, lse, delta, dk, dv, ws, stream=None):
+    """cfa_backward_dkdv: the chunk dK/dV half of the backward."""
+    _check(lib().cfa_backward_dkdv(ctypes.byref(args), _ptr(dout), _ptr(lse), _ptr(delta),
+                                   _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)),
+           "cfa_backward_dkdv")
+    return dk, dv
 
 
 def dequant_q8_0(blocks: torch.Tensor, stream=None):

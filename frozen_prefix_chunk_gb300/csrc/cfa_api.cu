@@ -252,57 +252,121 @@ int cfa_backward_preprocess(const cfa_args* a, const void* o, const void* dout, 
   return CFA_OK;
 }
 
-int cfa_backward(const cfa_args* a, const void* dout, const float* lse, const float* delta,
-                 void* dq, void* dk_chunk, void* dv_chunk, void* ws, size_t ws_bytes,
-                 void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared set-up of the backward halves: validation, plan, workspace check,
+// status-word clear, TMA maps and the kernel argument block.  Returns a
+// status; *skip is set when there is nothing to compute.
+int prepare_backward(const cfa_args* a, const void* dout, const float* lse, const float* delta,
+                     void* ws, size_t ws_bytes, bool need_partials, cudaStream_t s, Plan* p,
+                     Maps* m, BwdArgs* ba, bool* skip) {
+  *skip = false;
   int st = validate(a);
   if (st) return st;
-  if (a->total_lc > 0 && (!dout || !lse || !delta || !dq || !dk_chunk || !dv_chunk ||
-                          !aligned16(dout) || !aligned16(dq) || !aligned16(dk_chunk) ||
-                          !aligned16(dv_chunk)))
-    return CFA_ERR_INVALID_ARG;
-  Plan p;
-  if ((st = make_plan(a, &p))) return st;
-  if ((st = check_ws(ws, ws_bytes, p.ws_bwd))) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a->total_lc > 0 && (!dout || !lse || !delta || !aligned16(dout))) return CFA_ERR_INVALID_ARG;
+  if ((st = make_plan(a, p))) return st;
+  if ((st = check_ws(ws, ws_bytes, need_partials ? p->ws_bwd : kWsHeader))) return st;
   if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return CFA_ERR_LAUNCH;
-  if (a->total_lc == 0 || a->max_lc == 0) return CFA_OK;
-
-  Maps m;
-  std::memset(&m, 0, sizeof(m));
-  const Tiling& tl = p.dq;
-  if ((st = make_map_bf16(&m.q, a->q, a->head_dim, a->hq, a->total_lc, tl.g, tl.tpt))) return st;
-  if ((st = make_map_bf16(&m.dout, dout, a->head_dim, a->hq, a->total_lc, tl.g, tl.tpt)))
+  if (a->total_lc == 0 || a->max_lc == 0) {
+    *skip = true;
+    return CFA_OK;
+  }
+  std::memset(m, 0, sizeof(*m));
+  const Tiling& tl = p->dq;
+  if ((st = make_map_bf16(&m->q, a->q, a->head_dim, a->hq, a->total_lc, tl.g, tl.tpt))) return st;
+  if ((st = make_map_bf16(&m->dout, dout, a->head_dim, a->hq, a->total_lc, tl.g, tl.tpt)))
     return st;
-  if ((st = encode_kv_maps(a, &m))) return st;
-
-  BwdArgs ba;
-  ba.cu_p = a->cu_seqlens_prefix;
-  ba.cu_c = a->cu_seqlens_chunk;
-  ba.hq = a->hq;
-  ba.hkv = a->hkv;
-  ba.total_lc = a->total_lc;
-  ba.tl = tl;
-  ba.scale_log2 = a->softmax_scale * kLog2e;
-  ba.scale = a->softmax_scale;
-  ba.lse = lse;
-  ba.delta = delta;
-  ba.dq = static_cast<__nv_bfloat16*>(dq);
-  ba.dk = static_cast<__nv_bfloat16*>(dk_chunk);
-  ba.dv = static_cast<__nv_bfloat16*>(dv_chunk);
+  if ((st = encode_kv_maps(a, m))) return st;
+  ba->cu_p = a->cu_seqlens_prefix;
+  ba->cu_c = a->cu_seqlens_chunk;
+  ba->hq = a->hq;
+  ba->hkv = a->hkv;
+  ba->total_lc = a->total_lc;
+  ba->tl = tl;
+  ba->scale_log2 = a->softmax_scale * kLog2e;
+  ba->scale = a->softmax_scale;
+  ba->lse = lse;
+  ba->delta = delta;
+  ba->dq = ba->dk = ba->dv = nullptr;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  ba.dq_part = p.off_dqpart ? reinterpret_cast<float*>(w + p.off_dqpart) : nullptr;
-  ba.status = reinterpret_cast<int*>(w);
-  ba.limit_ns = wait_limit_ns();
+  ba->dq_part = (need_partials && p->off_dqpart) ? reinterpret_cast<float*>(w + p->off_dqpart)
+                                                 : nullptr;
+  ba->status = reinterpret_cast<int*>(w);
+  ba->limit_ns = wait_limit_ns();
+  return CFA_OK;
+}
 
-  dim3 grid_dq((unsigned)(tl.n_qblk_max * tl.n_split_max), (unsigned)a->hkv, (unsigned)a->batch);
-  if (launch_bwd_dq(m, ba, a->head_dim, 0, grid_dq, s) != cudaSuccess) return CFA_ERR_LAUNCH;
-  dim3 grid_kv((unsigned)p.n_kc_max, (unsigned)a->hkv, (unsigned)a->batch);
-  if (launch_bwd_dkdv(m, ba, a->head_dim, grid_kv, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+int run_dq(const cfa_args* a, const Plan& p, const Maps& m, const BwdArgs& ba, cudaStream_t s) {
+  const Tiling& tl = p.dq;
+  dim3 grid((unsigned)(tl.n_qblk_max * tl.n_split_max), (unsigned)a->hkv, (unsigned)a->batch);
+  if (launch_bwd_dq(m, ba, a->head_dim, 0, grid, s) != cudaSuccess) return CFA_ERR_LAUNCH;
   if (tl.n_split_max > 1 &&
       launch_bwd_dq_reduce(ba, a->head_dim, a->batch, a->max_lc, s) != cudaSuccess)
     return CFA_ERR_LAUNCH;
   return CFA_OK;
+}
+
+int run_dkdv(const cfa_args* a, const Plan& p, const Maps& m, const BwdArgs& ba, cudaStream_t s) {
+  dim3 grid((unsigned)p.n_kc_max, (unsigned)a->hkv, (unsigned)a->batch);
+  if (launch_bwd_dkdv(m, ba, a->head_dim, grid, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  return CFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cfa_backward(const cfa_args* a, const void* dout, const float* lse, const float* delta,
+                 void* dq, void* dk_chunk, void* dv_chunk, void* ws, size_t ws_bytes,
+                 void* stream) {
+  if (a && a->total_lc > 0 && (!dq || !dk_chunk || !dv_chunk || !aligned16(dq) ||
+                               !aligned16(dk_chunk) || !aligned16(dv_chunk)))
+    return CFA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Plan p;
+  Maps m;
+  BwdArgs ba;
+  bool skip;
+  int st = prepare_backward(a, dout, lse, delta, ws, ws_bytes, true, s, &p, &m, &ba, &skip);
+  if (st || skip) return st;
+  ba.dq = static_cast<__nv_bfloat16*>(dq);
+  ba.dk = static_cast<__nv_bfloat16*>(dk_chunk);
+  ba.dv = static_cast<__nv_bfloat16*>(dv_chunk);
+  if ((st = run_dq(a, p, m, ba, s))) return st;
+  return run_dkdv(a, p, m, ba, s);
+}
+
+int cfa_backward_dq(const cfa_args* a, const void* dout, const float* lse, const float* delta,
+                    void* dq, void* ws, size_t ws_bytes, void* stream) {
+  if (a && a->total_lc > 0 && (!dq || !aligned16(dq))) return CFA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Plan p;
+  Maps m;
+  BwdArgs ba;
+  bool skip;
+  int st = prepare_backward(a, dout, lse, delta, ws, ws_bytes, true, s, &p, &m, &ba, &skip);
+  if (st || skip) return st;
+  ba.dq = static_cast<__nv_bfloat16*>(dq);
+  return run_dq(a, p, m, ba, s);
+}
+
+int cfa_backward_dkdv(const cfa_args* a, const void* dout, const float* lse, const float* delta,
+                      void* dk_chunk, void* dv_chunk, void* ws, size_t ws_bytes, void* stream) {
+  if (a && a->total_lc > 0 && (!dk_chunk || !dv_chunk || !aligned16(dk_chunk) ||
+                               !aligned16(dv_chunk)))
+    return CFA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Plan p;
+  Maps m;
+  BwdArgs ba;
+  bool skip;
+  int st = prepare_backward(a, dout, lse, delta, ws, ws_bytes, false, s, &p, &m, &ba, &skip);
+  if (st || skip) return st;
+  ba.dk = static_cast<__nv_bfloat16*>(dk_chunk);
+  ba.dv = static_cast<__nv_bfloat16*>(dv_chunk);
+  return run_dkdv(a, p, m, ba, s);
 }
 
 int cfa_dequant_q8_0(const void* blocks, long long n_blocks, float* out_f32, void* out_bf16,

@@ -126,6 +126,17 @@ int cfa_backward(const cfa_args* a, const void* dout, const float* lse, const fl
                  void* dq, void* dk_chunk, void* dv_chunk, void* ws, size_t ws_bytes,
                  void* stream);
 
+/* The two independent halves of cfa_backward, for callers that schedule them
+ * separately (e.g. on two streams).  cfa_backward_dq writes dq (it needs the
+ * cfa_workspace_size(CFA_WS_BACKWARD) workspace for its split partials);
+ * cfa_backward_dkdv writes dk_chunk and dv_chunk and needs only the 256-byte
+ * status header of a workspace.  Both clear the status word of the workspace
+ * they are given, so concurrent halves need separate workspaces. */
+int cfa_backward_dq(const cfa_args* a, const void* dout, const float* lse, const float* delta,
+                    void* dq, void* ws, size_t ws_bytes, void* stream);
+int cfa_backward_dkdv(const cfa_args* a, const void* dout, const float* lse, const float* delta,
+                      void* dk_chunk, void* dv_chunk, void* ws, size_t ws_bytes, void* stream);
+
 /* q8_0 dequantisation of n_blocks contiguous 34-byte blocks into 32*n_blocks
  * values: out_f32 = fp32(d) * q (exact), out_bf16 = that value rounded to
  * nearest-even bf16 -- the operand the attention kernels multiply with.

@@ -154,28 +154,3 @@ def make_inputs(w: Workload) -> dict:
     return dict(q=q, k_prefix=kp, v_prefix=vp, k_chunk=kc, v_chunk=vc, dout=dout,
                 cu_seqlens_prefix=cu_seqlens(w.lp), cu_seqlens_chunk=cu_seqlens(w.lc),
                 workload=w)
-
-
-def useful_flops(w: Workload) -> dict:
-    """Useful FLOPs of one fwd+bwd step (masked halves and the prefix dK/dV
-    that the method never computes are not counted)."""
-    np_pairs = sum(c * p for c, p in zip(w.lc, w.lp))
-    nc_pairs = sum(c * (c + 1) // 2 for c in w.lc)
-    d = w.head_dim
-    fwd = 4 * d * (np_pairs + nc_pairs) * w.hq
-    bwd = (6 * d * np_pairs + 10 * d * nc_pairs) * w.hq
-    return dict(fwd=fwd, bwd=bwd, total=fwd + bwd)
-
-
-def algorithmic_bytes(w: Workload) -> dict:
-    """Bytes each pass must move at least once (split partials excluded)."""
-    d, tp, tc = w.head_dim, sum(w.lp), sum(w.lc)
-    pref = (Q8_0_BYTES / Q8_0_BLOCK) if w.prefix_dtype == PREFIX_Q8_0 else 2.0
-    qb = tc * w.hq * d * 2
-    kvp = 2 * tp * w.hkv * d * pref
-    kvc = 2 * tc * w.hkv * d * 2
-    lse = tc * w.hq * 4
-    fwd = qb + kvp + kvc + qb + lse                       # read q,k,v ; write O, LSE
-    pre = 2 * qb + lse                                     # read O, dO ; write delta
-    bwd = 2 * qb + 2 * lse + kvp + kvc + qb + kvc          # read q,dO,lse,delta,k,v ; write dQ,dK_c,dV_c
-    return dict(fwd=fwd, pre=pre, bwd=bwd, total=fwd + pre + bwd)
