@@ -73,6 +73,10 @@ def lib(build_if_missing: bool = False):
             L.cfa_backward_dkdv.argtypes = [ap, vp, vp, vp, vp, vp, vp, sz, vp]
             L.cfa_dequant_q8_0.argtypes = [vp, ctypes.c_longlong, vp, vp, vp]
             L.cfa_read_status.argtypes = [vp, vp]
+            L.cfa_forward_noalloc.argtypes = [ap, vp, vp, vp]
+            L.cfa_forward_noalloc.restype = ctypes.c_int
+            L.cfa_noalloc_scratch_bytes.argtypes = []
+            L.cfa_noalloc_scratch_bytes.restype = sz
             L.cfa_status_string.argtypes = [ctypes.c_int]
             L.cfa_status_string.restype = ctypes.c_char_p
             for f in ("cfa_forward", "cfa_backward_preprocess", "cfa_backward",
@@ -147,6 +151,16 @@ def forward(args: Args, q: torch.Tensor, o=None, lse=None, ws=None, stream=None)
     _check(lib().cfa_forward(ctypes.byref(args), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
                              _stream(stream)), "cfa_forward")
     return o, lse, ws
+
+
+def forward_noalloc(args: Args, o: torch.Tensor, lse: torch.Tensor, stream=None):
+    """cfa_forward_noalloc: the forward for callers that cannot allocate; its
+    split partials live in the library's fixed device scratch array instead
+    of a caller workspace.  o and lse are caller-provided; nothing is
+    allocated.  Calls overlapping on the GPU race on the shared scratch."""
+    _check(lib().cfa_forward_noalloc(ctypes.byref(args), _ptr(o), _ptr(lse), _stream(stream)),
+           "cfa_forward_noalloc")
+    return o, lse
 
 
 def backward_preprocess(args: Args, o, dout, delta=None, stream=None):

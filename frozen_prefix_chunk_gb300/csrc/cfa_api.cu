@@ -185,6 +185,7 @@ const char* cfa_status_string(int s) {
     case CFA_ERR_LAUNCH: return "kernel launch failed";
     case CFA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case CFA_ERR_CUDA: return "CUDA error";
+    case CFA_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of cfa_forward_noalloc";
     default: return "unknown status";
   }
 }

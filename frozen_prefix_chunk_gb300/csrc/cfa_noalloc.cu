@@ -1,0 +1,67 @@
+// cfa_forward_noalloc: the forward pass for callers that cannot allocate.
+//
+// cfa_forward needs a caller-provided workspace for its split partials.  Some
+// callers cannot call cudaMalloc (or any allocator) to make one: a trainer
+// that runs beside an inference server which reserved the GPU's memory up
+// front, or a plain C program whose device memory is handed out by someone
+// else's pool.  This entry point runs the same forward with its scratch in a
+// fixed-size array that lives in this file's device module instead, so the
+// caller only passes inputs and outputs.
+//
+// The array is kScratchBytes long.  Every GPU on which this entry point runs
+// holds it from its first call until the process exits.  All calls share it
+// and it keeps the last call's contents; the status word at its start is
+// cleared at the start of every call and the split partials are fully
+// rewritten before they are read, so nothing else needs clearing.  Calls that
+// overlap on the GPU (different streams, or different host threads on one
+// device) race on the array and must be serialised by the caller.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "cfa.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
+
+std::mutex g_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_scratch on the current device.  The first call on a
+// device looks it up (this loads the module that holds the array); later
+// calls reuse the cached address.
+int scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CFA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return CFA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return CFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t cfa_noalloc_scratch_bytes(void) { return kScratchBytes; }
+
+int cfa_forward_noalloc(const cfa_args* a, void* o, float* lse, void* stream) {
+  const size_t need = cfa_workspace_size(a, CFA_WS_FORWARD);
+  if (need == 0) return CFA_ERR_INVALID_ARG;
+  if (need > kScratchBytes) return CFA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  int st = scratch_address(&scratch);
+  if (st) return st;
+  return cfa_forward(a, o, lse, scratch, kScratchBytes, stream);
+}
+
+}  // extern "C"

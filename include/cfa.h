@@ -75,7 +75,9 @@ typedef enum cfa_status {
   CFA_ERR_WORKSPACE = -3,       /* workspace missing, misaligned or too small */
   CFA_ERR_LAUNCH = -4,          /* a kernel launch or stream operation failed */
   CFA_ERR_DEVICE_TIMEOUT = -5,  /* a device-side wait ran out (see cfa_read_status) */
-  CFA_ERR_CUDA = -6             /* other CUDA runtime/driver error */
+  CFA_ERR_CUDA = -6,            /* other CUDA runtime/driver error */
+  CFA_ERR_SCRATCH_LIMIT = -7    /* request needs more than the fixed scratch of
+                                   cfa_forward_noalloc */
 } cfa_status;
 
 enum { CFA_PREFIX_BF16 = 0, CFA_PREFIX_Q8_0 = 1 };
@@ -143,6 +145,26 @@ int cfa_backward_dkdv(const cfa_args* a, const void* dout, const float* lse, con
  * Either output may be NULL.  Device pointers; blocks need 2-byte alignment. */
 int cfa_dequant_q8_0(const void* blocks, long long n_blocks, float* out_f32, void* out_bf16,
                      void* stream);
+
+/* Forward without a caller workspace, for callers that cannot allocate device
+ * memory: a trainer sharing the GPU with an inference server that reserved
+ * the memory up front, or a C program whose device memory comes only from
+ * someone else's pool.  The pages have no counterpart to this entry point.
+ * Same inputs and outputs as cfa_forward; the split partials live in a
+ * fixed array of cfa_noalloc_scratch_bytes() bytes (32 MiB) inside the
+ * library, which every GPU that runs this call holds until the process
+ * exits.  The first call on a device looks up that array's address (this
+ * loads the module that holds it), so make it before any stream capture.
+ * Calls whose forward workspace would exceed the array return
+ * CFA_ERR_SCRATCH_LIMIT before anything is enqueued.  Nothing is allocated.
+ * All calls share the array: calls that overlap on the GPU (other streams or
+ * threads on the same device) race and must be serialised by the caller.
+ * The device status word is the array's first word (not readable through
+ * cfa_read_status, which takes a caller workspace). */
+int cfa_forward_noalloc(const cfa_args* a, void* o, float* lse, void* stream);
+
+/* Size in bytes of the fixed scratch array used by cfa_forward_noalloc. */
+size_t cfa_noalloc_scratch_bytes(void);
 
 /* Waits for `stream`, then returns the status word that the kernels of the
  * last cfa_forward / cfa_backward on this workspace left (CFA_OK or

@@ -1,0 +1,75 @@
+"""cfa_forward_noalloc, the forward for callers that cannot allocate.
+
+Some callers have no way to allocate device memory -- a trainer running next
+to an inference server that reserved the GPU's memory up front, or a C
+program whose device memory comes only from someone else's pool -- so they
+cannot provide cfa_forward's workspace.  cfa_forward_noalloc keeps the split
+partials in a fixed scratch array inside the library instead.  These tests
+call it through the C ABI and compare it with cfa_forward on the same inputs,
+twice in a row with different inputs (the shared scratch keeps the previous
+call's contents), and check that an oversized request is refused.
+
+The file is named so that pytest collects it last.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _forward_both(seed):
+    import frozen_prefix_chunk_gb300 as cfa
+
+    # Lp=1536, Lc=512, Hq=16, Hkv=8: the forward is split along the keys, so
+    # the scratch array really holds partials
+    w = synth.workload("qwen3_1p7b", seed=seed)
+    d = gu.to_device(synth.make_inputs(w))
+    args = gu.make_args(d)
+    need = cfa.workspace_size(args, cfa.WS_FORWARD)
+    assert 256 < need <= cfa.lib().cfa_noalloc_scratch_bytes()
+    o_ref, lse_ref, _ = cfa.forward(args, d["q"])
+    o = torch.empty_like(o_ref)
+    lse = torch.empty_like(lse_ref)
+    cfa.forward_noalloc(args, o, lse)
+    torch.cuda.synchronize()
+    return o_ref, lse_ref, o, lse
+
+
+def _compare(o_ref, lse_ref, o, lse):
+    err_o = ((o.double() - o_ref.double()).abs().max() / o_ref.double().abs().max()).item()
+    err_lse = (lse.double() - lse_ref.double()).abs().max().item()
+    assert err_o <= gu.TOL_O, err_o
+    assert err_lse <= gu.TOL_LSE, err_lse
+
+
+def test_noalloc_forward_matches_forward_twice():
+    import frozen_prefix_chunk_gb300 as cfa
+
+    cfa.lib(build_if_missing=True)
+    first = _forward_both(seed=0)
+    _compare(*first)
+    second = _forward_both(seed=1)
+    _compare(*second)
+    # the second call saw different inputs, so its output differs from the first
+    assert not torch.equal(first[2], second[2])
+
+
+def test_noalloc_forward_refuses_requests_beyond_its_scratch():
+    import frozen_prefix_chunk_gb300 as cfa
+
+    cfa.lib(build_if_missing=True)
+    # a long prefix split many ways needs more partials than the fixed array
+    w = synth.custom(hq=32, hkv=8, head_dim=128, lp=[16128], lc=[256], seed=0)
+    d = gu.to_device(synth.make_inputs(w))
+    args = gu.make_args(d)
+    assert cfa.workspace_size(args, cfa.WS_FORWARD) > cfa.lib().cfa_noalloc_scratch_bytes()
+    o = torch.empty_like(d["q"])
+    lse = torch.empty(w.hq, sum(w.lc), dtype=torch.float32, device="cuda")
+    st = cfa.lib().cfa_forward_noalloc(ctypes.byref(args), ctypes.c_void_p(o.data_ptr()),
+                                       ctypes.c_void_p(lse.data_ptr()), None)
+    assert st == -7, st
