@@ -78,11 +78,16 @@ int validate(const cfa_args* a) {
   if (!a->cu_seqlens_prefix || !a->cu_seqlens_chunk) return CFA_ERR_INVALID_ARG;
   if (a->total_lc > 0 && (!a->q || !a->k_chunk || !a->v_chunk)) return CFA_ERR_INVALID_ARG;
   if (a->total_lp > 0 && (!a->k_prefix || !a->v_prefix)) return CFA_ERR_INVALID_ARG;
-  if (!aligned16(a->q) || !aligned16(a->k_chunk) || !aligned16(a->v_chunk) ||
-      !aligned16(a->k_prefix) || !aligned16(a->v_prefix))
+  if (!aligned16(a->q) || !aligned16(a->k_chunk) || !aligned16(a->v_chunk))
     return CFA_ERR_INVALID_ARG;
+  if (a->prefix_dtype == CFA_PREFIX_Q8_0) {
+    // q8_0 blocks are 34 bytes: the fp16 scale needs 2-byte alignment
+    if ((reinterpret_cast<uintptr_t>(a->k_prefix) | reinterpret_cast<uintptr_t>(a->v_prefix)) & 1u)
+      return CFA_ERR_INVALID_ARG;
+  } else if (!aligned16(a->k_prefix) || !aligned16(a->v_prefix)) {
+    return CFA_ERR_INVALID_ARG;
+  }
   if ((long long)a->total_lc * a->hq * a->head_dim >= (1ll << 40)) return CFA_ERR_UNSUPPORTED;
-  if (a->prefix_dtype == CFA_PREFIX_Q8_0) return CFA_ERR_UNSUPPORTED;
   return CFA_OK;
 }
 
@@ -91,6 +96,8 @@ struct Plan {
   int n_kc_max;        // 128-key chunk tiles per window, upper bound
   size_t off_opart, off_lsepart, ws_fwd;
   size_t off_dqpart, ws_bwd;
+  size_t off_kp16;       // forward workspace: bf16 copies of a q8_0 prefix, K then V
+  size_t off_kp16_bwd;   // the same copies in the backward workspace
 };
 
 int sm_count(int* n) {
@@ -136,14 +143,21 @@ int make_plan(const cfa_args* a, Plan* p) {
     p->off_lsepart = off;
     off = align256(off + (size_t)p->fwd.n_split_max * rows * 4);
   }
-  p->ws_fwd = off;
+  // a q8_0 prefix is expanded to bf16 rows in the workspace before the
+  // attention kernels read it
+  const size_t kv16 = (a->prefix_dtype == CFA_PREFIX_Q8_0)
+                          ? align256((size_t)a->total_lp * a->hkv * a->head_dim * 2)
+                          : 0;
+  p->off_kp16 = kv16 ? off : 0;
+  p->ws_fwd = off + 2 * kv16;
   off = kWsHeader;
   p->off_dqpart = 0;
   if (p->dq.n_split_max > 1) {
     p->off_dqpart = off;
     off = align256(off + (size_t)p->dq.n_split_max * rows * a->head_dim * 4);
   }
-  p->ws_bwd = off;
+  p->off_kp16_bwd = kv16 ? off : 0;
+  p->ws_bwd = off + 2 * kv16;
   return CFA_OK;
 }
 
@@ -161,13 +175,42 @@ int check_ws(void* ws, size_t ws_bytes, size_t need) {
   return CFA_OK;
 }
 
-int encode_kv_maps(const cfa_args* a, Maps* m) {
+// Chunk maps always; prefix maps over `kp16`/`vp16` (bf16 rows), or none
+// when those are null (the dK/dV half never reads the prefix).
+int encode_kv_maps(const cfa_args* a, const void* kp16, const void* vp16, Maps* m) {
   const int d = a->head_dim;
+  const long long lp_rows = (kp16 && vp16) ? a->total_lp : 0;
   int st = make_map_bf16(&m->kc, a->k_chunk, d, a->hkv, a->total_lc, 1, kTileN);
   if (!st) st = make_map_bf16(&m->vc, a->v_chunk, d, a->hkv, a->total_lc, 1, kTileN);
-  if (!st) st = make_map_bf16(&m->kp, a->k_prefix, d, a->hkv, a->total_lp, 1, kTileN);
-  if (!st) st = make_map_bf16(&m->vp, a->v_prefix, d, a->hkv, a->total_lp, 1, kTileN);
+  if (!st) st = make_map_bf16(&m->kp, kp16, d, a->hkv, lp_rows, 1, kTileN);
+  if (!st) st = make_map_bf16(&m->vp, vp16, d, a->hkv, lp_rows, 1, kTileN);
   return st;
+}
+
+// The bf16 prefix rows the attention kernels read: the caller's tensors, or
+// for q8_0 the workspace copies, filled here (on the stream) by the dequant
+// kernel.
+int prefix_rows_bf16(const cfa_args* a, uint8_t* ws, size_t off_k, cudaStream_t s,
+                     const void** kp16, const void** vp16) {
+  if (a->total_lp == 0) {
+    *kp16 = *vp16 = nullptr;
+    return CFA_OK;
+  }
+  if (a->prefix_dtype == CFA_PREFIX_BF16) {
+    *kp16 = a->k_prefix;
+    *vp16 = a->v_prefix;
+    return CFA_OK;
+  }
+  const size_t kv16 = align256((size_t)a->total_lp * a->hkv * a->head_dim * 2);
+  __nv_bfloat16* k16 = reinterpret_cast<__nv_bfloat16*>(ws + off_k);
+  __nv_bfloat16* v16 = reinterpret_cast<__nv_bfloat16*>(ws + off_k + kv16);
+  const long long nb = (long long)a->total_lp * a->hkv * (a->head_dim / 32);
+  if (launch_dequant_prefix(static_cast<const uint8_t*>(a->k_prefix), nb, k16, s) != cudaSuccess ||
+      launch_dequant_prefix(static_cast<const uint8_t*>(a->v_prefix), nb, v16, s) != cudaSuccess)
+    return CFA_ERR_LAUNCH;
+  *kp16 = k16;
+  *vp16 = v16;
+  return CFA_OK;
 }
 
 }  // namespace
@@ -214,7 +257,10 @@ int cfa_forward(const cfa_args* a, void* o, float* lse, void* ws, size_t ws_byte
   std::memset(&m, 0, sizeof(m));
   const Tiling& tl = p.fwd;
   if ((st = make_map_bf16(&m.q, a->q, a->head_dim, a->hq, a->total_lc, tl.g, tl.tpt))) return st;
-  if ((st = encode_kv_maps(a, &m))) return st;
+  const void *kp16 = nullptr, *vp16 = nullptr;
+  if ((st = prefix_rows_bf16(a, static_cast<uint8_t*>(ws), p.off_kp16, s, &kp16, &vp16)))
+    return st;
+  if ((st = encode_kv_maps(a, kp16, vp16, &m))) return st;
 
   FwdArgs fa;
   fa.cu_p = a->cu_seqlens_prefix;
@@ -279,7 +325,11 @@ int prepare_backward(const cfa_args* a, const void* dout, const float* lse, cons
   if ((st = make_map_bf16(&m->q, a->q, a->head_dim, a->hq, a->total_lc, tl.g, tl.tpt))) return st;
   if ((st = make_map_bf16(&m->dout, dout, a->head_dim, a->hq, a->total_lc, tl.g, tl.tpt)))
     return st;
-  if ((st = encode_kv_maps(a, m))) return st;
+  const void *kp16 = nullptr, *vp16 = nullptr;
+  if (need_partials &&
+      (st = prefix_rows_bf16(a, static_cast<uint8_t*>(ws), p->off_kp16_bwd, s, &kp16, &vp16)))
+    return st;
+  if ((st = encode_kv_maps(a, kp16, vp16, m))) return st;
   ba->cu_p = a->cu_seqlens_prefix;
   ba->cu_c = a->cu_seqlens_chunk;
   ba->hq = a->hq;

@@ -618,7 +618,38 @@ __global__ void dequant_q8_0_kernel(const uint8_t* __restrict__ blocks, long lon
   if (out_bf16) out_bf16[idx] = __float2bfloat16_rn(v);
 }
 
+// q8_0 prefix -> bf16 rows for the attention kernels' TMA maps.  One thread
+// per 34-byte block; the value is fp32(d) * q (exact) rounded to nearest-even
+// bf16, the same operand the export kernel above produces.
+__global__ void __launch_bounds__(256) dequant_prefix_kernel(const uint8_t* __restrict__ blocks,
+                                                             long long n_blocks,
+                                                             __nv_bfloat16* __restrict__ out) {
+  const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= n_blocks) return;
+  const uint16_t* p = reinterpret_cast<const uint16_t*>(blocks + b * 34);
+  const float d = __half2float(__ushort_as_half(p[0]));
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint16_t two = p[1 + i];
+    const float lo = d * (float)(int8_t)(two & 0xff);
+    const float hi = d * (float)(int8_t)(two >> 8);
+    w[i] = pack_bf16x2(lo, hi);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out + b * 32);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+}
+
 }  // namespace
+
+cudaError_t launch_dequant_prefix(const uint8_t* blocks, long long n_blocks, __nv_bfloat16* out,
+                                  cudaStream_t st) {
+  if (n_blocks <= 0) return cudaSuccess;
+  const unsigned grid = (unsigned)((n_blocks + 255) / 256);
+  dequant_prefix_kernel<<<grid, 256, 0, st>>>(blocks, n_blocks, out);
+  return cudaGetLastError();
+}
 
 int bwd_dq_smem_bytes(int d, int q8) {
   (void)q8;

@@ -85,3 +85,38 @@ def test_dequant_q8_0_bit_exact():
     rf64, rf32, rbf = oracle.dequant_q8_0(blocks.numpy())
     assert np.array_equal(f32.cpu().numpy().view(np.uint32), rf32.view(np.uint32))
     assert np.array_equal(bf.cpu().view(torch.int16).numpy().view(np.uint16), rbf)
+
+
+Q8 = [
+    dict(hq=4, hkv=2, head_dim=128, lp=[300, 0, 1000], lc=[77, 5, 256]),
+    dict(hq=6, hkv=3, head_dim=64, lp=[513], lc=[130]),
+]
+
+
+@pytest.mark.parametrize("cfg", Q8, ids=[str(i) for i in range(len(Q8))])
+def test_q8_0_prefix_edge_shapes(cfg):
+    w = synth.custom(**cfg, prefix_dtype=synth.PREFIX_Q8_0, seed=5, dout_std=1.0)
+    _check(synth.make_inputs(w))
+
+
+def test_window_63k_q8_sampled_group():
+    inp = synth.make_inputs(synth.workload("window_63k_q8"))
+    _check(inp, groups=[(0, 3)])
+
+
+def test_q8_0_prefix_equals_bf16_of_its_dequant_bitwise():
+    # the q8_0 path multiplies with bf16(fp32(d) * q); feeding those bf16 values
+    # as a bf16 prefix must give bitwise the same outputs
+    w = synth.custom(hq=8, hkv=2, head_dim=128, lp=[700, 129], lc=[100, 256],
+                     prefix_dtype=synth.PREFIX_Q8_0, seed=8)
+    inp = synth.make_inputs(w)
+    a = gu.run_cuda(inp)
+    inp16 = dict(inp)
+    for k in ("k_prefix", "v_prefix"):
+        _, _, bf = oracle.dequant_q8_0(inp[k].numpy())
+        inp16[k] = torch.from_numpy(bf.view(np.int16)).view(torch.bfloat16)
+    inp16["workload"] = synth.custom(hq=8, hkv=2, head_dim=128, lp=[700, 129], lc=[100, 256],
+                                     seed=8)
+    b = gu.run_cuda(inp16)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
