@@ -18,7 +18,6 @@ using namespace cfa;
 namespace {
 
 constexpr int kMinTilesPerSplit = 4;   // key tiles per split, at least
-constexpr int kWavesTarget = 4;        // CTAs per SM the split count aims for
 constexpr size_t kWsHeader = 256;      // status word + padding
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 
@@ -108,6 +107,13 @@ int sm_count(int* n) {
   return CFA_OK;
 }
 
+// Splits per query block: pick the count that minimises the estimated time
+// waves * (tiles per split + per-CTA overhead), where a wave is one CTA per
+// SM (the attention kernels use all of an SM's TMEM and most of its shared
+// memory).  Few long splits keep the partials small; enough splits fill the
+// SMs.
+constexpr int kCtaOverheadTiles = 3;  // prologue + epilogue, in key-tile units
+
 Tiling make_tiling(const cfa_args* a, int q_per_cta, int sms) {
   Tiling t;
   t.g = a->hq / a->hkv;
@@ -116,14 +122,25 @@ Tiling make_tiling(const cfa_args* a, int q_per_cta, int sms) {
   t.q_per_cta = q_per_cta;
   const int tok_blk = q_per_cta * t.tpt;
   t.n_qblk_max = ceil_div(a->max_lc > 0 ? a->max_lc : 1, tok_blk);
-  const int n_kt_max = ceil_div(a->max_lp, kTileN) + ceil_div(a->max_lc > 0 ? a->max_lc : 1, kTileN);
+  const int n_kt_max =
+      ceil_div(a->max_lp, kTileN) + ceil_div(a->max_lc > 0 ? a->max_lc : 1, kTileN);
   const long long base = (long long)a->batch * a->hkv * t.n_qblk_max;
-  const long long target = (long long)kWavesTarget * sms;
-  const int want = (int)(base >= target ? 1 : (target + base - 1) / base);
-  int tps = ceil_div(n_kt_max, want);
-  if (tps < kMinTilesPerSplit) tps = kMinTilesPerSplit;
-  t.tiles_per_split = tps;
-  t.n_split_max = ceil_div(n_kt_max, tps);
+  long long best_cost = -1;
+  int best_tps = n_kt_max;
+  const int max_splits = n_kt_max < 64 ? n_kt_max : 64;
+  for (int s = 1; s <= max_splits; ++s) {
+    const int tps = ceil_div(n_kt_max, s);
+    if (tps < kMinTilesPerSplit && s > 1) break;
+    const int splits = ceil_div(n_kt_max, tps);
+    const long long waves = (base * splits + sms - 1) / sms;
+    const long long cost = waves * (tps + kCtaOverheadTiles);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_tps = tps;
+    }
+  }
+  t.tiles_per_split = best_tps;
+  t.n_split_max = ceil_div(n_kt_max, best_tps);
   return t;
 }
 

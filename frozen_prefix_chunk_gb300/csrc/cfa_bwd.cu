@@ -66,13 +66,18 @@ template <int D>
 struct DqCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  // K(i) is read by S(i) and, late, by dQ(i); V(i) only by dP(i).  Separate
+  // rings let V refill early and give K one extra stage of lead.
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kDOOff = kTileBytes;
   static constexpr int kKOff = 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(8 * (1 + 2 * kKStages + 2 * kVStages + 7) <= 240, "barrier area");
 };
 
 template <int D>
@@ -84,7 +89,8 @@ __global__ void __launch_bounds__(320, 1)
                   const __grid_constant__ CUtensorMap map_kc,
                   const __grid_constant__ CUtensorMap map_vc, const BwdArgs a) {
   using C = DqCfg<D>;
-  constexpr int S = C::kStages;
+  constexpr int SK = C::kKStages;
+  constexpr int SV = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_addr(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -107,24 +113,28 @@ __global__ void __launch_bounds__(320, 1)
 
   const uint32_t bars = base + C::kBarOff;
   const uint32_t bar_qdo = bars;
-  const uint32_t bar_kfull = bars + 8;
-  const uint32_t bar_vfull = bars + 8 * (1 + S);
-  const uint32_t bar_kvempty = bars + 8 * (1 + 2 * S);
-  const uint32_t bar_sfull = bars + 8 * (1 + 3 * S);  // [2]
+  const uint32_t bar_kfull = bars + 8;                // [SK]
+  const uint32_t bar_kempty = bar_kfull + 8 * SK;     // [SK]
+  const uint32_t bar_vfull = bar_kempty + 8 * SK;     // [SV]
+  const uint32_t bar_vempty = bar_vfull + 8 * SV;     // [SV]
+  const uint32_t bar_sfull = bar_vempty + 8 * SV;     // [2]
   const uint32_t bar_dpfull = bar_sfull + 16;
   const uint32_t bar_dpfree = bar_dpfull + 8;
   const uint32_t bar_dsfull = bar_dpfree + 8;
   const uint32_t bar_dqfull = bar_dsfull + 8;
   const uint32_t bar_drain = bar_dqfull + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 240);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 244);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_qdo, 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SK; ++s) {
       mbar_init(bar_kfull + 8 * s, 1);
+      mbar_init(bar_kempty + 8 * s, 1);
+    }
+    for (int s = 0; s < SV; ++s) {
       mbar_init(bar_vfull + 8 * s, 1);
-      mbar_init(bar_kvempty + 8 * s, 1);
+      mbar_init(bar_vempty + 8 * s, 1);
     }
     mbar_init(bar_sfull, 1);
     mbar_init(bar_sfull + 8, 1);
@@ -155,10 +165,8 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(base + C::kDOOff + kb * kBoxBytes, &map_do, bar_qdo, kb * 64, hk * tl.g,
                     c0 + t0);
       }
-      int issued = 0;
+      int issued_k = 0, issued_v = 0;
       for (int i = 0; i < n; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(W, bar_kvempty + 8 * s, ((uint32_t)(i / S) & 1u) ^ 1u)) break;
         const int kt = kt0 + i;
         const CUtensorMap* mk = &map_kc;
         const CUtensorMap* mv = &map_vc;
@@ -168,56 +176,63 @@ __global__ void __launch_bounds__(320, 1)
           mv = &map_vp;
           row0 = p0 + kt * kTileN;
         }
-        mbar_arrive_expect_tx(bar_kfull + 8 * s, C::kTileBytes);
+        const int sk = i % SK, sv = i % SV;
+        if (!mbar_wait(W, bar_kempty + 8 * sk, ((uint32_t)(i / SK) & 1u) ^ 1u)) break;
+        mbar_arrive_expect_tx(bar_kfull + 8 * sk, C::kTileBytes);
         for (int kb = 0; kb < C::kBoxes; ++kb)
-          tma_load_3d(base + C::kKOff + s * C::kTileBytes + kb * kBoxBytes, mk, bar_kfull + 8 * s,
-                      kb * 64, hk, row0);
-        mbar_arrive_expect_tx(bar_vfull + 8 * s, C::kTileBytes);
+          tma_load_3d(base + C::kKOff + sk * C::kTileBytes + kb * kBoxBytes, mk,
+                      bar_kfull + 8 * sk, kb * 64, hk, row0);
+        issued_k = i + 1;
+        if (!mbar_wait(W, bar_vempty + 8 * sv, ((uint32_t)(i / SV) & 1u) ^ 1u)) break;
+        mbar_arrive_expect_tx(bar_vfull + 8 * sv, C::kTileBytes);
         for (int kb = 0; kb < C::kBoxes; ++kb)
-          tma_load_3d(base + C::kVOff + s * C::kTileBytes + kb * kBoxBytes, mv, bar_vfull + 8 * s,
-                      kb * 64, hk, row0);
-        issued = i + 1;
+          tma_load_3d(base + C::kVOff + sv * C::kTileBytes + kb * kBoxBytes, mv,
+                      bar_vfull + 8 * sv, kb * 64, hk, row0);
+        issued_v = i + 1;
       }
       mbar_wait_bounded(bar_qdo, 0, kDrainLimitNs);
-      for (int i = (issued > S ? issued - S : 0); i < issued; ++i) {
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        mbar_wait_bounded(bar_kfull + 8 * (i % S), ph, kDrainLimitNs);
-        mbar_wait_bounded(bar_vfull + 8 * (i % S), ph, kDrainLimitNs);
-      }
+      for (int i = (issued_k > SK ? issued_k - SK : 0); i < issued_k; ++i)
+        mbar_wait_bounded(bar_kfull + 8 * (i % SK), (uint32_t)(i / SK) & 1u, kDrainLimitNs);
+      for (int i = (issued_v > SV ? issued_v - SV : 0); i < issued_v; ++i)
+        mbar_wait_bounded(bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u, kDrainLimitNs);
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      bool ok = mbar_wait(W, bar_qdo, 0);
-      tc_fence_after_sync();
+      bool ok = mbar_wait(W, bar_qdo, 0) && mbar_wait(W, bar_kfull, 0) && mbar_wait(W, bar_vfull, 0);
       const uint32_t t_dq = tmem + 384;
+      // Issue order per key tile i:  S(i), dP(i), dQ(i-1).  dP(i) needs only
+      // that dP(i-1) has been read, so it runs while dS(i-1) is computed.  The
+      // waits for K(i+1) / V(i+1) sit at the end of the iteration, off the
+      // critical path.
       for (int i = 0; ok && i < n; ++i) {
-        const int s = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        if (!(ok = mbar_wait(W, bar_kfull + 8 * s, ph))) break;
-        tc_fence_after_sync();
+        const int sk = i % SK, sv = i % SV;
         issue_nt<D>(tmem + (uint32_t)(i & 1) * 128u, base + C::kQOff,
-                    base + C::kKOff + s * C::kTileBytes);
+                    base + C::kKOff + sk * C::kTileBytes);
         tc_commit(bar_sfull + 8 * (i & 1));
+        if (i > 0 && !(ok = mbar_wait(W, bar_dpfree, (uint32_t)(i - 1) & 1u))) break;
+        tc_fence_after_sync();
+        issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + sv * C::kTileBytes);
+        tc_commit(bar_dpfull);
+        tc_commit(bar_vempty + 8 * sv);
         if (i > 0) {
-          const int sp = (i - 1) % S;
+          const int skp = (i - 1) % SK;
           if (!(ok = mbar_wait(W, bar_dsfull, (uint32_t)(i - 1) & 1u))) break;
           tc_fence_after_sync();
           issue_tn<D>(t_dq, tmem + (uint32_t)((i - 1) & 1) * 128u,
-                      base + C::kKOff + sp * C::kTileBytes, i - 1 > 0);
-          tc_commit(bar_kvempty + 8 * sp);
-          if (!(ok = mbar_wait(W, bar_dpfree, (uint32_t)(i - 1) & 1u))) break;
-          tc_fence_after_sync();
+                      base + C::kKOff + skp * C::kTileBytes, i - 1 > 0);
+          tc_commit(bar_kempty + 8 * skp);
         }
-        if (!(ok = mbar_wait(W, bar_vfull + 8 * s, ph))) break;
-        tc_fence_after_sync();
-        issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + s * C::kTileBytes);
-        tc_commit(bar_dpfull);
+        if (i + 1 < n) {
+          const int j = i + 1;
+          if (!(ok = mbar_wait(W, bar_kfull + 8 * (j % SK), (uint32_t)(j / SK) & 1u))) break;
+          if (!(ok = mbar_wait(W, bar_vfull + 8 * (j % SV), (uint32_t)(j / SV) & 1u))) break;
+        }
       }
       if (ok) {
-        const int i = n - 1, s = i % S;
+        const int i = n - 1, sk = i % SK;
         if (mbar_wait(W, bar_dsfull, (uint32_t)i & 1u)) {
           tc_fence_after_sync();
-          issue_tn<D>(t_dq, tmem + (uint32_t)(i & 1) * 128u, base + C::kKOff + s * C::kTileBytes,
+          issue_tn<D>(t_dq, tmem + (uint32_t)(i & 1) * 128u, base + C::kKOff + sk * C::kTileBytes,
                       i > 0);
           tc_commit(bar_dqfull);
         }
@@ -250,8 +265,11 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t r[64];
         tmem_ld_x64(t_lane + sb, r);
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
-          p[j] = (j < lim) ? ex2_approx(fmaf(__uint_as_float(r[j]), sl2, -lse2)) : 0.f;
+        for (int j = 0; j < 64; ++j) p[j] = ex2_approx(fmaf(__uint_as_float(r[j]), sl2, -lse2));
+        if (lim < 64) {  // edge tiles only: the prefix tail, the causal diagonal, padding rows
+#pragma unroll
+          for (int j = 0; j < 64; ++j) p[j] = (j < lim) ? p[j] : 0.f;
+        }
       }
       if (!(ok = warp_wait(W, bar_dpfull, (uint32_t)i & 1u))) break;
       tc_fence_after_sync();

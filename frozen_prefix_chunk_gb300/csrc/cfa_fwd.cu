@@ -37,13 +37,18 @@ template <int D>
 struct FwdCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  // K and V have rings of their own: K(i) is free once the last S MMA of
+  // tile i is done, V(i) only after the last PV, so K can be refilled early.
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
   static constexpr int kThreads = 320;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(8 * (1 + 2 * kKStages + 2 * kVStages + 7) <= 240, "barrier area");
 };
 
 // S_t = Q_t K^T: A = Q tile, B = K tile, both K-major 128B-swizzled; one MMA
@@ -82,7 +87,8 @@ __global__ void __launch_bounds__(320, 1)
                const __grid_constant__ CUtensorMap map_kc,
                const __grid_constant__ CUtensorMap map_vc, const FwdArgs a) {
   using C = FwdCfg<D>;
-  constexpr int S = C::kStages;
+  constexpr int SK = C::kKStages;
+  constexpr int SV = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_addr(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -107,22 +113,26 @@ __global__ void __launch_bounds__(320, 1)
 
   const uint32_t bars = base + C::kBarOff;
   const uint32_t bar_q = bars;
-  const uint32_t bar_kfull = bars + 8;               // [S]
-  const uint32_t bar_vfull = bars + 8 * (1 + S);     // [S]
-  const uint32_t bar_kvempty = bars + 8 * (1 + 2 * S);
-  const uint32_t bar_sfull = bars + 8 * (1 + 3 * S);  // [2]
-  const uint32_t bar_pfull = bar_sfull + 16;           // [2]
-  const uint32_t bar_ofull = bar_pfull + 16;           // [2]
+  const uint32_t bar_kfull = bars + 8;                  // [SK]
+  const uint32_t bar_kempty = bar_kfull + 8 * SK;       // [SK]
+  const uint32_t bar_vfull = bar_kempty + 8 * SK;       // [SV]
+  const uint32_t bar_vempty = bar_vfull + 8 * SV;       // [SV]
+  const uint32_t bar_sfull = bar_vempty + 8 * SV;       // [2]
+  const uint32_t bar_pfull = bar_sfull + 16;            // [2]
+  const uint32_t bar_ofull = bar_pfull + 16;            // [2]
   const uint32_t bar_drain = bar_ofull + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 240);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 244);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SK; ++s) {
       mbar_init(bar_kfull + 8 * s, 1);
+      mbar_init(bar_kempty + 8 * s, 1);
+    }
+    for (int s = 0; s < SV; ++s) {
       mbar_init(bar_vfull + 8 * s, 1);
-      mbar_init(bar_kvempty + 8 * s, 1);
+      mbar_init(bar_vempty + 8 * s, 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_sfull + 8 * t, 1);
@@ -160,11 +170,8 @@ __global__ void __launch_bounds__(320, 1)
         for (int kb = 0; kb < C::kBoxes; ++kb)
           tma_load_3d(base + C::kQOff + (qt * C::kBoxes + kb) * kBoxBytes, &map_q, bar_q, kb * 64,
                       hk * tl.g, c0 + t0 + qt * tl.tpt);
-      int issued = 0;
+      int issued_k = 0, issued_v = 0;
       for (int i = 0; i < n; ++i) {
-        const int s = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        if (!mbar_wait(W, bar_kvempty + 8 * s, ph ^ 1u)) break;
         const int kt = kt0 + i;
         const CUtensorMap* mk = &map_kc;
         const CUtensorMap* mv = &map_vc;
@@ -174,59 +181,64 @@ __global__ void __launch_bounds__(320, 1)
           mv = &map_vp;
           row0 = p0 + kt * kTileN;
         }
-        mbar_arrive_expect_tx(bar_kfull + 8 * s, C::kTileBytes);
+        const int sk = i % SK, sv = i % SV;
+        if (!mbar_wait(W, bar_kempty + 8 * sk, ((uint32_t)(i / SK) & 1u) ^ 1u)) break;
+        mbar_arrive_expect_tx(bar_kfull + 8 * sk, C::kTileBytes);
         for (int kb = 0; kb < C::kBoxes; ++kb)
-          tma_load_3d(base + C::kKOff + s * C::kTileBytes + kb * kBoxBytes, mk, bar_kfull + 8 * s,
-                      kb * 64, hk, row0);
-        mbar_arrive_expect_tx(bar_vfull + 8 * s, C::kTileBytes);
+          tma_load_3d(base + C::kKOff + sk * C::kTileBytes + kb * kBoxBytes, mk,
+                      bar_kfull + 8 * sk, kb * 64, hk, row0);
+        issued_k = i + 1;
+        if (!mbar_wait(W, bar_vempty + 8 * sv, ((uint32_t)(i / SV) & 1u) ^ 1u)) break;
+        mbar_arrive_expect_tx(bar_vfull + 8 * sv, C::kTileBytes);
         for (int kb = 0; kb < C::kBoxes; ++kb)
-          tma_load_3d(base + C::kVOff + s * C::kTileBytes + kb * kBoxBytes, mv, bar_vfull + 8 * s,
-                      kb * 64, hk, row0);
-        issued = i + 1;
+          tma_load_3d(base + C::kVOff + sv * C::kTileBytes + kb * kBoxBytes, mv,
+                      bar_vfull + 8 * sv, kb * 64, hk, row0);
+        issued_v = i + 1;
       }
       // Unwind: every copy this thread issued has landed before the CTA exits.
       mbar_wait_bounded(bar_q, 0, kDrainLimitNs);
-      for (int i = (issued > S ? issued - S : 0); i < issued; ++i) {
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        mbar_wait_bounded(bar_kfull + 8 * (i % S), ph, kDrainLimitNs);
-        mbar_wait_bounded(bar_vfull + 8 * (i % S), ph, kDrainLimitNs);
-      }
+      for (int i = (issued_k > SK ? issued_k - SK : 0); i < issued_k; ++i)
+        mbar_wait_bounded(bar_kfull + 8 * (i % SK), (uint32_t)(i / SK) & 1u, kDrainLimitNs);
+      for (int i = (issued_v > SV ? issued_v - SV : 0); i < issued_v; ++i)
+        mbar_wait_bounded(bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u, kDrainLimitNs);
     }
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issue
     if (lane == 0) {
-      bool ok = mbar_wait(W, bar_q, 0);
-      tc_fence_after_sync();
+      bool ok = mbar_wait(W, bar_q, 0) && mbar_wait(W, bar_kfull, 0);
+      // Issue order per key tile i:  PV0(i-1) S0(i) PV1(i-1) S1(i).  PV of the
+      // previous tile goes first (it does not need K(i)); S_t(i) reuses the
+      // TMEM columns of P_t(i-1), which the in-order MMA pipe has consumed.
+      // The K(i+1) / V(i) waits sit at the end of the iteration, where the
+      // tensor pipe is still busy with the work just issued; only the P
+      // hand-offs remain on the critical path.
       for (int i = 0; ok && i < n; ++i) {
-        const int s = i % S;
-        if (!(ok = mbar_wait(W, bar_kfull + 8 * s, (uint32_t)(i / S) & 1u))) break;
-        tc_fence_after_sync();
-        const int sp = (i + S - 1) % S;
-        if (i > 0) {
-          if (!(ok = mbar_wait(W, bar_vfull + 8 * sp, (uint32_t)((i - 1) / S) & 1u))) break;
-          tc_fence_after_sync();
-        }
+        const int sk = i % SK, svp = (i + SV - 1) % SV;
         for (int qt = 0; qt < nq; ++qt) {
           if (i > 0) {
             if (!(ok = mbar_wait(W, bar_pfull + 8 * qt, (uint32_t)(i - 1) & 1u))) break;
             tc_fence_after_sync();
-            issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128, base + C::kVOff + sp * C::kTileBytes,
+            issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128, base + C::kVOff + svp * C::kTileBytes,
                         i - 1 > 0);
-            if (qt == nq - 1) tc_commit(bar_kvempty + 8 * sp);
+            if (qt == nq - 1) tc_commit(bar_vempty + 8 * svp);
           }
           issue_qk<D>(tmem + qt * 128, base + C::kQOff + qt * C::kTileBytes,
-                      base + C::kKOff + s * C::kTileBytes);
+                      base + C::kKOff + sk * C::kTileBytes);
           tc_commit(bar_sfull + 8 * qt);
+          if (qt == nq - 1) tc_commit(bar_kempty + 8 * sk);
         }
+        if (!ok) break;
+        if (i + 1 < n &&
+            !(ok = mbar_wait(W, bar_kfull + 8 * ((i + 1) % SK), (uint32_t)((i + 1) / SK) & 1u)))
+          break;
+        ok = mbar_wait(W, bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u);
       }
       if (ok) {
-        const int i = n - 1, s = i % S;
-        ok = mbar_wait(W, bar_vfull + 8 * s, (uint32_t)(i / S) & 1u);
-        tc_fence_after_sync();
+        const int i = n - 1, sv = i % SV;
         for (int qt = 0; ok && qt < nq; ++qt) {
           if (!(ok = mbar_wait(W, bar_pfull + 8 * qt, (uint32_t)i & 1u))) break;
           tc_fence_after_sync();
-          issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128, base + C::kVOff + s * C::kTileBytes,
+          issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128, base + C::kVOff + sv * C::kTileBytes,
                       i > 0);
           tc_commit(bar_ofull + 8 * qt);
         }
@@ -256,13 +268,10 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after_sync();
         float s[128];
         {
-          uint32_t r[64];
-          tmem_ld_x64(t_lane + s_col, r);
+          uint32_t r[128];
+          tmem_ld_x128(t_lane + s_col, r);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(r[c]);
-          tmem_ld_x64(t_lane + s_col + 64, r);
-#pragma unroll
-          for (int c = 0; c < 64; ++c) s[64 + c] = __uint_as_float(r[c]);
+          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
         }
         const int kt = kt0 + i;
         // keys [0, lim) of this tile are visible to this row
@@ -271,9 +280,13 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
         }
-        float mx = -INFINITY;
+        // row max: four independent chains of 3-input maxes
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < 128; c += 8)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mx4[j] = fmax3(mx4[j], s[c + 2 * j], s[c + 2 * j + 1]);
+        float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
         mx *= sl2;
         const float m_new = fmaxf(m, mx);
         const bool resc = m_new > m + 8.f;
@@ -295,15 +308,16 @@ __global__ void __launch_bounds__(320, 1)
           m = m_new;
         }
         const float mref = (m == -INFINITY) ? 0.f : m;
-        float rs = 0.f;
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const float e0 = ex2_approx(fmaf(s[2 * c], sl2, -mref));
           const float e1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -mref));
-          rs += e0 + e1;
+          rs4[c & 3] += e0 + e1;
           pk[c] = pack_bf16x2(e0, e1);
         }
+        const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         l += rs;
         tmem_st_x64(t_lane + s_col, pk);
         tmem_st_wait();

@@ -63,11 +63,19 @@ def test_noalloc_forward_refuses_requests_beyond_its_scratch():
     import frozen_prefix_chunk_gb300 as cfa
 
     cfa.lib(build_if_missing=True)
-    # a long prefix split many ways needs more partials than the fixed array
-    w = synth.custom(hq=32, hkv=8, head_dim=128, lp=[16128], lc=[256], seed=0)
-    d = gu.to_device(synth.make_inputs(w))
-    args = gu.make_args(d)
-    assert cfa.workspace_size(args, cfa.WS_FORWARD) > cfa.lib().cfa_noalloc_scratch_bytes()
+    # a long prefix split several ways over many query blocks needs more
+    # partials than the fixed array; take the first shape whose forward
+    # workspace is larger than the scratch on this GPU
+    limit = cfa.lib().cfa_noalloc_scratch_bytes()
+    for lc, lp in ((768, 60000), (768, 120000), (1536, 120000), (3072, 120000)):
+        w = synth.custom(hq=32, hkv=8, head_dim=128, lp=[lp], lc=[lc], seed=0)
+        d = gu.to_device(synth.make_inputs(w))
+        args = gu.make_args(d)
+        if cfa.workspace_size(args, cfa.WS_FORWARD) > limit:
+            break
+        del d
+    else:
+        pytest.fail("no test shape needs more than the fixed scratch")
     o = torch.empty_like(d["q"])
     lse = torch.empty(w.hq, sum(w.lc), dtype=torch.float32, device="cuda")
     st = cfa.lib().cfa_forward_noalloc(ctypes.byref(args), ctypes.c_void_p(o.data_ptr()),
