@@ -17,7 +17,6 @@ using namespace cfa;
 
 namespace {
 
-constexpr int kMinTilesPerSplit = 4;   // key tiles per split, at least
 constexpr size_t kWsHeader = 256;      // status word + padding
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 
@@ -93,8 +92,8 @@ int validate(const cfa_args* a) {
 struct Plan {
   Tiling fwd, dq;
   int n_kc_max;        // 128-key chunk tiles per window, upper bound
-  size_t off_opart, off_lsepart, ws_fwd;
-  size_t off_dqpart, ws_bwd;
+  size_t off_wp_fwd, off_opart, off_lsepart, ws_fwd;
+  size_t off_wp_bwd, off_dqpart, ws_bwd;
   size_t off_kp16;       // forward workspace: bf16 copies of a q8_0 prefix, K then V
   size_t off_kp16_bwd;   // the same copies in the backward workspace
 };
@@ -107,43 +106,22 @@ int sm_count(int* n) {
   return CFA_OK;
 }
 
-// Splits per query block: pick the count that minimises the estimated time
-// waves * (tiles per split + per-CTA overhead), where a wave is one CTA per
-// SM (the attention kernels use all of an SM's TMEM and most of its shared
-// memory).  Few long splits keep the partials small; enough splits fill the
-// SMs.
-constexpr int kCtaOverheadTiles = 3;  // prologue + epilogue, in key-tile units
-
 Tiling make_tiling(const cfa_args* a, int q_per_cta, int sms) {
   Tiling t;
   t.g = a->hq / a->hkv;
   t.tpt = kTileM / t.g;
   t.rows = t.tpt * t.g;
   t.q_per_cta = q_per_cta;
-  const int tok_blk = q_per_cta * t.tpt;
-  t.n_qblk_max = ceil_div(a->max_lc > 0 ? a->max_lc : 1, tok_blk);
-  const int n_kt_max =
-      ceil_div(a->max_lp, kTileN) + ceil_div(a->max_lc > 0 ? a->max_lc : 1, kTileN);
-  const long long base = (long long)a->batch * a->hkv * t.n_qblk_max;
-  long long best_cost = -1;
-  int best_tps = n_kt_max;
-  const int max_splits = n_kt_max < 64 ? n_kt_max : 64;
-  for (int s = 1; s <= max_splits; ++s) {
-    const int tps = ceil_div(n_kt_max, s);
-    if (tps < kMinTilesPerSplit && s > 1) break;
-    const int splits = ceil_div(n_kt_max, tps);
-    const long long waves = (base * splits + sms - 1) / sms;
-    const long long cost = waves * (tps + kCtaOverheadTiles);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best_tps = tps;
-    }
-  }
-  t.tiles_per_split = best_tps;
-  t.n_split_max = ceil_div(n_kt_max, best_tps);
+  t.grid = sms;  // persistent: one CTA per SM (each uses all of TMEM)
   return t;
 }
 
+// Workspace layout (every region 256-byte aligned):
+//   [0, 256)           status word
+//   win_prefix         int64 [batch + 1]  (stream-K plan)
+//   partials           fp32, two slots per CTA: forward O [G, 2, 256, d] and
+//                      LSE [G, 2, 256]; backward dQ [G, 2, 128, d]
+//   bf16 prefix        K then V [total_lp, hkv, d], only for a q8_0 prefix
 int make_plan(const cfa_args* a, Plan* p) {
   int sms = 0;
   int st = sm_count(&sms);
@@ -151,28 +129,25 @@ int make_plan(const cfa_args* a, Plan* p) {
   p->fwd = make_tiling(a, 2, sms);
   p->dq = make_tiling(a, 1, sms);
   p->n_kc_max = ceil_div(a->max_lc > 0 ? a->max_lc : 1, kTileN);
-  const size_t rows = (size_t)a->total_lc * a->hq;
-  size_t off = kWsHeader;
-  p->off_opart = p->off_lsepart = 0;
-  if (p->fwd.n_split_max > 1) {
-    p->off_opart = off;
-    off = align256(off + (size_t)p->fwd.n_split_max * rows * a->head_dim * 4);
-    p->off_lsepart = off;
-    off = align256(off + (size_t)p->fwd.n_split_max * rows * 4);
-  }
-  // a q8_0 prefix is expanded to bf16 rows in the workspace before the
-  // attention kernels read it
+  const size_t G = (size_t)sms;
+  const size_t wp = align256((size_t)(a->batch + 1) * 8);
   const size_t kv16 = (a->prefix_dtype == CFA_PREFIX_Q8_0)
                           ? align256((size_t)a->total_lp * a->hkv * a->head_dim * 2)
                           : 0;
+  size_t off = kWsHeader;
+  p->off_wp_fwd = off;
+  off += wp;
+  p->off_opart = off;
+  off = align256(off + G * 2 * 256 * a->head_dim * 4);
+  p->off_lsepart = off;
+  off = align256(off + G * 2 * 256 * 4);
   p->off_kp16 = kv16 ? off : 0;
   p->ws_fwd = off + 2 * kv16;
   off = kWsHeader;
-  p->off_dqpart = 0;
-  if (p->dq.n_split_max > 1) {
-    p->off_dqpart = off;
-    off = align256(off + (size_t)p->dq.n_split_max * rows * a->head_dim * 4);
-  }
+  p->off_wp_bwd = off;
+  off += wp;
+  p->off_dqpart = off;
+  off = align256(off + G * 2 * 128 * a->head_dim * 4);
   p->off_kp16_bwd = kv16 ? off : 0;
   p->ws_bwd = off + 2 * kv16;
   return CFA_OK;
@@ -184,6 +159,15 @@ unsigned long long wait_limit_ns() {
   char* end = nullptr;
   unsigned long long v = std::strtoull(e, &end, 10);
   return (end && *end == 0) ? v : kDefaultWaitNs;
+}
+
+// Test hook for the failure-detection tests: with CFA_DEBUG_WAIT_NEVER=1 the
+// attention kernels' MMA thread first waits on a barrier that nothing arrives
+// on, so the bounded wait runs out and the kernel reports
+// CFA_ERR_DEVICE_TIMEOUT instead of computing.
+int debug_wait_never() {
+  const char* e = std::getenv("CFA_DEBUG_WAIT_NEVER");
+  return (e && e[0] == '1') ? 1 : 0;
 }
 
 int check_ws(void* ws, size_t ws_bytes, size_t need) {
@@ -279,9 +263,12 @@ int cfa_forward(const cfa_args* a, void* o, float* lse, void* ws, size_t ws_byte
     return st;
   if ((st = encode_kv_maps(a, kp16, vp16, &m))) return st;
 
+  uint8_t* w = static_cast<uint8_t*>(ws);
   FwdArgs fa;
   fa.cu_p = a->cu_seqlens_prefix;
   fa.cu_c = a->cu_seqlens_chunk;
+  fa.win_prefix = reinterpret_cast<long long*>(w + p.off_wp_fwd);
+  fa.batch = a->batch;
   fa.hq = a->hq;
   fa.hkv = a->hkv;
   fa.total_lc = a->total_lc;
@@ -289,17 +276,14 @@ int cfa_forward(const cfa_args* a, void* o, float* lse, void* ws, size_t ws_byte
   fa.scale_log2 = a->softmax_scale * kLog2e;
   fa.o = static_cast<__nv_bfloat16*>(o);
   fa.lse = lse;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  fa.o_part = p.off_opart ? reinterpret_cast<float*>(w + p.off_opart) : nullptr;
-  fa.lse_part = p.off_lsepart ? reinterpret_cast<float*>(w + p.off_lsepart) : nullptr;
+  fa.o_part = reinterpret_cast<float*>(w + p.off_opart);
+  fa.lse_part = reinterpret_cast<float*>(w + p.off_lsepart);
   fa.status = reinterpret_cast<int*>(w);
   fa.limit_ns = wait_limit_ns();
+  fa.debug_wait_never = debug_wait_never();
 
-  dim3 grid((unsigned)(tl.n_qblk_max * tl.n_split_max), (unsigned)a->hkv, (unsigned)a->batch);
-  if (launch_fwd(m, fa, a->head_dim, 0, grid, s) != cudaSuccess) return CFA_ERR_LAUNCH;
-  if (tl.n_split_max > 1 &&
-      launch_fwd_combine(fa, a->head_dim, a->batch, a->max_lc, s) != cudaSuccess)
-    return CFA_ERR_LAUNCH;
+  if (launch_fwd(m, fa, a->head_dim, 0, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  if (launch_fwd_merge(fa, a->head_dim, a->max_lc, s) != cudaSuccess) return CFA_ERR_LAUNCH;
   return CFA_OK;
 }
 
@@ -349,6 +333,8 @@ int prepare_backward(const cfa_args* a, const void* dout, const float* lse, cons
   if ((st = encode_kv_maps(a, kp16, vp16, m))) return st;
   ba->cu_p = a->cu_seqlens_prefix;
   ba->cu_c = a->cu_seqlens_chunk;
+  ba->win_prefix = reinterpret_cast<long long*>(static_cast<uint8_t*>(ws) + p->off_wp_bwd);
+  ba->batch = a->batch;
   ba->hq = a->hq;
   ba->hkv = a->hkv;
   ba->total_lc = a->total_lc;
@@ -359,20 +345,16 @@ int prepare_backward(const cfa_args* a, const void* dout, const float* lse, cons
   ba->delta = delta;
   ba->dq = ba->dk = ba->dv = nullptr;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  ba->dq_part = (need_partials && p->off_dqpart) ? reinterpret_cast<float*>(w + p->off_dqpart)
-                                                 : nullptr;
+  ba->dq_part = need_partials ? reinterpret_cast<float*>(w + p->off_dqpart) : nullptr;
   ba->status = reinterpret_cast<int*>(w);
   ba->limit_ns = wait_limit_ns();
+  ba->debug_wait_never = debug_wait_never();
   return CFA_OK;
 }
 
 int run_dq(const cfa_args* a, const Plan& p, const Maps& m, const BwdArgs& ba, cudaStream_t s) {
-  const Tiling& tl = p.dq;
-  dim3 grid((unsigned)(tl.n_qblk_max * tl.n_split_max), (unsigned)a->hkv, (unsigned)a->batch);
-  if (launch_bwd_dq(m, ba, a->head_dim, 0, grid, s) != cudaSuccess) return CFA_ERR_LAUNCH;
-  if (tl.n_split_max > 1 &&
-      launch_bwd_dq_reduce(ba, a->head_dim, a->batch, a->max_lc, s) != cudaSuccess)
-    return CFA_ERR_LAUNCH;
+  if (launch_bwd_dq(m, ba, a->head_dim, 0, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  if (launch_bwd_dq_reduce(ba, a->head_dim, a->max_lc, s) != cudaSuccess) return CFA_ERR_LAUNCH;
   return CFA_OK;
 }
 

@@ -7,11 +7,12 @@
 //
 // Two kernels split the work so that neither needs atomics:
 //
-// * bwd_dq_kernel -- query-major.  A CTA owns one 128-row query tile and one
-//   split of its key-tile list (prefix tiles, then visible chunk tiles) and
-//   streams K/V through three MMAs per tile: S = Q K^T, dP = dO V^T,
-//   dQ += dS K.  Prefix tiles never produce dK/dV.  Split partials of dQ go
-//   to the workspace and bwd_dq_reduce_kernel sums them in split order.
+// * bwd_dq_kernel -- query-major, persistent stream-K (cfa_sched.cuh): a
+//   CTA walks an equal share of the (128-row query tile, key tile)
+//   iterations and streams K/V through three MMAs per tile: S = Q K^T,
+//   dP = dO V^T, dQ += dS K.  Prefix tiles never produce dK/dV.  Query tiles
+//   cut by CTA boundaries leave fp32 partials that bwd_dq_reduce_kernel sums
+//   in CTA order.
 //     warps 0-7  elementwise (two warps per TMEM lane quadrant, each owning
 //                64 of the 128 key columns): P, dS, bf16 dS into TMEM
 //     warp  8    TMA producer      warp 9  TMEM owner + MMA issuer
@@ -77,7 +78,7 @@ struct DqCfg {
   static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(8 * (1 + 2 * kKStages + 2 * kVStages + 7) <= 240, "barrier area");
+  static_assert(8 * (2 + 2 * kKStages + 2 * kVStages + 8) <= 240, "barrier area");
 };
 
 template <int D>
@@ -98,22 +99,25 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Tiling tl = a.tl;
-  const int b = blockIdx.z, hk = blockIdx.y;
-  const int qblk = blockIdx.x / tl.n_split_max, split = blockIdx.x % tl.n_split_max;
-  const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
-  const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
-  const int t0 = qblk * tl.tpt;
-  if (t0 >= lc) return;
-  const int np_t = ceil_div(lp, kTileN);
-  const int n_kt = block_key_tiles(lp, lc, t0, tl.tpt);
-  const int n_split = ceil_div(n_kt, tl.tiles_per_split);
-  if (split >= n_split) return;
-  const int kt0 = split * tl.tiles_per_split;
-  const int n = min(tl.tiles_per_split, n_kt - kt0);
+  {
+    // schedule prologue: shared scratch in the (not yet used) barrier area
+    long long* sched = reinterpret_cast<long long*>(gbase + C::kBarOff);
+    plan_schedule(a.cu_p, a.cu_c, a.batch, a.hkv, tl, a.win_prefix, sched + 4, sched,
+                  reinterpret_cast<int*>(sched + 1), sched + 2);
+  }
+  SegmentWalker walk;
+  {
+    const long long* sched = reinterpret_cast<const long long*>(gbase + C::kBarOff);
+    walk.init(a.cu_p, a.cu_c, a.batch, a.hkv, tl, blockIdx.x, sched[0],
+              *reinterpret_cast<const int*>(sched + 1), sched[2]);
+  }
+  __syncthreads();  // the barrier area is initialised below
+  if (walk.cur >= walk.end) return;
 
   const uint32_t bars = base + C::kBarOff;
   const uint32_t bar_qdo = bars;
-  const uint32_t bar_kfull = bars + 8;                // [SK]
+  const uint32_t bar_qempty = bars + 8;
+  const uint32_t bar_kfull = bars + 16;               // [SK]
   const uint32_t bar_kempty = bar_kfull + 8 * SK;     // [SK]
   const uint32_t bar_vfull = bar_kempty + 8 * SK;     // [SV]
   const uint32_t bar_vempty = bar_vfull + 8 * SV;     // [SV]
@@ -122,12 +126,14 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t bar_dpfree = bar_dpfull + 8;
   const uint32_t bar_dsfull = bar_dpfree + 8;
   const uint32_t bar_dqfull = bar_dsfull + 8;
-  const uint32_t bar_drain = bar_dqfull + 8;
+  const uint32_t bar_dqfree = bar_dqfull + 8;
+  const uint32_t bar_drain = bar_dqfree + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 240);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 244);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_qdo, 1);
+    mbar_init(bar_qempty, 1);
     for (int s = 0; s < SK; ++s) {
       mbar_init(bar_kfull + 8 * s, 1);
       mbar_init(bar_kempty + 8 * s, 1);
@@ -142,6 +148,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_dpfree, 8);
     mbar_init(bar_dsfull, 8);
     mbar_init(bar_dqfull, 1);
+    mbar_init(bar_dqfree, 8);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -155,178 +162,237 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const Waiter W{a.limit_ns, abort_flag, a.status};
+  Segment sg;
 
   if (warp == 8) {
-    if (lane == 0) {
-      const uint32_t qbytes = (uint32_t)(C::kBoxes * 128 * tl.rows);
-      mbar_arrive_expect_tx(bar_qdo, 2 * qbytes);
-      for (int kb = 0; kb < C::kBoxes; ++kb) {
-        tma_load_3d(base + C::kQOff + kb * kBoxBytes, &map_q, bar_qdo, kb * 64, hk * tl.g, c0 + t0);
-        tma_load_3d(base + C::kDOOff + kb * kBoxBytes, &map_do, bar_qdo, kb * 64, hk * tl.g,
-                    c0 + t0);
+    // producer: the whole warp walks and waits (converged); lane 0 issues
+    const bool leader = lane == 0;
+    const uint32_t qbytes = (uint32_t)(C::kBoxes * 128 * tl.rows);
+    int it = 0, seg = 0, issued_k = 0, issued_v = 0;
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      // Q and dO are reused: the previous segment's S and dP must be done
+      if (seg > 0 && !(ok = warp_wait(W, bar_qempty, (uint32_t)(seg - 1) & 1u))) break;
+      const int tok = sg.c0 + sg.qb * tl.tpt;
+      if (leader) {
+        mbar_arrive_expect_tx(bar_qdo, 2 * qbytes);
+        for (int kb = 0; kb < C::kBoxes; ++kb) {
+          tma_load_3d(base + C::kQOff + kb * kBoxBytes, &map_q, bar_qdo, kb * 64, sg.hk * tl.g,
+                      tok);
+          tma_load_3d(base + C::kDOOff + kb * kBoxBytes, &map_do, bar_qdo, kb * 64, sg.hk * tl.g,
+                      tok);
+        }
       }
-      int issued_k = 0, issued_v = 0;
-      for (int i = 0; i < n; ++i) {
-        const int kt = kt0 + i;
+      __syncwarp();
+      ++seg;
+      const int np_t = ceil_div(sg.lp, kTileN);
+      for (int kt = sg.t_begin; kt < sg.t_end; ++kt, ++it) {
         const CUtensorMap* mk = &map_kc;
         const CUtensorMap* mv = &map_vc;
-        int row0 = c0 + (kt - np_t) * kTileN;
+        int row0 = sg.c0 + (kt - np_t) * kTileN;
         if (kt < np_t) {
           mk = &map_kp;
           mv = &map_vp;
-          row0 = p0 + kt * kTileN;
+          row0 = sg.p0 + kt * kTileN;
         }
-        const int sk = i % SK, sv = i % SV;
-        if (!mbar_wait(W, bar_kempty + 8 * sk, ((uint32_t)(i / SK) & 1u) ^ 1u)) break;
-        mbar_arrive_expect_tx(bar_kfull + 8 * sk, C::kTileBytes);
-        for (int kb = 0; kb < C::kBoxes; ++kb)
-          tma_load_3d(base + C::kKOff + sk * C::kTileBytes + kb * kBoxBytes, mk,
-                      bar_kfull + 8 * sk, kb * 64, hk, row0);
-        issued_k = i + 1;
-        if (!mbar_wait(W, bar_vempty + 8 * sv, ((uint32_t)(i / SV) & 1u) ^ 1u)) break;
-        mbar_arrive_expect_tx(bar_vfull + 8 * sv, C::kTileBytes);
-        for (int kb = 0; kb < C::kBoxes; ++kb)
-          tma_load_3d(base + C::kVOff + sv * C::kTileBytes + kb * kBoxBytes, mv,
-                      bar_vfull + 8 * sv, kb * 64, hk, row0);
-        issued_v = i + 1;
+        const int sk = it % SK, sv = it % SV;
+        if (!(ok = warp_wait(W, bar_kempty + 8 * sk, ((uint32_t)(it / SK) & 1u) ^ 1u))) break;
+        if (leader) {
+          mbar_arrive_expect_tx(bar_kfull + 8 * sk, C::kTileBytes);
+          for (int kb = 0; kb < C::kBoxes; ++kb)
+            tma_load_3d(base + C::kKOff + sk * C::kTileBytes + kb * kBoxBytes, mk,
+                        bar_kfull + 8 * sk, kb * 64, sg.hk, row0);
+        }
+        __syncwarp();
+        issued_k = it + 1;
+        if (!(ok = warp_wait(W, bar_vempty + 8 * sv, ((uint32_t)(it / SV) & 1u) ^ 1u))) break;
+        if (leader) {
+          mbar_arrive_expect_tx(bar_vfull + 8 * sv, C::kTileBytes);
+          for (int kb = 0; kb < C::kBoxes; ++kb)
+            tma_load_3d(base + C::kVOff + sv * C::kTileBytes + kb * kBoxBytes, mv,
+                        bar_vfull + 8 * sv, kb * 64, sg.hk, row0);
+        }
+        __syncwarp();
+        issued_v = it + 1;
       }
-      mbar_wait_bounded(bar_qdo, 0, kDrainLimitNs);
-      for (int i = (issued_k > SK ? issued_k - SK : 0); i < issued_k; ++i)
-        mbar_wait_bounded(bar_kfull + 8 * (i % SK), (uint32_t)(i / SK) & 1u, kDrainLimitNs);
-      for (int i = (issued_v > SV ? issued_v - SV : 0); i < issued_v; ++i)
-        mbar_wait_bounded(bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u, kDrainLimitNs);
     }
+    if (seg > 0) mbar_wait_bounded(bar_qdo, (uint32_t)(seg - 1) & 1u, kDrainLimitNs);
+    for (int i = (issued_k > SK ? issued_k - SK : 0); i < issued_k; ++i)
+      mbar_wait_bounded(bar_kfull + 8 * (i % SK), (uint32_t)(i / SK) & 1u, kDrainLimitNs);
+    for (int i = (issued_v > SV ? issued_v - SV : 0); i < issued_v; ++i)
+      mbar_wait_bounded(bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u, kDrainLimitNs);
   } else if (warp == 9) {
-    if (lane == 0) {
-      bool ok = mbar_wait(W, bar_qdo, 0) && mbar_wait(W, bar_kfull, 0) && mbar_wait(W, bar_vfull, 0);
-      const uint32_t t_dq = tmem + 384;
-      // Issue order per key tile i:  S(i), dP(i), dQ(i-1).  dP(i) needs only
-      // that dP(i-1) has been read, so it runs while dS(i-1) is computed.  The
-      // waits for K(i+1) / V(i+1) sit at the end of the iteration, off the
-      // critical path.
+    // Issue order per key tile g:  S(g), dP(g), dQ(g-1).  dP(g) needs only
+    // that dP(g-1) has been read, so it runs while dS(g-1) is computed.  The
+    // waits for K / V of the next tile sit at the end of the iteration, off
+    // the critical path.  Tile counters run across segments.  The whole warp
+    // waits (converged); lane 0 issues the MMAs and commits.
+    const bool leader = lane == 0;
+    const uint32_t t_dq = tmem + 384;
+    int it = 0, seg = 0;
+    // test hook: see the forward kernel
+    bool ok = !(a.debug_wait_never && !warp_wait(W, bar_drain, 0));
+    while (ok && walk.next(sg)) {
+      const int n = sg.t_end - sg.t_begin;
+      if (!(ok = warp_wait(W, bar_qdo, (uint32_t)seg & 1u))) break;
+      if (!(ok = warp_wait(W, bar_kfull + 8 * (it % SK), (uint32_t)(it / SK) & 1u))) break;
+      if (!(ok = warp_wait(W, bar_vfull + 8 * (it % SV), (uint32_t)(it / SV) & 1u))) break;
       for (int i = 0; ok && i < n; ++i) {
-        const int sk = i % SK, sv = i % SV;
-        issue_nt<D>(tmem + (uint32_t)(i & 1) * 128u, base + C::kQOff,
-                    base + C::kKOff + sk * C::kTileBytes);
-        tc_commit(bar_sfull + 8 * (i & 1));
-        if (i > 0 && !(ok = mbar_wait(W, bar_dpfree, (uint32_t)(i - 1) & 1u))) break;
+        const int g = it + i;
+        const int sk = g % SK, sv = g % SV;
+        if (leader) {
+          issue_nt<D>(tmem + (uint32_t)(g & 1) * 128u, base + C::kQOff,
+                      base + C::kKOff + sk * C::kTileBytes);
+          tc_commit(bar_sfull + 8 * (g & 1));
+        }
+        __syncwarp();
+        if (g > 0 && !(ok = warp_wait(W, bar_dpfree, (uint32_t)(g - 1) & 1u))) break;
         tc_fence_after_sync();
-        issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + sv * C::kTileBytes);
-        tc_commit(bar_dpfull);
-        tc_commit(bar_vempty + 8 * sv);
+        if (leader) {
+          issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + sv * C::kTileBytes);
+          tc_commit(bar_dpfull);
+          tc_commit(bar_vempty + 8 * sv);
+          if (i == n - 1) tc_commit(bar_qempty);  // last S and dP of the segment
+        }
+        __syncwarp();
         if (i > 0) {
-          const int skp = (i - 1) % SK;
-          if (!(ok = mbar_wait(W, bar_dsfull, (uint32_t)(i - 1) & 1u))) break;
+          const int skp = (g - 1) % SK;
+          // the first dQ of a segment overwrites the accumulator: the previous
+          // segment's epilogue must have read it
+          if (i == 1 && seg > 0 && !(ok = warp_wait(W, bar_dqfree, (uint32_t)(seg - 1) & 1u)))
+            break;
+          if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)(g - 1) & 1u))) break;
           tc_fence_after_sync();
-          issue_tn<D>(t_dq, tmem + (uint32_t)((i - 1) & 1) * 128u,
-                      base + C::kKOff + skp * C::kTileBytes, i - 1 > 0);
-          tc_commit(bar_kempty + 8 * skp);
+          if (leader) {
+            issue_tn<D>(t_dq, tmem + (uint32_t)((g - 1) & 1) * 128u,
+                        base + C::kKOff + skp * C::kTileBytes, i - 1 > 0);
+            tc_commit(bar_kempty + 8 * skp);
+          }
+          __syncwarp();
         }
         if (i + 1 < n) {
-          const int j = i + 1;
-          if (!(ok = mbar_wait(W, bar_kfull + 8 * (j % SK), (uint32_t)(j / SK) & 1u))) break;
-          if (!(ok = mbar_wait(W, bar_vfull + 8 * (j % SV), (uint32_t)(j / SV) & 1u))) break;
+          const int j = g + 1;
+          if (!(ok = warp_wait(W, bar_kfull + 8 * (j % SK), (uint32_t)(j / SK) & 1u))) break;
+          if (!(ok = warp_wait(W, bar_vfull + 8 * (j % SV), (uint32_t)(j / SV) & 1u))) break;
         }
       }
-      if (ok) {
-        const int i = n - 1, sk = i % SK;
-        if (mbar_wait(W, bar_dsfull, (uint32_t)i & 1u)) {
-          tc_fence_after_sync();
-          issue_tn<D>(t_dq, tmem + (uint32_t)(i & 1) * 128u, base + C::kKOff + sk * C::kTileBytes,
-                      i > 0);
-          tc_commit(bar_dqfull);
-        }
+      if (!ok) break;
+      const int gl = it + n - 1, skl = gl % SK;
+      if (n == 1 && seg > 0 && !(ok = warp_wait(W, bar_dqfree, (uint32_t)(seg - 1) & 1u))) break;
+      if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)gl & 1u))) break;
+      tc_fence_after_sync();
+      if (leader) {
+        issue_tn<D>(t_dq, tmem + (uint32_t)(gl & 1) * 128u, base + C::kKOff + skl * C::kTileBytes,
+                    n > 1);
+        tc_commit(bar_kempty + 8 * skl);
+        tc_commit(bar_dqfull);
       }
-      tc_commit(bar_drain);
-      mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
+      __syncwarp();
+      it += n;
+      ++seg;
     }
+    if (leader) tc_commit(bar_drain);
+    __syncwarp();
+    mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
   } else {
     const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    const int token = t0 + row / tl.g;
-    const int head = hk * tl.g + row % tl.g;
-    const bool row_valid = row < tl.rows && token < lc;
-    const size_t grow = (size_t)(c0 + (row_valid ? token : 0));
-    const float lse2 = row_valid ? a.lse[(size_t)head * a.total_lc + grow] * kLog2e : 0.f;
-    const float dl = row_valid ? a.delta[(size_t)head * a.total_lc + grow] : 0.f;
     const float sl2 = a.scale_log2;
+    int u = 0, seg = 0;  // tiles and segments processed
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      const uint32_t sb = (uint32_t)(i & 1) * 128u + (uint32_t)half * 64u;
-      if (!(ok = warp_wait(W, bar_sfull + 8 * (i & 1), (uint32_t)(i >> 1) & 1u))) break;
-      tc_fence_after_sync();
-      const int kt = kt0 + i;
-      int lim = (kt < np_t) ? (lp - kt * kTileN) : (token - (kt - np_t) * kTileN + 1);
-      if (!row_valid) lim = 0;
-      lim -= half * 64;  // visible columns [0, lim) of this warp's 64
-      float p[64];
-      {
-        uint32_t r[64];
-        tmem_ld_x64(t_lane + sb, r);
+    while (ok && walk.next(sg)) {
+      const int n = sg.t_end - sg.t_begin;
+      const int np_t = ceil_div(sg.lp, kTileN);
+      const int token = sg.qb * tl.tpt + row / tl.g;
+      const int head = sg.hk * tl.g + row % tl.g;
+      const bool row_valid = row < tl.rows && token < sg.lc;
+      const size_t grow = (size_t)(sg.c0 + (row_valid ? token : 0));
+      const float lse2 = row_valid ? a.lse[(size_t)head * a.total_lc + grow] * kLog2e : 0.f;
+      const float dl = row_valid ? a.delta[(size_t)head * a.total_lc + grow] : 0.f;
+      for (int i = 0; i < n; ++i, ++u) {
+        const uint32_t sb = (uint32_t)(u & 1) * 128u + (uint32_t)half * 64u;
+        if (!(ok = warp_wait(W, bar_sfull + 8 * (u & 1), (uint32_t)(u >> 1) & 1u))) break;
+        tc_fence_after_sync();
+        const int kt = sg.t_begin + i;
+        int lim = (kt < np_t) ? (sg.lp - kt * kTileN) : (token - (kt - np_t) * kTileN + 1);
+        if (!row_valid) lim = 0;
+        lim -= half * 64;  // visible columns [0, lim) of this warp's 64
+        float p[64];
+        {
+          uint32_t r[64];
+          tmem_ld_x64(t_lane + sb, r);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) p[j] = ex2_approx(fmaf(__uint_as_float(r[j]), sl2, -lse2));
-        if (lim < 64) {  // edge tiles only: the prefix tail, the causal diagonal, padding rows
+          for (int j = 0; j < 64; ++j) p[j] = ex2_approx(fmaf(__uint_as_float(r[j]), sl2, -lse2));
+          if (lim < 64) {  // edge tiles only: the prefix tail, the causal diagonal, padding rows
 #pragma unroll
-          for (int j = 0; j < 64; ++j) p[j] = (j < lim) ? p[j] : 0.f;
+            for (int j = 0; j < 64; ++j) p[j] = (j < lim) ? p[j] : 0.f;
+          }
         }
-      }
-      if (!(ok = warp_wait(W, bar_dpfull, (uint32_t)i & 1u))) break;
-      tc_fence_after_sync();
-      uint32_t pk[32];
-      {
-        uint32_t r[64];
-        tmem_ld_x64(t_lane + 256 + half * 64, r);
+        if (!(ok = warp_wait(W, bar_dpfull, (uint32_t)u & 1u))) break;
+        tc_fence_after_sync();
+        uint32_t pk[32];
+        {
+          uint32_t r[64];
+          tmem_ld_x64(t_lane + 256 + half * 64, r);
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dpfree);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            pk[j] = pack_bf16x2(p[2 * j] * (__uint_as_float(r[2 * j]) - dl),
+                                p[2 * j + 1] * (__uint_as_float(r[2 * j + 1]) - dl));
+        }
+        tmem_st_x32(t_lane + sb, pk);
+        tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_dpfree);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          pk[j] = pack_bf16x2(p[2 * j] * (__uint_as_float(r[2 * j]) - dl),
-                              p[2 * j + 1] * (__uint_as_float(r[2 * j + 1]) - dl));
+        if (lane == 0) mbar_arrive(bar_dsfull);
       }
-      tmem_st_x32(t_lane + sb, pk);
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dsfull);
-    }
-    if (ok) ok = warp_wait(W, bar_dqfull, 0);
-    if (ok) {
+      if (!ok) break;
+      if (!(ok = warp_wait(W, bar_dqfull, (uint32_t)seg & 1u))) break;
       tc_fence_after_sync();
-      const bool single = (n_split == 1);
+      const bool final_out = !sg.head && !sg.tail;
+      const int slot = sg.head ? 0 : 1;
+      const size_t pslot = (size_t)blockIdx.x * 2 + slot;
 #pragma unroll
       for (int cb = half * (D / 2); cb < (half + 1) * (D / 2); cb += 32) {
         uint32_t r[32];
         tmem_ld_x32(t_lane + 384 + cb, r);
         if (row_valid) {
-          if (single) {
+          if (final_out) {
             uint4* dst = reinterpret_cast<uint4*>(a.dq + (grow * a.hq + head) * D + cb);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * a.scale,
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * a.scale,
                                 __uint_as_float(r[8 * v + 1]) * a.scale);
-              u.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * a.scale,
+              w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * a.scale,
                                 __uint_as_float(r[8 * v + 3]) * a.scale);
-              u.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * a.scale,
+              w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * a.scale,
                                 __uint_as_float(r[8 * v + 5]) * a.scale);
-              u.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * a.scale,
+              w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * a.scale,
                                 __uint_as_float(r[8 * v + 7]) * a.scale);
-              dst[v] = u;
+              dst[v] = w;
             }
           } else {
-            float4* dst = reinterpret_cast<float4*>(
-                a.dq_part + (((size_t)split * a.total_lc + grow) * a.hq + head) * D + cb);
+            // feature-major partial [D/4][128][4]: a warp's store is one
+            // contiguous 512-byte run
+            float4* dst = reinterpret_cast<float4*>(a.dq_part) + pslot * (D / 4) * kTileM +
+                          (size_t)(cb / 4) * kTileM + row;
 #pragma unroll
             for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(r[4 * v + 0]) * a.scale,
-                                   __uint_as_float(r[4 * v + 1]) * a.scale,
-                                   __uint_as_float(r[4 * v + 2]) * a.scale,
-                                   __uint_as_float(r[4 * v + 3]) * a.scale);
+              dst[(size_t)v * kTileM] = make_float4(__uint_as_float(r[4 * v + 0]) * a.scale,
+                                                    __uint_as_float(r[4 * v + 1]) * a.scale,
+                                                    __uint_as_float(r[4 * v + 2]) * a.scale,
+                                                    __uint_as_float(r[4 * v + 3]) * a.scale);
           }
         }
       }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dqfree);
+      ++seg;
     }
   }
 
@@ -438,7 +504,7 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      bool ok = mbar_wait(W, bar_kv, 0);
+      bool ok = !(a.debug_wait_never && !mbar_wait(W, bar_drain, 0)) && mbar_wait(W, bar_kv, 0);
       tc_fence_after_sync();
       for (int i = 0; ok && i < n; ++i) {
         const int s = i % S;
@@ -566,31 +632,62 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-// Sum the dQ split partials in split order (deterministic) and round to bf16.
+// Sum the dQ partials of every query tile that CTA boundaries cut, in CTA
+// order (deterministic), and round to bf16.  One CTA per (query tile, 32
+// rows); thread 0 lists the tile's parts once; thread t takes row t % 32 of
+// the chunk and column slice t / 32, so a warp reads consecutive rows of the
+// feature-major partials (coalesced).
+constexpr int kReduceRows = 32;
+constexpr int kMaxParts = 1024;
+
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
-  constexpr int E = D / 32;
-  const int b = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rid = blockIdx.x * 8 + warp;
-  const int t = rid / a.hq, h = rid % a.hq;
+  constexpr int CW = D / 8;
+  __shared__ int parts[kMaxParts];
+  __shared__ int n_parts;
+  const Tiling tl = a.tl;
+  const int chunks = kTileM / kReduceRows;
+  const int b = blockIdx.z, hk = blockIdx.y;
+  const int qb = blockIdx.x / chunks;
+  const int row = (blockIdx.x % chunks) * kReduceRows + (threadIdx.x & 31);
+  const int c0col = (threadIdx.x >> 5) * CW;
   const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
   const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
-  if (t >= lc) return;
-  const int ns = block_splits(a.tl, lp, lc, t / a.tl.tpt);
-  if (ns <= 1) return;
-  const size_t grow = (size_t)(c0 + t);
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float* src = a.dq_part + (((size_t)s * a.total_lc + grow) * a.hq + h) * D + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] += src[e];
+  if (qb >= blocks_of_window(tl, lc)) return;
+  if (threadIdx.x == 0) {
+    long long bs = a.win_prefix[b] + (long long)hk * head_work(tl, lp, lc);
+    for (int q = 0; q < qb; ++q) bs += block_key_tiles(lp, lc, q * tl.tpt, tl.tpt);
+    const long long be = bs + block_key_tiles(lp, lc, qb * tl.tpt, tl.tpt);
+    n_parts = block_parts(bs, be, a.win_prefix[a.batch], tl.grid, parts, kMaxParts);
   }
-  __nv_bfloat16* dst = a.dq + (grow * a.hq + h) * D + lane * E;
+  __syncthreads();
+  const int np = n_parts;
+  if (np == 0) return;
+  const int token = qb * tl.tpt + row / tl.g;
+  if (row >= tl.rows || token >= lc) return;
+  const int head = hk * tl.g + row % tl.g;
+  float acc[CW];
 #pragma unroll
-  for (int e = 0; e < E; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e], acc[e + 1]);
+  for (int e = 0; e < CW; ++e) acc[e] = 0.f;
+  for (int j = 0; j < np; ++j) {
+    const size_t slot = (size_t)parts[j] * 2 + (j == 0);
+    const float4* src = reinterpret_cast<const float4*>(a.dq_part) + slot * (D / 4) * kTileM;
+#pragma unroll
+    for (int e = 0; e < CW; e += 4) {
+      const float4 v = src[(size_t)((c0col + e) >> 2) * kTileM + row];
+      acc[e] += v.x;
+      acc[e + 1] += v.y;
+      acc[e + 2] += v.z;
+      acc[e + 3] += v.w;
+    }
+  }
+  const size_t grow = (size_t)(c0 + token);
+  uint4* dst = reinterpret_cast<uint4*>(a.dq + (grow * a.hq + head) * D + c0col);
+#pragma unroll
+  for (int e = 0; e < CW; e += 8)
+    dst[e / 8] = make_uint4(pack_bf16x2(acc[e], acc[e + 1]), pack_bf16x2(acc[e + 2], acc[e + 3]),
+                            pack_bf16x2(acc[e + 4], acc[e + 5]),
+                            pack_bf16x2(acc[e + 6], acc[e + 7]));
 }
 
 // delta[h, t] = sum_c dO[t, h, c] * O[t, h, c]; one warp per (t, h) row.
@@ -677,9 +774,9 @@ int bwd_dkdv_smem_bytes(int d) {
   return d == 128 ? DkvCfg<128>::kSmemBytes : DkvCfg<64>::kSmemBytes;
 }
 
-cudaError_t launch_bwd_dq(const Maps& m, const BwdArgs& a, int d, int q8, dim3 grid,
-                          cudaStream_t st) {
+cudaError_t launch_bwd_dq(const Maps& m, const BwdArgs& a, int d, int q8, cudaStream_t st) {
   (void)q8;
+  const dim3 grid((unsigned)a.tl.grid);
   if (d == 128) {
     auto k = bwd_dq_kernel<128>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -713,9 +810,9 @@ cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, dim3 grid, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq_reduce(const BwdArgs& a, int d, int batch, int max_lc, cudaStream_t st) {
-  const long long rows = (long long)max_lc * a.hq;
-  dim3 grid((unsigned)((rows + 7) / 8), (unsigned)batch);
+cudaError_t launch_bwd_dq_reduce(const BwdArgs& a, int d, int max_lc, cudaStream_t st) {
+  const int nblk = ceil_div(max_lc > 0 ? max_lc : 1, a.tl.tpt);
+  dim3 grid((unsigned)(nblk * (kTileM / kReduceRows)), (unsigned)a.hkv, (unsigned)a.batch);
   if (d == 128)
     bwd_dq_reduce_kernel<128><<<grid, 256, 0, st>>>(a);
   else

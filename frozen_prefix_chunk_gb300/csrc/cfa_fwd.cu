@@ -1,12 +1,14 @@
 // Forward pass of frozen-prefix chunk attention on sm_103a.
 //
-// One CTA takes a query block (two 128-row query tiles of one KV head, rows
-// packed token-major over the g query heads of the group) and one split of
-// its key-tile list (prefix tiles, then the visible chunk tiles).  Roles:
+// Persistent stream-K kernel: one CTA per SM takes an equal, contiguous range
+// of (query block, key tile) iterations (see cfa_sched.cuh) and walks it as
+// segments, one per query block.  A query block is two 128-row query tiles of
+// one KV head, rows packed token-major over the g query heads of the group.
+// Roles:
 //
 //   warps 0-3  softmax for query tile 0      (TMEM lanes 0-127, one row each)
 //   warps 4-7  softmax for query tile 1
-//   warp  8    TMA producer: Q once, then K and V tiles into a ring of stages
+//   warp  8    TMA producer: Q per segment, K and V tiles into two rings
 //   warp  9    TMEM owner and single-thread tcgen05.mma issuer
 //
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,...).
@@ -21,10 +23,10 @@
 // last prefix tile beyond Lp, and chunk keys j > t (row t sits at absolute
 // position Lp + t, so it sees the whole prefix).
 //
-// A single-split block writes bf16 O and LSE directly; otherwise each split
-// writes its normalised fp32 O and its LSE to the workspace and
-// fwd_combine_kernel merges them:  LSE = log sum_k exp(LSE_k),
-// O = sum_k exp(LSE_k - LSE) O_k.
+// A segment that covers its whole query block writes bf16 O and LSE; the
+// pieces of a block cut by CTA boundaries write normalised fp32 O and LSE
+// partials, which fwd_merge_kernel combines in CTA order:
+// LSE = log sum_k exp(LSE_k),  O = sum_k exp(LSE_k - LSE) O_k.
 #include "cfa_kernels.cuh"
 #include "cfa_ptx.cuh"
 
@@ -48,7 +50,7 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
   static constexpr int kThreads = 320;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(8 * (1 + 2 * kKStages + 2 * kVStages + 7) <= 240, "barrier area");
+  static_assert(8 * (2 + 2 * kKStages + 2 * kVStages + 9) <= 240, "barrier area");
 };
 
 // S_t = Q_t K^T: A = Q tile, B = K tile, both K-major 128B-swizzled; one MMA
@@ -96,36 +98,41 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Tiling tl = a.tl;
-  const int b = blockIdx.z, hk = blockIdx.y;
-  const int qblk = blockIdx.x / tl.n_split_max, split = blockIdx.x % tl.n_split_max;
-  const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
-  const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
   const int tok_blk = tl.q_per_cta * tl.tpt;
-  const int t0 = qblk * tok_blk;
-  if (t0 >= lc) return;
-  const int nq = min(tl.q_per_cta, ceil_div(lc - t0, tl.tpt));
-  const int np_t = ceil_div(lp, kTileN);
-  const int n_kt = block_key_tiles(lp, lc, t0, tok_blk);
-  const int n_split = ceil_div(n_kt, tl.tiles_per_split);
-  if (split >= n_split) return;
-  const int kt0 = split * tl.tiles_per_split;
-  const int n = min(tl.tiles_per_split, n_kt - kt0);
+  const int rows_blk = tl.q_per_cta * kTileM;
+  {
+    // schedule prologue: shared scratch in the (not yet used) barrier area
+    long long* sched = reinterpret_cast<long long*>(gbase + C::kBarOff);
+    plan_schedule(a.cu_p, a.cu_c, a.batch, a.hkv, tl, a.win_prefix, sched + 4, sched,
+                  reinterpret_cast<int*>(sched + 1), sched + 2);
+  }
+  SegmentWalker walk;
+  {
+    const long long* sched = reinterpret_cast<const long long*>(gbase + C::kBarOff);
+    walk.init(a.cu_p, a.cu_c, a.batch, a.hkv, tl, blockIdx.x, sched[0],
+              *reinterpret_cast<const int*>(sched + 1), sched[2]);
+  }
+  __syncthreads();  // the barrier area is initialised below
+  if (walk.cur >= walk.end) return;
 
   const uint32_t bars = base + C::kBarOff;
   const uint32_t bar_q = bars;
-  const uint32_t bar_kfull = bars + 8;                  // [SK]
+  const uint32_t bar_qempty = bars + 8;
+  const uint32_t bar_kfull = bars + 16;                 // [SK]
   const uint32_t bar_kempty = bar_kfull + 8 * SK;       // [SK]
   const uint32_t bar_vfull = bar_kempty + 8 * SK;       // [SV]
   const uint32_t bar_vempty = bar_vfull + 8 * SV;       // [SV]
   const uint32_t bar_sfull = bar_vempty + 8 * SV;       // [2]
   const uint32_t bar_pfull = bar_sfull + 16;            // [2]
   const uint32_t bar_ofull = bar_pfull + 16;            // [2]
-  const uint32_t bar_drain = bar_ofull + 16;
+  const uint32_t bar_ofree = bar_ofull + 16;            // [2]
+  const uint32_t bar_drain = bar_ofree + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 240);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 244);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
+    mbar_init(bar_qempty, 1);
     for (int s = 0; s < SK; ++s) {
       mbar_init(bar_kfull + 8 * s, 1);
       mbar_init(bar_kempty + 8 * s, 1);
@@ -138,6 +145,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar_sfull + 8 * t, 1);
       mbar_init(bar_pfull + 8 * t, 4);
       mbar_init(bar_ofull + 8 * t, 1);
+      mbar_init(bar_ofree + 8 * t, 4);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -151,226 +159,300 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch_map(&map_q);
     tma_prefetch_map(&map_kc);
     tma_prefetch_map(&map_vc);
-    if (np_t > 0) {
-      tma_prefetch_map(&map_kp);
-      tma_prefetch_map(&map_vp);
-    }
+    tma_prefetch_map(&map_kp);
+    tma_prefetch_map(&map_vp);
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const Waiter W{a.limit_ns, abort_flag, a.status};
+  Segment sg;
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, (uint32_t)(nq * C::kBoxes * 128 * tl.rows));
-      for (int qt = 0; qt < nq; ++qt)
-        for (int kb = 0; kb < C::kBoxes; ++kb)
-          tma_load_3d(base + C::kQOff + (qt * C::kBoxes + kb) * kBoxBytes, &map_q, bar_q, kb * 64,
-                      hk * tl.g, c0 + t0 + qt * tl.tpt);
-      int issued_k = 0, issued_v = 0;
-      for (int i = 0; i < n; ++i) {
-        const int kt = kt0 + i;
+    // The whole warp walks the schedule and waits (converged); lane 0 issues.
+    const bool leader = lane == 0;
+    int it = 0, seg = 0, issued_k = 0, issued_v = 0;
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      // the Q tiles are reused: the previous segment's S MMAs must be done
+      if (seg > 0 && !(ok = warp_wait(W, bar_qempty, (uint32_t)(seg - 1) & 1u))) break;
+      CFA_TRACE(4, seg, 0);
+      if (leader) {
+        mbar_arrive_expect_tx(bar_q, (uint32_t)(sg.nq * C::kBoxes * 128 * tl.rows));
+        for (int qt = 0; qt < sg.nq; ++qt)
+          for (int kb = 0; kb < C::kBoxes; ++kb)
+            tma_load_3d(base + C::kQOff + (qt * C::kBoxes + kb) * kBoxBytes, &map_q, bar_q,
+                        kb * 64, sg.hk * tl.g, sg.c0 + sg.qb * tok_blk + qt * tl.tpt);
+      }
+      __syncwarp();
+      ++seg;
+      const int np_t = ceil_div(sg.lp, kTileN);
+      for (int kt = sg.t_begin; kt < sg.t_end; ++kt, ++it) {
         const CUtensorMap* mk = &map_kc;
         const CUtensorMap* mv = &map_vc;
-        int row0 = c0 + (kt - np_t) * kTileN;
+        int row0 = sg.c0 + (kt - np_t) * kTileN;
         if (kt < np_t) {
           mk = &map_kp;
           mv = &map_vp;
-          row0 = p0 + kt * kTileN;
+          row0 = sg.p0 + kt * kTileN;
         }
-        const int sk = i % SK, sv = i % SV;
-        if (!mbar_wait(W, bar_kempty + 8 * sk, ((uint32_t)(i / SK) & 1u) ^ 1u)) break;
-        mbar_arrive_expect_tx(bar_kfull + 8 * sk, C::kTileBytes);
-        for (int kb = 0; kb < C::kBoxes; ++kb)
-          tma_load_3d(base + C::kKOff + sk * C::kTileBytes + kb * kBoxBytes, mk,
-                      bar_kfull + 8 * sk, kb * 64, hk, row0);
-        issued_k = i + 1;
-        if (!mbar_wait(W, bar_vempty + 8 * sv, ((uint32_t)(i / SV) & 1u) ^ 1u)) break;
-        mbar_arrive_expect_tx(bar_vfull + 8 * sv, C::kTileBytes);
-        for (int kb = 0; kb < C::kBoxes; ++kb)
-          tma_load_3d(base + C::kVOff + sv * C::kTileBytes + kb * kBoxBytes, mv,
-                      bar_vfull + 8 * sv, kb * 64, hk, row0);
-        issued_v = i + 1;
+        const int sk = it % SK, sv = it % SV;
+        if (!(ok = warp_wait(W, bar_kempty + 8 * sk, ((uint32_t)(it / SK) & 1u) ^ 1u))) break;
+        CFA_TRACE(3, it, 0);
+        if (leader) {
+          mbar_arrive_expect_tx(bar_kfull + 8 * sk, C::kTileBytes);
+          for (int kb = 0; kb < C::kBoxes; ++kb)
+            tma_load_3d(base + C::kKOff + sk * C::kTileBytes + kb * kBoxBytes, mk,
+                        bar_kfull + 8 * sk, kb * 64, sg.hk, row0);
+        }
+        __syncwarp();
+        issued_k = it + 1;
+        if (!(ok = warp_wait(W, bar_vempty + 8 * sv, ((uint32_t)(it / SV) & 1u) ^ 1u))) break;
+        CFA_TRACE(3, it, 1);
+        if (leader) {
+          mbar_arrive_expect_tx(bar_vfull + 8 * sv, C::kTileBytes);
+          for (int kb = 0; kb < C::kBoxes; ++kb)
+            tma_load_3d(base + C::kVOff + sv * C::kTileBytes + kb * kBoxBytes, mv,
+                        bar_vfull + 8 * sv, kb * 64, sg.hk, row0);
+        }
+        __syncwarp();
+        issued_v = it + 1;
       }
-      // Unwind: every copy this thread issued has landed before the CTA exits.
-      mbar_wait_bounded(bar_q, 0, kDrainLimitNs);
-      for (int i = (issued_k > SK ? issued_k - SK : 0); i < issued_k; ++i)
-        mbar_wait_bounded(bar_kfull + 8 * (i % SK), (uint32_t)(i / SK) & 1u, kDrainLimitNs);
-      for (int i = (issued_v > SV ? issued_v - SV : 0); i < issued_v; ++i)
-        mbar_wait_bounded(bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u, kDrainLimitNs);
     }
+    // Unwind: every copy this warp issued has landed before the CTA exits.
+    if (seg > 0) mbar_wait_bounded(bar_q, (uint32_t)(seg - 1) & 1u, kDrainLimitNs);
+    for (int i = (issued_k > SK ? issued_k - SK : 0); i < issued_k; ++i)
+      mbar_wait_bounded(bar_kfull + 8 * (i % SK), (uint32_t)(i / SK) & 1u, kDrainLimitNs);
+    for (int i = (issued_v > SV ? issued_v - SV : 0); i < issued_v; ++i)
+      mbar_wait_bounded(bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u, kDrainLimitNs);
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issue
-    if (lane == 0) {
-      bool ok = mbar_wait(W, bar_q, 0) && mbar_wait(W, bar_kfull, 0);
-      // Issue order per key tile i:  PV0(i-1) S0(i) PV1(i-1) S1(i).  PV of the
-      // previous tile goes first (it does not need K(i)); S_t(i) reuses the
-      // TMEM columns of P_t(i-1), which the in-order MMA pipe has consumed.
-      // The K(i+1) / V(i) waits sit at the end of the iteration, where the
-      // tensor pipe is still busy with the work just issued; only the P
-      // hand-offs remain on the critical path.
+    // Issue order per key tile i of a segment:  PV0(i-1) S0(i) PV1(i-1)
+    // S1(i).  PV of the previous tile goes first (it does not need K(i));
+    // S_t(i) reuses the TMEM columns of P_t(i-1), which the in-order MMA
+    // pipe has consumed.  The K(i+1) / V(i) waits sit at the end of the
+    // iteration, where the tensor pipe is still busy, so only the P
+    // hand-offs remain on the critical path.  The whole warp waits
+    // (converged); lane 0 issues the MMAs and commits.
+    const bool leader = lane == 0;
+    int it = 0, seg = 0;
+    int ut[2] = {0, 0}, us[2] = {0, 0};  // per query tile: tiles, segments done
+    // test hook: wait on a barrier nothing arrives on before the end, so the
+    // bounded wait runs out and the CTA unwinds
+    bool ok = !(a.debug_wait_never && !warp_wait(W, bar_drain, 0));
+    while (ok && walk.next(sg)) {
+      const int n = sg.t_end - sg.t_begin, nq = sg.nq;
+      CFA_TRACE(4, seg, 1);
+      if (!(ok = warp_wait(W, bar_q, (uint32_t)seg & 1u))) break;
+      CFA_TRACE(4, seg, 2);
+      if (!(ok = warp_wait(W, bar_kfull + 8 * (it % SK), (uint32_t)(it / SK) & 1u))) break;
+      CFA_TRACE(4, seg, 3);
       for (int i = 0; ok && i < n; ++i) {
-        const int sk = i % SK, svp = (i + SV - 1) % SV;
+        const int g = it + i;
+        const int sk = g % SK, svp = (g + SV - 1) % SV;
         for (int qt = 0; qt < nq; ++qt) {
           if (i > 0) {
-            if (!(ok = mbar_wait(W, bar_pfull + 8 * qt, (uint32_t)(i - 1) & 1u))) break;
+            // the first PV of a segment overwrites O_t: the previous
+            // segment's epilogue must have read it
+            if (i == 1 && us[qt] > 0 &&
+                !(ok = warp_wait(W, bar_ofree + 8 * qt, (uint32_t)(us[qt] - 1) & 1u)))
+              break;
+            if (!(ok = warp_wait(W, bar_pfull + 8 * qt, (uint32_t)(ut[qt] + i - 1) & 1u))) break;
+            CFA_TRACE(2, it + i, 2 * qt);
             tc_fence_after_sync();
-            issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128, base + C::kVOff + svp * C::kTileBytes,
-                        i - 1 > 0);
-            if (qt == nq - 1) tc_commit(bar_vempty + 8 * svp);
+            if (leader) {
+              issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128,
+                          base + C::kVOff + svp * C::kTileBytes, i - 1 > 0);
+              if (qt == nq - 1) tc_commit(bar_vempty + 8 * svp);
+            }
+            __syncwarp();
           }
-          issue_qk<D>(tmem + qt * 128, base + C::kQOff + qt * C::kTileBytes,
-                      base + C::kKOff + sk * C::kTileBytes);
-          tc_commit(bar_sfull + 8 * qt);
-          if (qt == nq - 1) tc_commit(bar_kempty + 8 * sk);
+          if (leader) {
+            issue_qk<D>(tmem + qt * 128, base + C::kQOff + qt * C::kTileBytes,
+                        base + C::kKOff + sk * C::kTileBytes);
+            tc_commit(bar_sfull + 8 * qt);
+            if (qt == nq - 1) tc_commit(bar_kempty + 8 * sk);
+            if (qt == nq - 1 && i == n - 1) tc_commit(bar_qempty);  // segment's last S
+          }
+          __syncwarp();
+          CFA_TRACE(2, it + i, 2 * qt + 1);
         }
         if (!ok) break;
         if (i + 1 < n &&
-            !(ok = mbar_wait(W, bar_kfull + 8 * ((i + 1) % SK), (uint32_t)((i + 1) / SK) & 1u)))
+            !(ok = warp_wait(W, bar_kfull + 8 * ((g + 1) % SK), (uint32_t)((g + 1) / SK) & 1u)))
           break;
-        ok = mbar_wait(W, bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u);
+        ok = warp_wait(W, bar_vfull + 8 * (g % SV), (uint32_t)(g / SV) & 1u);
+        CFA_TRACE(2, g, 4);
       }
-      if (ok) {
-        const int i = n - 1, sv = i % SV;
-        for (int qt = 0; ok && qt < nq; ++qt) {
-          if (!(ok = mbar_wait(W, bar_pfull + 8 * qt, (uint32_t)i & 1u))) break;
-          tc_fence_after_sync();
-          issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128, base + C::kVOff + sv * C::kTileBytes,
-                      i > 0);
+      if (!ok) break;
+      const int gl = it + n - 1, svl = gl % SV;
+      for (int qt = 0; ok && qt < nq; ++qt) {
+        if (n == 1 && us[qt] > 0 &&
+            !(ok = warp_wait(W, bar_ofree + 8 * qt, (uint32_t)(us[qt] - 1) & 1u)))
+          break;
+        if (!(ok = warp_wait(W, bar_pfull + 8 * qt, (uint32_t)(ut[qt] + n - 1) & 1u))) break;
+        tc_fence_after_sync();
+        if (leader) {
+          issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128, base + C::kVOff + svl * C::kTileBytes,
+                      n > 1);
           tc_commit(bar_ofull + 8 * qt);
         }
+        __syncwarp();
+        CFA_TRACE(4, seg, 4 + qt);
       }
-      // Unwind: all issued MMAs have completed before TMEM is released.
-      tc_commit(bar_drain);
-      mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
+      if (!ok) break;
+      if (leader) tc_commit(bar_vempty + 8 * svl);  // V of the segment's last tile
+      __syncwarp();
+      it += n;
+      ++seg;
+      for (int qt = 0; qt < nq; ++qt) {
+        ut[qt] += n;
+        ++us[qt];
+      }
     }
+    // Unwind: all issued MMAs have completed before TMEM is released.
+    if (leader) tc_commit(bar_drain);
+    __syncwarp();
+    mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
   } else {
     // ------------------------------------------------------------- softmax
     const int qt = warp >> 2;
-    if (qt < nq) {
-      const int quad = warp & 3;
-      const int row = quad * 32 + lane;
-      const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
-      const uint32_t s_col = (uint32_t)qt * 128u;
-      const uint32_t o_col = 256u + (uint32_t)(qt * D);
-      const int tok_tile = t0 + qt * tl.tpt;
-      const int token = tok_tile + row / tl.g;
-      const int head = hk * tl.g + row % tl.g;
-      const bool row_valid = row < tl.rows && token < lc;
-      const float sl2 = a.scale_log2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t s_col = (uint32_t)qt * 128u;
+    const uint32_t o_col = 256u + (uint32_t)(qt * D);
+    const float sl2 = a.scale_log2;
+    int u = 0, us = 0;  // tiles and segments this query tile has processed
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      if (qt >= sg.nq) continue;
+      const int n = sg.t_end - sg.t_begin;
+      const int np_t = ceil_div(sg.lp, kTileN);
+      const int token = sg.qb * tok_blk + qt * tl.tpt + row / tl.g;
+      const int head = sg.hk * tl.g + row % tl.g;
+      const bool row_valid = row < tl.rows && token < sg.lc;
       float m = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int i = 0; i < n; ++i) {
-        if (!(ok = warp_wait(W, bar_sfull + 8 * qt, (uint32_t)i & 1u))) break;
+      for (int i = 0; i < n; ++i, ++u) {
+        if (!(ok = warp_wait(W, bar_sfull + 8 * qt, (uint32_t)u & 1u))) break;
+        if (quad == 0 && lane == 0) CFA_TRACE(qt, u, 0);
         tc_fence_after_sync();
-        float s[128];
-        {
-          uint32_t r[128];
-          tmem_ld_x128(t_lane + s_col, r);
-#pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
-        }
-        const int kt = kt0 + i;
+        uint32_t r[128];  // S row; reused in place for the packed P
+        tmem_ld_x128(t_lane + s_col, r);
+        const int kt = sg.t_begin + i;
         // keys [0, lim) of this tile are visible to this row
-        const int lim = (kt < np_t) ? (lp - kt * kTileN) : (token - (kt - np_t) * kTileN + 1);
+        const int lim =
+            (kt < np_t) ? (sg.lp - kt * kTileN) : (token - (kt - np_t) * kTileN + 1);
         if (lim < 128) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+          for (int c = 0; c < 128; ++c) r[c] = (c < lim) ? r[c] : 0xff800000u;  // -inf
         }
         // row max: four independent chains of 3-input maxes
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < 128; c += 8)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) mx4[j] = fmax3(mx4[j], s[c + 2 * j], s[c + 2 * j + 1]);
-        float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
-        mx *= sl2;
+          for (int j = 0; j < 4; ++j)
+            mx4[j] = fmax3(mx4[j], __uint_as_float(r[c + 2 * j]), __uint_as_float(r[c + 2 * j + 1]));
+        const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * sl2;
         const float m_new = fmaxf(m, mx);
         const bool resc = m_new > m + 8.f;
-        if (i > 0 && __any_sync(0xffffffffu, resc)) {
-          // O is quiescent here: the commit behind S_t(i) also covers PV_t(i-1).
-          const float alpha = resc ? ex2_approx(m - m_new) : 1.f;
-#pragma unroll
-          for (int cb = 0; cb < D; cb += 32) {
-            uint32_t r[32];
-            tmem_ld_x32(t_lane + o_col + cb, r);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-            tmem_st_x32(t_lane + o_col + cb, r);
-          }
-          tmem_st_wait();
-        }
+        const float alpha = resc ? ex2_approx(m - m_new) : 1.f;
         if (resc) {
-          l *= ex2_approx(m - m_new);
+          l *= alpha;
           m = m_new;
         }
         const float mref = (m == -INFINITY) ? 0.f : m;
         float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float e0 = ex2_approx(fmaf(s[2 * c], sl2, -mref));
-          const float e1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -mref));
+          const float e0 = ex2_approx(fmaf(__uint_as_float(r[2 * c]), sl2, -mref));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(r[2 * c + 1]), sl2, -mref));
           rs4[c & 3] += e0 + e1;
-          pk[c] = pack_bf16x2(e0, e1);
+          r[c] = pack_bf16x2(e0, e1);  // r[2c], r[2c+1] are no longer needed
         }
-        const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
-        l += rs;
-        tmem_st_x64(t_lane + s_col, pk);
+        l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+        if (quad == 0 && lane == 0) CFA_TRACE(qt, u, 1);
+        tmem_st_x64(t_lane + s_col, reinterpret_cast<const uint32_t(&)[64]>(r));
         tmem_st_wait();
+        if (quad == 0 && lane == 0) CFA_TRACE(qt, u, 2);
+        if (i > 0 && __any_sync(0xffffffffu, resc)) {
+          // O is quiescent here (the commit behind S_t(i) also covers
+          // PV_t(i-1)) and PV_t(i) waits for our arrival below.
+#pragma unroll
+          for (int cb = 0; cb < D; cb += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(t_lane + o_col + cb, o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st_x32(t_lane + o_col + cb, o);
+          }
+          tmem_st_wait();
+        }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_pfull + 8 * qt);
       }
-      if (ok) ok = warp_wait(W, bar_ofull + 8 * qt, 0);
-      if (ok) {
-        tc_fence_after_sync();
-        const bool single = (n_split == 1);
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-        const size_t grow = (size_t)(c0 + token);
+      if (!ok) break;
+      if (!(ok = warp_wait(W, bar_ofull + 8 * qt, (uint32_t)us & 1u))) break;
+      if (quad == 0 && lane == 0) CFA_TRACE(5, us, 2 * qt);
+      tc_fence_after_sync();
+      const bool final_out = !sg.head && !sg.tail;
+      const int slot = sg.head ? 0 : 1;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      const size_t grow = (size_t)(sg.c0 + token);
+      const size_t pslot = (size_t)blockIdx.x * 2 + slot;
+      const int prow_in = qt * kTileM + row;
+      const size_t prow = pslot * rows_blk + prow_in;
 #pragma unroll
-        for (int cb = 0; cb < D; cb += 32) {
-          uint32_t r[32];
-          tmem_ld_x32(t_lane + o_col + cb, r);
-          if (row_valid) {
-            if (single) {
-              uint4* dst = reinterpret_cast<uint4*>(a.o + (grow * a.hq + head) * D + cb);
+      for (int cb = 0; cb < D; cb += 32) {
+        uint32_t r[32];
+        tmem_ld_x32(t_lane + o_col + cb, r);
+        if (row_valid) {
+          if (final_out) {
+            uint4* dst = reinterpret_cast<uint4*>(a.o + (grow * a.hq + head) * D + cb);
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                uint4 u;
-                u.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l,
-                                  __uint_as_float(r[8 * v + 1]) * inv_l);
-                u.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l,
-                                  __uint_as_float(r[8 * v + 3]) * inv_l);
-                u.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l,
-                                  __uint_as_float(r[8 * v + 5]) * inv_l);
-                u.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l,
-                                  __uint_as_float(r[8 * v + 7]) * inv_l);
-                dst[v] = u;
-              }
-            } else {
-              float4* dst = reinterpret_cast<float4*>(
-                  a.o_part + (((size_t)split * a.total_lc + grow) * a.hq + head) * D + cb);
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                dst[v] = make_float4(__uint_as_float(r[4 * v + 0]) * inv_l,
-                                     __uint_as_float(r[4 * v + 1]) * inv_l,
-                                     __uint_as_float(r[4 * v + 2]) * inv_l,
-                                     __uint_as_float(r[4 * v + 3]) * inv_l);
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l,
+                                __uint_as_float(r[8 * v + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l,
+                                __uint_as_float(r[8 * v + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l,
+                                __uint_as_float(r[8 * v + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l,
+                                __uint_as_float(r[8 * v + 7]) * inv_l);
+              dst[v] = w;
             }
+          } else {
+            // feature-major partial [D/4][rows][4]: a warp's store is one
+            // contiguous 512-byte run
+            float4* dst = reinterpret_cast<float4*>(a.o_part) + pslot * (D / 4) * rows_blk +
+                          (size_t)(cb / 4) * rows_blk + prow_in;
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[(size_t)v * rows_blk] = make_float4(__uint_as_float(r[4 * v + 0]) * inv_l,
+                                                      __uint_as_float(r[4 * v + 1]) * inv_l,
+                                                      __uint_as_float(r[4 * v + 2]) * inv_l,
+                                                      __uint_as_float(r[4 * v + 3]) * inv_l);
           }
         }
-        if (row_valid) {
-          if (single)
-            a.lse[(size_t)head * a.total_lc + grow] = lse_v;
-          else
-            a.lse_part[((size_t)split * a.hq + head) * a.total_lc + grow] = lse_v;
-        }
       }
+      if (row_valid) {
+        if (final_out)
+          a.lse[(size_t)head * a.total_lc + grow] = lse_v;
+        else
+          a.lse_part[prow] = lse_v;
+      }
+      if (quad == 0 && lane == 0) CFA_TRACE(5, us, 2 * qt + 1);
+      // O_t may now be overwritten by the next segment's first PV
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ofree + 8 * qt);
+      ++us;
     }
   }
 
@@ -382,46 +464,78 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-// Merge the split partials of every row whose query block was split.
-// One warp per (token, head) row; each lane owns D/32 consecutive columns.
+// Merge the partials of every query block that CTA boundaries cut.  One CTA
+// per (query block, 32 packed rows); thread 0 lists the block's parts once
+// (slot 1 of the first CTA, slot 0 of the others).  Thread t takes row
+// r0 + t % 32 and the column slice t / 32 (of 8), so the lanes of a warp read
+// consecutive rows of the feature-major partials (coalesced).
+constexpr int kMergeRows = 32;
+constexpr int kMaxParts = 1024;
+
 template <int D>
-__global__ void __launch_bounds__(256) fwd_combine_kernel(const FwdArgs a) {
-  constexpr int E = D / 32;
-  const int b = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rid = blockIdx.x * 8 + warp;
-  const int t = rid / a.hq, h = rid % a.hq;
+__global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
+  constexpr int CW = D / 8;  // columns per thread
+  __shared__ int parts[kMaxParts];
+  __shared__ int n_parts;
+  const Tiling tl = a.tl;
+  const int tok_blk = tl.q_per_cta * tl.tpt;
+  const int rows_blk = tl.q_per_cta * kTileM;
+  const int chunks = rows_blk / kMergeRows;
+  const int b = blockIdx.z, hk = blockIdx.y;
+  const int qb = blockIdx.x / chunks;
+  const int r = (blockIdx.x % chunks) * kMergeRows + (threadIdx.x & 31);
+  const int c0col = (threadIdx.x >> 5) * CW;
   const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
   const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
-  if (t >= lc) return;
-  const int tok_blk = a.tl.q_per_cta * a.tl.tpt;
-  const int ns = block_splits(a.tl, lp, lc, t / tok_blk);
-  if (ns <= 1) return;
-  const size_t grow = (size_t)(c0 + t);
+  if (qb >= blocks_of_window(tl, lc)) return;
+  if (threadIdx.x == 0) {
+    long long bs = a.win_prefix[b] + (long long)hk * head_work(tl, lp, lc);
+    for (int q = 0; q < qb; ++q) bs += block_key_tiles(lp, lc, q * tok_blk, tok_blk);
+    const long long be = bs + block_key_tiles(lp, lc, qb * tok_blk, tok_blk);
+    n_parts = block_parts(bs, be, a.win_prefix[a.batch], tl.grid, parts, kMaxParts);
+  }
+  __syncthreads();
+  const int np = n_parts;
+  if (np == 0) return;
+  const int qt = r / kTileM, row = r % kTileM;
+  const int token = qb * tok_blk + qt * tl.tpt + row / tl.g;
+  if (row >= tl.rows || token >= lc) return;
+  const int head = hk * tl.g + row % tl.g;
   float mx = -INFINITY;
-  for (int s = 0; s < ns; ++s)
-    mx = fmaxf(mx, a.lse_part[((size_t)s * a.hq + h) * a.total_lc + grow]);
+  for (int j = 0; j < np; ++j)
+    mx = fmaxf(mx, a.lse_part[((size_t)parts[j] * 2 + (j == 0)) * rows_blk + r]);
   float sum = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float ls = a.lse_part[((size_t)s * a.hq + h) * a.total_lc + grow];
+  for (int j = 0; j < np; ++j) {
+    const float ls = a.lse_part[((size_t)parts[j] * 2 + (j == 0)) * rows_blk + r];
     sum += (ls == -INFINITY) ? 0.f : expf(ls - mx);
   }
   const float lse = mx + logf(sum);
-  float acc[E];
+  float acc[CW];
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float ls = a.lse_part[((size_t)s * a.hq + h) * a.total_lc + grow];
+  for (int e = 0; e < CW; ++e) acc[e] = 0.f;
+  for (int j = 0; j < np; ++j) {
+    const size_t slot = (size_t)parts[j] * 2 + (j == 0);
+    const float ls = a.lse_part[slot * rows_blk + r];
     if (ls == -INFINITY) continue;
     const float w = expf(ls - lse);
-    const float* src = a.o_part + (((size_t)s * a.total_lc + grow) * a.hq + h) * D + lane * E;
+    const float4* src = reinterpret_cast<const float4*>(a.o_part) + slot * (D / 4) * rows_blk;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+    for (int e = 0; e < CW; e += 4) {
+      const float4 v = src[(size_t)((c0col + e) >> 2) * rows_blk + r];
+      acc[e] = fmaf(w, v.x, acc[e]);
+      acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+      acc[e + 2] = fmaf(w, v.z, acc[e + 2]);
+      acc[e + 3] = fmaf(w, v.w, acc[e + 3]);
+    }
   }
-  __nv_bfloat16* dst = a.o + (grow * a.hq + h) * D + lane * E;
+  const size_t grow = (size_t)(c0 + token);
+  uint4* dst = reinterpret_cast<uint4*>(a.o + (grow * a.hq + head) * D + c0col);
 #pragma unroll
-  for (int e = 0; e < E; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e], acc[e + 1]);
-  if (lane == 0) a.lse[(size_t)h * a.total_lc + grow] = lse;
+  for (int e = 0; e < CW; e += 8)
+    dst[e / 8] = make_uint4(pack_bf16x2(acc[e], acc[e + 1]), pack_bf16x2(acc[e + 2], acc[e + 3]),
+                            pack_bf16x2(acc[e + 4], acc[e + 5]),
+                            pack_bf16x2(acc[e + 6], acc[e + 7]));
+  if (threadIdx.x < 32) a.lse[(size_t)head * a.total_lc + grow] = lse;
 }
 
 }  // namespace
@@ -431,9 +545,9 @@ int fwd_smem_bytes(int d, int q8) {
   return d == 128 ? FwdCfg<128>::kSmemBytes : FwdCfg<64>::kSmemBytes;
 }
 
-cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, int q8, dim3 grid,
-                       cudaStream_t st) {
+cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, int q8, cudaStream_t st) {
   (void)q8;
+  const dim3 grid((unsigned)a.tl.grid);
   if (d == 128) {
     auto k = fwd_kernel<128>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -450,14 +564,27 @@ cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, int q8, dim3 grid
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_combine(const FwdArgs& a, int d, int batch, int max_lc, cudaStream_t st) {
-  const long long rows = (long long)max_lc * a.hq;
-  dim3 grid((unsigned)((rows + 7) / 8), (unsigned)batch);
+cudaError_t launch_fwd_merge(const FwdArgs& a, int d, int max_lc, cudaStream_t st) {
+  const int rows_blk = a.tl.q_per_cta * kTileM;
+  const int nblk = ceil_div(max_lc > 0 ? max_lc : 1, a.tl.q_per_cta * a.tl.tpt);
+  dim3 grid((unsigned)(nblk * (rows_blk / kMergeRows)), (unsigned)a.hkv, (unsigned)a.batch);
   if (d == 128)
-    fwd_combine_kernel<128><<<grid, 256, 0, st>>>(a);
+    fwd_merge_kernel<128><<<grid, 256, 0, st>>>(a);
   else
-    fwd_combine_kernel<64><<<grid, 256, 0, st>>>(a);
+    fwd_merge_kernel<64><<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace cfa
+
+#ifdef CFA_TRACE_BUILD
+extern "C" int cfa_trace_read_fwd(long long* dst, int clear) {
+  const size_t n = sizeof(long long) * cfa::kTraceRoles * cfa::kTraceIters * cfa::kTraceEvents;
+  if (dst && cudaMemcpyFromSymbol(dst, cfa::cfa_trace_buf, n) != cudaSuccess) return -1;
+  if (clear) {
+    static long long zero[cfa::kTraceRoles * cfa::kTraceIters * cfa::kTraceEvents];
+    if (cudaMemcpyToSymbol(cfa::cfa_trace_buf, zero, n) != cudaSuccess) return -1;
+  }
+  return 0;
+}
+#endif

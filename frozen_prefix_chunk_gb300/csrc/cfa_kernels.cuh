@@ -21,22 +21,25 @@ constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s
 struct FwdArgs {
   const int32_t* cu_p;
   const int32_t* cu_c;
-  int hq, hkv, total_lc;
+  long long* win_prefix;  // [batch + 1], written by CTA 0 for the merge kernel
+  int batch, hq, hkv, total_lc;
   Tiling tl;
   float scale_log2;      // softmax_scale * log2(e)
   __nv_bfloat16* o;      // [total_lc, hq, D]
   float* lse;            // [hq, total_lc]
-  float* o_part;         // [n_split_max, total_lc, hq, D]   (split partials)
-  float* lse_part;       // [n_split_max, hq, total_lc]
+  float* o_part;         // [grid, 2, rows per block, D]  partials of cut blocks
+  float* lse_part;       // [grid, 2, rows per block]
   int* status;           // workspace status word
   unsigned long long limit_ns;
+  int debug_wait_never;  // test hook: the MMA thread waits on a barrier nobody sets
 };
 
 struct BwdArgs {
   const int32_t* cu_p;
   const int32_t* cu_c;
-  int hq, hkv, total_lc;
-  Tiling tl;             // dQ tiling (one query tile per CTA)
+  long long* win_prefix;  // [batch + 1], written by CTA 0 for the reduce kernel
+  int batch, hq, hkv, total_lc;
+  Tiling tl;             // dQ tiling (one query tile per block)
   float scale_log2;
   float scale;
   const float* lse;      // [hq, total_lc]
@@ -44,9 +47,10 @@ struct BwdArgs {
   __nv_bfloat16* dq;     // [total_lc, hq, D]
   __nv_bfloat16* dk;     // [total_lc, hkv, D]
   __nv_bfloat16* dv;     // [total_lc, hkv, D]
-  float* dq_part;        // [n_split_max, total_lc, hq, D]
+  float* dq_part;        // [grid, 2, 128, D]  partials of cut query tiles
   int* status;
   unsigned long long limit_ns;
+  int debug_wait_never;  // test hook: the MMA thread waits on a barrier nobody sets
 };
 
 // The five TMA descriptors of one call.  Prefix maps describe bf16 K/V
@@ -58,16 +62,14 @@ struct Maps {
 
 // Launchers (return a cudaError_t of the launch).
 int fwd_smem_bytes(int d, int q8);
-cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, int q8, dim3 grid,
-                       cudaStream_t st);
-cudaError_t launch_fwd_combine(const FwdArgs& a, int d, int batch, int max_lc, cudaStream_t st);
+cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, int q8, cudaStream_t st);
+cudaError_t launch_fwd_merge(const FwdArgs& a, int d, int max_lc, cudaStream_t st);
 
 int bwd_dq_smem_bytes(int d, int q8);
 int bwd_dkdv_smem_bytes(int d);
-cudaError_t launch_bwd_dq(const Maps& m, const BwdArgs& a, int d, int q8, dim3 grid,
-                          cudaStream_t st);
+cudaError_t launch_bwd_dq(const Maps& m, const BwdArgs& a, int d, int q8, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, dim3 grid, cudaStream_t st);
-cudaError_t launch_bwd_dq_reduce(const BwdArgs& a, int d, int batch, int max_lc, cudaStream_t st);
+cudaError_t launch_bwd_dq_reduce(const BwdArgs& a, int d, int max_lc, cudaStream_t st);
 cudaError_t launch_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta,
                          int total_lc, int hq, int d, cudaStream_t st);
 cudaError_t launch_dequant_prefix(const uint8_t* blocks, long long n_blocks, __nv_bfloat16* out,

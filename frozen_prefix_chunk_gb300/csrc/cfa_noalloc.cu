@@ -24,7 +24,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
+constexpr size_t kScratchBytes = size_t(48) << 20;  // 48 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];

@@ -11,6 +11,25 @@
 
 namespace cfa {
 
+// Pipeline tracing for timeline probes.  Compiled out unless the library is
+// built with -DCFA_TRACE_BUILD; then CTA 0 of each kernel records clock64()
+// per (role, iteration, event) into its translation unit's cfa_trace_buf,
+// read back with cfa_trace_read_fwd() / cfa_trace_read_bwd().
+#ifdef CFA_TRACE_BUILD
+constexpr int kTraceRoles = 6, kTraceIters = 96, kTraceEvents = 8;
+static __device__ long long cfa_trace_buf[kTraceRoles * kTraceIters * kTraceEvents];
+#define CFA_TRACE(role, iter, ev)                                                          \
+  do {                                                                                     \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (iter) < cfa::kTraceIters) \
+      cfa::cfa_trace_buf[((role) * cfa::kTraceIters + (iter)) * cfa::kTraceEvents + (ev)] = \
+          clock64();                                                                       \
+  } while (0)
+#else
+#define CFA_TRACE(role, iter, ev) \
+  do {                            \
+  } while (0)
+#endif
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

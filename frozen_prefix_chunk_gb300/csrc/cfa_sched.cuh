@@ -6,12 +6,23 @@
 // tile therefore reads the same K/V tiles, and the causal edge of a tile spans
 // only tpt tokens.
 //
-// The keys of a window are walked as one list of 128-row tiles: the ceil(Lp /
-// 128) prefix tiles first, then the chunk tiles that some row of the query
-// block can see (chunk key j is visible to token t iff j <= t; the prefix is
-// fully visible).  A query block's list is cut into splits of
-// `tiles_per_split` tiles; each split is one CTA, and its partial (O, LSE) or
-// dQ is merged afterwards when a block has more than one split.
+// A query block is q_per_cta consecutive query tiles of one (window, KV head).
+// Its keys are walked as one list of 128-row tiles: the ceil(Lp / 128) prefix
+// tiles first, then the chunk tiles some row of the block can see (chunk key
+// j is visible to token t iff j <= t; the whole prefix is visible).
+//
+// Stream-K schedule.  The iterations (query block, key tile) are numbered
+// window-major, then KV head, then query block, then key tile; W is their
+// total.  A persistent grid of G CTAs gives CTA c the contiguous range
+// [floor(c W / G), floor((c+1) W / G)), so every CTA does the same amount of
+// tensor work whatever the window lengths.  A CTA walks its range as
+// segments, one per query block it touches.  A segment that covers its whole
+// block writes the final outputs; a block cut by CTA boundaries leaves one
+// partial per CTA, in slot 1 of the CTA holding its start and slot 0 of the
+// others, and a merge kernel combines them in CTA order (deterministic).
+// Every CTA scans the per-window work itself in its prologue (plan_schedule
+// below); CTA 0 also stores the prefix array win_prefix[b] (int64, [batch +
+// 1]) for the merge kernels that run afterwards.
 #pragma once
 
 #include <stdint.h>
@@ -22,13 +33,11 @@ constexpr int kTileM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kTileN = 128;  // keys per tile
 
 struct Tiling {
-  int g;                // query heads per KV head
-  int tpt;              // chunk tokens per query tile
-  int rows;             // valid rows per query tile = tpt * g
-  int q_per_cta;        // query tiles per CTA (a query block)
-  int tiles_per_split;  // key tiles per split
-  int n_qblk_max;       // query blocks per window, upper bound
-  int n_split_max;      // splits per query block, upper bound
+  int g;          // query heads per KV head
+  int tpt;        // chunk tokens per query tile
+  int rows;       // valid rows per query tile = tpt * g
+  int q_per_cta;  // query tiles per query block
+  int grid;       // persistent CTAs (G)
 };
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -40,9 +49,178 @@ __host__ __device__ inline int block_key_tiles(int lp, int lc, int t0, int tok_b
   return ceil_div(lp, kTileN) + ceil_div(t_hi, kTileN);
 }
 
-__host__ __device__ inline int block_splits(const Tiling& tl, int lp, int lc, int qblk) {
+__host__ __device__ inline int blocks_of_window(const Tiling& tl, int lc) {
+  return lc > 0 ? ceil_div(lc, tl.q_per_cta * tl.tpt) : 0;
+}
+
+// Iterations of one KV head's query blocks in a window.
+__host__ __device__ inline long long head_work(const Tiling& tl, int lp, int lc) {
   const int tok_blk = tl.q_per_cta * tl.tpt;
-  return ceil_div(block_key_tiles(lp, lc, qblk * tok_blk, tok_blk), tl.tiles_per_split);
+  long long w = 0;
+  for (int qb = 0, nb = blocks_of_window(tl, lc); qb < nb; ++qb)
+    w += block_key_tiles(lp, lc, qb * tok_blk, tok_blk);
+  return w;
+}
+
+// First iteration of CTA c, and the CTA that holds iteration x.
+__host__ __device__ inline long long cta_begin(long long c, long long W, int G) {
+  return c * W / G;
+}
+__host__ __device__ inline int cta_of(long long x, long long W, int G) {
+  return (int)(((x + 1) * G - 1) / W);
+}
+
+// One contiguous piece of a CTA's range inside one query block.
+struct Segment {
+  int b, hk, qb;         // the query block
+  int p0, lp, c0, lc;    // its window
+  int n_kt;              // key tiles of the block
+  int t_begin, t_end;    // key tiles [t_begin, t_end) of this segment
+  int nq;                // query tiles of the block that hold rows
+  bool head;             // the block started in an earlier CTA
+  bool tail;             // the block continues in a later CTA
+};
+
+// Walks a CTA's iteration range segment by segment.  Every role of the CTA
+// runs its own copy and sees the same sequence.
+struct SegmentWalker {
+  const int32_t* cu_p;
+  const int32_t* cu_c;
+  int batch, hkv;
+  Tiling tl;
+  long long cur, end;
+  int b, hk, qb, tile;
+
+  // Start at CTA `cta`'s first iteration: window b0 (whose first iteration
+  // is pre_b0) of a schedule with `total` iterations.
+  __device__ void init(const int32_t* cp, const int32_t* cc, int nb, int nkv, const Tiling& t,
+                       int cta, long long total, int b0, long long pre_b0) {
+    cu_p = cp;
+    cu_c = cc;
+    batch = nb;
+    hkv = nkv;
+    tl = t;
+    cur = cta_begin(cta, total, t.grid);
+    end = cta_begin(cta + 1, total, t.grid);
+    if (cur >= end) return;
+    b = b0;
+    const int lp = cu_p[b + 1] - cu_p[b], lc = cu_c[b + 1] - cu_c[b];
+    const long long hw = head_work(tl, lp, lc);
+    long long o = cur - pre_b0;
+    hk = (int)(o / hw);
+    o -= (long long)hk * hw;
+    const int tok_blk = tl.q_per_cta * tl.tpt;
+    qb = 0;
+    for (;;) {
+      const int nk = block_key_tiles(lp, lc, qb * tok_blk, tok_blk);
+      if (o < nk) break;
+      o -= nk;
+      ++qb;
+    }
+    tile = (int)o;
+  }
+
+  __device__ bool next(Segment& s) {
+    if (cur >= end) return false;
+    const int tok_blk = tl.q_per_cta * tl.tpt;
+    s.b = b;
+    s.hk = hk;
+    s.qb = qb;
+    s.p0 = cu_p[b];
+    s.lp = cu_p[b + 1] - s.p0;
+    s.c0 = cu_c[b];
+    s.lc = cu_c[b + 1] - s.c0;
+    s.n_kt = block_key_tiles(s.lp, s.lc, qb * tok_blk, tok_blk);
+    s.t_begin = tile;
+    const long long left = end - cur;
+    s.t_end = (left < (long long)(s.n_kt - tile)) ? tile + (int)left : s.n_kt;
+    s.nq = ceil_div(s.lc - qb * tok_blk, tl.tpt);
+    if (s.nq > tl.q_per_cta) s.nq = tl.q_per_cta;
+    s.head = tile > 0;
+    s.tail = s.t_end < s.n_kt;
+    cur += s.t_end - s.t_begin;
+    // advance to the next query block
+    tile = 0;
+    if (++qb >= blocks_of_window(tl, s.lc)) {
+      qb = 0;
+      if (++hk >= hkv) {
+        hk = 0;
+        do {
+          ++b;
+        } while (b < batch && cu_c[b + 1] - cu_c[b] == 0);
+      }
+    }
+    return true;
+  }
+};
+
+// The CTAs holding parts of the block whose iterations are [bs, be), in CTA
+// order: the one holding bs, then every later one up to the one holding
+// be - 1 whose range is not empty (ranges are only empty when there are fewer
+// iterations than CTAs).  Returns the count; 0 when one CTA holds the whole
+// block.  `parts` has room for `cap` entries.
+__device__ inline int block_parts(long long bs, long long be, long long total, int G, int* parts,
+                                  int cap) {
+  const int cf = cta_of(bs, total, G), cl = cta_of(be - 1, total, G);
+  if (cf == cl) return 0;
+  int n = 0;
+  for (int c = cf; c <= cl && n < cap; ++c) {
+    if (c > cf && total < G && cta_begin(c, total, G) == cta_begin(c + 1, total, G)) continue;
+    parts[n++] = c;
+  }
+  return n;
+}
+
+// Prologue of the persistent kernels, run by all `nthreads` threads of the
+// CTA: scans the per-window iteration counts (each thread sums a contiguous
+// run of windows; warp shuffles and a shared array of warp totals turn the
+// run sums into prefixes), finds the window holding this CTA's first
+// iteration, and lets CTA 0 store the prefix array for the merge kernels.
+// Results land in *total, *b0 and *pre_b0 (shared memory) after the closing
+// __syncthreads.  `warp_tot` needs one slot per warp.
+__device__ inline void plan_schedule(const int32_t* cu_p, const int32_t* cu_c, int batch, int hkv,
+                                     const Tiling& tl, long long* win_prefix_out,
+                                     long long* warp_tot, long long* total, int* b0,
+                                     long long* pre_b0) {
+  const int t = threadIdx.x, nt = blockDim.x;
+  const int lane = t & 31, warp = t >> 5, nwarps = nt >> 5;
+  const int per = ceil_div(batch, nt);
+  const int w0 = t * per;
+  const int w1 = (w0 + per < batch) ? w0 + per : batch;
+  long long sum = 0;
+  for (int b = w0; b < w1; ++b)
+    sum += (long long)hkv * head_work(tl, cu_p[b + 1] - cu_p[b], cu_c[b + 1] - cu_c[b]);
+  long long inc = sum;  // inclusive scan within the warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long v = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += v;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  long long base = 0, all = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    const long long v = warp_tot[w];
+    if (w < warp) base += v;
+    all += v;
+  }
+  long long run = base + inc - sum;  // exclusive prefix of window w0
+  const long long start = cta_begin(blockIdx.x, all, tl.grid);
+  for (int b = w0; b < w1; ++b) {
+    const long long wb =
+        (long long)hkv * head_work(tl, cu_p[b + 1] - cu_p[b], cu_c[b + 1] - cu_c[b]);
+    if (blockIdx.x == 0) win_prefix_out[b] = run;
+    if (wb > 0 && run <= start && start < run + wb) {
+      *b0 = b;
+      *pre_b0 = run;
+    }
+    run += wb;
+  }
+  if (t == 0) {
+    *total = all;
+    if (blockIdx.x == 0) win_prefix_out[batch] = all;
+  }
+  __syncthreads();
 }
 
 }  // namespace cfa

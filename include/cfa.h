@@ -151,7 +151,7 @@ int cfa_dequant_q8_0(const void* blocks, long long n_blocks, float* out_f32, voi
  * the memory up front, or a C program whose device memory comes only from
  * someone else's pool.  The pages have no counterpart to this entry point.
  * Same inputs and outputs as cfa_forward; the split partials live in a
- * fixed array of cfa_noalloc_scratch_bytes() bytes (32 MiB) inside the
+ * fixed array of cfa_noalloc_scratch_bytes() bytes (48 MiB) inside the
  * library, which every GPU that runs this call holds until the process
  * exits.  The first call on a device looks up that array's address (this
  * loads the module that holds it), so make it before any stream capture.

@@ -63,12 +63,12 @@ def test_noalloc_forward_refuses_requests_beyond_its_scratch():
     import frozen_prefix_chunk_gb300 as cfa
 
     cfa.lib(build_if_missing=True)
-    # a long prefix split several ways over many query blocks needs more
-    # partials than the fixed array; take the first shape whose forward
-    # workspace is larger than the scratch on this GPU
+    # a q8_0 prefix is expanded to bf16 in the workspace, so a long one needs
+    # more than the fixed array; take the first shape that does on this GPU
     limit = cfa.lib().cfa_noalloc_scratch_bytes()
-    for lc, lp in ((768, 60000), (768, 120000), (1536, 120000), (3072, 120000)):
-        w = synth.custom(hq=32, hkv=8, head_dim=128, lp=[lp], lc=[lc], seed=0)
+    for lp in (20000, 60000, 120000):
+        w = synth.custom(hq=32, hkv=8, head_dim=128, lp=[lp], lc=[256],
+                         prefix_dtype=synth.PREFIX_Q8_0, seed=0)
         d = gu.to_device(synth.make_inputs(w))
         args = gu.make_args(d)
         if cfa.workspace_size(args, cfa.WS_FORWARD) > limit:
