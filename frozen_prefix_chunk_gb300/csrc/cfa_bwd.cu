@@ -42,11 +42,12 @@ __device__ __forceinline__ uint32_t staged_col(int k) {
 template <int D>
 __device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+  constexpr uint32_t hi = sw128_desc_hi(1024);
+  const uint32_t a_lo = sw128_desc_lo(a_addr, 16), b_lo = sw128_desc_lo(b_addr, 16);
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
-    const uint32_t off = (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
-    mma_bf16_ss(d_tmem, smem_desc_sw128(a_addr + off, 16, 1024),
-                smem_desc_sw128(b_addr + off, 16, 1024), idesc, k > 0 ? 1u : 0u);
+    const uint32_t off = ((uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u) >> 4;
+    mma_bf16_ss_hl(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, k > 0 ? 1u : 0u);
   }
 }
 
@@ -55,12 +56,12 @@ template <int D>
 __device__ __forceinline__ void issue_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_addr,
                                          bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
+  constexpr uint32_t hi = sw128_desc_hi(1024);
+  const uint32_t b_lo = sw128_desc_lo(b_addr, kBoxBytes);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    mma_bf16_ts(d_tmem, a_tmem + staged_col(k),
-                smem_desc_sw128(b_addr + (uint32_t)k * 2048u, kBoxBytes, 1024), idesc,
-                (accumulate || k > 0) ? 1u : 0u);
-  }
+  for (int k = 0; k < 8; ++k)
+    mma_bf16_ts_hl(d_tmem, a_tmem + staged_col(k), b_lo + (uint32_t)k * (2048u >> 4), hi, idesc,
+                   (accumulate || k > 0) ? 1u : 0u);
 }
 
 template <int D>
@@ -145,7 +146,6 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_sfull, 1);
     mbar_init(bar_sfull + 8, 1);
     mbar_init(bar_dpfull, 1);
-    mbar_init(bar_dpfree, 8);
     mbar_init(bar_dsfull, 8);
     mbar_init(bar_dqfull, 1);
     mbar_init(bar_dqfree, 8);
@@ -222,11 +222,12 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = (issued_v > SV ? issued_v - SV : 0); i < issued_v; ++i)
       mbar_wait_bounded(bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u, kDrainLimitNs);
   } else if (warp == 9) {
-    // Issue order per key tile g:  S(g), dP(g), dQ(g-1).  dP(g) needs only
-    // that dP(g-1) has been read, so it runs while dS(g-1) is computed.  The
-    // waits for K / V of the next tile sit at the end of the iteration, off
-    // the critical path.  Tile counters run across segments.  The whole warp
-    // waits (converged); lane 0 issues the MMAs and commits.
+    // Issue order per key tile g:  S(g), dP(g), dQ(g-1), after a single wait
+    // for dS(g-1).  The tensor pipe holds about one MMA beyond the one
+    // executing, so every wait here is a bubble; dS(g-1) being ready implies
+    // that dP(g-1) has been read, and the elementwise warps wait for K(g) and
+    // V(g) before they hand over dS(g-1).  Tile counters run across segments.
+    // The whole warp waits (converged); lane 0 issues the MMAs and commits.
     const bool leader = lane == 0;
     const uint32_t t_dq = tmem + 384;
     int it = 0, seg = 0;
@@ -239,42 +240,30 @@ __global__ void __launch_bounds__(320, 1)
       if (!(ok = warp_wait(W, bar_vfull + 8 * (it % SV), (uint32_t)(it / SV) & 1u))) break;
       for (int i = 0; ok && i < n; ++i) {
         const int g = it + i;
-        const int sk = g % SK, sv = g % SV;
-        if (leader) {
-          issue_nt<D>(tmem + (uint32_t)(g & 1) * 128u, base + C::kQOff,
-                      base + C::kKOff + sk * C::kTileBytes);
-          tc_commit(bar_sfull + 8 * (g & 1));
-        }
-        __syncwarp();
-        if (g > 0 && !(ok = warp_wait(W, bar_dpfree, (uint32_t)(g - 1) & 1u))) break;
-        tc_fence_after_sync();
-        if (leader) {
-          issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + sv * C::kTileBytes);
-          tc_commit(bar_dpfull);
-          tc_commit(bar_vempty + 8 * sv);
-          if (i == n - 1) tc_commit(bar_qempty);  // last S and dP of the segment
-        }
-        __syncwarp();
+        const int sk = g % SK, sv = g % SV, skp = (g + SK - 1) % SK;
         if (i > 0) {
-          const int skp = (g - 1) % SK;
           // the first dQ of a segment overwrites the accumulator: the previous
           // segment's epilogue must have read it
           if (i == 1 && seg > 0 && !(ok = warp_wait(W, bar_dqfree, (uint32_t)(seg - 1) & 1u)))
             break;
           if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)(g - 1) & 1u))) break;
           tc_fence_after_sync();
-          if (leader) {
+        }
+        if (leader) {
+          issue_nt<D>(tmem + (uint32_t)(g & 1) * 128u, base + C::kQOff,
+                      base + C::kKOff + sk * C::kTileBytes);
+          tc_commit(bar_sfull + 8 * (g & 1));
+          issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + sv * C::kTileBytes);
+          tc_commit(bar_dpfull);
+          tc_commit(bar_vempty + 8 * sv);
+          if (i == n - 1) tc_commit(bar_qempty);  // last S and dP of the segment
+          if (i > 0) {
             issue_tn<D>(t_dq, tmem + (uint32_t)((g - 1) & 1) * 128u,
                         base + C::kKOff + skp * C::kTileBytes, i - 1 > 0);
             tc_commit(bar_kempty + 8 * skp);
           }
-          __syncwarp();
         }
-        if (i + 1 < n) {
-          const int j = g + 1;
-          if (!(ok = warp_wait(W, bar_kfull + 8 * (j % SK), (uint32_t)(j / SK) & 1u))) break;
-          if (!(ok = warp_wait(W, bar_vfull + 8 * (j % SV), (uint32_t)(j / SV) & 1u))) break;
-        }
+        __syncwarp();
       }
       if (!ok) break;
       const int gl = it + n - 1, skl = gl % SK;
@@ -335,9 +324,6 @@ __global__ void __launch_bounds__(320, 1)
         {
           uint32_t r[64];
           tmem_ld_x64(t_lane + 256 + half * 64, r);
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_dpfree);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             pk[j] = pack_bf16x2(p[2 * j] * (__uint_as_float(r[2 * j]) - dl),
@@ -345,6 +331,13 @@ __global__ void __launch_bounds__(320, 1)
         }
         tmem_st_x32(t_lane + sb, pk);
         tmem_st_wait();
+        if (warp == 0 && i + 1 < n) {
+          // K and V of the next tile are in shared memory before dS(u) is
+          // handed over, so the MMA warp need not wait for them itself
+          const int v = u + 1;
+          if (!(ok = warp_wait(W, bar_kfull + 8 * (v % SK), (uint32_t)(v / SK) & 1u))) break;
+          if (!(ok = warp_wait(W, bar_vfull + 8 * (v % SV), (uint32_t)(v / SV) & 1u))) break;
+        }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_dsfull);

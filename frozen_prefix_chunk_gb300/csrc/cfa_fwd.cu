@@ -59,11 +59,12 @@ struct FwdCfg {
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+  constexpr uint32_t hi = sw128_desc_hi(1024);
+  const uint32_t a_lo = sw128_desc_lo(a_addr, 16), b_lo = sw128_desc_lo(b_addr, 16);
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
-    const uint32_t off = (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
-    mma_bf16_ss(d_tmem, smem_desc_sw128(a_addr + off, 16, 1024),
-                smem_desc_sw128(b_addr + off, 16, 1024), idesc, k > 0 ? 1u : 0u);
+    const uint32_t off = ((uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u) >> 4;
+    mma_bf16_ss_hl(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, k > 0 ? 1u : 0u);
   }
 }
 
@@ -74,12 +75,12 @@ template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr,
                                          bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
+  constexpr uint32_t hi = sw128_desc_hi(1024);
+  const uint32_t b_lo = sw128_desc_lo(v_addr, kBoxBytes);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    mma_bf16_ts(d_tmem, p_tmem + (uint32_t)(k * 8),
-                smem_desc_sw128(v_addr + (uint32_t)k * 2048u, kBoxBytes, 1024), idesc,
-                (accumulate || k > 0) ? 1u : 0u);
-  }
+  for (int k = 0; k < 8; ++k)
+    mma_bf16_ts_hl(d_tmem, p_tmem + (uint32_t)(k * 8), b_lo + (uint32_t)k * (2048u >> 4), hi,
+                   idesc, (accumulate || k > 0) ? 1u : 0u);
 }
 
 template <int D>
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* gbase = smem_raw + (base - raw_base);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  CFA_TRACE_CTA(0);
   const Tiling tl = a.tl;
   const int tok_blk = tl.q_per_cta * tl.tpt;
   const int rows_blk = tl.q_per_cta * kTileM;
@@ -232,10 +234,11 @@ __global__ void __launch_bounds__(320, 1)
     // Issue order per key tile i of a segment:  PV0(i-1) S0(i) PV1(i-1)
     // S1(i).  PV of the previous tile goes first (it does not need K(i));
     // S_t(i) reuses the TMEM columns of P_t(i-1), which the in-order MMA
-    // pipe has consumed.  The K(i+1) / V(i) waits sit at the end of the
-    // iteration, where the tensor pipe is still busy, so only the P
-    // hand-offs remain on the critical path.  The whole warp waits
-    // (converged); lane 0 issues the MMAs and commits.
+    // pipe has consumed.  The tensor pipe holds about one MMA beyond the one
+    // executing, so every wait here is a bubble: the softmax warps of query
+    // tile 0 wait for K(i+1) and V(i) before they hand over P0(i), and this
+    // warp waits only for the P hand-offs (and K at a segment's start).  The
+    // whole warp waits (converged); lane 0 issues the MMAs and commits.
     const bool leader = lane == 0;
     int it = 0, seg = 0;
     int ut[2] = {0, 0}, us[2] = {0, 0};  // per query tile: tiles, segments done
@@ -252,7 +255,9 @@ __global__ void __launch_bounds__(320, 1)
       for (int i = 0; ok && i < n; ++i) {
         const int g = it + i;
         const int sk = g % SK, svp = (g + SV - 1) % SV;
-        for (int qt = 0; qt < nq; ++qt) {
+#pragma unroll
+        for (int qt = 0; qt < 2; ++qt) {
+          if (qt >= nq) break;
           if (i > 0) {
             // the first PV of a segment overwrites O_t: the previous
             // segment's epilogue must have read it
@@ -280,15 +285,13 @@ __global__ void __launch_bounds__(320, 1)
           CFA_TRACE(2, it + i, 2 * qt + 1);
         }
         if (!ok) break;
-        if (i + 1 < n &&
-            !(ok = warp_wait(W, bar_kfull + 8 * ((g + 1) % SK), (uint32_t)((g + 1) / SK) & 1u)))
-          break;
-        ok = warp_wait(W, bar_vfull + 8 * (g % SV), (uint32_t)(g / SV) & 1u);
         CFA_TRACE(2, g, 4);
       }
       if (!ok) break;
       const int gl = it + n - 1, svl = gl % SV;
-      for (int qt = 0; ok && qt < nq; ++qt) {
+#pragma unroll
+      for (int qt = 0; qt < 2; ++qt) {
+        if (!ok || qt >= nq) break;
         if (n == 1 && us[qt] > 0 &&
             !(ok = warp_wait(W, bar_ofree + 8 * qt, (uint32_t)(us[qt] - 1) & 1u)))
           break;
@@ -307,9 +310,12 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       it += n;
       ++seg;
-      for (int qt = 0; qt < nq; ++qt) {
-        ut[qt] += n;
-        ++us[qt];
+#pragma unroll
+      for (int qt = 0; qt < 2; ++qt) {
+        if (qt < nq) {
+          ut[qt] += n;
+          ++us[qt];
+        }
       }
     }
     // Unwind: all issued MMAs have completed before TMEM is released.
@@ -391,6 +397,14 @@ __global__ void __launch_bounds__(320, 1)
           }
           tmem_st_wait();
         }
+        if (qt == 0 && quad == 0) {
+          // tile u's V and tile u+1's K are in shared memory before P0(u) is
+          // handed over, so the MMA warp need not wait for them itself
+          if (!(ok = warp_wait(W, bar_vfull + 8 * (u % SV), (uint32_t)(u / SV) & 1u))) break;
+          if (i + 1 < n &&
+              !(ok = warp_wait(W, bar_kfull + 8 * ((u + 1) % SK), (uint32_t)((u + 1) / SK) & 1u)))
+            break;
+        }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_pfull + 8 * qt);
@@ -458,6 +472,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  CFA_TRACE_CTA(1);
   if (warp == 9) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
@@ -578,6 +593,11 @@ cudaError_t launch_fwd_merge(const FwdArgs& a, int d, int max_lc, cudaStream_t s
 }  // namespace cfa
 
 #ifdef CFA_TRACE_BUILD
+extern "C" int cfa_trace_read_cta_fwd(unsigned long long* dst) {
+  return cudaMemcpyFromSymbol(dst, cfa::cfa_trace_cta, sizeof(unsigned long long) * 2048) ==
+                 cudaSuccess ? 0 : -1;
+}
+
 extern "C" int cfa_trace_read_fwd(long long* dst, int clear) {
   const size_t n = sizeof(long long) * cfa::kTraceRoles * cfa::kTraceIters * cfa::kTraceEvents;
   if (dst && cudaMemcpyFromSymbol(dst, cfa::cfa_trace_buf, n) != cudaSuccess) return -1;

@@ -15,9 +15,21 @@ namespace cfa {
 // built with -DCFA_TRACE_BUILD; then CTA 0 of each kernel records clock64()
 // per (role, iteration, event) into its translation unit's cfa_trace_buf,
 // read back with cfa_trace_read_fwd() / cfa_trace_read_bwd().
+__device__ __forceinline__ unsigned long long global_timer_ns_raw() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 #ifdef CFA_TRACE_BUILD
 constexpr int kTraceRoles = 6, kTraceIters = 96, kTraceEvents = 8;
 static __device__ long long cfa_trace_buf[kTraceRoles * kTraceIters * kTraceEvents];
+static __device__ unsigned long long cfa_trace_cta[2 * 1024];  // per-CTA start / end (ns)
+#define CFA_TRACE_CTA(ev)                                                     \
+  do {                                                                        \
+    if (threadIdx.x == 0 && blockIdx.x < 1024)                                \
+      cfa::cfa_trace_cta[2 * blockIdx.x + (ev)] = cfa::global_timer_ns_raw(); \
+  } while (0)
 #define CFA_TRACE(role, iter, ev)                                                          \
   do {                                                                                     \
     if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (iter) < cfa::kTraceIters) \
@@ -27,6 +39,9 @@ static __device__ long long cfa_trace_buf[kTraceRoles * kTraceIters * kTraceEven
 #else
 #define CFA_TRACE(role, iter, ev) \
   do {                            \
+  } while (0)
+#define CFA_TRACE_CTA(ev) \
+  do {                    \
   } while (0)
 #endif
 
@@ -208,6 +223,50 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// The same descriptor as two 32-bit halves, for issue loops: the low half
+// holds the start address (>> 4) and the leading byte offset, so stepping
+// through a tile is one 32-bit add of (byte offset >> 4); the high half
+// (stride byte offset, version, swizzle) is a constant.
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sw128_desc_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+// D[tmem] (+)= A[smem] * B[smem] with the descriptors given as halves.
+__device__ __forceinline__ void mma_bf16_ss_hl(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                               uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      ".reg .b64 da, db;\n"
+      "setp.ne.b32 p, %6, 0;\n"
+      "mov.b64 da, {%1, %2};\n"
+      "mov.b64 db, {%3, %4};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem] with the B descriptor given as halves.
+__device__ __forceinline__ void mma_bf16_ts_hl(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      ".reg .b64 db;\n"
+      "setp.ne.b32 p, %5, 0;\n"
+      "mov.b64 db, {%2, %3};\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
