@@ -23,7 +23,9 @@
 // * bwd_dkdv_kernel -- key-major over the chunk keys.  A CTA owns one
 //   128-key chunk tile and walks the query tiles that can see it:
 //   S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q, with P^T and dS^T
-//   staged bf16 in TMEM.  TMEM: S^T [0,128) dP^T [128,256) dV, dK.
+//   staged bf16 in TMEM and handed over separately, so the MMAs of one query
+//   tile overlap the elementwise work of the neighbouring one.
+//   TMEM: S^T [0,128) dP^T [128,256) dV, dK.
 #include "cfa_kernels.cuh"
 #include "cfa_ptx.cuh"
 
@@ -438,11 +440,12 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t bar_qempty = bars + 8 * (1 + S);    // [S]
   const uint32_t bar_stfull = bars + 8 * (1 + 2 * S);
   const uint32_t bar_dptfull = bar_stfull + 8;
-  const uint32_t bar_pdsfull = bar_dptfull + 8;
-  const uint32_t bar_dkvfull = bar_pdsfull + 8;
+  const uint32_t bar_pfull = bar_dptfull + 8;
+  const uint32_t bar_dsfull = bar_pfull + 8;
+  const uint32_t bar_dkvfull = bar_dsfull + 8;
   const uint32_t bar_drain = bar_dkvfull + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 240);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 244);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
@@ -452,7 +455,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(bar_stfull, 1);
     mbar_init(bar_dptfull, 1);
-    mbar_init(bar_pdsfull, 8);
+    mbar_init(bar_pfull, 8);
+    mbar_init(bar_dsfull, 8);
     mbar_init(bar_dkvfull, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -470,18 +474,23 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t t_dv = tmem + 256, t_dk = tmem + 256 + D;
 
   if (warp == 8) {
-    if (lane == 0) {
+    // producer: the whole warp waits (converged); lane 0 issues
+    const bool leader = lane == 0;
+    if (leader) {
       mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
       for (int kb = 0; kb < C::kBoxes; ++kb) {
         tma_load_3d(base + C::kKOff + kb * kBoxBytes, &map_kc, bar_kv, kb * 64, hk, c0 + key0);
         tma_load_3d(base + C::kVOff + kb * kBoxBytes, &map_vc, bar_kv, kb * 64, hk, c0 + key0);
       }
-      const uint32_t qbytes = (uint32_t)(C::kBoxes * 128 * tl.rows);
-      int issued = 0;
-      for (int i = 0; i < n; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(W, bar_qempty + 8 * s, ((uint32_t)(i / S) & 1u) ^ 1u)) break;
-        const int tok = c0 + (qi_lo + i) * tl.tpt;
+    }
+    __syncwarp();
+    const uint32_t qbytes = (uint32_t)(C::kBoxes * 128 * tl.rows);
+    int issued = 0;
+    for (int i = 0; i < n; ++i) {
+      const int s = i % S;
+      if (!warp_wait(W, bar_qempty + 8 * s, ((uint32_t)(i / S) & 1u) ^ 1u)) break;
+      const int tok = c0 + (qi_lo + i) * tl.tpt;
+      if (leader) {
         mbar_arrive_expect_tx(bar_qfull + 8 * s, 2 * qbytes);
         for (int kb = 0; kb < C::kBoxes; ++kb) {
           tma_load_3d(base + C::kQOff + (2 * s) * C::kTileBytes + kb * kBoxBytes, &map_q,
@@ -489,36 +498,69 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(base + C::kQOff + (2 * s + 1) * C::kTileBytes + kb * kBoxBytes, &map_do,
                       bar_qfull + 8 * s, kb * 64, hk * tl.g, tok);
         }
-        issued = i + 1;
       }
-      mbar_wait_bounded(bar_kv, 0, kDrainLimitNs);
-      for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
-        mbar_wait_bounded(bar_qfull + 8 * (i % S), (uint32_t)(i / S) & 1u, kDrainLimitNs);
+      __syncwarp();
+      issued = i + 1;
     }
+    mbar_wait_bounded(bar_kv, 0, kDrainLimitNs);
+    for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
+      mbar_wait_bounded(bar_qfull + 8 * (i % S), (uint32_t)(i / S) & 1u, kDrainLimitNs);
   } else if (warp == 9) {
-    if (lane == 0) {
-      bool ok = !(a.debug_wait_never && !mbar_wait(W, bar_drain, 0)) && mbar_wait(W, bar_kv, 0);
-      tc_fence_after_sync();
-      for (int i = 0; ok && i < n; ++i) {
-        const int s = i % S;
-        if (!(ok = mbar_wait(W, bar_qfull + 8 * s, (uint32_t)(i / S) & 1u))) break;
-        tc_fence_after_sync();
-        const uint32_t q_addr = base + C::kQOff + (2 * s) * C::kTileBytes;
-        const uint32_t do_addr = q_addr + C::kTileBytes;
-        issue_nt<D>(tmem, base + C::kKOff, q_addr);            // S^T = K Q^T
+    // Issue order:  S^T(0) dP^T(0), then per query tile i:
+    //   dV(i) [after P^T(i)]  S^T(i+1)  dK(i) [after dS^T(i)]  dP^T(i+1)
+    // so dV(i) and S^T(i+1) run while dS^T(i) is computed and dK(i),
+    // dP^T(i+1) while P^T(i+1) is.  S^T(i+1) reuses the columns of P^T(i)
+    // and dP^T(i+1) those of dS^T(i), each consumed by the MMA issued just
+    // before it (the MMA pipe is in order).  Whole warp waits; lane 0 issues.
+    const bool leader = lane == 0;
+    bool ok = !(a.debug_wait_never && !warp_wait(W, bar_drain, 0)) && warp_wait(W, bar_kv, 0) &&
+              warp_wait(W, bar_qfull, 0);
+    if (ok) {
+      if (leader) {
+        issue_nt<D>(tmem, base + C::kKOff, base + C::kQOff);                   // S^T = K Q^T
         tc_commit(bar_stfull);
-        issue_nt<D>(tmem + 128, base + C::kVOff, do_addr);     // dP^T = V dO^T
+        issue_nt<D>(tmem + 128, base + C::kVOff, base + C::kQOff + C::kTileBytes);  // dP^T = V dO^T
         tc_commit(bar_dptfull);
-        if (!(ok = mbar_wait(W, bar_pdsfull, (uint32_t)i & 1u))) break;
-        tc_fence_after_sync();
-        issue_tn<D>(t_dv, tmem, do_addr, i > 0);                // dV += P^T dO
-        issue_tn<D>(t_dk, tmem + 128, q_addr, i > 0);           // dK += dS^T Q
-        tc_commit(bar_qempty + 8 * s);
       }
-      if (ok) tc_commit(bar_dkvfull);
-      tc_commit(bar_drain);
-      mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
+      __syncwarp();
     }
+    for (int i = 0; ok && i < n; ++i) {
+      const int s = i % S, s1 = (i + 1) % S;
+      const uint32_t q_addr = base + C::kQOff + (2 * s) * C::kTileBytes;
+      const uint32_t do_addr = q_addr + C::kTileBytes;
+      const uint32_t q1_addr = base + C::kQOff + (2 * s1) * C::kTileBytes;
+      CFA_TRACE(2, i, 0);
+      if (!(ok = warp_wait(W, bar_pfull, (uint32_t)i & 1u))) break;
+      CFA_TRACE(2, i, 1);
+      tc_fence_after_sync();
+      if (leader) issue_tn<D>(t_dv, tmem, do_addr, i > 0);                      // dV += P^T dO
+      __syncwarp();
+      if (i + 1 < n) {
+        if (!(ok = warp_wait(W, bar_qfull + 8 * s1, (uint32_t)((i + 1) / S) & 1u))) break;
+        if (leader) {
+          issue_nt<D>(tmem, base + C::kKOff, q1_addr);                          // S^T(i+1)
+          tc_commit(bar_stfull);
+        }
+        __syncwarp();
+      }
+      CFA_TRACE(2, i, 2);
+      if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)i & 1u))) break;
+      CFA_TRACE(2, i, 3);
+      tc_fence_after_sync();
+      if (leader) {
+        issue_tn<D>(t_dk, tmem + 128, q_addr, i > 0);                           // dK += dS^T Q
+        tc_commit(bar_qempty + 8 * s);
+        if (i + 1 < n) {
+          issue_nt<D>(tmem + 128, base + C::kVOff, q1_addr + C::kTileBytes);    // dP^T(i+1)
+          tc_commit(bar_dptfull);
+        }
+      }
+      __syncwarp();
+    }
+    if (ok && leader) tc_commit(bar_dkvfull);
+    if (leader) tc_commit(bar_drain);
+    __syncwarp();
+    mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
   } else {
     const int quad = warp & 3, half = warp >> 2;
     const int krow = quad * 32 + lane;
@@ -528,20 +570,34 @@ __global__ void __launch_bounds__(320, 1)
     float* my_lse = reinterpret_cast<float*>(gbase + C::kRowOff) + warp * 128;
     float* my_dl = my_lse + 64;
     const float sl2 = a.scale_log2;
-    bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      const int tok0 = (qi_lo + i) * tl.tpt;
-      // columns r of this warp are half*64 + j; row r is (token tok0 + r / g, head r % g)
+    // LSE and delta of this warp's 64 query rows, loaded one tile ahead so the
+    // global-memory latency stays off the critical path
+    float lse_n[2], dl_n[2];
+    auto fetch_rows = [&](int qi) {
+      const int tok0 = qi * tl.tpt;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int r = half * 64 + u * 32 + lane;
         const int tok = tok0 + r / tl.g;
         const bool v = r < tl.rows && tok < lc;
         const size_t idx = (size_t)(hk * tl.g + r % tl.g) * a.total_lc + (size_t)(c0 + tok);
-        my_lse[u * 32 + lane] = v ? a.lse[idx] * kLog2e : 0.f;
-        my_dl[u * 32 + lane] = v ? a.delta[idx] : 0.f;
+        lse_n[u] = v ? a.lse[idx] * kLog2e : 0.f;
+        dl_n[u] = v ? a.delta[idx] : 0.f;
+      }
+    };
+    fetch_rows(qi_lo);
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int tok0 = (qi_lo + i) * tl.tpt;
+      // columns r of this warp are half*64 + j; row r is (token tok0 + r / g, head r % g)
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        my_lse[u * 32 + lane] = lse_n[u];
+        my_dl[u * 32 + lane] = dl_n[u];
       }
       __syncwarp();
+      if (i + 1 < n) fetch_rows(qi_lo + i + 1);
       // visible columns: r_min <= r < r_max (key <= token, token < Lc, r < rows)
       int r_lo = (key - tok0) * tl.g;
       r_lo = r_lo < 0 ? 0 : r_lo;
@@ -550,7 +606,9 @@ __global__ void __launch_bounds__(320, 1)
       if (!key_valid) r_hi = 0;
       r_lo -= half * 64;
       r_hi -= half * 64;
+      if (warp == 0 && lane == 0) CFA_TRACE(0, i, 0);
       if (!(ok = warp_wait(W, bar_stfull, (uint32_t)i & 1u))) break;
+      if (warp == 0 && lane == 0) CFA_TRACE(0, i, 1);
       tc_fence_after_sync();
       float p[64];
       {
@@ -565,7 +623,13 @@ __global__ void __launch_bounds__(320, 1)
         for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
         tmem_st_x32(t_lane + half * 64, pk);
       }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pfull);  // P^T(i) is in TMEM: dV(i) may start
+      if (warp == 0 && lane == 0) CFA_TRACE(0, i, 2);
       if (!(ok = warp_wait(W, bar_dptfull, (uint32_t)i & 1u))) break;
+      if (warp == 0 && lane == 0) CFA_TRACE(0, i, 3);
       tc_fence_after_sync();
       {
         uint32_t r[64];
@@ -580,7 +644,8 @@ __global__ void __launch_bounds__(320, 1)
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pdsfull);
+      if (lane == 0) mbar_arrive(bar_dsfull);
+      if (warp == 0 && lane == 0) CFA_TRACE(0, i, 4);
     }
     if (ok) ok = warp_wait(W, bar_dkvfull, 0);
     if (ok) {
@@ -833,3 +898,15 @@ cudaError_t launch_dequant_q8_0(const uint8_t* blocks, long long n_blocks, float
 }
 
 }  // namespace cfa
+
+#ifdef CFA_TRACE_BUILD
+extern "C" int cfa_trace_read_bwd(long long* dst, int clear) {
+  const size_t n = sizeof(long long) * cfa::kTraceRoles * cfa::kTraceIters * cfa::kTraceEvents;
+  if (dst && cudaMemcpyFromSymbol(dst, cfa::cfa_trace_buf, n) != cudaSuccess) return -1;
+  if (clear) {
+    static long long zero[cfa::kTraceRoles * cfa::kTraceIters * cfa::kTraceEvents];
+    if (cudaMemcpyToSymbol(cfa::cfa_trace_buf, zero, n) != cudaSuccess) return -1;
+  }
+  return 0;
+}
+#endif
