@@ -49,7 +49,7 @@ __device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_addr, uint3
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
     const uint32_t off = ((uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u) >> 4;
-    mma_bf16_ss_hl(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, k > 0 ? 1u : 0u);
+    mma_ss_warp(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, k > 0 ? 1u : 0u);
   }
 }
 
@@ -62,8 +62,8 @@ __device__ __forceinline__ void issue_tn(uint32_t d_tmem, uint32_t a_tmem, uint3
   const uint32_t b_lo = sw128_desc_lo(b_addr, kBoxBytes);
 #pragma unroll
   for (int k = 0; k < 8; ++k)
-    mma_bf16_ts_hl(d_tmem, a_tmem + staged_col(k), b_lo + (uint32_t)k * (2048u >> 4), hi, idesc,
-                   (accumulate || k > 0) ? 1u : 0u);
+    mma_ts_warp(d_tmem, a_tmem + staged_col(k), b_lo + (uint32_t)k * (2048u >> 4), hi, idesc,
+                (accumulate || k > 0) ? 1u : 0u);
 }
 
 template <int D>
@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(320, 1)
     // executing, so every wait here is a bubble; dS(g-1) being ready implies
     // that dP(g-1) has been read, and the elementwise warps wait for K(g) and
     // V(g) before they hand over dS(g-1).  Tile counters run across segments.
-    // The whole warp waits (converged); lane 0 issues the MMAs and commits.
-    const bool leader = lane == 0;
+    // The whole warp waits and issues (converged); elect.sync picks the lane
+    // that issues the MMAs and commits.
     const uint32_t t_dq = tmem + 384;
     int it = 0, seg = 0;
     // test hook: see the forward kernel
@@ -251,39 +251,32 @@ __global__ void __launch_bounds__(320, 1)
           if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)(g - 1) & 1u))) break;
           tc_fence_after_sync();
         }
-        if (leader) {
-          issue_nt<D>(tmem + (uint32_t)(g & 1) * 128u, base + C::kQOff,
-                      base + C::kKOff + sk * C::kTileBytes);
-          tc_commit(bar_sfull + 8 * (g & 1));
-          issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + sv * C::kTileBytes);
-          tc_commit(bar_dpfull);
-          tc_commit(bar_vempty + 8 * sv);
-          if (i == n - 1) tc_commit(bar_qempty);  // last S and dP of the segment
-          if (i > 0) {
-            issue_tn<D>(t_dq, tmem + (uint32_t)((g - 1) & 1) * 128u,
-                        base + C::kKOff + skp * C::kTileBytes, i - 1 > 0);
-            tc_commit(bar_kempty + 8 * skp);
-          }
+        issue_nt<D>(tmem + (uint32_t)(g & 1) * 128u, base + C::kQOff,
+                    base + C::kKOff + sk * C::kTileBytes);
+        tc_commit_warp(bar_sfull + 8 * (g & 1));
+        issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + sv * C::kTileBytes);
+        tc_commit_warp(bar_dpfull);
+        tc_commit_warp(bar_vempty + 8 * sv);
+        if (i == n - 1) tc_commit_warp(bar_qempty);  // last S and dP of the segment
+        if (i > 0) {
+          issue_tn<D>(t_dq, tmem + (uint32_t)((g - 1) & 1) * 128u,
+                      base + C::kKOff + skp * C::kTileBytes, i - 1 > 0);
+          tc_commit_warp(bar_kempty + 8 * skp);
         }
-        __syncwarp();
       }
       if (!ok) break;
       const int gl = it + n - 1, skl = gl % SK;
       if (n == 1 && seg > 0 && !(ok = warp_wait(W, bar_dqfree, (uint32_t)(seg - 1) & 1u))) break;
       if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)gl & 1u))) break;
       tc_fence_after_sync();
-      if (leader) {
-        issue_tn<D>(t_dq, tmem + (uint32_t)(gl & 1) * 128u, base + C::kKOff + skl * C::kTileBytes,
-                    n > 1);
-        tc_commit(bar_kempty + 8 * skl);
-        tc_commit(bar_dqfull);
-      }
-      __syncwarp();
+      issue_tn<D>(t_dq, tmem + (uint32_t)(gl & 1) * 128u, base + C::kKOff + skl * C::kTileBytes,
+                  n > 1);
+      tc_commit_warp(bar_kempty + 8 * skl);
+      tc_commit_warp(bar_dqfull);
       it += n;
       ++seg;
     }
-    if (leader) tc_commit(bar_drain);
-    __syncwarp();
+    tc_commit_warp(bar_drain);
     mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
   } else {
     const int quad = warp & 3, half = warp >> 2;
@@ -511,18 +504,15 @@ __global__ void __launch_bounds__(320, 1)
     // so dV(i) and S^T(i+1) run while dS^T(i) is computed and dK(i),
     // dP^T(i+1) while P^T(i+1) is.  S^T(i+1) reuses the columns of P^T(i)
     // and dP^T(i+1) those of dS^T(i), each consumed by the MMA issued just
-    // before it (the MMA pipe is in order).  Whole warp waits; lane 0 issues.
-    const bool leader = lane == 0;
+    // before it (the MMA pipe is in order).  The whole warp waits and issues
+    // (converged); elect.sync picks the issuing lane.
     bool ok = !(a.debug_wait_never && !warp_wait(W, bar_drain, 0)) && warp_wait(W, bar_kv, 0) &&
               warp_wait(W, bar_qfull, 0);
     if (ok) {
-      if (leader) {
-        issue_nt<D>(tmem, base + C::kKOff, base + C::kQOff);                   // S^T = K Q^T
-        tc_commit(bar_stfull);
-        issue_nt<D>(tmem + 128, base + C::kVOff, base + C::kQOff + C::kTileBytes);  // dP^T = V dO^T
-        tc_commit(bar_dptfull);
-      }
-      __syncwarp();
+      issue_nt<D>(tmem, base + C::kKOff, base + C::kQOff);                     // S^T = K Q^T
+      tc_commit_warp(bar_stfull);
+      issue_nt<D>(tmem + 128, base + C::kVOff, base + C::kQOff + C::kTileBytes);  // dP^T = V dO^T
+      tc_commit_warp(bar_dptfull);
     }
     for (int i = 0; ok && i < n; ++i) {
       const int s = i % S, s1 = (i + 1) % S;
@@ -533,33 +523,25 @@ __global__ void __launch_bounds__(320, 1)
       if (!(ok = warp_wait(W, bar_pfull, (uint32_t)i & 1u))) break;
       CFA_TRACE(2, i, 1);
       tc_fence_after_sync();
-      if (leader) issue_tn<D>(t_dv, tmem, do_addr, i > 0);                      // dV += P^T dO
-      __syncwarp();
+      issue_tn<D>(t_dv, tmem, do_addr, i > 0);                                  // dV += P^T dO
       if (i + 1 < n) {
         if (!(ok = warp_wait(W, bar_qfull + 8 * s1, (uint32_t)((i + 1) / S) & 1u))) break;
-        if (leader) {
-          issue_nt<D>(tmem, base + C::kKOff, q1_addr);                          // S^T(i+1)
-          tc_commit(bar_stfull);
-        }
-        __syncwarp();
+        issue_nt<D>(tmem, base + C::kKOff, q1_addr);                            // S^T(i+1)
+        tc_commit_warp(bar_stfull);
       }
       CFA_TRACE(2, i, 2);
       if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)i & 1u))) break;
       CFA_TRACE(2, i, 3);
       tc_fence_after_sync();
-      if (leader) {
-        issue_tn<D>(t_dk, tmem + 128, q_addr, i > 0);                           // dK += dS^T Q
-        tc_commit(bar_qempty + 8 * s);
-        if (i + 1 < n) {
-          issue_nt<D>(tmem + 128, base + C::kVOff, q1_addr + C::kTileBytes);    // dP^T(i+1)
-          tc_commit(bar_dptfull);
-        }
+      issue_tn<D>(t_dk, tmem + 128, q_addr, i > 0);                             // dK += dS^T Q
+      tc_commit_warp(bar_qempty + 8 * s);
+      if (i + 1 < n) {
+        issue_nt<D>(tmem + 128, base + C::kVOff, q1_addr + C::kTileBytes);      // dP^T(i+1)
+        tc_commit_warp(bar_dptfull);
       }
-      __syncwarp();
     }
-    if (ok && leader) tc_commit(bar_dkvfull);
-    if (leader) tc_commit(bar_drain);
-    __syncwarp();
+    if (ok) tc_commit_warp(bar_dkvfull);
+    tc_commit_warp(bar_drain);
     mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
   } else {
     const int quad = warp & 3, half = warp >> 2;

@@ -48,7 +48,7 @@ struct FwdCfg {
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(8 * (2 + 2 * kKStages + 2 * kVStages + 9) <= 240, "barrier area");
 };
@@ -64,7 +64,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_addr, uint3
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
     const uint32_t off = ((uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u) >> 4;
-    mma_bf16_ss_hl(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, k > 0 ? 1u : 0u);
+    mma_ss_warp(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, k > 0 ? 1u : 0u);
   }
 }
 
@@ -79,12 +79,12 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
   const uint32_t b_lo = sw128_desc_lo(v_addr, kBoxBytes);
 #pragma unroll
   for (int k = 0; k < 8; ++k)
-    mma_bf16_ts_hl(d_tmem, p_tmem + (uint32_t)(k * 8), b_lo + (uint32_t)k * (2048u >> 4), hi,
-                   idesc, (accumulate || k > 0) ? 1u : 0u);
+    mma_ts_warp(d_tmem, p_tmem + (uint32_t)(k * 8), b_lo + (uint32_t)k * (2048u >> 4), hi, idesc,
+                (accumulate || k > 0) ? 1u : 0u);
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kp,
                const __grid_constant__ CUtensorMap map_vp,
                const __grid_constant__ CUtensorMap map_kc,
@@ -172,10 +172,13 @@ __global__ void __launch_bounds__(320, 1)
   Segment sg;
 
   if (warp == 8) {
-    // ------------------------------------------------------------ producer
+    // ---------------------------------------------------- Q and K producer
     // The whole warp walks the schedule and waits (converged); lane 0 issues.
+    // V has a warp of its own (below), so a V stage still held by a PV never
+    // holds back the K load queued behind it: K(i+1) is needed one P
+    // hand-off before V(i+1).
     const bool leader = lane == 0;
-    int it = 0, seg = 0, issued_k = 0, issued_v = 0;
+    int it = 0, seg = 0, issued_k = 0;
     bool ok = true;
     while (ok && walk.next(sg)) {
       // the Q tiles are reused: the previous segment's S MMAs must be done
@@ -192,41 +195,48 @@ __global__ void __launch_bounds__(320, 1)
       ++seg;
       const int np_t = ceil_div(sg.lp, kTileN);
       for (int kt = sg.t_begin; kt < sg.t_end; ++kt, ++it) {
-        const CUtensorMap* mk = &map_kc;
-        const CUtensorMap* mv = &map_vc;
-        int row0 = sg.c0 + (kt - np_t) * kTileN;
-        if (kt < np_t) {
-          mk = &map_kp;
-          mv = &map_vp;
-          row0 = sg.p0 + kt * kTileN;
-        }
-        const int sk = it % SK, sv = it % SV;
+        const bool pre = kt < np_t;
+        const int row0 = pre ? sg.p0 + kt * kTileN : sg.c0 + (kt - np_t) * kTileN;
+        const int sk = it % SK;
         if (!(ok = warp_wait(W, bar_kempty + 8 * sk, ((uint32_t)(it / SK) & 1u) ^ 1u))) break;
         CFA_TRACE(3, it, 0);
         if (leader) {
           mbar_arrive_expect_tx(bar_kfull + 8 * sk, C::kTileBytes);
           for (int kb = 0; kb < C::kBoxes; ++kb)
-            tma_load_3d(base + C::kKOff + sk * C::kTileBytes + kb * kBoxBytes, mk,
-                        bar_kfull + 8 * sk, kb * 64, sg.hk, row0);
+            tma_load_3d(base + C::kKOff + sk * C::kTileBytes + kb * kBoxBytes,
+                        pre ? &map_kp : &map_kc, bar_kfull + 8 * sk, kb * 64, sg.hk, row0);
         }
         __syncwarp();
         issued_k = it + 1;
-        if (!(ok = warp_wait(W, bar_vempty + 8 * sv, ((uint32_t)(it / SV) & 1u) ^ 1u))) break;
-        CFA_TRACE(3, it, 1);
-        if (leader) {
-          mbar_arrive_expect_tx(bar_vfull + 8 * sv, C::kTileBytes);
-          for (int kb = 0; kb < C::kBoxes; ++kb)
-            tma_load_3d(base + C::kVOff + sv * C::kTileBytes + kb * kBoxBytes, mv,
-                        bar_vfull + 8 * sv, kb * 64, sg.hk, row0);
-        }
-        __syncwarp();
-        issued_v = it + 1;
       }
     }
     // Unwind: every copy this warp issued has landed before the CTA exits.
     if (seg > 0) mbar_wait_bounded(bar_q, (uint32_t)(seg - 1) & 1u, kDrainLimitNs);
     for (int i = (issued_k > SK ? issued_k - SK : 0); i < issued_k; ++i)
       mbar_wait_bounded(bar_kfull + 8 * (i % SK), (uint32_t)(i / SK) & 1u, kDrainLimitNs);
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ V producer
+    const bool leader = lane == 0;
+    int it = 0, issued_v = 0;
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      const int np_t = ceil_div(sg.lp, kTileN);
+      for (int kt = sg.t_begin; kt < sg.t_end; ++kt, ++it) {
+        const bool pre = kt < np_t;
+        const int row0 = pre ? sg.p0 + kt * kTileN : sg.c0 + (kt - np_t) * kTileN;
+        const int sv = it % SV;
+        if (!(ok = warp_wait(W, bar_vempty + 8 * sv, ((uint32_t)(it / SV) & 1u) ^ 1u))) break;
+        CFA_TRACE(3, it, 1);
+        if (leader) {
+          mbar_arrive_expect_tx(bar_vfull + 8 * sv, C::kTileBytes);
+          for (int kb = 0; kb < C::kBoxes; ++kb)
+            tma_load_3d(base + C::kVOff + sv * C::kTileBytes + kb * kBoxBytes,
+                        pre ? &map_vp : &map_vc, bar_vfull + 8 * sv, kb * 64, sg.hk, row0);
+        }
+        __syncwarp();
+        issued_v = it + 1;
+      }
+    }
     for (int i = (issued_v > SV ? issued_v - SV : 0); i < issued_v; ++i)
       mbar_wait_bounded(bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u, kDrainLimitNs);
   } else if (warp == 9) {
@@ -238,8 +248,8 @@ __global__ void __launch_bounds__(320, 1)
     // executing, so every wait here is a bubble: the softmax warps of query
     // tile 0 wait for K(i+1) and V(i) before they hand over P0(i), and this
     // warp waits only for the P hand-offs (and K at a segment's start).  The
-    // whole warp waits (converged); lane 0 issues the MMAs and commits.
-    const bool leader = lane == 0;
+    // whole warp waits and issues (converged); elect.sync picks the lane that
+    // issues the MMAs and commits.
     int it = 0, seg = 0;
     int ut[2] = {0, 0}, us[2] = {0, 0};  // per query tile: tiles, segments done
     // test hook: wait on a barrier nothing arrives on before the end, so the
@@ -267,21 +277,15 @@ __global__ void __launch_bounds__(320, 1)
             if (!(ok = warp_wait(W, bar_pfull + 8 * qt, (uint32_t)(ut[qt] + i - 1) & 1u))) break;
             CFA_TRACE(2, it + i, 2 * qt);
             tc_fence_after_sync();
-            if (leader) {
-              issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128,
-                          base + C::kVOff + svp * C::kTileBytes, i - 1 > 0);
-              if (qt == nq - 1) tc_commit(bar_vempty + 8 * svp);
-            }
-            __syncwarp();
+            issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128,
+                        base + C::kVOff + svp * C::kTileBytes, i - 1 > 0);
+            if (qt == nq - 1) tc_commit_warp(bar_vempty + 8 * svp);
           }
-          if (leader) {
-            issue_qk<D>(tmem + qt * 128, base + C::kQOff + qt * C::kTileBytes,
-                        base + C::kKOff + sk * C::kTileBytes);
-            tc_commit(bar_sfull + 8 * qt);
-            if (qt == nq - 1) tc_commit(bar_kempty + 8 * sk);
-            if (qt == nq - 1 && i == n - 1) tc_commit(bar_qempty);  // segment's last S
-          }
-          __syncwarp();
+          issue_qk<D>(tmem + qt * 128, base + C::kQOff + qt * C::kTileBytes,
+                      base + C::kKOff + sk * C::kTileBytes);
+          tc_commit_warp(bar_sfull + 8 * qt);
+          if (qt == nq - 1) tc_commit_warp(bar_kempty + 8 * sk);
+          if (qt == nq - 1 && i == n - 1) tc_commit_warp(bar_qempty);  // segment's last S
           CFA_TRACE(2, it + i, 2 * qt + 1);
         }
         if (!ok) break;
@@ -297,17 +301,13 @@ __global__ void __launch_bounds__(320, 1)
           break;
         if (!(ok = warp_wait(W, bar_pfull + 8 * qt, (uint32_t)(ut[qt] + n - 1) & 1u))) break;
         tc_fence_after_sync();
-        if (leader) {
-          issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128, base + C::kVOff + svl * C::kTileBytes,
-                      n > 1);
-          tc_commit(bar_ofull + 8 * qt);
-        }
-        __syncwarp();
+        issue_pv<D>(tmem + 256 + qt * D, tmem + qt * 128, base + C::kVOff + svl * C::kTileBytes,
+                    n > 1);
+        tc_commit_warp(bar_ofull + 8 * qt);
         CFA_TRACE(4, seg, 4 + qt);
       }
       if (!ok) break;
-      if (leader) tc_commit(bar_vempty + 8 * svl);  // V of the segment's last tile
-      __syncwarp();
+      tc_commit_warp(bar_vempty + 8 * svl);  // V of the segment's last tile
       it += n;
       ++seg;
 #pragma unroll
@@ -319,8 +319,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     // Unwind: all issued MMAs have completed before TMEM is released.
-    if (leader) tc_commit(bar_drain);
-    __syncwarp();
+    tc_commit_warp(bar_drain);
     mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
   } else {
     // ------------------------------------------------------------- softmax

@@ -181,54 +181,14 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far
-// has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem], bf16 in, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], bf16 in, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes
 // with CU_TENSOR_MAP_SWIZZLE_128B: 8 rows of 128 bytes per 1024-byte atom,
-// 16-byte chunks XOR-ed with the row index within the atom).  `lbo` / `sbo`
-// are the leading / stride byte offsets; bit 46 is the fixed version field of
-// the tcgen05 descriptor; layout type 2 (bits 61-63) = SWIZZLE_128B.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// The same descriptor as two 32-bit halves, for issue loops: the low half
-// holds the start address (>> 4) and the leading byte offset, so stepping
-// through a tile is one 32-bit add of (byte offset >> 4); the high half
-// (stride byte offset, version, swizzle) is a constant.
+// 16-byte chunks XOR-ed with the row index within the atom), as two 32-bit
+// halves.  The low half holds the start address (>> 4) and the leading byte
+// offset, so stepping through a tile is one 32-bit add of (byte offset >> 4);
+// the high half holds the stride byte offset, the fixed version field of the
+// tcgen05 descriptor (bit 46 of the 64-bit value) and layout type 2
+// (bits 61-63) = SWIZZLE_128B.
 __device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lbo) {
   return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
@@ -236,36 +196,58 @@ __host__ __device__ constexpr uint32_t sw128_desc_hi(uint32_t sbo) {
   return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
 
-// D[tmem] (+)= A[smem] * B[smem] with the descriptors given as halves.
-__device__ __forceinline__ void mma_bf16_ss_hl(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
-                                               uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
-                                               uint32_t accumulate) {
+// Warp-collective MMA issue.  Every lane of a converged warp calls these with
+// the same arguments and elect.sync picks one lane (the lowest) to issue, so
+// the operands stay warp-uniform and no branch surrounds the issue.  The
+// tensor pipe holds only about one MMA beyond the one executing, so the issue
+// loop is on the critical path: with the softmax warps busy on the same
+// sub-partitions, a lane-0 branch around each MMA stretched a 128x128x16 MMA
+// from 64 to 77-97 cycles, the converged form stays at 65-67.
+//
+// D[tmem] (+)= A[smem] * B[smem], bf16 in, fp32 accumulate, descriptors given
+// as halves.
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                            uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                            uint32_t accumulate) {
   asm volatile(
       "{\n"
-      ".reg .pred p;\n"
+      ".reg .pred p, e;\n"
       ".reg .b64 da, db;\n"
       "setp.ne.b32 p, %6, 0;\n"
       "mov.b64 da, {%1, %2};\n"
       "mov.b64 db, {%3, %4};\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n"
       "}\n" ::"r"(d_tmem),
       "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem] with the B descriptor given as halves.
-__device__ __forceinline__ void mma_bf16_ts_hl(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                               uint32_t b_hi, uint32_t idesc,
-                                               uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem], the B descriptor given as halves.
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                            uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n"
-      ".reg .pred p;\n"
+      ".reg .pred p, e;\n"
       ".reg .b64 db;\n"
       "setp.ne.b32 p, %5, 0;\n"
       "mov.b64 db, {%2, %3};\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n"
       "}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-collective tc_commit: the lane elect.sync picks, the same lane that
+// issued the MMAs above, arrives on `bar` once they have all completed.
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n"
+      ".reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "}\n" ::"r"(bar)
       : "memory");
 }
 
