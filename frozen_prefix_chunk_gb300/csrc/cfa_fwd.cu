@@ -341,6 +341,15 @@ __global__ void __launch_bounds__(352, 1)
       const bool row_valid = row < tl.rows && token < sg.lc;
       float m = -INFINITY, l = 0.f;
       for (int i = 0; i < n; ++i, ++u) {
+        if (qt == 0 && quad == 0) {
+          // V(u) and K(u+1) are in shared memory before P0(u) is handed over,
+          // so the MMA warp need not wait for them itself; checking here,
+          // before S0(u) is ready, keeps the waits off the hand-off
+          if (!(ok = warp_wait(W, bar_vfull + 8 * (u % SV), (uint32_t)(u / SV) & 1u))) break;
+          if (i + 1 < n &&
+              !(ok = warp_wait(W, bar_kfull + 8 * ((u + 1) % SK), (uint32_t)((u + 1) / SK) & 1u)))
+            break;
+        }
         if (!(ok = warp_wait(W, bar_sfull + 8 * qt, (uint32_t)u & 1u))) break;
         if (quad == 0 && lane == 0) CFA_TRACE(qt, u, 0);
         tc_fence_after_sync();
@@ -370,19 +379,27 @@ __global__ void __launch_bounds__(352, 1)
           m = m_new;
         }
         const float mref = (m == -INFINITY) ? 0.f : m;
-        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+        // exponentials in pairs: the scale-and-subtract and the row sums run
+        // as packed f32x2 instructions
+        const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(-mref, -mref);
+        uint64_t rs2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float e0 = ex2_approx(fmaf(__uint_as_float(r[2 * c]), sl2, -mref));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(r[2 * c + 1]), sl2, -mref));
-          rs4[c & 3] += e0 + e1;
+          const uint64_t e = ex2_sfu_x2(
+              f2_fma(f2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sl2x2, nmx2));
+          rs2[c & 1] = f2_add(rs2[c & 1], e);
+          float e0, e1;
+          f2_split(e, e0, e1);
           r[c] = pack_bf16x2(e0, e1);  // r[2c], r[2c+1] are no longer needed
         }
-        l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+        float l0, l1, l2, l3;
+        f2_split(rs2[0], l0, l1);
+        f2_split(rs2[1], l2, l3);
+        l += (l0 + l1) + (l2 + l3);
         if (quad == 0 && lane == 0) CFA_TRACE(qt, u, 1);
         tmem_st_x64(t_lane + s_col, reinterpret_cast<const uint32_t(&)[64]>(r));
         tmem_st_wait();
-        if (quad == 0 && lane == 0) CFA_TRACE(qt, u, 2);
+        if (quad == 0 && lane == 0) CFA_TRACE(qt, u, 2);  // P stored
         if (i > 0 && __any_sync(0xffffffffu, resc)) {
           // O is quiescent here (the commit behind S_t(i) also covers
           // PV_t(i-1)) and PV_t(i) waits for our arrival below.
@@ -396,16 +413,9 @@ __global__ void __launch_bounds__(352, 1)
           }
           tmem_st_wait();
         }
-        if (qt == 0 && quad == 0) {
-          // tile u's V and tile u+1's K are in shared memory before P0(u) is
-          // handed over, so the MMA warp need not wait for them itself
-          if (!(ok = warp_wait(W, bar_vfull + 8 * (u % SV), (uint32_t)(u / SV) & 1u))) break;
-          if (i + 1 < n &&
-              !(ok = warp_wait(W, bar_kfull + 8 * ((u + 1) % SK), (uint32_t)((u + 1) / SK) & 1u)))
-            break;
-        }
         tc_fence_before_sync();
         __syncwarp();
+        if (lane == 0) CFA_TRACE(qt, u, quad == 0 ? 3 : 4 + quad);  // hand-off
         if (lane == 0) mbar_arrive(bar_pfull + 8 * qt);
       }
       if (!ok) break;
