@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         const int sk = it % SK, sv = it % SV;
         if (!(ok = warp_wait(W, bar_kempty + 8 * sk, ((uint32_t)(it / SK) & 1u) ^ 1u))) break;
+        CFA_TRACE(3, it, 0);
         if (leader) {
           mbar_arrive_expect_tx(bar_kfull + 8 * sk, C::kTileBytes);
           for (int kb = 0; kb < C::kBoxes; ++kb)
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
         issued_k = it + 1;
         if (!(ok = warp_wait(W, bar_vempty + 8 * sv, ((uint32_t)(it / SV) & 1u) ^ 1u))) break;
+        CFA_TRACE(3, it, 1);
         if (leader) {
           mbar_arrive_expect_tx(bar_vfull + 8 * sv, C::kTileBytes);
           for (int kb = 0; kb < C::kBoxes; ++kb)
@@ -224,54 +226,78 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = (issued_v > SV ? issued_v - SV : 0); i < issued_v; ++i)
       mbar_wait_bounded(bar_vfull + 8 * (i % SV), (uint32_t)(i / SV) & 1u, kDrainLimitNs);
   } else if (warp == 9) {
-    // Issue order per key tile g:  S(g), dP(g), dQ(g-1), after a single wait
-    // for dS(g-1).  The tensor pipe holds about one MMA beyond the one
-    // executing, so every wait here is a bubble; dS(g-1) being ready implies
-    // that dP(g-1) has been read, and the elementwise warps wait for K(g) and
-    // V(g) before they hand over dS(g-1).  Tile counters run across segments.
+    // Issue order: S runs one key tile ahead.  A segment starts with S(0),
+    // dP(0), S(1); then for every later tile g, after the single wait for
+    // dS(g-1):  dQ(g-1)  dP(g)  S(g+1).  S(g+1) goes to the S buffer that
+    // dS(g-1) occupied, which dQ(g-1) has read by then (the pipe is in
+    // order); so the elementwise warps find S(g) ready the moment they hand
+    // over dS(g-1) and compute P(g) while dQ(g-1) and dP(g) run.  dQ(g-1)
+    // goes first so that K(g-1)'s stage frees early: K(g+2) then has most of
+    // two tiles' time to arrive.  This warp waits for K(g+1) itself, right
+    // after queueing dP(g), so the tensor pipe still has work during the
+    // check; V(g) is checked by an elementwise warp before it hands over
+    // dS(g-1), at a point where it waits for dP(g-1) anyway.
     // The whole warp waits and issues (converged); elect.sync picks the lane
     // that issues the MMAs and commits.
     const uint32_t t_dq = tmem + 384;
     int it = 0, seg = 0;
     // test hook: see the forward kernel
     bool ok = !(a.debug_wait_never && !warp_wait(W, bar_drain, 0));
+    auto issue_s = [&](int g) {
+      issue_nt<D>(tmem + (uint32_t)(g & 1) * 128u, base + C::kQOff,
+                  base + C::kKOff + (g % SK) * C::kTileBytes);
+      tc_commit_warp(bar_sfull + 8 * (g & 1));
+    };
+    auto issue_dp = [&](int g, bool last) {
+      issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + (g % SV) * C::kTileBytes);
+      tc_commit_warp(bar_dpfull);
+      tc_commit_warp(bar_vempty + 8 * (g % SV));
+      if (last) tc_commit_warp(bar_qempty);  // the segment's last S and dP
+    };
+    auto issue_dq = [&](int g, bool accumulate) {
+      issue_tn<D>(t_dq, tmem + (uint32_t)(g & 1) * 128u,
+                  base + C::kKOff + (g % SK) * C::kTileBytes, accumulate);
+      tc_commit_warp(bar_kempty + 8 * (g % SK));
+    };
     while (ok && walk.next(sg)) {
       const int n = sg.t_end - sg.t_begin;
       if (!(ok = warp_wait(W, bar_qdo, (uint32_t)seg & 1u))) break;
       if (!(ok = warp_wait(W, bar_kfull + 8 * (it % SK), (uint32_t)(it / SK) & 1u))) break;
       if (!(ok = warp_wait(W, bar_vfull + 8 * (it % SV), (uint32_t)(it / SV) & 1u))) break;
-      for (int i = 0; ok && i < n; ++i) {
+      issue_s(it);
+      issue_dp(it, n == 1);
+      if (n > 1) {
+        if (!(ok = warp_wait(W, bar_kfull + 8 * ((it + 1) % SK), (uint32_t)((it + 1) / SK) & 1u)))
+          break;
+        issue_s(it + 1);
+      }
+      for (int i = 1; i < n; ++i) {
         const int g = it + i;
-        const int sk = g % SK, sv = g % SV, skp = (g + SK - 1) % SK;
-        if (i > 0) {
-          // the first dQ of a segment overwrites the accumulator: the previous
-          // segment's epilogue must have read it
-          if (i == 1 && seg > 0 && !(ok = warp_wait(W, bar_dqfree, (uint32_t)(seg - 1) & 1u)))
+        // the first dQ of a segment overwrites the accumulator: the previous
+        // segment's epilogue must have read it
+        if (i == 1 && seg > 0 && !(ok = warp_wait(W, bar_dqfree, (uint32_t)(seg - 1) & 1u))) break;
+        CFA_TRACE(2, g, 0);
+        if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)(g - 1) & 1u))) break;
+        CFA_TRACE(2, g, 1);
+        tc_fence_after_sync();
+        issue_dq(g - 1, i > 1);
+        CFA_TRACE(2, g, 2);
+        issue_dp(g, i == n - 1);  // V(g): checked by the elementwise warps
+        CFA_TRACE(2, g, 3);
+        if (i + 1 < n) {
+          if (!(ok = warp_wait(W, bar_kfull + 8 * ((g + 1) % SK), (uint32_t)((g + 1) / SK) & 1u)))
             break;
-          if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)(g - 1) & 1u))) break;
-          tc_fence_after_sync();
+          CFA_TRACE(2, g, 6);
+          issue_s(g + 1);
         }
-        issue_nt<D>(tmem + (uint32_t)(g & 1) * 128u, base + C::kQOff,
-                    base + C::kKOff + sk * C::kTileBytes);
-        tc_commit_warp(bar_sfull + 8 * (g & 1));
-        issue_nt<D>(tmem + 256, base + C::kDOOff, base + C::kVOff + sv * C::kTileBytes);
-        tc_commit_warp(bar_dpfull);
-        tc_commit_warp(bar_vempty + 8 * sv);
-        if (i == n - 1) tc_commit_warp(bar_qempty);  // last S and dP of the segment
-        if (i > 0) {
-          issue_tn<D>(t_dq, tmem + (uint32_t)((g - 1) & 1) * 128u,
-                      base + C::kKOff + skp * C::kTileBytes, i - 1 > 0);
-          tc_commit_warp(bar_kempty + 8 * skp);
-        }
+        CFA_TRACE(2, g, 4);
       }
       if (!ok) break;
-      const int gl = it + n - 1, skl = gl % SK;
+      const int gl = it + n - 1;
       if (n == 1 && seg > 0 && !(ok = warp_wait(W, bar_dqfree, (uint32_t)(seg - 1) & 1u))) break;
       if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)gl & 1u))) break;
       tc_fence_after_sync();
-      issue_tn<D>(t_dq, tmem + (uint32_t)(gl & 1) * 128u, base + C::kKOff + skl * C::kTileBytes,
-                  n > 1);
-      tc_commit_warp(bar_kempty + 8 * skl);
+      issue_dq(gl, n > 1);
       tc_commit_warp(bar_dqfull);
       it += n;
       ++seg;
@@ -297,6 +323,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int i = 0; i < n; ++i, ++u) {
         const uint32_t sb = (uint32_t)(u & 1) * 128u + (uint32_t)half * 64u;
         if (!(ok = warp_wait(W, bar_sfull + 8 * (u & 1), (uint32_t)(u >> 1) & 1u))) break;
+        if (warp < 2 && lane == 0) CFA_TRACE(warp, u, 0);
         tc_fence_after_sync();
         const int kt = sg.t_begin + i;
         int lim = (kt < np_t) ? (sg.lp - kt * kTileN) : (token - (kt - np_t) * kTileN + 1);
@@ -306,35 +333,48 @@ __global__ void __launch_bounds__(320, 1)
         {
           uint32_t r[64];
           tmem_ld_x64(t_lane + sb, r);
+          const uint64_t sl2x2 = f2(sl2, sl2), nl2 = f2(-lse2, -lse2);
 #pragma unroll
-          for (int j = 0; j < 64; ++j) p[j] = ex2_approx(fmaf(__uint_as_float(r[j]), sl2, -lse2));
+          for (int j = 0; j < 32; ++j)
+            f2_split(ex2_sfu_x2(f2_fma(f2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
+                                       sl2x2, nl2)),
+                     p[2 * j], p[2 * j + 1]);
           if (lim < 64) {  // edge tiles only: the prefix tail, the causal diagonal, padding rows
 #pragma unroll
             for (int j = 0; j < 64; ++j) p[j] = (j < lim) ? p[j] : 0.f;
           }
         }
+        if (warp < 2 && lane == 0) CFA_TRACE(warp, u, 1);
+        if (warp == 0 && i + 1 < n) {
+          // V(u+1) is in shared memory before dS(u) is handed over, so the
+          // MMA warp need not wait for it before dP(u+1); checked here, where
+          // this warp waits for dP(u) anyway
+          const int v = u + 1;
+          if (!(ok = warp_wait(W, bar_vfull + 8 * (v % SV), (uint32_t)(v / SV) & 1u))) break;
+        }
         if (!(ok = warp_wait(W, bar_dpfull, (uint32_t)u & 1u))) break;
+        if (warp < 2 && lane == 0) CFA_TRACE(warp, u, 2);
         tc_fence_after_sync();
         uint32_t pk[32];
         {
           uint32_t r[64];
           tmem_ld_x64(t_lane + 256 + half * 64, r);
+          const uint64_t dl2 = f2(dl, dl);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            pk[j] = pack_bf16x2(p[2 * j] * (__uint_as_float(r[2 * j]) - dl),
-                                p[2 * j + 1] * (__uint_as_float(r[2 * j + 1]) - dl));
+          for (int j = 0; j < 32; ++j) {
+            float d0, d1;
+            f2_split(f2_mul(f2(p[2 * j], p[2 * j + 1]),
+                            f2_sub(f2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), dl2)),
+                     d0, d1);
+            pk[j] = pack_bf16x2(d0, d1);
+          }
         }
         tmem_st_x32(t_lane + sb, pk);
         tmem_st_wait();
-        if (warp == 0 && i + 1 < n) {
-          // K and V of the next tile are in shared memory before dS(u) is
-          // handed over, so the MMA warp need not wait for them itself
-          const int v = u + 1;
-          if (!(ok = warp_wait(W, bar_kfull + 8 * (v % SK), (uint32_t)(v / SK) & 1u))) break;
-          if (!(ok = warp_wait(W, bar_vfull + 8 * (v % SV), (uint32_t)(v / SV) & 1u))) break;
-        }
+        if (warp < 2 && lane == 0) CFA_TRACE(warp, u, 3);
         tc_fence_before_sync();
         __syncwarp();
+        if (warp < 2 && lane == 0) CFA_TRACE(warp, u, 4);
         if (lane == 0) mbar_arrive(bar_dsfull);
       }
       if (!ok) break;

@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(352, 1)
             if (i == 1 && us[qt] > 0 &&
                 !(ok = warp_wait(W, bar_ofree + 8 * qt, (uint32_t)(us[qt] - 1) & 1u)))
               break;
+            CFA_TRACE(2, it + i, 5 + qt);
             if (!(ok = warp_wait(W, bar_pfull + 8 * qt, (uint32_t)(ut[qt] + i - 1) & 1u))) break;
             CFA_TRACE(2, it + i, 2 * qt);
             tc_fence_after_sync();
