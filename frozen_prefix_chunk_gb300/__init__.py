@@ -206,16 +206,20 @@ def backward_dkdv(args: Args, dout, lse, delta, dk, dv, ws, stream=None):
     return dk, dv
 
 
-def dequant_q8_0(blocks: torch.Tensor, stream=None):
+def dequant_q8_0(blocks: torch.Tensor, stream=None, out_bf16=None, want_f32=True):
     """cfa_dequant_q8_0 on uint8 blocks (last dim a multiple of 34).
-    Returns (fp32 values, bf16 values) with last dim = 32 per block."""
+    Returns (fp32 values or None, bf16 values) with last dim = 32 per block;
+    out_bf16 may be given (preallocated), and want_f32=False skips the fp32
+    output."""
     assert blocks.dtype == torch.uint8 and blocks.shape[-1] % 34 == 0
     nb = blocks.numel() // 34
     shape = tuple(blocks.shape[:-1]) + (blocks.shape[-1] // 34 * 32,)
-    f32 = torch.empty(shape, dtype=torch.float32, device=blocks.device)
-    bf = torch.empty(shape, dtype=torch.bfloat16, device=blocks.device)
-    _check(lib().cfa_dequant_q8_0(_ptr(blocks), nb, _ptr(f32), _ptr(bf), _stream(stream)),
-           "cfa_dequant_q8_0")
+    f32 = torch.empty(shape, dtype=torch.float32, device=blocks.device) if want_f32 else None
+    bf = out_bf16 if out_bf16 is not None else torch.empty(shape, dtype=torch.bfloat16,
+                                                           device=blocks.device)
+    assert bf.dtype == torch.bfloat16 and bf.numel() == nb * 32 and bf.is_contiguous()
+    _check(lib().cfa_dequant_q8_0(_ptr(blocks), nb, _ptr(f32) if f32 is not None else None,
+                                  _ptr(bf), _stream(stream)), "cfa_dequant_q8_0")
     return f32, bf
 
 

@@ -206,8 +206,9 @@ int prefix_rows_bf16(const cfa_args* a, uint8_t* ws, size_t off_k, cudaStream_t 
   __nv_bfloat16* k16 = reinterpret_cast<__nv_bfloat16*>(ws + off_k);
   __nv_bfloat16* v16 = reinterpret_cast<__nv_bfloat16*>(ws + off_k + kv16);
   const long long nb = (long long)a->total_lp * a->hkv * (a->head_dim / 32);
-  if (launch_dequant_prefix(static_cast<const uint8_t*>(a->k_prefix), nb, k16, s) != cudaSuccess ||
-      launch_dequant_prefix(static_cast<const uint8_t*>(a->v_prefix), nb, v16, s) != cudaSuccess)
+  if (launch_dequant_prefix(static_cast<const uint8_t*>(a->k_prefix),
+                            static_cast<const uint8_t*>(a->v_prefix), nb, k16, v16,
+                            s) != cudaSuccess)
     return CFA_ERR_LAUNCH;
   *kp16 = k16;
   *vp16 = v16;
@@ -427,10 +428,15 @@ int cfa_dequant_q8_0(const void* blocks, long long n_blocks, float* out_f32, voi
   if ((reinterpret_cast<uintptr_t>(blocks) & 1u) || (reinterpret_cast<uintptr_t>(out_f32) & 3u) ||
       (reinterpret_cast<uintptr_t>(out_bf16) & 1u))
     return CFA_ERR_INVALID_ARG;
-  if (launch_dequant_q8_0(static_cast<const uint8_t*>(blocks), n_blocks, out_f32,
-                          static_cast<__nv_bfloat16*>(out_bf16),
-                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return CFA_ERR_LAUNCH;
+  cudaError_t e;
+  if (!out_f32 && (reinterpret_cast<uintptr_t>(out_bf16) & 15u) == 0)
+    e = launch_dequant_prefix(static_cast<const uint8_t*>(blocks), nullptr, n_blocks,
+                              static_cast<__nv_bfloat16*>(out_bf16), nullptr,
+                              static_cast<cudaStream_t>(stream));
+  else
+    e = launch_dequant_q8_0(static_cast<const uint8_t*>(blocks), n_blocks, out_f32,
+                            static_cast<__nv_bfloat16*>(out_bf16), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return CFA_ERR_LAUNCH;
   return CFA_OK;
 }
 

@@ -813,36 +813,58 @@ __global__ void dequant_q8_0_kernel(const uint8_t* __restrict__ blocks, long lon
   if (out_bf16) out_bf16[idx] = __float2bfloat16_rn(v);
 }
 
-// q8_0 prefix -> bf16 rows for the attention kernels' TMA maps.  One thread
-// per 34-byte block; the value is fp32(d) * q (exact) rounded to nearest-even
-// bf16, the same operand the export kernel above produces.
-__global__ void __launch_bounds__(256) dequant_prefix_kernel(const uint8_t* __restrict__ blocks,
-                                                             long long n_blocks,
-                                                             __nv_bfloat16* __restrict__ out) {
-  const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= n_blocks) return;
-  const uint16_t* p = reinterpret_cast<const uint16_t*>(blocks + b * 34);
+// q8_0 prefix -> bf16 rows for the attention kernels' TMA maps, K and V in
+// one launch (blockIdx.y).  A warp takes 32 consecutive 34-byte blocks
+// (1088 bytes): it stages them in shared memory with coalesced 16-byte loads
+// (2-byte loads for a ragged or unaligned chunk), then each lane expands one
+// block to 32 values, fp32(d) * q (exact) rounded to nearest-even bf16 -- the
+// same operand the export kernel above produces -- and writes its 64 bytes.
+constexpr int kDqWarps = 8;
+__global__ void __launch_bounds__(kDqWarps * 32)
+    dequant_prefix_kernel(const uint8_t* __restrict__ k_blocks, const uint8_t* __restrict__ v_blocks,
+                          long long n_blocks, __nv_bfloat16* __restrict__ k_out,
+                          __nv_bfloat16* __restrict__ v_out) {
+  __shared__ uint4 stage[kDqWarps][68];
+  const uint8_t* src = blockIdx.y ? v_blocks : k_blocks;
+  __nv_bfloat16* out = blockIdx.y ? v_out : k_out;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long b0 = ((long long)blockIdx.x * kDqWarps + warp) * 32;
+  if (b0 >= n_blocks) return;
+  const int nb = (n_blocks - b0 < 32) ? (int)(n_blocks - b0) : 32;
+  const uint8_t* chunk = src + b0 * 34;
+  uint8_t* st = reinterpret_cast<uint8_t*>(stage[warp]);
+  if (nb == 32 && (reinterpret_cast<uintptr_t>(chunk) & 15u) == 0) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(chunk);
+    for (int i = lane; i < 68; i += 32) stage[warp][i] = s4[i];
+  } else {
+    const uint16_t* s2 = reinterpret_cast<const uint16_t*>(chunk);
+    for (int i = lane; i < nb * 17; i += 32) reinterpret_cast<uint16_t*>(st)[i] = s2[i];
+  }
+  __syncwarp();
+  if (lane >= nb) return;
+  const uint16_t* p = reinterpret_cast<const uint16_t*>(st + lane * 34);
   const float d = __half2float(__ushort_as_half(p[0]));
   uint32_t w[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint16_t two = p[1 + i];
-    const float lo = d * (float)(int8_t)(two & 0xff);
-    const float hi = d * (float)(int8_t)(two >> 8);
-    w[i] = pack_bf16x2(lo, hi);
+    w[i] = pack_bf16x2(d * (float)(int8_t)(two & 0xff), d * (float)(int8_t)(two >> 8));
   }
-  uint4* dst = reinterpret_cast<uint4*>(out + b * 32);
+  uint4* dst = reinterpret_cast<uint4*>(out + (b0 + lane) * 32);
 #pragma unroll
   for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
 }
 
 }  // namespace
 
-cudaError_t launch_dequant_prefix(const uint8_t* blocks, long long n_blocks, __nv_bfloat16* out,
-                                  cudaStream_t st) {
+cudaError_t launch_dequant_prefix(const uint8_t* k_blocks, const uint8_t* v_blocks,
+                                  long long n_blocks, __nv_bfloat16* k_out,
+                                  __nv_bfloat16* v_out, cudaStream_t st) {
   if (n_blocks <= 0) return cudaSuccess;
-  const unsigned grid = (unsigned)((n_blocks + 255) / 256);
-  dequant_prefix_kernel<<<grid, 256, 0, st>>>(blocks, n_blocks, out);
+  const long long per_cta = 32LL * kDqWarps;
+  const dim3 grid((unsigned)((n_blocks + per_cta - 1) / per_cta), v_blocks ? 2 : 1);
+  dequant_prefix_kernel<<<grid, kDqWarps * 32, 0, st>>>(k_blocks, v_blocks, n_blocks, k_out,
+                                                        v_out);
   return cudaGetLastError();
 }
 

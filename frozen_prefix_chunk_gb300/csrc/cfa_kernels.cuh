@@ -72,8 +72,11 @@ cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, dim3 grid, c
 cudaError_t launch_bwd_dq_reduce(const BwdArgs& a, int d, int max_lc, cudaStream_t st);
 cudaError_t launch_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta,
                          int total_lc, int hq, int d, cudaStream_t st);
-cudaError_t launch_dequant_prefix(const uint8_t* blocks, long long n_blocks, __nv_bfloat16* out,
-                                  cudaStream_t st);
+// q8_0 -> bf16 of one or two tensors of n_blocks blocks each (v_blocks may be
+// null); outputs 16-byte aligned.
+cudaError_t launch_dequant_prefix(const uint8_t* k_blocks, const uint8_t* v_blocks,
+                                  long long n_blocks, __nv_bfloat16* k_out,
+                                  __nv_bfloat16* v_out, cudaStream_t st);
 cudaError_t launch_dequant_q8_0(const uint8_t* blocks, long long n_blocks, float* out_f32,
                                 __nv_bfloat16* out_bf16, cudaStream_t st);
 
