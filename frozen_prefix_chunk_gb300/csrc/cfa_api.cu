@@ -347,6 +347,7 @@ int prepare_backward(const cfa_args* a, const void* dout, const float* lse, cons
   ba->dq = ba->dk = ba->dv = nullptr;
   uint8_t* w = static_cast<uint8_t*>(ws);
   ba->dq_part = need_partials ? reinterpret_cast<float*>(w + p->off_dqpart) : nullptr;
+  ba->dkv_tiles = p->n_kc_max;
   ba->status = reinterpret_cast<int*>(w);
   ba->limit_ns = wait_limit_ns();
   ba->debug_wait_never = debug_wait_never();
@@ -359,9 +360,57 @@ int run_dq(const cfa_args* a, const Plan& p, const Maps& m, const BwdArgs& ba, c
   return CFA_OK;
 }
 
-int run_dkdv(const cfa_args* a, const Plan& p, const Maps& m, const BwdArgs& ba, cudaStream_t s) {
-  dim3 grid((unsigned)p.n_kc_max, (unsigned)a->hkv, (unsigned)a->batch);
-  if (launch_bwd_dkdv(m, ba, a->head_dim, grid, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+// dK/dV work items (chunk key tile x window x KV head slots, some empty).
+long long dkdv_items(const cfa_args* a, const Plan& p) {
+  return (long long)p.n_kc_max * a->batch * a->hkv;
+}
+
+int run_dkdv(const cfa_args* a, const Plan& p, const Maps& m, const BwdArgs& ba, int ctas,
+             cudaStream_t s) {
+  if (launch_bwd_dkdv(m, ba, a->head_dim, ctas, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  return CFA_OK;
+}
+
+// SMs given to the dK/dV kernel when it runs beside the dQ kernel: its share
+// of the tensor work, estimated from window lengths averaged over the batch
+// (a dK/dV step -- query tile x chunk key tile -- is four 128x128xD products,
+// a dQ step -- query tile x key tile -- three), rounded up and one more, since
+// a dK/dV item cannot be split and a late dK/dV ends the backward.
+int dkdv_share(const cfa_args* a, const Tiling& tl, int sms, long long items) {
+  const double B = a->batch;
+  const double lc = (double)a->total_lc / B, lp = (double)a->total_lp / B;
+  const double qt = std::ceil(lc / tl.tpt);
+  const double nk = std::ceil(lc / kTileN);
+  const double kv_steps = nk * qt - (double)kTileN / tl.tpt * nk * (nk - 1) / 2;
+  const double dq_steps = qt * (std::ceil(lp / kTileN) + (nk + 1) / 2);
+  const double w_kv = 4 * kv_steps, w_dq = 3 * dq_steps;
+  long long k = (long long)std::ceil(sms * w_kv / (w_kv + w_dq)) + 1;
+  if (k > sms / 2) k = sms / 2;
+  if (k > items) k = items;
+  return k < 1 ? 1 : (int)k;
+}
+
+// The second stream and the fork / join events cfa_backward uses to run the
+// dK/dV kernel beside the dQ kernel, one set per device, made on first use.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_side_mutex;
+SideStream g_side[kMaxDevices];
+
+int side_stream(SideStream** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CFA_ERR_CUDA;
+  SideStream& ss = g_side[dev];
+  if (!ss.stream) {
+    if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+      return CFA_ERR_CUDA;
+  }
+  *out = &ss;
   return CFA_OK;
 }
 
@@ -385,8 +434,25 @@ int cfa_backward(const cfa_args* a, const void* dout, const float* lse, const fl
   ba.dq = static_cast<__nv_bfloat16*>(dq);
   ba.dk = static_cast<__nv_bfloat16*>(dk_chunk);
   ba.dv = static_cast<__nv_bfloat16*>(dv_chunk);
-  if ((st = run_dq(a, p, m, ba, s))) return st;
-  return run_dkdv(a, p, m, ba, s);
+  // The two halves share no outputs: the dK/dV kernel runs on a few SMs of
+  // its own, on a second stream forked from and joined back into `s`, while
+  // the dQ kernel's persistent grid takes the rest.
+  const long long items = dkdv_items(a, p);
+  const int k = dkdv_share(a, p.dq, p.dq.grid, items);
+  ba.tl.grid = p.dq.grid - k;
+  std::lock_guard<std::mutex> lock(g_side_mutex);
+  SideStream* ss = nullptr;
+  if ((st = side_stream(&ss))) return st;
+  if (cudaEventRecord(ss->fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
+    return CFA_ERR_LAUNCH;
+  const int st_kv = run_dkdv(a, p, m, ba, k, ss->stream);
+  const int st_dq = run_dq(a, p, m, ba, s);
+  // join even after a failed launch, so `s` never runs ahead of the side stream
+  if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess ||
+      cudaStreamWaitEvent(s, ss->join, 0) != cudaSuccess)
+    return CFA_ERR_LAUNCH;
+  return st_kv ? st_kv : st_dq;
 }
 
 int cfa_backward_dq(const cfa_args* a, const void* dout, const float* lse, const float* delta,
@@ -417,7 +483,8 @@ int cfa_backward_dkdv(const cfa_args* a, const void* dout, const float* lse, con
   if (st || skip) return st;
   ba.dk = static_cast<__nv_bfloat16*>(dk_chunk);
   ba.dv = static_cast<__nv_bfloat16*>(dv_chunk);
-  return run_dkdv(a, p, m, ba, s);
+  const long long items = dkdv_items(a, p);
+  return run_dkdv(a, p, m, ba, (int)(items < p.dq.grid ? items : p.dq.grid), s);
 }
 
 int cfa_dequant_q8_0(const void* blocks, long long n_blocks, float* out_f32, void* out_bf16,

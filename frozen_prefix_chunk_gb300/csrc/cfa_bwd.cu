@@ -445,6 +445,27 @@ struct DkvCfg {
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
 };
 
+// Work items of the dK/dV kernel: (128-key chunk tile kt, window b, KV head
+// hk), numbered kt-major so that the longest items (kt = 0 sees every query
+// tile of its window) come first; CTA c takes items c, c + G, c + 2G, ...
+struct DkvItem {
+  int kt, b, hk;
+  int c0, lc, key0, qi_lo, n;  // window rows, first key, query tiles [qi_lo, qi_lo + n)
+};
+
+__device__ inline bool dkv_item(const BwdArgs& a, long long j, DkvItem& it) {
+  it.hk = (int)(j % a.hkv);
+  it.b = (int)((j / a.hkv) % a.batch);
+  it.kt = (int)(j / ((long long)a.hkv * a.batch));
+  it.c0 = a.cu_c[it.b];
+  it.lc = a.cu_c[it.b + 1] - it.c0;
+  it.key0 = it.kt * kTileN;
+  if (it.key0 >= it.lc) return false;
+  it.qi_lo = it.key0 / a.tl.tpt;
+  it.n = ceil_div(it.lc, a.tl.tpt) - it.qi_lo;
+  return true;
+}
+
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -460,12 +481,9 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Tiling tl = a.tl;
-  const int b = blockIdx.z, hk = blockIdx.y;
-  const int key0 = blockIdx.x * kTileN;
-  const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
-  if (key0 >= lc) return;
-  const int qi_lo = key0 / tl.tpt;
-  const int n = ceil_div(lc, tl.tpt) - qi_lo;
+  const long long n_items = (long long)a.dkv_tiles * a.batch * a.hkv;
+  if ((long long)blockIdx.x >= n_items) return;
+  const long long j0 = blockIdx.x, jstep = gridDim.x;
 
   const uint32_t bars = base + C::kBarOff;
   const uint32_t bar_kv = bars;
@@ -476,7 +494,9 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t bar_pfull = bar_dptfull + 8;
   const uint32_t bar_dsfull = bar_pfull + 8;
   const uint32_t bar_dkvfull = bar_dsfull + 8;
-  const uint32_t bar_drain = bar_dkvfull + 8;
+  const uint32_t bar_dkvfree = bar_dkvfull + 8;
+  const uint32_t bar_kvfree = bar_dkvfree + 8;
+  const uint32_t bar_drain = bar_kvfree + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 240);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 244);
 
@@ -491,6 +511,8 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_pfull, 8);
     mbar_init(bar_dsfull, 8);
     mbar_init(bar_dkvfull, 1);
+    mbar_init(bar_dkvfree, 8);
+    mbar_init(bar_kvfree, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -505,174 +527,208 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_slot;
   const Waiter W{a.limit_ns, abort_flag, a.status};
   const uint32_t t_dv = tmem + 256, t_dk = tmem + 256 + D;
+  DkvItem it;
 
   if (warp == 8) {
-    // producer: the whole warp waits (converged); lane 0 issues
+    // producer: the whole warp waits (converged); lane 0 issues.  K/V of an
+    // item reuse one buffer: they load once the previous item's last S^T and
+    // dP^T are done (kvfree), while its dV and dK still run.
     const bool leader = lane == 0;
-    if (leader) {
-      mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
-      for (int kb = 0; kb < C::kBoxes; ++kb) {
-        tma_load_3d(base + C::kKOff + kb * kBoxBytes, &map_kc, bar_kv, kb * 64, hk, c0 + key0);
-        tma_load_3d(base + C::kVOff + kb * kBoxBytes, &map_vc, bar_kv, kb * 64, hk, c0 + key0);
-      }
-    }
-    __syncwarp();
     const uint32_t qbytes = (uint32_t)(C::kBoxes * 128 * tl.rows);
-    int issued = 0;
-    for (int i = 0; i < n; ++i) {
-      const int s = i % S;
-      if (!warp_wait(W, bar_qempty + 8 * s, ((uint32_t)(i / S) & 1u) ^ 1u)) break;
-      const int tok = c0 + (qi_lo + i) * tl.tpt;
+    int qn = 0, items = 0, issued = 0;
+    bool ok = true;
+    for (long long j = j0; ok && j < n_items; j += jstep) {
+      if (!dkv_item(a, j, it)) continue;
+      if (items > 0 && !(ok = warp_wait(W, bar_kvfree, (uint32_t)(items - 1) & 1u))) break;
       if (leader) {
-        mbar_arrive_expect_tx(bar_qfull + 8 * s, 2 * qbytes);
+        mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
         for (int kb = 0; kb < C::kBoxes; ++kb) {
-          tma_load_3d(base + C::kQOff + (2 * s) * C::kTileBytes + kb * kBoxBytes, &map_q,
-                      bar_qfull + 8 * s, kb * 64, hk * tl.g, tok);
-          tma_load_3d(base + C::kQOff + (2 * s + 1) * C::kTileBytes + kb * kBoxBytes, &map_do,
-                      bar_qfull + 8 * s, kb * 64, hk * tl.g, tok);
+          tma_load_3d(base + C::kKOff + kb * kBoxBytes, &map_kc, bar_kv, kb * 64, it.hk,
+                      it.c0 + it.key0);
+          tma_load_3d(base + C::kVOff + kb * kBoxBytes, &map_vc, bar_kv, kb * 64, it.hk,
+                      it.c0 + it.key0);
         }
       }
       __syncwarp();
-      issued = i + 1;
+      ++items;
+      for (int i = 0; i < it.n; ++i, ++qn) {
+        const int s = qn % S;
+        if (!(ok = warp_wait(W, bar_qempty + 8 * s, ((uint32_t)(qn / S) & 1u) ^ 1u))) break;
+        const int tok = it.c0 + (it.qi_lo + i) * tl.tpt;
+        if (leader) {
+          mbar_arrive_expect_tx(bar_qfull + 8 * s, 2 * qbytes);
+          for (int kb = 0; kb < C::kBoxes; ++kb) {
+            tma_load_3d(base + C::kQOff + (2 * s) * C::kTileBytes + kb * kBoxBytes, &map_q,
+                        bar_qfull + 8 * s, kb * 64, it.hk * tl.g, tok);
+            tma_load_3d(base + C::kQOff + (2 * s + 1) * C::kTileBytes + kb * kBoxBytes, &map_do,
+                        bar_qfull + 8 * s, kb * 64, it.hk * tl.g, tok);
+          }
+        }
+        __syncwarp();
+        issued = qn + 1;
+      }
     }
-    mbar_wait_bounded(bar_kv, 0, kDrainLimitNs);
+    // Unwind: every copy this warp issued has landed before the CTA exits.
+    if (items > 0) mbar_wait_bounded(bar_kv, (uint32_t)(items - 1) & 1u, kDrainLimitNs);
     for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
       mbar_wait_bounded(bar_qfull + 8 * (i % S), (uint32_t)(i / S) & 1u, kDrainLimitNs);
   } else if (warp == 9) {
-    // Issue order:  S^T(0) dP^T(0), then per query tile i:
+    // Issue order per item:  S^T(0) dP^T(0), then per query tile i:
     //   dV(i) [after P^T(i)]  S^T(i+1)  dK(i) [after dS^T(i)]  dP^T(i+1)
     // so dV(i) and S^T(i+1) run while dS^T(i) is computed and dK(i),
     // dP^T(i+1) while P^T(i+1) is.  S^T(i+1) reuses the columns of P^T(i)
     // and dP^T(i+1) those of dS^T(i), each consumed by the MMA issued just
-    // before it (the MMA pipe is in order).  The whole warp waits and issues
-    // (converged); elect.sync picks the issuing lane.
-    bool ok = !(a.debug_wait_never && !warp_wait(W, bar_drain, 0)) && warp_wait(W, bar_kv, 0) &&
-              warp_wait(W, bar_qfull, 0);
-    if (ok) {
-      issue_nt<D>(tmem, base + C::kKOff, base + C::kQOff);                     // S^T = K Q^T
-      tc_commit_warp(bar_stfull);
-      issue_nt<D>(tmem + 128, base + C::kVOff, base + C::kQOff + C::kTileBytes);  // dP^T = V dO^T
+    // before it (the MMA pipe is in order).  The first dV of an item
+    // overwrites the accumulators, so it waits for the previous item's
+    // epilogue (dkvfree).  Query-tile counters run across items.  The whole
+    // warp waits and issues (converged); elect.sync picks the issuing lane.
+    int qn = 0, items = 0;
+    bool ok = !(a.debug_wait_never && !warp_wait(W, bar_drain, 0));
+    for (long long j = j0; ok && j < n_items; j += jstep) {
+      if (!dkv_item(a, j, it)) continue;
+      const int n = it.n;
+      if (!(ok = warp_wait(W, bar_kv, (uint32_t)items & 1u))) break;
+      if (!(ok = warp_wait(W, bar_qfull + 8 * (qn % S), (uint32_t)(qn / S) & 1u))) break;
+      issue_nt<D>(tmem, base + C::kKOff, base + C::kQOff + (2 * (qn % S)) * C::kTileBytes);
+      tc_commit_warp(bar_stfull);                                                 // S^T = K Q^T
+      issue_nt<D>(tmem + 128, base + C::kVOff,
+                  base + C::kQOff + (2 * (qn % S) + 1) * C::kTileBytes);          // dP^T = V dO^T
       tc_commit_warp(bar_dptfull);
-    }
-    for (int i = 0; ok && i < n; ++i) {
-      const int s = i % S, s1 = (i + 1) % S;
-      const uint32_t q_addr = base + C::kQOff + (2 * s) * C::kTileBytes;
-      const uint32_t do_addr = q_addr + C::kTileBytes;
-      const uint32_t q1_addr = base + C::kQOff + (2 * s1) * C::kTileBytes;
-      CFA_TRACE(2, i, 0);
-      if (!(ok = warp_wait(W, bar_pfull, (uint32_t)i & 1u))) break;
-      CFA_TRACE(2, i, 1);
-      tc_fence_after_sync();
-      issue_tn<D>(t_dv, tmem, do_addr, i > 0);                                  // dV += P^T dO
-      if (i + 1 < n) {
-        if (!(ok = warp_wait(W, bar_qfull + 8 * s1, (uint32_t)((i + 1) / S) & 1u))) break;
-        issue_nt<D>(tmem, base + C::kKOff, q1_addr);                            // S^T(i+1)
-        tc_commit_warp(bar_stfull);
+      if (n == 1) tc_commit_warp(bar_kvfree);
+      for (int i = 0; i < n; ++i) {
+        const int t = qn + i;
+        const int s = t % S, s1 = (t + 1) % S;
+        const uint32_t q_addr = base + C::kQOff + (2 * s) * C::kTileBytes;
+        const uint32_t do_addr = q_addr + C::kTileBytes;
+        const uint32_t q1_addr = base + C::kQOff + (2 * s1) * C::kTileBytes;
+        CFA_TRACE(2, t, 0);
+        if (!(ok = warp_wait(W, bar_pfull, (uint32_t)t & 1u))) break;
+        if (i == 0 && items > 0 &&
+            !(ok = warp_wait(W, bar_dkvfree, (uint32_t)(items - 1) & 1u)))
+          break;
+        CFA_TRACE(2, t, 1);
+        tc_fence_after_sync();
+        issue_tn<D>(t_dv, tmem, do_addr, i > 0);                                  // dV += P^T dO
+        if (i + 1 < n) {
+          if (!(ok = warp_wait(W, bar_qfull + 8 * s1, (uint32_t)((t + 1) / S) & 1u))) break;
+          issue_nt<D>(tmem, base + C::kKOff, q1_addr);                            // S^T(i+1)
+          tc_commit_warp(bar_stfull);
+        }
+        CFA_TRACE(2, t, 2);
+        if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)t & 1u))) break;
+        CFA_TRACE(2, t, 3);
+        tc_fence_after_sync();
+        issue_tn<D>(t_dk, tmem + 128, q_addr, i > 0);                             // dK += dS^T Q
+        tc_commit_warp(bar_qempty + 8 * s);
+        if (i + 1 < n) {
+          issue_nt<D>(tmem + 128, base + C::kVOff, q1_addr + C::kTileBytes);      // dP^T(i+1)
+          tc_commit_warp(bar_dptfull);
+          if (i + 2 == n) tc_commit_warp(bar_kvfree);  // the item's last S^T and dP^T
+        }
       }
-      CFA_TRACE(2, i, 2);
-      if (!(ok = warp_wait(W, bar_dsfull, (uint32_t)i & 1u))) break;
-      CFA_TRACE(2, i, 3);
-      tc_fence_after_sync();
-      issue_tn<D>(t_dk, tmem + 128, q_addr, i > 0);                             // dK += dS^T Q
-      tc_commit_warp(bar_qempty + 8 * s);
-      if (i + 1 < n) {
-        issue_nt<D>(tmem + 128, base + C::kVOff, q1_addr + C::kTileBytes);      // dP^T(i+1)
-        tc_commit_warp(bar_dptfull);
-      }
+      if (!ok) break;
+      tc_commit_warp(bar_dkvfull);
+      qn += n;
+      ++items;
     }
-    if (ok) tc_commit_warp(bar_dkvfull);
     tc_commit_warp(bar_drain);
     mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
   } else {
     const int quad = warp & 3, half = warp >> 2;
     const int krow = quad * 32 + lane;
-    const int key = key0 + krow;
-    const bool key_valid = key < lc;
     const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16);
     float* my_lse = reinterpret_cast<float*>(gbase + C::kRowOff) + warp * 128;
     float* my_dl = my_lse + 64;
     const float sl2 = a.scale_log2;
-    // LSE and delta of this warp's 64 query rows, loaded one tile ahead so the
-    // global-memory latency stays off the critical path
     float lse_n[2], dl_n[2];
+    // LSE and delta of this warp's 64 query rows of query tile qi, loaded
+    // one tile ahead so the global-memory latency stays off the critical path
     auto fetch_rows = [&](int qi) {
       const int tok0 = qi * tl.tpt;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int r = half * 64 + u * 32 + lane;
         const int tok = tok0 + r / tl.g;
-        const bool v = r < tl.rows && tok < lc;
-        const size_t idx = (size_t)(hk * tl.g + r % tl.g) * a.total_lc + (size_t)(c0 + tok);
+        const bool v = r < tl.rows && tok < it.lc;
+        const size_t idx = (size_t)(it.hk * tl.g + r % tl.g) * a.total_lc + (size_t)(it.c0 + tok);
         lse_n[u] = v ? a.lse[idx] * kLog2e : 0.f;
         dl_n[u] = v ? a.delta[idx] : 0.f;
       }
     };
-    fetch_rows(qi_lo);
+    int qn = 0, items = 0;
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
-      const int tok0 = (qi_lo + i) * tl.tpt;
-      // columns r of this warp are half*64 + j; row r is (token tok0 + r / g, head r % g)
-      __syncwarp();
+    for (long long j = j0; ok && j < n_items; j += jstep) {
+      if (!dkv_item(a, j, it)) continue;
+      const int n = it.n;
+      const int key = it.key0 + krow;
+      const bool key_valid = key < it.lc;
+      fetch_rows(it.qi_lo);
+      for (int i = 0; i < n; ++i) {
+        const int t = qn + i;
+        const int tok0 = (it.qi_lo + i) * tl.tpt;
+        // columns r of this warp are half*64 + j; row r is (token tok0 + r / g, head r % g)
+        __syncwarp();
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        my_lse[u * 32 + lane] = lse_n[u];
-        my_dl[u * 32 + lane] = dl_n[u];
+        for (int u = 0; u < 2; ++u) {
+          my_lse[u * 32 + lane] = lse_n[u];
+          my_dl[u * 32 + lane] = dl_n[u];
+        }
+        __syncwarp();
+        if (i + 1 < n) fetch_rows(it.qi_lo + i + 1);
+        // visible columns: r_min <= r < r_max (key <= token, token < Lc, r < rows)
+        int r_lo = (key - tok0) * tl.g;
+        r_lo = r_lo < 0 ? 0 : r_lo;
+        int r_hi = (it.lc - tok0) * tl.g;
+        r_hi = r_hi < tl.rows ? r_hi : tl.rows;
+        if (!key_valid) r_hi = 0;
+        r_lo -= half * 64;
+        r_hi -= half * 64;
+        if (warp == 0 && lane == 0) CFA_TRACE(0, t, 0);
+        if (!(ok = warp_wait(W, bar_stfull, (uint32_t)t & 1u))) break;
+        if (warp == 0 && lane == 0) CFA_TRACE(0, t, 1);
+        tc_fence_after_sync();
+        float p[64];
+        {
+          uint32_t r[64];
+          tmem_ld_x64(t_lane + half * 64, r);
+          uint32_t pk[32];
+#pragma unroll
+          for (int jj = 0; jj < 64; ++jj)
+            p[jj] = (jj >= r_lo && jj < r_hi)
+                        ? ex2_approx(fmaf(__uint_as_float(r[jj]), sl2, -my_lse[jj]))
+                        : 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) pk[jj] = pack_bf16x2(p[2 * jj], p[2 * jj + 1]);
+          tmem_st_x32(t_lane + half * 64, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_pfull);  // P^T(i) is in TMEM: dV(i) may start
+        if (warp == 0 && lane == 0) CFA_TRACE(0, t, 2);
+        if (!(ok = warp_wait(W, bar_dptfull, (uint32_t)t & 1u))) break;
+        if (warp == 0 && lane == 0) CFA_TRACE(0, t, 3);
+        tc_fence_after_sync();
+        {
+          uint32_t r[64];
+          tmem_ld_x64(t_lane + 128 + half * 64, r);
+          uint32_t pk[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            pk[jj] = pack_bf16x2(p[2 * jj] * (__uint_as_float(r[2 * jj]) - my_dl[2 * jj]),
+                                 p[2 * jj + 1] * (__uint_as_float(r[2 * jj + 1]) - my_dl[2 * jj + 1]));
+          tmem_st_x32(t_lane + 128 + half * 64, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_dsfull);
+        if (warp == 0 && lane == 0) CFA_TRACE(0, t, 4);
       }
-      __syncwarp();
-      if (i + 1 < n) fetch_rows(qi_lo + i + 1);
-      // visible columns: r_min <= r < r_max (key <= token, token < Lc, r < rows)
-      int r_lo = (key - tok0) * tl.g;
-      r_lo = r_lo < 0 ? 0 : r_lo;
-      int r_hi = (lc - tok0) * tl.g;
-      r_hi = r_hi < tl.rows ? r_hi : tl.rows;
-      if (!key_valid) r_hi = 0;
-      r_lo -= half * 64;
-      r_hi -= half * 64;
-      if (warp == 0 && lane == 0) CFA_TRACE(0, i, 0);
-      if (!(ok = warp_wait(W, bar_stfull, (uint32_t)i & 1u))) break;
-      if (warp == 0 && lane == 0) CFA_TRACE(0, i, 1);
+      if (!ok) break;
+      if (!(ok = warp_wait(W, bar_dkvfull, (uint32_t)items & 1u))) break;
       tc_fence_after_sync();
-      float p[64];
-      {
-        uint32_t r[64];
-        tmem_ld_x64(t_lane + half * 64, r);
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 64; ++j)
-          p[j] = (j >= r_lo && j < r_hi) ? ex2_approx(fmaf(__uint_as_float(r[j]), sl2, -my_lse[j]))
-                                         : 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
-        tmem_st_x32(t_lane + half * 64, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pfull);  // P^T(i) is in TMEM: dV(i) may start
-      if (warp == 0 && lane == 0) CFA_TRACE(0, i, 2);
-      if (!(ok = warp_wait(W, bar_dptfull, (uint32_t)i & 1u))) break;
-      if (warp == 0 && lane == 0) CFA_TRACE(0, i, 3);
-      tc_fence_after_sync();
-      {
-        uint32_t r[64];
-        tmem_ld_x64(t_lane + 128 + half * 64, r);
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          pk[j] = pack_bf16x2(p[2 * j] * (__uint_as_float(r[2 * j]) - my_dl[2 * j]),
-                              p[2 * j + 1] * (__uint_as_float(r[2 * j + 1]) - my_dl[2 * j + 1]));
-        tmem_st_x32(t_lane + 128 + half * 64, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dsfull);
-      if (warp == 0 && lane == 0) CFA_TRACE(0, i, 4);
-    }
-    if (ok) ok = warp_wait(W, bar_dkvfull, 0);
-    if (ok) {
-      tc_fence_after_sync();
-      const size_t grow = (size_t)(c0 + key) * a.hkv + hk;
+      const size_t grow = (size_t)(it.c0 + key) * a.hkv + it.hk;
 #pragma unroll
       for (int cb = half * (D / 2); cb < (half + 1) * (D / 2); cb += 32) {
         uint32_t rv[32], rk[32];
@@ -701,6 +757,11 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
       }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dkvfree);  // dK/dV read: the next item may overwrite
+      qn += n;
+      ++items;
     }
   }
 
@@ -895,7 +956,8 @@ cudaError_t launch_bwd_dq(const Maps& m, const BwdArgs& a, int d, int q8, cudaSt
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, dim3 grid, cudaStream_t st) {
+cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, int ctas, cudaStream_t st) {
+  const dim3 grid((unsigned)ctas);
   if (d == 128) {
     auto k = bwd_dkdv_kernel<128>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -48,6 +48,7 @@ struct BwdArgs {
   __nv_bfloat16* dk;     // [total_lc, hkv, D]
   __nv_bfloat16* dv;     // [total_lc, hkv, D]
   float* dq_part;        // [grid, 2, 128, D]  partials of cut query tiles
+  int dkv_tiles;         // 128-key chunk tiles of the longest window (dK/dV items)
   int* status;
   unsigned long long limit_ns;
   int debug_wait_never;  // test hook: the MMA thread waits on a barrier nobody sets
@@ -68,7 +69,7 @@ cudaError_t launch_fwd_merge(const FwdArgs& a, int d, int max_lc, cudaStream_t s
 int bwd_dq_smem_bytes(int d, int q8);
 int bwd_dkdv_smem_bytes(int d);
 cudaError_t launch_bwd_dq(const Maps& m, const BwdArgs& a, int d, int q8, cudaStream_t st);
-cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, dim3 grid, cudaStream_t st);
+cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, int ctas, cudaStream_t st);
 cudaError_t launch_bwd_dq_reduce(const BwdArgs& a, int d, int max_lc, cudaStream_t st);
 cudaError_t launch_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta,
                          int total_lc, int hq, int d, cudaStream_t st);

@@ -123,7 +123,11 @@ int cfa_backward_preprocess(const cfa_args* a, const void* o, const void* dout, 
  * chunk keys; dk_chunk, dv_chunk ([total_lc, hkv, d]) for the chunk keys only,
  * summed over the query heads of each group.  No prefix gradient exists in
  * this interface.  Needs lse from cfa_forward and delta from
- * cfa_backward_preprocess. */
+ * cfa_backward_preprocess.  The dK/dV half runs on a few SMs beside the dQ
+ * half: on a second stream that the library owns (one per device), forked
+ * from `stream` and joined back into it with events, so to the caller the
+ * call is ordered on `stream` like any other.  Calls from several host
+ * threads are serialised around that fork and join. */
 int cfa_backward(const cfa_args* a, const void* dout, const float* lse, const float* delta,
                  void* dq, void* dk_chunk, void* dv_chunk, void* ws, size_t ws_bytes,
                  void* stream);
