@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(320, 1)
                   const __grid_constant__ CUtensorMap map_vp,
                   const __grid_constant__ CUtensorMap map_kc,
                   const __grid_constant__ CUtensorMap map_vc, const BwdArgs a) {
+  pdl_start();
   using C = DqCfg<D>;
   constexpr int SK = C::kKStages;
   constexpr int SV = C::kVStages;
@@ -472,6 +473,7 @@ __global__ void __launch_bounds__(320, 1)
                     const __grid_constant__ CUtensorMap map_do,
                     const __grid_constant__ CUtensorMap map_kc,
                     const __grid_constant__ CUtensorMap map_vc, const BwdArgs a) {
+  pdl_start();
   using C = DkvCfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -783,6 +785,7 @@ constexpr int kMaxParts = 1024;
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
+  pdl_start();
   constexpr int CW = D / 8;
   __shared__ int parts[kMaxParts];
   __shared__ int n_parts;
@@ -837,6 +840,7 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
                                                     const __nv_bfloat16* __restrict__ dout,
                                                     float* __restrict__ delta, int total_lc,
                                                     int hq) {
+  pdl_start();
   constexpr int E = D / 32;
   const long long rid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -864,6 +868,7 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
 __global__ void dequant_q8_0_kernel(const uint8_t* __restrict__ blocks, long long n_values,
                                     float* __restrict__ out_f32,
                                     __nv_bfloat16* __restrict__ out_bf16) {
+  pdl_start();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n_values) return;
   const uint8_t* blk = blocks + (idx >> 5) * 34;
@@ -885,6 +890,7 @@ __global__ void __launch_bounds__(kDqWarps * 32)
     dequant_prefix_kernel(const uint8_t* __restrict__ k_blocks, const uint8_t* __restrict__ v_blocks,
                           long long n_blocks, __nv_bfloat16* __restrict__ k_out,
                           __nv_bfloat16* __restrict__ v_out) {
+  pdl_start();
   __shared__ uint4 stage[kDqWarps][68];
   const uint8_t* src = blockIdx.y ? v_blocks : k_blocks;
   __nv_bfloat16* out = blockIdx.y ? v_out : k_out;
@@ -945,15 +951,16 @@ cudaError_t launch_bwd_dq(const Maps& m, const BwdArgs& a, int d, int q8, cudaSt
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DqCfg<128>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    k<<<grid, 320, DqCfg<128>::kSmemBytes, st>>>(m.q, m.dout, m.kp, m.vp, m.kc, m.vc, a);
+    return launch_pdl(k, grid, 320, DqCfg<128>::kSmemBytes, st, m.q, m.dout, m.kp, m.vp, m.kc, m.vc,
+                      a);
   } else {
     auto k = bwd_dq_kernel<64>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DqCfg<64>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    k<<<grid, 320, DqCfg<64>::kSmemBytes, st>>>(m.q, m.dout, m.kp, m.vp, m.kc, m.vc, a);
+    return launch_pdl(k, grid, 320, DqCfg<64>::kSmemBytes, st, m.q, m.dout, m.kp, m.vp, m.kc, m.vc,
+                      a);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, int ctas, cudaStream_t st) {

@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_base);
 
+  pdl_start();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   CFA_TRACE_CTA(0);
   const Tiling tl = a.tl;
@@ -499,6 +500,7 @@ constexpr int kMaxParts = 1024;
 
 template <int D>
 __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
+  pdl_start();
   constexpr int CW = D / 8;  // columns per thread
   __shared__ int parts[kMaxParts];
   __shared__ int n_parts;
@@ -578,15 +580,16 @@ cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, int q8, cudaStrea
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          FwdCfg<128>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    k<<<grid, FwdCfg<128>::kThreads, FwdCfg<128>::kSmemBytes, st>>>(m.q, m.kp, m.vp, m.kc, m.vc, a);
+    return launch_pdl(k, grid, FwdCfg<128>::kThreads, FwdCfg<128>::kSmemBytes, st, m.q, m.kp, m.vp,
+                      m.kc, m.vc, a);
   } else {
     auto k = fwd_kernel<64>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          FwdCfg<64>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    k<<<grid, FwdCfg<64>::kThreads, FwdCfg<64>::kSmemBytes, st>>>(m.q, m.kp, m.vp, m.kc, m.vc, a);
+    return launch_pdl(k, grid, FwdCfg<64>::kThreads, FwdCfg<64>::kSmemBytes, st, m.q, m.kp, m.vp,
+                      m.kc, m.vc, a);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_merge(const FwdArgs& a, int d, int max_lc, cudaStream_t st) {

@@ -61,6 +61,28 @@ struct Maps {
   CUtensorMap q, dout, kp, vp, kc, vc;
 };
 
+// Launch `k` so that it may overlap the tail of the previous kernel in the
+// stream (programmatic stream serialisation); the kernel itself waits for that
+// kernel's completion in pdl_start() before touching memory.  Used for the
+// persistent attention kernels only (one CTA per SM, placed as the previous
+// grid's CTAs leave): a small grid launched this way would pile onto the
+// first SMs to free up and run on a fraction of the GPU.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
+
 // Launchers (return a cudaError_t of the launch).
 int fwd_smem_bytes(int d, int q8);
 cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, int q8, cudaStream_t st);

@@ -158,6 +158,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel of the library starts with
+// pdl_start(): it lets the next kernel in the stream be scheduled right away
+// (that kernel's CTAs take SMs as this grid's CTAs leave them) and then waits
+// until the previous kernel in the stream has completed and its memory is
+// visible.  Both are no-ops when the launch did not ask for the overlap.
+__device__ __forceinline__ void pdl_start() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05 --
 
 // Allocation is a warp-wide operation; the TMEM address lands in shared memory.
