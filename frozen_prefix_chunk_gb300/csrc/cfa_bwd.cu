@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(320, 1)
                   const __grid_constant__ CUtensorMap map_kc,
                   const __grid_constant__ CUtensorMap map_vc, const BwdArgs a) {
   pdl_start();
+  CFA_TRACE_CTA(0);
   using C = DqCfg<D>;
   constexpr int SK = C::kKStages;
   constexpr int SV = C::kVStages;
@@ -384,24 +385,34 @@ __global__ void __launch_bounds__(320, 1)
       const bool final_out = !sg.head && !sg.tail;
       const int slot = sg.head ? 0 : 1;
       const size_t pslot = (size_t)blockIdx.x * 2 + slot;
+      // this warp's half of the dQ row in one TMEM load, then the hand-off
+      // (before the global stores, which the arrive would otherwise wait for)
+      constexpr int HW = D / 2;
+      uint32_t r[HW];
+      if constexpr (HW == 64)
+        tmem_ld_x64(t_lane + 384 + half * HW, r);
+      else
+        tmem_ld_x32(t_lane + 384 + half * HW, r);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dqfree);
 #pragma unroll
-      for (int cb = half * (D / 2); cb < (half + 1) * (D / 2); cb += 32) {
-        uint32_t r[32];
-        tmem_ld_x32(t_lane + 384 + cb, r);
+      for (int c = 0; c < HW; c += 32) {
+        const int cb = half * HW + c;
         if (row_valid) {
           if (final_out) {
             uint4* dst = reinterpret_cast<uint4*>(a.dq + (grow * a.hq + head) * D + cb);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * a.scale,
-                                __uint_as_float(r[8 * v + 1]) * a.scale);
-              w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * a.scale,
-                                __uint_as_float(r[8 * v + 3]) * a.scale);
-              w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * a.scale,
-                                __uint_as_float(r[8 * v + 5]) * a.scale);
-              w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * a.scale,
-                                __uint_as_float(r[8 * v + 7]) * a.scale);
+              w.x = pack_bf16x2(__uint_as_float(r[c + 8 * v + 0]) * a.scale,
+                                __uint_as_float(r[c + 8 * v + 1]) * a.scale);
+              w.y = pack_bf16x2(__uint_as_float(r[c + 8 * v + 2]) * a.scale,
+                                __uint_as_float(r[c + 8 * v + 3]) * a.scale);
+              w.z = pack_bf16x2(__uint_as_float(r[c + 8 * v + 4]) * a.scale,
+                                __uint_as_float(r[c + 8 * v + 5]) * a.scale);
+              w.w = pack_bf16x2(__uint_as_float(r[c + 8 * v + 6]) * a.scale,
+                                __uint_as_float(r[c + 8 * v + 7]) * a.scale);
               dst[v] = w;
             }
           } else {
@@ -411,22 +422,20 @@ __global__ void __launch_bounds__(320, 1)
                           (size_t)(cb / 4) * kTileM + row;
 #pragma unroll
             for (int v = 0; v < 8; ++v)
-              dst[(size_t)v * kTileM] = make_float4(__uint_as_float(r[4 * v + 0]) * a.scale,
-                                                    __uint_as_float(r[4 * v + 1]) * a.scale,
-                                                    __uint_as_float(r[4 * v + 2]) * a.scale,
-                                                    __uint_as_float(r[4 * v + 3]) * a.scale);
+              dst[(size_t)v * kTileM] = make_float4(__uint_as_float(r[c + 4 * v + 0]) * a.scale,
+                                                    __uint_as_float(r[c + 4 * v + 1]) * a.scale,
+                                                    __uint_as_float(r[c + 4 * v + 2]) * a.scale,
+                                                    __uint_as_float(r[c + 4 * v + 3]) * a.scale);
           }
         }
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dqfree);
       ++seg;
     }
   }
 
   tc_fence_before_sync();
   __syncthreads();
+  CFA_TRACE_CTA(1);
   if (warp == 9) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
@@ -731,37 +740,43 @@ __global__ void __launch_bounds__(320, 1)
       if (!(ok = warp_wait(W, bar_dkvfull, (uint32_t)items & 1u))) break;
       tc_fence_after_sync();
       const size_t grow = (size_t)(it.c0 + key) * a.hkv + it.hk;
-#pragma unroll
-      for (int cb = half * (D / 2); cb < (half + 1) * (D / 2); cb += 32) {
-        uint32_t rv[32], rk[32];
-        tmem_ld_x32(t_dv + ((uint32_t)(quad * 32) << 16) + cb, rv);
-        tmem_ld_x32(t_dk + ((uint32_t)(quad * 32) << 16) + cb, rk);
-        if (key_valid) {
-          uint4* dv = reinterpret_cast<uint4*>(a.dv + grow * D + cb);
-          uint4* dk = reinterpret_cast<uint4*>(a.dk + grow * D + cb);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 u, w;
-            u.x = pack_bf16x2(__uint_as_float(rv[8 * v + 0]), __uint_as_float(rv[8 * v + 1]));
-            u.y = pack_bf16x2(__uint_as_float(rv[8 * v + 2]), __uint_as_float(rv[8 * v + 3]));
-            u.z = pack_bf16x2(__uint_as_float(rv[8 * v + 4]), __uint_as_float(rv[8 * v + 5]));
-            u.w = pack_bf16x2(__uint_as_float(rv[8 * v + 6]), __uint_as_float(rv[8 * v + 7]));
-            w.x = pack_bf16x2(__uint_as_float(rk[8 * v + 0]) * a.scale,
-                              __uint_as_float(rk[8 * v + 1]) * a.scale);
-            w.y = pack_bf16x2(__uint_as_float(rk[8 * v + 2]) * a.scale,
-                              __uint_as_float(rk[8 * v + 3]) * a.scale);
-            w.z = pack_bf16x2(__uint_as_float(rk[8 * v + 4]) * a.scale,
-                              __uint_as_float(rk[8 * v + 5]) * a.scale);
-            w.w = pack_bf16x2(__uint_as_float(rk[8 * v + 6]) * a.scale,
-                              __uint_as_float(rk[8 * v + 7]) * a.scale);
-            dv[v] = u;
-            dk[v] = w;
-          }
-        }
+      // this warp's half of the dV and dK rows in two TMEM loads, then the
+      // hand-off (before the global stores, which the arrive would wait for)
+      constexpr int HW = D / 2;
+      uint32_t rv[HW], rk[HW];
+      const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+      if constexpr (HW == 64) {
+        tmem_ld_x64(t_dv + lane_off + half * HW, rv);
+        tmem_ld_x64(t_dk + lane_off + half * HW, rk);
+      } else {
+        tmem_ld_x32(t_dv + lane_off + half * HW, rv);
+        tmem_ld_x32(t_dk + lane_off + half * HW, rk);
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dkvfree);  // dK/dV read: the next item may overwrite
+      if (key_valid) {
+        uint4* dv = reinterpret_cast<uint4*>(a.dv + grow * D + half * HW);
+        uint4* dk = reinterpret_cast<uint4*>(a.dk + grow * D + half * HW);
+#pragma unroll
+        for (int v = 0; v < HW / 8; ++v) {
+          uint4 u, w;
+          u.x = pack_bf16x2(__uint_as_float(rv[8 * v + 0]), __uint_as_float(rv[8 * v + 1]));
+          u.y = pack_bf16x2(__uint_as_float(rv[8 * v + 2]), __uint_as_float(rv[8 * v + 3]));
+          u.z = pack_bf16x2(__uint_as_float(rv[8 * v + 4]), __uint_as_float(rv[8 * v + 5]));
+          u.w = pack_bf16x2(__uint_as_float(rv[8 * v + 6]), __uint_as_float(rv[8 * v + 7]));
+          w.x = pack_bf16x2(__uint_as_float(rk[8 * v + 0]) * a.scale,
+                            __uint_as_float(rk[8 * v + 1]) * a.scale);
+          w.y = pack_bf16x2(__uint_as_float(rk[8 * v + 2]) * a.scale,
+                            __uint_as_float(rk[8 * v + 3]) * a.scale);
+          w.z = pack_bf16x2(__uint_as_float(rk[8 * v + 4]) * a.scale,
+                            __uint_as_float(rk[8 * v + 5]) * a.scale);
+          w.w = pack_bf16x2(__uint_as_float(rk[8 * v + 6]) * a.scale,
+                            __uint_as_float(rk[8 * v + 7]) * a.scale);
+          dv[v] = u;
+          dk[v] = w;
+        }
+      }
       qn += n;
       ++items;
     }
@@ -799,9 +814,8 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
   const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
   if (qb >= blocks_of_window(tl, lc)) return;
   if (threadIdx.x == 0) {
-    long long bs = a.win_prefix[b] + (long long)hk * head_work(tl, lp, lc);
-    for (int q = 0; q < qb; ++q) bs += block_key_tiles(lp, lc, q * tl.tpt, tl.tpt);
-    const long long be = bs + block_key_tiles(lp, lc, qb * tl.tpt, tl.tpt);
+    long long bs, be;  // the block's key-tile iterations
+    block_span(tl, a.win_prefix[b], hk, qb, lp, lc, &bs, &be);
     n_parts = block_parts(bs, be, a.win_prefix[a.batch], tl.grid, parts, kMaxParts);
   }
   __syncthreads();
@@ -813,16 +827,30 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
   float acc[CW];
 #pragma unroll
   for (int e = 0; e < CW; ++e) acc[e] = 0.f;
-  for (int j = 0; j < np; ++j) {
-    const size_t slot = (size_t)parts[j] * 2 + (j == 0);
-    const float4* src = reinterpret_cast<const float4*>(a.dq_part) + slot * (D / 4) * kTileM;
+  // the loads of kBatch parts are issued before any is used (latency-bound:
+  // a handful of parts per row); parts are summed in CTA order
+  constexpr int kBatch = 4;
+  for (int j0 = 0; j0 < np; j0 += kBatch) {
+    float4 v[kBatch][CW / 4];
 #pragma unroll
-    for (int e = 0; e < CW; e += 4) {
-      const float4 v = src[(size_t)((c0col + e) >> 2) * kTileM + row];
-      acc[e] += v.x;
-      acc[e + 1] += v.y;
-      acc[e + 2] += v.z;
-      acc[e + 3] += v.w;
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = j0 + u;
+      const size_t slot = (size_t)parts[j < np ? j : 0] * 2 + (j == 0);
+      const float4* src = reinterpret_cast<const float4*>(a.dq_part) + slot * (D / 4) * kTileM;
+#pragma unroll
+      for (int e = 0; e < CW; e += 4)
+        v[u][e / 4] = (j < np) ? src[(size_t)((c0col + e) >> 2) * kTileM + row]
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+#pragma unroll
+      for (int e = 0; e < CW; e += 4) {
+        acc[e] += v[u][e / 4].x;
+        acc[e + 1] += v[u][e / 4].y;
+        acc[e + 2] += v[u][e / 4].z;
+        acc[e + 3] += v[u][e / 4].w;
+      }
     }
   }
   const size_t grow = (size_t)(c0 + token);
@@ -1013,6 +1041,11 @@ cudaError_t launch_dequant_q8_0(const uint8_t* blocks, long long n_blocks, float
 }  // namespace cfa
 
 #ifdef CFA_TRACE_BUILD
+extern "C" int cfa_trace_read_cta_bwd(unsigned long long* dst) {
+  return cudaMemcpyFromSymbol(dst, cfa::cfa_trace_cta, sizeof(unsigned long long) * 2048) ==
+                 cudaSuccess ? 0 : -1;
+}
+
 extern "C" int cfa_trace_read_bwd(long long* dst, int clear) {
   const size_t n = sizeof(long long) * cfa::kTraceRoles * cfa::kTraceIters * cfa::kTraceEvents;
   if (dst && cudaMemcpyFromSymbol(dst, cfa::cfa_trace_buf, n) != cudaSuccess) return -1;

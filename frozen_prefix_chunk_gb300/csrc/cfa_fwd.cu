@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(352, 1)
       const bool row_valid = row < tl.rows && token < sg.lc;
       float m = -INFINITY, l = 0.f;
       for (int i = 0; i < n; ++i, ++u) {
+        if (i == 0 && quad == 0 && lane == 0) CFA_TRACE(5, 10 + us, 4 * qt);
         if (qt == 0 && quad == 0) {
           // V(u) and K(u+1) are in shared memory before P0(u) is handed over,
           // so the MMA warp need not wait for them itself; checking here,
@@ -352,6 +353,7 @@ __global__ void __launch_bounds__(352, 1)
               !(ok = warp_wait(W, bar_kfull + 8 * ((u + 1) % SK), (uint32_t)((u + 1) / SK) & 1u)))
             break;
         }
+        if (i == 0 && quad == 0 && lane == 0) CFA_TRACE(5, 10 + us, 4 * qt + 1);
         if (!(ok = warp_wait(W, bar_sfull + 8 * qt, (uint32_t)u & 1u))) break;
         if (quad == 0 && lane == 0) CFA_TRACE(qt, u, 0);
         tc_fence_after_sync();
@@ -432,38 +434,45 @@ __global__ void __launch_bounds__(352, 1)
       const size_t pslot = (size_t)blockIdx.x * 2 + slot;
       const int prow_in = qt * kTileM + row;
       const size_t prow = pslot * rows_blk + prow_in;
+      // The whole O row in one TMEM load; O_t may be overwritten by the next
+      // segment's first PV as soon as it is in registers.  The hand-off goes
+      // before the global stores: an mbarrier arrive releases the thread's
+      // earlier writes, so after the stores it would wait for them to drain.
+      uint32_t r[D];
+      if constexpr (D == 128)
+        tmem_ld_x128(t_lane + o_col, r);
+      else
+        tmem_ld_x64(t_lane + o_col, r);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ofree + 8 * qt);
+      if (row_valid) {
+        if (final_out) {
+          uint4* dst = reinterpret_cast<uint4*>(a.o + (grow * a.hq + head) * D);
 #pragma unroll
-      for (int cb = 0; cb < D; cb += 32) {
-        uint32_t r[32];
-        tmem_ld_x32(t_lane + o_col + cb, r);
-        if (row_valid) {
-          if (final_out) {
-            uint4* dst = reinterpret_cast<uint4*>(a.o + (grow * a.hq + head) * D + cb);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l,
-                                __uint_as_float(r[8 * v + 1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l,
-                                __uint_as_float(r[8 * v + 3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l,
-                                __uint_as_float(r[8 * v + 5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l,
-                                __uint_as_float(r[8 * v + 7]) * inv_l);
-              dst[v] = w;
-            }
-          } else {
-            // feature-major partial [D/4][rows][4]: a warp's store is one
-            // contiguous 512-byte run
-            float4* dst = reinterpret_cast<float4*>(a.o_part) + pslot * (D / 4) * rows_blk +
-                          (size_t)(cb / 4) * rows_blk + prow_in;
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[(size_t)v * rows_blk] = make_float4(__uint_as_float(r[4 * v + 0]) * inv_l,
-                                                      __uint_as_float(r[4 * v + 1]) * inv_l,
-                                                      __uint_as_float(r[4 * v + 2]) * inv_l,
-                                                      __uint_as_float(r[4 * v + 3]) * inv_l);
+          for (int v = 0; v < D / 8; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l,
+                              __uint_as_float(r[8 * v + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l,
+                              __uint_as_float(r[8 * v + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l,
+                              __uint_as_float(r[8 * v + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l,
+                              __uint_as_float(r[8 * v + 7]) * inv_l);
+            dst[v] = w;
           }
+        } else {
+          // feature-major partial [D/4][rows][4]: a warp's store is one
+          // contiguous 512-byte run
+          float4* dst =
+              reinterpret_cast<float4*>(a.o_part) + pslot * (D / 4) * rows_blk + prow_in;
+#pragma unroll
+          for (int v = 0; v < D / 4; ++v)
+            dst[(size_t)v * rows_blk] = make_float4(__uint_as_float(r[4 * v + 0]) * inv_l,
+                                                    __uint_as_float(r[4 * v + 1]) * inv_l,
+                                                    __uint_as_float(r[4 * v + 2]) * inv_l,
+                                                    __uint_as_float(r[4 * v + 3]) * inv_l);
         }
       }
       if (row_valid) {
@@ -473,10 +482,6 @@ __global__ void __launch_bounds__(352, 1)
           a.lse_part[prow] = lse_v;
       }
       if (quad == 0 && lane == 0) CFA_TRACE(5, us, 2 * qt + 1);
-      // O_t may now be overwritten by the next segment's first PV
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_ofree + 8 * qt);
       ++us;
     }
   }
@@ -516,9 +521,8 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
   const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
   if (qb >= blocks_of_window(tl, lc)) return;
   if (threadIdx.x == 0) {
-    long long bs = a.win_prefix[b] + (long long)hk * head_work(tl, lp, lc);
-    for (int q = 0; q < qb; ++q) bs += block_key_tiles(lp, lc, q * tok_blk, tok_blk);
-    const long long be = bs + block_key_tiles(lp, lc, qb * tok_blk, tok_blk);
+    long long bs, be;  // the block's key-tile iterations
+    block_span(tl, a.win_prefix[b], hk, qb, lp, lc, &bs, &be);
     n_parts = block_parts(bs, be, a.win_prefix[a.batch], tl.grid, parts, kMaxParts);
   }
   __syncthreads();
@@ -528,31 +532,57 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
   const int token = qb * tok_blk + qt * tl.tpt + row / tl.g;
   if (row >= tl.rows || token >= lc) return;
   const int head = hk * tl.g + row % tl.g;
+  // Two passes over the parts, each issuing the loads of kBatch parts before
+  // using any of them (the merge is latency-bound: a handful of parts per
+  // row): the LSE of the merged row, then the weighted sum of the O parts.
+  constexpr int kBatch = 4;
+  auto lse_of = [&](int j) {
+    return a.lse_part[((size_t)parts[j] * 2 + (j == 0)) * rows_blk + r];
+  };
   float mx = -INFINITY;
-  for (int j = 0; j < np; ++j)
-    mx = fmaxf(mx, a.lse_part[((size_t)parts[j] * 2 + (j == 0)) * rows_blk + r]);
+  for (int j0 = 0; j0 < np; j0 += kBatch) {
+    float ls[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) ls[u] = (j0 + u < np) ? lse_of(j0 + u) : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) mx = fmaxf(mx, ls[u]);
+  }
   float sum = 0.f;
-  for (int j = 0; j < np; ++j) {
-    const float ls = a.lse_part[((size_t)parts[j] * 2 + (j == 0)) * rows_blk + r];
-    sum += (ls == -INFINITY) ? 0.f : expf(ls - mx);
+  for (int j0 = 0; j0 < np; j0 += kBatch) {
+    float ls[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) ls[u] = (j0 + u < np) ? lse_of(j0 + u) : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) sum += (ls[u] == -INFINITY) ? 0.f : expf(ls[u] - mx);
   }
   const float lse = mx + logf(sum);
   float acc[CW];
 #pragma unroll
   for (int e = 0; e < CW; ++e) acc[e] = 0.f;
-  for (int j = 0; j < np; ++j) {
-    const size_t slot = (size_t)parts[j] * 2 + (j == 0);
-    const float ls = a.lse_part[slot * rows_blk + r];
-    if (ls == -INFINITY) continue;
-    const float w = expf(ls - lse);
-    const float4* src = reinterpret_cast<const float4*>(a.o_part) + slot * (D / 4) * rows_blk;
+  for (int j0 = 0; j0 < np; j0 += kBatch) {
+    float w[kBatch];
+    float4 v[kBatch][CW / 4];
 #pragma unroll
-    for (int e = 0; e < CW; e += 4) {
-      const float4 v = src[(size_t)((c0col + e) >> 2) * rows_blk + r];
-      acc[e] = fmaf(w, v.x, acc[e]);
-      acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
-      acc[e + 2] = fmaf(w, v.z, acc[e + 2]);
-      acc[e + 3] = fmaf(w, v.w, acc[e + 3]);
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = j0 + u;
+      const size_t slot = (size_t)parts[j < np ? j : 0] * 2 + (j == 0);
+      const float ls = (j < np) ? a.lse_part[slot * rows_blk + r] : -INFINITY;
+      w[u] = (ls == -INFINITY) ? 0.f : expf(ls - lse);
+      const float4* src = reinterpret_cast<const float4*>(a.o_part) + slot * (D / 4) * rows_blk;
+#pragma unroll
+      for (int e = 0; e < CW; e += 4)
+        v[u][e / 4] = (j < np) ? src[(size_t)((c0col + e) >> 2) * rows_blk + r]
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+#pragma unroll
+      for (int e = 0; e < CW; e += 4) {
+        acc[e] = fmaf(w[u], v[u][e / 4].x, acc[e]);
+        acc[e + 1] = fmaf(w[u], v[u][e / 4].y, acc[e + 1]);
+        acc[e + 2] = fmaf(w[u], v[u][e / 4].z, acc[e + 2]);
+        acc[e + 3] = fmaf(w[u], v[u][e / 4].w, acc[e + 3]);
+      }
     }
   }
   const size_t grow = (size_t)(c0 + token);

@@ -22,6 +22,9 @@ __device__ __forceinline__ unsigned long long global_timer_ns_raw() {
 }
 
 #ifdef CFA_TRACE_BUILD
+#ifndef CFA_TRACE_BLOCK
+#define CFA_TRACE_BLOCK 0  // the CTA whose roles are traced
+#endif
 constexpr int kTraceRoles = 6, kTraceIters = 96, kTraceEvents = 8;
 static __device__ long long cfa_trace_buf[kTraceRoles * kTraceIters * kTraceEvents];
 static __device__ unsigned long long cfa_trace_cta[2 * 1024];  // per-CTA start / end (ns)
@@ -32,7 +35,8 @@ static __device__ unsigned long long cfa_trace_cta[2 * 1024];  // per-CTA start 
   } while (0)
 #define CFA_TRACE(role, iter, ev)                                                          \
   do {                                                                                     \
-    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (iter) < cfa::kTraceIters) \
+    if (blockIdx.x == CFA_TRACE_BLOCK && blockIdx.y == 0 && blockIdx.z == 0 &&            \
+        (iter) < cfa::kTraceIters)                                                         \
       cfa::cfa_trace_buf[((role) * cfa::kTraceIters + (iter)) * cfa::kTraceEvents + (ev)] = \
           clock64();                                                                       \
   } while (0)

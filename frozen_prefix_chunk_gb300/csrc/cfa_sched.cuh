@@ -38,6 +38,7 @@ struct Tiling {
   int rows;       // valid rows per query tile = tpt * g
   int q_per_cta;  // query tiles per query block
   int grid;       // persistent CTAs (G)
+  int setup;      // virtual iterations charged at the start of every query block
 };
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -53,13 +54,32 @@ __host__ __device__ inline int blocks_of_window(const Tiling& tl, int lc) {
   return lc > 0 ? ceil_div(lc, tl.q_per_cta * tl.tpt) : 0;
 }
 
+// Iterations charged to query block qb: its key tiles plus tl.setup virtual
+// ones at its start.  They stand for the fixed cost of taking up a block in a
+// CTA (its Q load, the epilogue of the block before, the pipeline refill), so
+// that a CTA whose range crosses a block start gets fewer key tiles and all
+// CTAs finish together.  Virtual iterations do no work.
+__host__ __device__ inline int block_iters(const Tiling& tl, int lp, int lc, int qb) {
+  const int tok_blk = tl.q_per_cta * tl.tpt;
+  return tl.setup + block_key_tiles(lp, lc, qb * tok_blk, tok_blk);
+}
+
 // Iterations of one KV head's query blocks in a window.
 __host__ __device__ inline long long head_work(const Tiling& tl, int lp, int lc) {
-  const int tok_blk = tl.q_per_cta * tl.tpt;
   long long w = 0;
-  for (int qb = 0, nb = blocks_of_window(tl, lc); qb < nb; ++qb)
-    w += block_key_tiles(lp, lc, qb * tok_blk, tok_blk);
+  for (int qb = 0, nb = blocks_of_window(tl, lc); qb < nb; ++qb) w += block_iters(tl, lp, lc, qb);
   return w;
+}
+
+// Iterations [*first, *end) holding the key tiles of query block (b, hk, qb),
+// given the window's first iteration w0 (its virtual iterations come before
+// *first).
+__host__ __device__ inline void block_span(const Tiling& tl, long long w0, int hk, int qb, int lp,
+                                           int lc, long long* first, long long* end) {
+  long long bs = w0 + (long long)hk * head_work(tl, lp, lc);
+  for (int q = 0; q < qb; ++q) bs += block_iters(tl, lp, lc, q);
+  *first = bs + tl.setup;
+  *end = bs + block_iters(tl, lp, lc, qb);
 }
 
 // First iteration of CTA c, and the CTA that holds iteration x.
@@ -109,48 +129,53 @@ struct SegmentWalker {
     long long o = cur - pre_b0;
     hk = (int)(o / hw);
     o -= (long long)hk * hw;
-    const int tok_blk = tl.q_per_cta * tl.tpt;
     qb = 0;
     for (;;) {
-      const int nk = block_key_tiles(lp, lc, qb * tok_blk, tok_blk);
+      const int nk = block_iters(tl, lp, lc, qb);
       if (o < nk) break;
       o -= nk;
       ++qb;
     }
-    tile = (int)o;
+    tile = (int)o;  // iteration within the block, virtual ones first
   }
 
+  // The next segment with key tiles; blocks of which this CTA holds only
+  // virtual iterations are passed over.
   __device__ bool next(Segment& s) {
-    if (cur >= end) return false;
-    const int tok_blk = tl.q_per_cta * tl.tpt;
-    s.b = b;
-    s.hk = hk;
-    s.qb = qb;
-    s.p0 = cu_p[b];
-    s.lp = cu_p[b + 1] - s.p0;
-    s.c0 = cu_c[b];
-    s.lc = cu_c[b + 1] - s.c0;
-    s.n_kt = block_key_tiles(s.lp, s.lc, qb * tok_blk, tok_blk);
-    s.t_begin = tile;
-    const long long left = end - cur;
-    s.t_end = (left < (long long)(s.n_kt - tile)) ? tile + (int)left : s.n_kt;
-    s.nq = ceil_div(s.lc - qb * tok_blk, tl.tpt);
-    if (s.nq > tl.q_per_cta) s.nq = tl.q_per_cta;
-    s.head = tile > 0;
-    s.tail = s.t_end < s.n_kt;
-    cur += s.t_end - s.t_begin;
-    // advance to the next query block
-    tile = 0;
-    if (++qb >= blocks_of_window(tl, s.lc)) {
-      qb = 0;
-      if (++hk >= hkv) {
-        hk = 0;
-        do {
-          ++b;
-        } while (b < batch && cu_c[b + 1] - cu_c[b] == 0);
+    while (cur < end) {
+      const int tok_blk = tl.q_per_cta * tl.tpt;
+      s.b = b;
+      s.hk = hk;
+      s.qb = qb;
+      s.p0 = cu_p[b];
+      s.lp = cu_p[b + 1] - s.p0;
+      s.c0 = cu_c[b];
+      s.lc = cu_c[b + 1] - s.c0;
+      const int ni = block_iters(tl, s.lp, s.lc, qb);
+      s.n_kt = ni - tl.setup;
+      const long long left = end - cur;
+      const int v_end = (left < (long long)(ni - tile)) ? tile + (int)left : ni;
+      s.t_begin = tile > tl.setup ? tile - tl.setup : 0;
+      s.t_end = v_end - tl.setup;
+      s.nq = ceil_div(s.lc - qb * tok_blk, tl.tpt);
+      if (s.nq > tl.q_per_cta) s.nq = tl.q_per_cta;
+      s.head = s.t_begin > 0;
+      s.tail = s.t_end < s.n_kt;
+      cur += v_end - tile;
+      // advance to the next query block
+      tile = 0;
+      if (++qb >= blocks_of_window(tl, s.lc)) {
+        qb = 0;
+        if (++hk >= hkv) {
+          hk = 0;
+          do {
+            ++b;
+          } while (b < batch && cu_c[b + 1] - cu_c[b] == 0);
+        }
       }
+      if (s.t_end > s.t_begin) return true;
     }
-    return true;
+    return false;
   }
 };
 
