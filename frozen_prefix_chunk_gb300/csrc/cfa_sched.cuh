@@ -27,6 +27,12 @@
 
 #include <stdint.h>
 
+#ifndef __CUDACC__
+// host-only build of the schedule logic (the CPU schedule test)
+#define __host__
+#define __device__
+#endif
+
 namespace cfa {
 
 constexpr int kTileM = 128;  // query rows per tile (TMEM lanes)
@@ -113,8 +119,9 @@ struct SegmentWalker {
 
   // Start at CTA `cta`'s first iteration: window b0 (whose first iteration
   // is pre_b0) of a schedule with `total` iterations.
-  __device__ void init(const int32_t* cp, const int32_t* cc, int nb, int nkv, const Tiling& t,
-                       int cta, long long total, int b0, long long pre_b0) {
+  __host__ __device__ void init(const int32_t* cp, const int32_t* cc, int nb, int nkv,
+                                const Tiling& t, int cta, long long total, int b0,
+                                long long pre_b0) {
     cu_p = cp;
     cu_c = cc;
     batch = nb;
@@ -141,7 +148,7 @@ struct SegmentWalker {
 
   // The next segment with key tiles; blocks of which this CTA holds only
   // virtual iterations are passed over.
-  __device__ bool next(Segment& s) {
+  __host__ __device__ bool next(Segment& s) {
     while (cur < end) {
       const int tok_blk = tl.q_per_cta * tl.tpt;
       s.b = b;
@@ -184,8 +191,8 @@ struct SegmentWalker {
 // be - 1 whose range is not empty (ranges are only empty when there are fewer
 // iterations than CTAs).  Returns the count; 0 when one CTA holds the whole
 // block.  `parts` has room for `cap` entries.
-__device__ inline int block_parts(long long bs, long long be, long long total, int G, int* parts,
-                                  int cap) {
+__host__ __device__ inline int block_parts(long long bs, long long be, long long total, int G,
+                                           int* parts, int cap) {
   const int cf = cta_of(bs, total, G), cl = cta_of(be - 1, total, G);
   if (cf == cl) return 0;
   int n = 0;
@@ -196,6 +203,7 @@ __device__ inline int block_parts(long long bs, long long be, long long total, i
   return n;
 }
 
+#ifdef __CUDACC__
 // Prologue of the persistent kernels, run by all `nthreads` threads of the
 // CTA: scans the per-window iteration counts (each thread sums a contiguous
 // run of windows; warp shuffles and a shared array of warp totals turn the
@@ -247,5 +255,7 @@ __device__ inline void plan_schedule(const int32_t* cu_p, const int32_t* cu_c, i
   }
   __syncthreads();
 }
+
+#endif  // __CUDACC__
 
 }  // namespace cfa

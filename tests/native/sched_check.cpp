@@ -1,0 +1,111 @@
+// Host-side check of the stream-K schedule in cfa_sched.cuh (the logic every
+// persistent kernel runs on the device): for one configuration read from the
+// command line it walks every CTA's iteration range and checks that
+//   * every key tile of every query block is covered by exactly one segment,
+//     in increasing order, and no segment is empty;
+//   * a segment's head / tail flags say whether earlier / later key tiles of
+//     its block belong to other CTAs;
+//   * block_parts lists exactly the CTAs holding a segment of the block, in
+//     CTA order, the one without `head` first;
+//   * each CTA's iterations, virtual setup ones included, are within one of
+//     the mean.
+// Prints "OK <total iterations> <segments>" or the first violation.
+#include <cstdio>
+#include <cstdlib>
+#include <map>
+#include <vector>
+
+#include "cfa_sched.cuh"
+
+using namespace cfa;
+
+int main(int argc, char** argv) {
+  // args: G hkv g q_per_cta setup batch lp_0 lc_0 lp_1 lc_1 ...
+  if (argc < 7) return 2;
+  const int G = atoi(argv[1]), hkv = atoi(argv[2]), g = atoi(argv[3]);
+  const int qpc = atoi(argv[4]), setup = atoi(argv[5]), batch = atoi(argv[6]);
+  if (argc != 7 + 2 * batch) return 2;
+  std::vector<int32_t> cu_p(batch + 1, 0), cu_c(batch + 1, 0);
+  for (int b = 0; b < batch; ++b) {
+    cu_p[b + 1] = cu_p[b] + atoi(argv[7 + 2 * b]);
+    cu_c[b + 1] = cu_c[b] + atoi(argv[8 + 2 * b]);
+  }
+  Tiling tl;
+  tl.g = g;
+  tl.tpt = kTileM / g;
+  tl.rows = tl.tpt * g;
+  tl.q_per_cta = qpc;
+  tl.grid = G;
+  tl.setup = setup;
+  // window prefixes, as plan_schedule computes them on the device
+  std::vector<long long> wp(batch + 1, 0);
+  for (int b = 0; b < batch; ++b)
+    wp[b + 1] = wp[b] + (long long)hkv * head_work(tl, cu_p[b + 1] - cu_p[b], cu_c[b + 1] - cu_c[b]);
+  const long long W = wp[batch];
+  // (b, hk, qb) -> segments as (cta, t_begin, t_end, head, tail)
+  struct Seg { int cta, tb, te; bool head, tail; };
+  std::map<long long, std::vector<Seg>> by_block;
+  long long n_seg = 0;
+  for (int c = 0; c < G; ++c) {
+    const long long start = cta_begin(c, W, G);
+    if (start >= cta_begin(c + 1, W, G)) continue;
+    int b0 = -1;
+    for (int b = 0; b < batch; ++b)
+      if (wp[b + 1] > wp[b] && wp[b] <= start && start < wp[b + 1]) b0 = b;
+    if (b0 < 0) { printf("FAIL cta %d: no window holds iteration %lld\n", c, start); return 1; }
+    SegmentWalker walk;
+    walk.init(cu_p.data(), cu_c.data(), batch, hkv, tl, c, W, b0, wp[b0]);
+    Segment sg;
+    long long last_key = -1;
+    while (walk.next(sg)) {
+      ++n_seg;
+      if (sg.t_end <= sg.t_begin) { printf("FAIL cta %d: empty segment\n", c); return 1; }
+      const long long key = ((long long)sg.b * hkv + sg.hk) * 1000000 + sg.qb;
+      if (key <= last_key) { printf("FAIL cta %d: blocks out of order\n", c); return 1; }
+      last_key = key;
+      by_block[key].push_back({c, sg.t_begin, sg.t_end, sg.head, sg.tail});
+    }
+  }
+  long long n_blocks = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int lp = cu_p[b + 1] - cu_p[b], lc = cu_c[b + 1] - cu_c[b];
+    for (int hk = 0; hk < hkv; ++hk)
+      for (int qb = 0, nb = blocks_of_window(tl, lc); qb < nb; ++qb) {
+        ++n_blocks;
+        const long long key = ((long long)b * hkv + hk) * 1000000 + qb;
+        const int nk = block_iters(tl, lp, lc, qb) - setup;
+        const auto& v = by_block[key];
+        int next = 0;
+        for (size_t i = 0; i < v.size(); ++i) {
+          if (v[i].tb != next) { printf("FAIL block %lld: gap or overlap at tile %d\n", key, next); return 1; }
+          if (v[i].head != (v[i].tb > 0) || v[i].tail != (v[i].te < nk)) {
+            printf("FAIL block %lld: head/tail flags\n", key); return 1;
+          }
+          if (i > 0 && v[i].cta <= v[i - 1].cta) { printf("FAIL block %lld: CTA order\n", key); return 1; }
+          next = v[i].te;
+        }
+        if (next != nk) { printf("FAIL block %lld: covers %d of %d tiles\n", key, next, nk); return 1; }
+        long long first, end;
+        block_span(tl, wp[b], hk, qb, lp, lc, &first, &end);
+        int parts[4096];
+        const int np = block_parts(first, end, W, G, parts, 4096);
+        if (v.size() == 1) {
+          if (np != 0) { printf("FAIL block %lld: one holder but %d parts\n", key, np); return 1; }
+        } else {
+          if (np != (int)v.size()) { printf("FAIL block %lld: %d parts, %zu holders\n", key, np, v.size()); return 1; }
+          for (int i = 0; i < np; ++i)
+            if (parts[i] != v[i].cta) { printf("FAIL block %lld: part %d is CTA %d, holder %d\n", key, i, parts[i], v[i].cta); return 1; }
+        }
+      }
+  }
+  // balance: iterations per CTA differ by at most one
+  long long lo = W, hi = 0;
+  for (int c = 0; c < G; ++c) {
+    const long long n = cta_begin(c + 1, W, G) - cta_begin(c, W, G);
+    lo = n < lo ? n : lo;
+    hi = n > hi ? n : hi;
+  }
+  if (hi - lo > 1) { printf("FAIL balance %lld..%lld\n", lo, hi); return 1; }
+  printf("OK %lld %lld %lld\n", W, n_seg, n_blocks);
+  return 0;
+}

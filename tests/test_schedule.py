@@ -1,0 +1,61 @@
+"""The stream-K schedule (cfa_sched.cuh) checked on the host.
+
+The persistent forward and dQ kernels split the (query block, key tile)
+iterations of every window and KV head evenly over the grid; the same header
+compiles for the host, and tests/native/sched_check.cpp walks every CTA's
+range and checks coverage, ordering, the head/tail flags and the part lists
+the split merges use.  Configurations span the benchmark layers, GQA group
+sizes, ragged and empty windows and grids larger than the work.
+"""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "tests", "native", "sched_check.cpp")
+INC = os.path.join(ROOT, "frozen_prefix_chunk_gb300", "csrc")
+
+
+@pytest.fixture(scope="module")
+def checker(tmp_path_factory):
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if not cxx:
+        pytest.skip("no C++ compiler")
+    exe = str(tmp_path_factory.mktemp("sched") / "sched_check")
+    subprocess.check_call([cxx, "-O1", "-std=c++17", "-x", "c++", "-I", INC, SRC, "-o", exe])
+    return exe
+
+
+VARLEN8_LP = [7328, 14558, 6267, 22159, 13492, 16783, 15051, 21922]
+
+CASES = [
+    # G, hkv, g, q_per_cta, setup, [(lp, lc), ...]
+    (152, 8, 4, 2, 2, [(16128, 256)]),                  # 8B layer, forward tiling
+    (152, 8, 4, 1, 2, [(16128, 256)]),                  # 8B layer, dQ tiling
+    (149, 8, 4, 1, 2, [(16128, 256)]),                  # dQ beside dK/dV on 3 SMs
+    (152, 8, 4, 2, 2, [(lp, 256) for lp in VARLEN8_LP]),
+    (150, 8, 4, 1, 2, [(lp, 256) for lp in VARLEN8_LP]),
+    (152, 8, 4, 2, 2, [(62976, 512)]),                  # 63k window
+    (152, 8, 2, 2, 2, [(1536, 512)]),                   # 1.7B layer
+    (152, 1, 2, 1, 2, [(256, 64)]),                     # tiny: fewer iterations than CTAs
+    (152, 2, 4, 2, 0, [(5, 37), (0, 100), (700, 0), (128, 256)]),
+    (152, 2, 4, 1, 3, [(5, 37), (0, 100), (700, 0), (128, 256)]),
+    (7, 4, 1, 2, 2, [(129, 130), (4096, 3)]),
+    (13, 2, 3, 1, 2, [(257, 77), (1000, 200)]),
+    (152, 1, 8, 2, 2, [(1000, 200)]),
+    (1, 2, 4, 2, 2, [(300, 1), (0, 64)]),
+    (64, 4, 4, 1, 5, [(1000, 512), (300, 256)]),        # CTA boundaries inside setup iterations
+    (40, 8, 4, 1, 4, [(2000, 256), (500, 128), (64, 64)]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
+def test_schedule_covers_every_tile_once(checker, case):
+    G, hkv, g, qpc, setup, wins = case
+    args = [str(x) for x in (G, hkv, g, qpc, setup, len(wins))]
+    for lp, lc in wins:
+        args += [str(lp), str(lc)]
+    r = subprocess.run([checker] + args, capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.startswith("OK"), r.stdout + r.stderr
