@@ -65,7 +65,7 @@ int validate(const cfa_args* a) {
   if (!a) return CFA_ERR_INVALID_ARG;
   if (a->batch < 1 || a->batch > 65535) return CFA_ERR_INVALID_ARG;
   if (a->hq < 1 || a->hkv < 1 || a->hkv > 65535 || a->hq % a->hkv != 0) return CFA_ERR_INVALID_ARG;
-  if (a->hq / a->hkv > 128) return CFA_ERR_UNSUPPORTED;
+  if (a->hq / a->hkv > 128 || a->hq > 65535) return CFA_ERR_UNSUPPORTED;
   if (a->head_dim != 64 && a->head_dim != 128) return CFA_ERR_UNSUPPORTED;
   if (a->prefix_dtype != CFA_PREFIX_BF16 && a->prefix_dtype != CFA_PREFIX_Q8_0)
     return CFA_ERR_INVALID_ARG;

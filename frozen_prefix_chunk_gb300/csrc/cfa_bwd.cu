@@ -862,33 +862,48 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
                             pack_bf16x2(acc[e + 6], acc[e + 7]));
 }
 
-// delta[h, t] = sum_c dO[t, h, c] * O[t, h, c]; one warp per (t, h) row.
+// delta[h, t] = sum_c dO[t, h, c] * O[t, h, c].  A CTA takes kDeltaRows
+// consecutive tokens of one head (blockIdx.y), so its delta writes are one
+// contiguous run; D/8 threads share a row, each loading 16 bytes of O and of
+// dO, with every load of the thread issued before the first use.
+constexpr int kDeltaRows = 32;
 template <int D>
 __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restrict__ o,
                                                     const __nv_bfloat16* __restrict__ dout,
                                                     float* __restrict__ delta, int total_lc,
                                                     int hq) {
   pdl_start();
-  constexpr int E = D / 32;
-  const long long rid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (rid >= (long long)total_lc * hq) return;
-  const __nv_bfloat16* po = o + rid * D + lane * E;
-  const __nv_bfloat16* pd = dout + rid * D + lane * E;
-  float sum = 0.f;
+  constexpr int TPR = D / 8;              // threads per row
+  constexpr int RPP = 256 / TPR;          // rows per pass of the CTA
+  constexpr int NP = kDeltaRows / RPP;    // passes
+  const int h = blockIdx.y;
+  const int sub = threadIdx.x / TPR, part = threadIdx.x % TPR;
+  uint4 xo[NP], xd[NP];
 #pragma unroll
-  for (int e = 0; e < E; e += 2) {
-    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(po + e);
-    const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(pd + e);
-    const float2 fx = __bfloat1622float2(x), fy = __bfloat1622float2(y);
-    sum = fmaf(fx.x, fy.x, sum);
-    sum = fmaf(fx.y, fy.y, sum);
+  for (int p = 0; p < NP; ++p) {
+    const long long t = (long long)blockIdx.x * kDeltaRows + p * RPP + sub;
+    xo[p] = xd[p] = make_uint4(0u, 0u, 0u, 0u);
+    if (t < total_lc) {
+      const size_t off = ((size_t)t * hq + h) * D + part * 8;
+      xo[p] = *reinterpret_cast<const uint4*>(o + off);
+      xd[p] = *reinterpret_cast<const uint4*>(dout + off);
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  if (lane == 0) {
-    const long long t = rid / hq, h = rid % hq;
-    delta[h * total_lc + t] = sum;
+  for (int p = 0; p < NP; ++p) {
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&xo[p]);
+    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&xd[p]);
+    float sum = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fx = __bfloat1622float2(x[e]), fy = __bfloat1622float2(y[e]);
+      sum = fmaf(fx.x, fy.x, sum);
+      sum = fmaf(fx.y, fy.y, sum);
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const long long t = (long long)blockIdx.x * kDeltaRows + p * RPP + sub;
+    if (part == 0 && t < total_lc) delta[(size_t)h * total_lc + t] = sum;
   }
 }
 
@@ -1021,8 +1036,7 @@ cudaError_t launch_bwd_dq_reduce(const BwdArgs& a, int d, int max_lc, cudaStream
 
 cudaError_t launch_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, float* delta,
                          int total_lc, int hq, int d, cudaStream_t st) {
-  const long long threads = (long long)total_lc * hq * 32;
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  const dim3 blocks((unsigned)((total_lc + kDeltaRows - 1) / kDeltaRows), (unsigned)hq);
   if (d == 128)
     delta_kernel<128><<<blocks, 256, 0, st>>>(o, dout, delta, total_lc, hq);
   else

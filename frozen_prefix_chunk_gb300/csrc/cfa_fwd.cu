@@ -532,57 +532,75 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
   const int token = qb * tok_blk + qt * tl.tpt + row / tl.g;
   if (row >= tl.rows || token >= lc) return;
   const int head = hk * tl.g + row % tl.g;
-  // Two passes over the parts, each issuing the loads of kBatch parts before
-  // using any of them (the merge is latency-bound: a handful of parts per
-  // row): the LSE of the merged row, then the weighted sum of the O parts.
+  // The merge is latency-bound (a handful of parts per row): loads are issued
+  // kBatch parts at a time before any is used.  With at most kBatch parts (the
+  // common case) the LSE and O loads go out together, one round trip; more
+  // parts take an online max/sum pass over the LSEs, then the O pass.
   constexpr int kBatch = 4;
-  auto lse_of = [&](int j) {
-    return a.lse_part[((size_t)parts[j] * 2 + (j == 0)) * rows_blk + r];
-  };
-  float mx = -INFINITY;
-  for (int j0 = 0; j0 < np; j0 += kBatch) {
-    float ls[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) ls[u] = (j0 + u < np) ? lse_of(j0 + u) : -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) mx = fmaxf(mx, ls[u]);
-  }
-  float sum = 0.f;
-  for (int j0 = 0; j0 < np; j0 += kBatch) {
-    float ls[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) ls[u] = (j0 + u < np) ? lse_of(j0 + u) : -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) sum += (ls[u] == -INFINITY) ? 0.f : expf(ls[u] - mx);
-  }
-  const float lse = mx + logf(sum);
+  auto slot_of = [&](int j) { return (size_t)parts[j < np ? j : 0] * 2 + (j == 0); };
+  const float4* o4 = reinterpret_cast<const float4*>(a.o_part);
   float acc[CW];
 #pragma unroll
   for (int e = 0; e < CW; ++e) acc[e] = 0.f;
-  for (int j0 = 0; j0 < np; j0 += kBatch) {
-    float w[kBatch];
-    float4 v[kBatch][CW / 4];
+  float lse;
+  auto accumulate = [&](int j0, const float (&ls)[kBatch], const float4 (&v)[kBatch][CW / 4]) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const float w = (j0 + u < np && ls[u] != -INFINITY) ? expf(ls[u] - lse) : 0.f;
+#pragma unroll
+      for (int e = 0; e < CW; e += 4) {
+        acc[e] = fmaf(w, v[u][e / 4].x, acc[e]);
+        acc[e + 1] = fmaf(w, v[u][e / 4].y, acc[e + 1]);
+        acc[e + 2] = fmaf(w, v[u][e / 4].z, acc[e + 2]);
+        acc[e + 3] = fmaf(w, v[u][e / 4].w, acc[e + 3]);
+      }
+    }
+  };
+  auto load_batch = [&](int j0, float (&ls)[kBatch], float4 (&v)[kBatch][CW / 4]) {
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int j = j0 + u;
-      const size_t slot = (size_t)parts[j < np ? j : 0] * 2 + (j == 0);
-      const float ls = (j < np) ? a.lse_part[slot * rows_blk + r] : -INFINITY;
-      w[u] = (ls == -INFINITY) ? 0.f : expf(ls - lse);
-      const float4* src = reinterpret_cast<const float4*>(a.o_part) + slot * (D / 4) * rows_blk;
+      const size_t slot = slot_of(j);
+      ls[u] = (j < np) ? a.lse_part[slot * rows_blk + r] : -INFINITY;
 #pragma unroll
       for (int e = 0; e < CW; e += 4)
-        v[u][e / 4] = (j < np) ? src[(size_t)((c0col + e) >> 2) * rows_blk + r]
+        v[u][e / 4] = (j < np) ? o4[slot * (D / 4) * rows_blk + (size_t)((c0col + e) >> 2) * rows_blk + r]
                                : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  };
+  if (np <= kBatch) {
+    float ls[kBatch];
+    float4 v[kBatch][CW / 4];
+    load_batch(0, ls, v);
+    float mx = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
+    for (int u = 0; u < kBatch; ++u) mx = fmaxf(mx, ls[u]);
+    float sum = 0.f;
 #pragma unroll
-      for (int e = 0; e < CW; e += 4) {
-        acc[e] = fmaf(w[u], v[u][e / 4].x, acc[e]);
-        acc[e + 1] = fmaf(w[u], v[u][e / 4].y, acc[e + 1]);
-        acc[e + 2] = fmaf(w[u], v[u][e / 4].z, acc[e + 2]);
-        acc[e + 3] = fmaf(w[u], v[u][e / 4].w, acc[e + 3]);
-      }
+    for (int u = 0; u < kBatch; ++u) sum += (ls[u] == -INFINITY) ? 0.f : expf(ls[u] - mx);
+    lse = mx + logf(sum);
+    accumulate(0, ls, v);
+  } else {
+    float mx = -INFINITY, sum = 0.f;
+    for (int j0 = 0; j0 < np; j0 += kBatch) {
+      float ls[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) ls[u] = (j0 + u < np) ? a.lse_part[slot_of(j0 + u) * rows_blk + r] : -INFINITY;
+      float bm = mx;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, ls[u]);
+      if (bm == -INFINITY) continue;
+      sum = (mx == -INFINITY) ? 0.f : sum * expf(mx - bm);
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) sum += (ls[u] == -INFINITY) ? 0.f : expf(ls[u] - bm);
+      mx = bm;
+    }
+    lse = mx + logf(sum);
+    for (int j0 = 0; j0 < np; j0 += kBatch) {
+      float ls[kBatch];
+      float4 v[kBatch][CW / 4];
+      load_batch(j0, ls, v);
+      accumulate(j0, ls, v);
     }
   }
   const size_t grow = (size_t)(c0 + token);

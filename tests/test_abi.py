@@ -65,6 +65,7 @@ BAD = [
     (dict(batch=0), -1),
     (dict(head_dim=96), -2),            # unsupported head_dim
     (dict(hq=256, hkv=1), -2),          # group wider than a tile
+    (dict(hq=65536 * 2, hkv=2048), -2),  # more query heads than a grid dimension holds
     (dict(prefix_dtype=7), -1),
     (dict(softmax_scale=0.0), -1),
     (dict(softmax_scale=math.inf), -1),
