@@ -60,6 +60,10 @@ def lib():
                 ctypes.c_void_p, ctypes.c_long, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_int]
             _lib.cfa_oracle_threads.restype = ctypes.c_int
+            _lib.cfa_oracle_group_prefix_grad.restype = None
+            _lib.cfa_oracle_group_prefix_grad.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
     return _lib
 
 
@@ -115,6 +119,21 @@ def group(lp, lc, g, d, scale, q, kp, vp, kc, vc, dout, mutation=0, backward=Tru
     return dict(o=o, lse=lse, delta=delta, dq=dq, dk=dk, dv=dv)
 
 
+def prefix_grad(lp, lc, g, d, scale, q, kp, vp, dout, lse, delta, mutation=0):
+    """Exact dK, dV [lp, d] of the prefix rows of one (window, KV head) group,
+    given fp64 arrays q, dout [lc, g, d]; kp, vp [lp, d]; lse, delta [g, lc]
+    (from ``group``)."""
+    q, kp, vp, dout, lse, delta = (_f64(a) for a in (q, kp, vp, dout, lse, delta))
+    dkp = np.zeros((lp, d))
+    dvp = np.zeros((lp, d))
+    if lp == 0 or lc == 0:
+        return dkp, dvp
+    lib().cfa_oracle_group_prefix_grad(lp, lc, g, d, float(scale), _ptr(q), _ptr(kp), _ptr(vp),
+                                       _ptr(dout), _ptr(lse), _ptr(delta), _ptr(dkp),
+                                       _ptr(dvp), mutation)
+    return dkp, dvp
+
+
 def _prefix_rows(x: torch.Tensor, p0: int, p1: int, hk: int, d: int, q8: bool,
                  mutation: int) -> np.ndarray:
     if q8:
@@ -124,7 +143,8 @@ def _prefix_rows(x: torch.Tensor, p0: int, p1: int, hk: int, d: int, q8: bool,
     return _f64(x[p0:p1, hk])
 
 
-def run(inputs: dict, groups=None, mutation: int = 0, head_map=None, backward=True) -> dict:
+def run(inputs: dict, groups=None, mutation: int = 0, head_map=None, backward=True,
+        prefix_grad_rows: bool = False) -> dict:
     """Oracle outputs for packed inputs from ``synth.make_inputs``.
 
     ``groups``: iterable of (window, kv_head) pairs to compute (default: all).
@@ -133,7 +153,8 @@ def run(inputs: dict, groups=None, mutation: int = 0, head_map=None, backward=Tr
     hkv) to the list of query heads read; default is the contiguous grouping
     h // g == kv_head.
     Returns O [tc, hq, d], LSE [hq, tc], delta [hq, tc], dQ [tc, hq, d],
-    dK_c / dV_c [tc, hkv, d] (float64 numpy).
+    dK_c / dV_c [tc, hkv, d] (float64 numpy); with ``prefix_grad_rows`` also
+    dK_p / dV_p [tp, hkv, d] (``dkp``, ``dvp``) for every prefix row.
     """
     w = inputs["workload"]
     hq, hkv, d = w.hq, w.hkv, w.head_dim
@@ -145,6 +166,10 @@ def run(inputs: dict, groups=None, mutation: int = 0, head_map=None, backward=Tr
     out = dict(o=np.full((tc, hq, d), np.nan), lse=np.full((hq, tc), np.nan),
                delta=np.full((hq, tc), np.nan), dq=np.full((tc, hq, d), np.nan),
                dk=np.full((tc, hkv, d), np.nan), dv=np.full((tc, hkv, d), np.nan))
+    if prefix_grad_rows:
+        tp = cu_p[-1]
+        out["dkp"] = np.full((tp, hkv, d), np.nan)
+        out["dvp"] = np.full((tp, hkv, d), np.nan)
     if groups is None:
         groups = [(b, hk) for b in range(w.batch) for hk in range(hkv)]
     for b, hk in groups:
@@ -166,4 +191,9 @@ def run(inputs: dict, groups=None, mutation: int = 0, head_map=None, backward=Tr
             out["dq"][c0:c1, heads] = r["dq"]
             out["dk"][c0:c1, hk] = r["dk"]
             out["dv"][c0:c1, hk] = r["dv"]
+        if prefix_grad_rows:
+            dkp, dvp = prefix_grad(lp, lc, g, d, w.softmax_scale, qg, kp, vp, dog, r["lse"],
+                                   r["delta"], mutation=mutation)
+            out["dkp"][p0:p1, hk] = dkp
+            out["dvp"][p0:p1, hk] = dvp
     return out

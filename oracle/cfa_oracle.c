@@ -32,7 +32,9 @@
  *     dK_c,j  = scale * sum_{h in group} sum_{t >= j} dS_tj q_t   (chunk keys only)
  *     dV_c,j  =         sum_{h in group} sum_{t >= j} P_tj dO_t    (chunk keys only)
  *
- *   The prefix gets no gradient: none is computed or returned.
+ *   The prefix gets no gradient from cfa_oracle_group; the horizon
+ *   extension below (cfa_oracle_group_prefix_grad) gives the exact one for the
+ *   rows a caller keeps.
  *
  * q8_0 (the llama.cpp cache type named in "train: walk the window"): a block
  * is a little-endian IEEE binary16 scale d followed by 32 signed 8-bit codes;
@@ -234,6 +236,48 @@ int cfa_oracle_group(int lp, int lc, int g, int d, double scale,
     free(lse_own);
     free(delta_own);
     return fail ? -1 : 0;
+}
+
+/*
+ * Gradients of the frozen prefix's keys and values under the same loss, for
+ * the "exact reverse pass with horizon H" that "train: walk the window" ("Why
+ * it's a draft") asks for, and for the full k/v backward on context rows of
+ * the prime-rl POC ("Mechanism"): every chunk row sees every prefix key, so
+ * for prefix key j
+ *
+ *     dK_p,j = scale * sum_{h in group} sum_{t < Lc} dS_tj q_t
+ *     dV_p,j =         sum_{h in group} sum_{t < Lc} P_tj dO_t
+ *
+ * with P_tj = exp(S_tj - LSE_t) and dS_tj = P_tj (dO_t . v_j - delta_t), LSE
+ * and delta as cfa_oracle_group returns them.  Which prefix rows receive a
+ * gradient (the horizon) is the caller's choice; this returns all of them.
+ *   q, dout : [lc][g][d]   kp, vp, dkp, dvp : [lp][d]   lse, delta : [g][lc]
+ */
+void cfa_oracle_group_prefix_grad(int lp, int lc, int g, int d, double scale,
+                                  const double *q, const double *kp, const double *vp,
+                                  const double *dout, const double *lse,
+                                  const double *delta, double *dkp, double *dvp,
+                                  int mutation)
+{
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int j = 0; j < lp; ++j) {
+        const double *kj = kp + (size_t)j * d, *vj = vp + (size_t)j * d;
+        double *dk = dkp + (size_t)j * d, *dv = dvp + (size_t)j * d;
+        for (int c = 0; c < d; ++c) dk[c] = dv[c] = 0.0;
+        for (int t = 0; t < lc; ++t) {
+            for (int hh = 0; hh < g; ++hh) {
+                if (mutation == 14 && hh > 0) continue;   /* planted: drop the group sum */
+                const int r = t * g + hh;
+                const double *qt = q + (size_t)r * d;
+                const double *dot_ = dout + (size_t)r * d;
+                const double p = exp(scale * dot(qt, kj, d) - lse[(size_t)hh * lc + t]);
+                const double ds = p * (dot(dot_, vj, d) - delta[(size_t)hh * lc + t]);
+                const double fk = (mutation == 13) ? ds : scale * ds;  /* planted: scale dropped */
+                for (int c = 0; c < d; ++c) dk[c] += fk * qt[c];
+                for (int c = 0; c < d; ++c) dv[c] += p * dot_[c];
+            }
+        }
+    }
 }
 
 /* Number of threads the parallel regions above use. */

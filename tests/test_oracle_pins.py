@@ -11,6 +11,9 @@
 * Closed forms: Q = 0 gives uniform weights and LSE = ln(#visible keys);
   identical keys give dQ = 0; with Lp = 0 the chunk dV sums to the dO sum;
   identical heads in a group scale dK/dV by g.
+* Prefix gradients for the horizon extension (the exact reverse pass):
+  central finite differences wrt the prefix K/V, and full-window attention
+  with the prefix NOT detached (torch fp64 autograd).
 * Planted mistakes in the oracle each fail at least one of the above.
 """
 import math
@@ -333,3 +336,89 @@ def test_pins_catch_transposed_head_map():
     def strided(hk, g, hkv):
         return [h for h in range(g * hkv) if h % hkv == hk]
     assert not _packed_ok(head_map=strided)
+
+
+# ------------------------------------------- prefix gradients (horizon H) --
+
+def _prefix_grad(x, lp, lc, g, d, scale, mutation=0):
+    r = _oracle(x, lp, lc, g, d, scale)
+    return oracle.prefix_grad(lp, lc, g, d, scale, x["q"], x["kp"], x["vp"], x["dout"],
+                              r["lse"], r["delta"], mutation=mutation)
+
+
+def _prefix_fd_ok(lp, lc, g, d, seed, mutation=0, tol=1e-7):
+    scale = 1.0 / math.sqrt(d)
+    x = _rand_group(lp, lc, g, d, seed)
+    dkp, dvp = _prefix_grad(x, lp, lc, g, d, scale, mutation)
+    h = 1e-6
+    ok = True
+    for name, grad in (("kp", dkp), ("vp", dvp)):
+        fd = np.zeros_like(x[name])
+        it = np.nditer(x[name], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            xp = {k: v.copy() for k, v in x.items()}
+            xm = {k: v.copy() for k, v in x.items()}
+            xp[name][idx] += h
+            xm[name][idx] -= h
+            fd[idx] = (_loss(xp, lp, lc, g, d, scale) - _loss(xm, lp, lc, g, d, scale)) / (2 * h)
+        ok &= _rel(grad, fd) <= tol
+    return bool(ok)
+
+
+@pytest.mark.parametrize("lp,lc,g,d", [(5, 4, 2, 8), (7, 3, 1, 4), (3, 1, 3, 8)])
+def test_prefix_gradient_matches_finite_differences(lp, lc, g, d):
+    assert _prefix_fd_ok(lp, lc, g, d, seed=lp * 17 + lc)
+
+
+def _full_window_prefix_grads(x, lp, lc, g, d, scale):
+    """Full-window causal attention with the prefix K/V trainable: grads of
+    <O_chunk, dO> wrt the prefix keys and values."""
+    q = torch.tensor(x["q"]).permute(1, 0, 2).contiguous()
+    kp = torch.tensor(x["kp"]).requires_grad_(True)
+    vp = torch.tensor(x["vp"]).requires_grad_(True)
+    k = torch.cat([kp, torch.tensor(x["kc"])], 0)[None].expand(g, lp + lc, d)
+    v = torch.cat([vp, torch.tensor(x["vc"])], 0)[None].expand(g, lp + lc, d)
+    mask = torch.arange(lp + lc)[None, :] <= torch.arange(lp, lp + lc)[:, None]
+    o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)
+    (o * torch.tensor(x["dout"]).permute(1, 0, 2)).sum().backward()
+    return kp.grad.numpy(), vp.grad.numpy()
+
+
+def _prefix_full_window_ok(lp, lc, g, d, seed, mutation=0, tol=1e-12):
+    scale = 1.0 / math.sqrt(d) * 1.3
+    x = _rand_group(lp, lc, g, d, seed)
+    dkp, dvp = _prefix_grad(x, lp, lc, g, d, scale, mutation)
+    rk, rv = _full_window_prefix_grads(x, lp, lc, g, d, scale)
+    return _rel(dkp, rk) <= tol and _rel(dvp, rv) <= tol
+
+
+@pytest.mark.parametrize("lp,lc,g,d", [(37, 19, 2, 16), (130, 5, 1, 32), (6, 17, 4, 8)])
+def test_prefix_gradient_matches_full_window_autograd(lp, lc, g, d):
+    assert _prefix_full_window_ok(lp, lc, g, d, seed=lp + 3 * lc)
+
+
+def test_truncated_prefix_derivative_is_the_horizon_gradient():
+    # the derivative the stop-gradient drops is exactly what prefix_grad returns
+    lp, lc, g, d = 4, 3, 2, 8
+    x = _rand_group(lp, lc, g, d, 11)
+    scale = 1 / math.sqrt(d)
+    h = 1e-6
+    xp = {k: v.copy() for k, v in x.items()}
+    xp["kp"][1, 2] += h
+    xm = {k: v.copy() for k, v in x.items()}
+    xm["kp"][1, 2] -= h
+    fd = (_loss(xp, lp, lc, g, d, scale) - _loss(xm, lp, lc, g, d, scale)) / (2 * h)
+    dkp, _ = _prefix_grad(x, lp, lc, g, d, scale)
+    assert abs(dkp[1, 2] - fd) <= 1e-7 * max(1.0, abs(fd))
+
+
+PREFIX_MUTATIONS = {13: "softmax scale dropped from the prefix dK",
+                    14: "prefix dK/dV sum only the first head of the group"}
+
+
+@pytest.mark.parametrize("mutation", sorted(PREFIX_MUTATIONS))
+def test_pins_catch_planted_prefix_gradient_mistake(mutation):
+    ok = _prefix_fd_ok(5, 4, 2, 8, seed=2, mutation=mutation)
+    ok &= _prefix_full_window_ok(6, 17, 4, 8, seed=5, mutation=mutation)
+    assert not ok, PREFIX_MUTATIONS[mutation]
