@@ -69,6 +69,8 @@ def lib(build_if_missing: bool = False):
             L.cfa_forward.argtypes = [ap, vp, vp, vp, sz, vp]
             L.cfa_backward_preprocess.argtypes = [ap, vp, vp, vp, vp]
             L.cfa_backward.argtypes = [ap, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.cfa_backward_horizon.argtypes = [ap, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp,
+                                               vp, sz, vp]
             L.cfa_backward_dq.argtypes = [ap, vp, vp, vp, vp, vp, sz, vp]
             L.cfa_backward_dkdv.argtypes = [ap, vp, vp, vp, vp, vp, vp, sz, vp]
             L.cfa_dequant_q8_0.argtypes = [vp, ctypes.c_longlong, vp, vp, vp]
@@ -188,6 +190,34 @@ def backward(args: Args, dout, lse, delta, dq=None, dk=None, dv=None, ws=None, s
                               _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)),
            "cfa_backward")
     return dq, dk, dv, ws
+
+
+def backward_horizon(args: Args, horizon: int, dout, lse, delta, dq=None, dk=None, dv=None,
+                     dkp=None, dvp=None, ws=None, stream=None):
+    """cfa_backward_horizon: cfa_backward plus dK/dV of the last ``horizon``
+    prefix rows of every window.  Returns (dQ, dK_chunk, dV_chunk, dK_prefix,
+    dV_prefix, ws); prefix rows outside the horizon are left as given (zeros
+    when the buffers are allocated here)."""
+    dev = dout.device
+    if dq is None:
+        dq = torch.empty_like(dout)
+    shape_kv = (args.total_lc, args.hkv, args.head_dim)
+    shape_p = (args.total_lp, args.hkv, args.head_dim)
+    if dk is None:
+        dk = torch.empty(shape_kv, dtype=torch.bfloat16, device=dev)
+    if dv is None:
+        dv = torch.empty(shape_kv, dtype=torch.bfloat16, device=dev)
+    if dkp is None:
+        dkp = torch.zeros(shape_p, dtype=torch.bfloat16, device=dev)
+    if dvp is None:
+        dvp = torch.zeros(shape_p, dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = _workspace(args, WS_BACKWARD, dev)
+    _check(lib().cfa_backward_horizon(ctypes.byref(args), int(horizon), _ptr(dout), _ptr(lse),
+                                      _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dkp),
+                                      _ptr(dvp), _ptr(ws), ws.numel(), _stream(stream)),
+           "cfa_backward_horizon")
+    return dq, dk, dv, dkp, dvp, ws
 
 
 def backward_dq(args: Args, dout, lse, delta, dq, ws, stream=None):

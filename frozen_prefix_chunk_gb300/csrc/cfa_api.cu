@@ -351,6 +351,9 @@ int prepare_backward(const cfa_args* a, const void* dout, const float* lse, cons
   uint8_t* w = static_cast<uint8_t*>(ws);
   ba->dq_part = need_partials ? reinterpret_cast<float*>(w + p->off_dqpart) : nullptr;
   ba->dkv_tiles = p->n_kc_max;
+  ba->horizon = 0;
+  ba->pre_tiles = 0;
+  ba->dk_p = ba->dv_p = nullptr;
   ba->status = reinterpret_cast<int*>(w);
   ba->limit_ns = wait_limit_ns();
   ba->debug_wait_never = debug_wait_never();
@@ -363,9 +366,9 @@ int run_dq(const cfa_args* a, const Plan& p, const Maps& m, const BwdArgs& ba, c
   return CFA_OK;
 }
 
-// dK/dV work items (chunk key tile x window x KV head slots, some empty).
-long long dkdv_items(const cfa_args* a, const Plan& p) {
-  return (long long)p.n_kc_max * a->batch * a->hkv;
+// dK/dV work items (key tile slot x window x KV head, some empty).
+long long dkdv_items(const cfa_args* a, const BwdArgs& ba) {
+  return (long long)(ba.pre_tiles + ba.dkv_tiles) * a->batch * a->hkv;
 }
 
 int run_dkdv(const cfa_args* a, const Plan& p, const Maps& m, const BwdArgs& ba, int ctas,
@@ -379,12 +382,15 @@ int run_dkdv(const cfa_args* a, const Plan& p, const Maps& m, const BwdArgs& ba,
 // (a dK/dV step -- query tile x chunk key tile -- is four 128x128xD products,
 // a dQ step -- query tile x key tile -- three), rounded up and one more, since
 // a dK/dV item cannot be split and a late dK/dV ends the backward.
-int dkdv_share(const cfa_args* a, const Tiling& tl, int sms, long long items) {
+int dkdv_share(const cfa_args* a, const Tiling& tl, int sms, long long items, int horizon) {
   const double B = a->batch;
   const double lc = (double)a->total_lc / B, lp = (double)a->total_lp / B;
   const double qt = std::ceil(lc / tl.tpt);
   const double nk = std::ceil(lc / kTileN);
-  const double kv_steps = nk * qt - (double)kTileN / tl.tpt * nk * (nk - 1) / 2;
+  // chunk key tiles see the query tiles from their own on; horizon prefix
+  // tiles see all of them
+  const double nh = std::ceil(std::min((double)horizon, lp) / kTileN);
+  const double kv_steps = nk * qt - (double)kTileN / tl.tpt * nk * (nk - 1) / 2 + nh * qt;
   const double dq_steps = qt * (std::ceil(lp / kTileN) + (nk + 1) / 2);
   const double w_kv = 4 * kv_steps, w_dq = 3 * dq_steps;
   long long k = (long long)std::ceil(sms * w_kv / (w_kv + w_dq)) + 1;
@@ -424,8 +430,21 @@ extern "C" {
 int cfa_backward(const cfa_args* a, const void* dout, const float* lse, const float* delta,
                  void* dq, void* dk_chunk, void* dv_chunk, void* ws, size_t ws_bytes,
                  void* stream) {
+  return cfa_backward_horizon(a, 0, dout, lse, delta, dq, dk_chunk, dv_chunk, nullptr, nullptr,
+                              ws, ws_bytes, stream);
+}
+
+int cfa_backward_horizon(const cfa_args* a, int horizon, const void* dout, const float* lse,
+                         const float* delta, void* dq, void* dk_chunk, void* dv_chunk,
+                         void* dk_prefix, void* dv_prefix, void* ws, size_t ws_bytes,
+                         void* stream) {
+  if (horizon < 0) return CFA_ERR_INVALID_ARG;
   if (a && a->total_lc > 0 && (!dq || !dk_chunk || !dv_chunk || !aligned16(dq) ||
                                !aligned16(dk_chunk) || !aligned16(dv_chunk)))
+    return CFA_ERR_INVALID_ARG;
+  const bool want_prefix = a && horizon > 0 && a->total_lp > 0;
+  if (want_prefix &&
+      (!dk_prefix || !dv_prefix || !aligned16(dk_prefix) || !aligned16(dv_prefix)))
     return CFA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Plan p;
@@ -433,15 +452,33 @@ int cfa_backward(const cfa_args* a, const void* dout, const float* lse, const fl
   BwdArgs ba;
   bool skip;
   int st = prepare_backward(a, dout, lse, delta, ws, ws_bytes, true, s, &p, &m, &ba, &skip);
-  if (st || skip) return st;
+  if (st) return st;
   ba.dq = static_cast<__nv_bfloat16*>(dq);
   ba.dk = static_cast<__nv_bfloat16*>(dk_chunk);
   ba.dv = static_cast<__nv_bfloat16*>(dv_chunk);
+  if (want_prefix) {
+    // the last `horizon` prefix rows of a window span at most this many tiles
+    const int h = horizon < a->max_lp ? horizon : a->max_lp;
+    const int spans = ceil_div(h, kTileN) + 1, tiles = ceil_div(a->max_lp, kTileN);
+    ba.horizon = horizon;
+    ba.pre_tiles = spans < tiles ? spans : tiles;
+    ba.dk_p = static_cast<__nv_bfloat16*>(dk_prefix);
+    ba.dv_p = static_cast<__nv_bfloat16*>(dv_prefix);
+  }
+  if (skip) {
+    // no chunk rows anywhere: nothing attends to the prefix, so the horizon
+    // rows' gradients are zero
+    if (want_prefix &&
+        launch_zero_horizon(a->cu_seqlens_prefix, a->batch, a->hkv, a->head_dim, horizon,
+                            ba.dk_p, ba.dv_p, s) != cudaSuccess)
+      return CFA_ERR_LAUNCH;
+    return CFA_OK;
+  }
   // The two halves share no outputs: the dK/dV kernel runs on a few SMs of
   // its own, on a second stream forked from and joined back into `s`, while
   // the dQ kernel's persistent grid takes the rest.
-  const long long items = dkdv_items(a, p);
-  const int k = dkdv_share(a, p.dq, p.dq.grid, items);
+  const long long items = dkdv_items(a, ba);
+  const int k = dkdv_share(a, p.dq, p.dq.grid, items, ba.horizon);
   ba.tl.grid = p.dq.grid - k;
   std::lock_guard<std::mutex> lock(g_side_mutex);
   SideStream* ss = nullptr;
@@ -486,7 +523,7 @@ int cfa_backward_dkdv(const cfa_args* a, const void* dout, const float* lse, con
   if (st || skip) return st;
   ba.dk = static_cast<__nv_bfloat16*>(dk_chunk);
   ba.dv = static_cast<__nv_bfloat16*>(dv_chunk);
-  const long long items = dkdv_items(a, p);
+  const long long items = dkdv_items(a, ba);
   return run_dkdv(a, p, m, ba, (int)(items < p.dq.grid ? items : p.dq.grid), s);
 }
 

@@ -455,22 +455,49 @@ struct DkvCfg {
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
 };
 
-// Work items of the dK/dV kernel: (128-key chunk tile kt, window b, KV head
-// hk), numbered kt-major so that the longest items (kt = 0 sees every query
-// tile of its window) come first; CTA c takes items c, c + G, c + 2G, ...
+// Work items of the dK/dV kernel: (key tile, window b, KV head hk), numbered
+// tile-slot-major so that the longest items come first; CTA c takes items c,
+// c + G, c + 2G, ...  The first a.pre_tiles slots are prefix key tiles of the
+// horizon (the last a.horizon prefix rows of each window, whose gradient the
+// caller asked for; every chunk row sees them), the next a.dkv_tiles slots
+// the 128-key chunk tiles (chunk key j seen by chunk rows t >= j).
 struct DkvItem {
-  int kt, b, hk;
-  int c0, lc, key0, qi_lo, n;  // window rows, first key, query tiles [qi_lo, qi_lo + n)
+  int b, hk;
+  bool pre;          // a prefix key tile
+  int c0, lc;        // the window's chunk rows
+  int k0, krows;     // first row of the key tile in its tensor, and the keys there are
+  int kmin;          // keys below this index in the tile get no gradient written
+  int key0;          // key index of the tile's first key within the chunk (chunk tiles)
+  int qi_lo, n;      // query tiles [qi_lo, qi_lo + n)
 };
 
 __device__ inline bool dkv_item(const BwdArgs& a, long long j, DkvItem& it) {
   it.hk = (int)(j % a.hkv);
   it.b = (int)((j / a.hkv) % a.batch);
-  it.kt = (int)(j / ((long long)a.hkv * a.batch));
+  const int slot = (int)(j / ((long long)a.hkv * a.batch));
   it.c0 = a.cu_c[it.b];
   it.lc = a.cu_c[it.b + 1] - it.c0;
-  it.key0 = it.kt * kTileN;
+  it.pre = slot < a.pre_tiles;
+  if (it.pre) {
+    const int p0 = a.cu_p[it.b], lp = a.cu_p[it.b + 1] - p0;
+    const int h = a.horizon < lp ? a.horizon : lp;
+    const int first = lp - h;                       // first prefix row in the horizon
+    const int kt = first / kTileN + slot;
+    if (h == 0 || kt * kTileN >= lp) return false;
+    it.k0 = p0 + kt * kTileN;
+    it.krows = lp - kt * kTileN;
+    it.kmin = first - kt * kTileN;
+    it.key0 = 0;
+    it.qi_lo = 0;
+    it.n = ceil_div(it.lc, a.tl.tpt);               // every chunk row sees the prefix
+    return true;
+  }
+  const int kt = slot - a.pre_tiles;
+  it.key0 = kt * kTileN;
   if (it.key0 >= it.lc) return false;
+  it.k0 = it.c0 + it.key0;
+  it.krows = it.lc - it.key0;
+  it.kmin = 0;
   it.qi_lo = it.key0 / a.tl.tpt;
   it.n = ceil_div(it.lc, a.tl.tpt) - it.qi_lo;
   return true;
@@ -481,7 +508,9 @@ __global__ void __launch_bounds__(320, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_do,
                     const __grid_constant__ CUtensorMap map_kc,
-                    const __grid_constant__ CUtensorMap map_vc, const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap map_vc,
+                    const __grid_constant__ CUtensorMap map_kp,
+                    const __grid_constant__ CUtensorMap map_vp, const BwdArgs a) {
   pdl_start();
   using C = DkvCfg<D>;
   constexpr int S = C::kStages;
@@ -492,7 +521,7 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Tiling tl = a.tl;
-  const long long n_items = (long long)a.dkv_tiles * a.batch * a.hkv;
+  const long long n_items = (long long)(a.pre_tiles + a.dkv_tiles) * a.batch * a.hkv;
   if ((long long)blockIdx.x >= n_items) return;
   const long long j0 = blockIdx.x, jstep = gridDim.x;
 
@@ -549,15 +578,15 @@ __global__ void __launch_bounds__(320, 1)
     int qn = 0, items = 0, issued = 0;
     bool ok = true;
     for (long long j = j0; ok && j < n_items; j += jstep) {
-      if (!dkv_item(a, j, it)) continue;
+      if (!dkv_item(a, j, it) || it.n == 0) continue;
       if (items > 0 && !(ok = warp_wait(W, bar_kvfree, (uint32_t)(items - 1) & 1u))) break;
       if (leader) {
         mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
         for (int kb = 0; kb < C::kBoxes; ++kb) {
-          tma_load_3d(base + C::kKOff + kb * kBoxBytes, &map_kc, bar_kv, kb * 64, it.hk,
-                      it.c0 + it.key0);
-          tma_load_3d(base + C::kVOff + kb * kBoxBytes, &map_vc, bar_kv, kb * 64, it.hk,
-                      it.c0 + it.key0);
+          tma_load_3d(base + C::kKOff + kb * kBoxBytes, it.pre ? &map_kp : &map_kc, bar_kv,
+                      kb * 64, it.hk, it.k0);
+          tma_load_3d(base + C::kVOff + kb * kBoxBytes, it.pre ? &map_vp : &map_vc, bar_kv,
+                      kb * 64, it.hk, it.k0);
         }
       }
       __syncwarp();
@@ -596,7 +625,7 @@ __global__ void __launch_bounds__(320, 1)
     int qn = 0, items = 0;
     bool ok = !(a.debug_wait_never && !warp_wait(W, bar_drain, 0));
     for (long long j = j0; ok && j < n_items; j += jstep) {
-      if (!dkv_item(a, j, it)) continue;
+      if (!dkv_item(a, j, it) || it.n == 0) continue;
       const int n = it.n;
       if (!(ok = warp_wait(W, bar_kv, (uint32_t)items & 1u))) break;
       if (!(ok = warp_wait(W, bar_qfull + 8 * (qn % S), (uint32_t)(qn / S) & 1u))) break;
@@ -671,8 +700,24 @@ __global__ void __launch_bounds__(320, 1)
     for (long long j = j0; ok && j < n_items; j += jstep) {
       if (!dkv_item(a, j, it)) continue;
       const int n = it.n;
+      // this thread's key: row krow of the tile; its gradient is written when
+      // it exists and lies in the horizon (prefix) / the chunk
+      const bool key_valid = krow < it.krows;
+      const bool key_out = key_valid && krow >= it.kmin;
+      __nv_bfloat16* const dk_base = it.pre ? a.dk_p : a.dk;
+      __nv_bfloat16* const dv_base = it.pre ? a.dv_p : a.dv;
+      const size_t grow = (size_t)(it.k0 + krow) * a.hkv + it.hk;
+      if (n == 0) {
+        // a window without chunk rows: its horizon rows' gradient is zero
+        if (key_out) {
+          uint4* dv = reinterpret_cast<uint4*>(dv_base + grow * D + half * (D / 2));
+          uint4* dk = reinterpret_cast<uint4*>(dk_base + grow * D + half * (D / 2));
+#pragma unroll
+          for (int v = 0; v < D / 16; ++v) dv[v] = dk[v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
       const int key = it.key0 + krow;
-      const bool key_valid = key < it.lc;
       fetch_rows(it.qi_lo);
       for (int i = 0; i < n; ++i) {
         const int t = qn + i;
@@ -686,8 +731,9 @@ __global__ void __launch_bounds__(320, 1)
         }
         __syncwarp();
         if (i + 1 < n) fetch_rows(it.qi_lo + i + 1);
-        // visible columns: r_min <= r < r_max (key <= token, token < Lc, r < rows)
-        int r_lo = (key - tok0) * tl.g;
+        // visible columns: r_min <= r < r_max (chunk keys: key <= token;
+        // token < Lc, r < rows)
+        int r_lo = it.pre ? 0 : (key - tok0) * tl.g;
         r_lo = r_lo < 0 ? 0 : r_lo;
         int r_hi = (it.lc - tok0) * tl.g;
         r_hi = r_hi < tl.rows ? r_hi : tl.rows;
@@ -739,7 +785,6 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) break;
       if (!(ok = warp_wait(W, bar_dkvfull, (uint32_t)items & 1u))) break;
       tc_fence_after_sync();
-      const size_t grow = (size_t)(it.c0 + key) * a.hkv + it.hk;
       // this warp's half of the dV and dK rows in two TMEM loads, then the
       // hand-off (before the global stores, which the arrive would wait for)
       constexpr int HW = D / 2;
@@ -755,9 +800,9 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dkvfree);  // dK/dV read: the next item may overwrite
-      if (key_valid) {
-        uint4* dv = reinterpret_cast<uint4*>(a.dv + grow * D + half * HW);
-        uint4* dk = reinterpret_cast<uint4*>(a.dk + grow * D + half * HW);
+      if (key_out) {
+        uint4* dv = reinterpret_cast<uint4*>(dv_base + grow * D + half * HW);
+        uint4* dk = reinterpret_cast<uint4*>(dk_base + grow * D + half * HW);
 #pragma unroll
         for (int v = 0; v < HW / 8; ++v) {
           uint4 u, w;
@@ -965,6 +1010,22 @@ __global__ void __launch_bounds__(kDqWarps * 32)
   for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
 }
 
+// Zero the horizon rows of the prefix gradients of every window (used when
+// no window has chunk rows, so nothing attends to the prefix).  One CTA per
+// window; the rows of a window are contiguous.
+__global__ void __launch_bounds__(256) zero_horizon_kernel(const int32_t* __restrict__ cu_p,
+                                                           int hkv, int d, int horizon,
+                                                           __nv_bfloat16* __restrict__ dk_p,
+                                                           __nv_bfloat16* __restrict__ dv_p) {
+  const int b = blockIdx.x;
+  const int p0 = cu_p[b], lp = cu_p[b + 1] - p0;
+  const int h = horizon < lp ? horizon : lp;
+  const size_t first = (size_t)(p0 + lp - h) * hkv * d / 8, count = (size_t)h * hkv * d / 8;
+  uint4* k = reinterpret_cast<uint4*>(dk_p) + first;
+  uint4* v = reinterpret_cast<uint4*>(dv_p) + first;
+  for (size_t i = threadIdx.x; i < count; i += blockDim.x) k[i] = v[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 }  // namespace
 
 cudaError_t launch_dequant_prefix(const uint8_t* k_blocks, const uint8_t* v_blocks,
@@ -1013,13 +1074,13 @@ cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, int ctas, cu
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DkvCfg<128>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    k<<<grid, 320, DkvCfg<128>::kSmemBytes, st>>>(m.q, m.dout, m.kc, m.vc, a);
+    k<<<grid, 320, DkvCfg<128>::kSmemBytes, st>>>(m.q, m.dout, m.kc, m.vc, m.kp, m.vp, a);
   } else {
     auto k = bwd_dkdv_kernel<64>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DkvCfg<64>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    k<<<grid, 320, DkvCfg<64>::kSmemBytes, st>>>(m.q, m.dout, m.kc, m.vc, a);
+    k<<<grid, 320, DkvCfg<64>::kSmemBytes, st>>>(m.q, m.dout, m.kc, m.vc, m.kp, m.vp, a);
   }
   return cudaGetLastError();
 }
@@ -1041,6 +1102,12 @@ cudaError_t launch_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, floa
     delta_kernel<128><<<blocks, 256, 0, st>>>(o, dout, delta, total_lc, hq);
   else
     delta_kernel<64><<<blocks, 256, 0, st>>>(o, dout, delta, total_lc, hq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_horizon(const int32_t* cu_p, int batch, int hkv, int d, int horizon,
+                                __nv_bfloat16* dk_p, __nv_bfloat16* dv_p, cudaStream_t st) {
+  zero_horizon_kernel<<<batch, 256, 0, st>>>(cu_p, hkv, d, horizon, dk_p, dv_p);
   return cudaGetLastError();
 }
 

@@ -49,6 +49,10 @@ struct BwdArgs {
   __nv_bfloat16* dv;     // [total_lc, hkv, D]
   float* dq_part;        // [grid, 2, 128, D]  partials of cut query tiles
   int dkv_tiles;         // 128-key chunk tiles of the longest window (dK/dV items)
+  int horizon;           // prefix rows per window (the last ones) that get dK/dV
+  int pre_tiles;         // prefix key tiles a horizon can span (dK/dV items)
+  __nv_bfloat16* dk_p;   // [total_lp, hkv, D]  prefix gradients in the horizon
+  __nv_bfloat16* dv_p;
   int* status;
   unsigned long long limit_ns;
   int debug_wait_never;  // test hook: the MMA thread waits on a barrier nobody sets
@@ -102,6 +106,8 @@ cudaError_t launch_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, floa
 cudaError_t launch_dequant_prefix(const uint8_t* k_blocks, const uint8_t* v_blocks,
                                   long long n_blocks, __nv_bfloat16* k_out,
                                   __nv_bfloat16* v_out, cudaStream_t st);
+cudaError_t launch_zero_horizon(const int32_t* cu_p, int batch, int hkv, int d, int horizon,
+                                __nv_bfloat16* dk_p, __nv_bfloat16* dv_p, cudaStream_t st);
 cudaError_t launch_dequant_q8_0(const uint8_t* blocks, long long n_blocks, float* out_f32,
                                 __nv_bfloat16* out_bf16, cudaStream_t st);
 

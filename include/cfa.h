@@ -132,6 +132,25 @@ int cfa_backward(const cfa_args* a, const void* dout, const float* lse, const fl
                  void* dq, void* dk_chunk, void* dv_chunk, void* ws, size_t ws_bytes,
                  void* stream);
 
+/* The backward with gradients for the frozen prefix's last rows: the "exact
+ * reverse pass with horizon H" that "train: walk the window" ("Why it's a
+ * draft") asks for, and the full k/v backward on context rows of the
+ * prime-rl POC ("Mechanism") when the horizon covers the whole prefix.
+ *   Everything cfa_backward writes, plus dk_prefix / dv_prefix
+ *   ([total_lp, hkv, d] bf16, caller-owned, 16-byte aligned): for window b
+ *   the rows [Lp_b - min(horizon, Lp_b), Lp_b) of its prefix get
+ *   dK_p,j = s * sum dS_tj q_t and dV_p,j = sum P_tj dO_t over all chunk rows t
+ *   (every one sees the prefix) and the group's query heads.  Other prefix
+ *   rows are not written.  horizon = 0 is cfa_backward (the prefix pointers
+ *   may then be NULL); horizon >= Lp_b gives every row of window b.  A q8_0
+ *   prefix gets bf16 gradients of its dequantised values.  Same workspace as
+ *   cfa_backward.  Errors: horizon < 0 or a NULL / misaligned prefix gradient
+ *   pointer with horizon > 0 -> CFA_ERR_INVALID_ARG. */
+int cfa_backward_horizon(const cfa_args* a, int horizon, const void* dout, const float* lse,
+                         const float* delta, void* dq, void* dk_chunk, void* dv_chunk,
+                         void* dk_prefix, void* dv_prefix, void* ws, size_t ws_bytes,
+                         void* stream);
+
 /* The two independent halves of cfa_backward, for callers that schedule them
  * separately (e.g. on two streams).  cfa_backward_dq writes dq (it needs the
  * cfa_workspace_size(CFA_WS_BACKWARD) workspace for its split partials);

@@ -176,6 +176,10 @@ def run(inputs: dict, groups=None, mutation: int = 0, head_map=None, backward=Tr
         p0, p1, c0, c1 = cu_p[b], cu_p[b + 1], cu_c[b], cu_c[b + 1]
         lp, lc = p1 - p0, c1 - c0
         if lc == 0:
+            if prefix_grad_rows:
+                # no chunk row attends to this prefix: its gradient is the empty sum
+                out["dkp"][p0:p1, hk] = 0.0
+                out["dvp"][p0:p1, hk] = 0.0
             continue
         heads = head_map(hk, g, hkv) if head_map else list(range(hk * g, (hk + 1) * g))
         qg = inputs["q"][c0:c1, heads]

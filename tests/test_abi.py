@@ -100,3 +100,16 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(cfa, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         cfa.lib()
+
+
+def test_backward_horizon_rejects_bad_arguments_on_the_host(L):
+    a = _args()
+    f = L.cfa_backward_horizon
+    # negative horizon
+    assert f(ctypes.byref(a), -1, 4096, 4096, 4096, 4096, 4096, 4096, 4096, 4096, 4096,
+             1 << 20, None) == -1
+    # a horizon needs both prefix gradient buffers, 16-byte aligned
+    assert f(ctypes.byref(a), 4, 4096, 4096, 4096, 4096, 4096, 4096, None, 4096, 4096,
+             1 << 20, None) == -1
+    assert f(ctypes.byref(a), 4, 4096, 4096, 4096, 4096, 4096, 4096, 4096, 4104, 4096,
+             1 << 20, None) == -1
