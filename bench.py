@@ -48,20 +48,23 @@ L2_FLUSH_BYTES = 256 << 20
 
 # ------------------------------------------------------------- accounting --
 
-def useful_flops(w) -> dict:
+def useful_flops(w, horizon=0) -> dict:
     np_pairs = sum(c * p for c, p in zip(w.lc, w.lp))
     nc_pairs = sum(c * (c + 1) // 2 for c in w.lc)
+    # pairs (chunk row, prefix key in the horizon): their dK and dV
+    nh_pairs = sum(c * min(horizon, p) for c, p in zip(w.lc, w.lp))
     d, h = w.head_dim, w.hq
     fwd = 4 * d * (np_pairs + nc_pairs) * h
-    bwd = (6 * d * np_pairs + 10 * d * nc_pairs) * h
+    bwd = (6 * d * np_pairs + 4 * d * nh_pairs + 10 * d * nc_pairs) * h
     # the dQ kernel's own contraction work: S, dP and dQ over every visible pair
     dq_kernel = 6 * d * (np_pairs + nc_pairs) * h
     return dict(fwd=fwd, bwd=bwd, total=fwd + bwd, dq_kernel=dq_kernel, dkdv_kernel=bwd - dq_kernel)
 
 
-def algorithmic_bytes(w) -> dict:
+def algorithmic_bytes(w, horizon=0) -> dict:
     """Bytes each pass must move at least once (split partials excluded)."""
     d, tp, tc = w.head_dim, sum(w.lp), sum(w.lc)
+    th = sum(min(horizon, p) for p in w.lp)          # prefix rows in the horizon
     pref = 34 / 32 if w.prefix_dtype == synth.PREFIX_Q8_0 else 2.0
     qb = tc * w.hq * d * 2
     kvp = 2 * tp * w.hkv * d * pref
@@ -71,6 +74,7 @@ def algorithmic_bytes(w) -> dict:
     pre = 2 * qb + lse                                # read O, dO; write delta
     dq_kernel = 2 * qb + 2 * lse + kvp + kvc + qb     # read q, dO, lse, delta, k, v; write dQ
     bwd = dq_kernel + 2 * qb + 2 * lse + kvc + kvc    # + dK/dV half: q, dO, lse, delta, kc/vc, dK/dV
+    bwd += 2 * th * w.hkv * d * 2                     # + dK/dV of the horizon's prefix rows
     return dict(fwd=fwd, pre=pre, bwd=bwd, dq_kernel=dq_kernel, total=fwd + pre + bwd)
 
 
@@ -233,8 +237,8 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w, l2):
-    return {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv,
+def config_of(w, l2, horizon=0):
+    return {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "horizon": horizon,
             "head_dim": w.head_dim, "lp": w.lp, "lc": w.lc,
             "prefix": ("q8_0 (dequantised to bf16 once per step, read by both passes)"
                        if w.prefix_dtype == synth.PREFIX_Q8_0 else "bf16"),
@@ -252,6 +256,8 @@ def main():
     ap.add_argument("--workload", default="qwen3_8b", choices=list(synth.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--horizon", type=int, default=0,
+                    help="prefix rows per window that get dK/dV (cfa_backward_horizon)")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -303,6 +309,10 @@ def main():
     ws_f = torch.empty(cfa.workspace_size(a, cfa.WS_FORWARD), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(cfa.workspace_size(a, cfa.WS_BACKWARD), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    dkp = dvp = None
+    if args.horizon:
+        dkp = torch.zeros(sum(w.lp), w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
+        dvp = torch.zeros_like(dkp)
     stream = torch.cuda.current_stream()
     # kernels launched per step: forward (+ split combine), delta, dQ (+ split
     # reduce), dK/dV; a workspace beyond its 256-byte header holds partials
@@ -322,7 +332,11 @@ def main():
             ev[2].record(stream)
         # dQ on this stream; the library runs dK/dV beside it on a few SMs of
         # a second stream and joins it back before returning
-        cfa.backward(a, d["dout"], lse, delta, dq, dk, dv, ws_b)
+        if args.horizon:
+            cfa.backward_horizon(a, args.horizon, d["dout"], lse, delta, dq, dk, dv, dkp, dvp,
+                                 ws_b)
+        else:
+            cfa.backward(a, d["dout"], lse, delta, dq, dk, dv, ws_b)
         if ev:
             ev[3].record(stream)
 
@@ -361,8 +375,8 @@ def main():
         tot_ms = float(t.item())
     ms_per_step = tot_ms / args.steps
 
-    flops = useful_flops(w)
-    byts = algorithmic_bytes(w)
+    flops = useful_flops(w, args.horizon)
+    byts = algorithmic_bytes(w, args.horizon)
     value = world * flops["total"] / (ms_per_step * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
@@ -390,7 +404,8 @@ def main():
 
     # ---- end to end through the public API, host buffers, copies timed
     pin = {k: host[k].pin_memory() for k in names}
-    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+    outs = [o, lse, dq, dk, dv] + ([dkp, dvp] if args.horizon else [])
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in pin.values())
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
     e2e_ms = []
@@ -402,7 +417,7 @@ def main():
         for n in names:
             d[n].copy_(pin[n], non_blocking=True)
         step()
-        for src, dst in zip((o, lse, dq, dk, dv), outs_h):
+        for src, dst in zip(outs, outs_h):
             dst.copy_(src, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
@@ -422,7 +437,8 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v, N(0,0.1) dO)",
-                "config": config_of(w, "flushed before every timed step (256 MiB write)"),
+                "config": config_of(w, "flushed before every timed step (256 MiB write)",
+                                    args.horizon),
                 "roofline": roofline, "step_roofline": step_roof,
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

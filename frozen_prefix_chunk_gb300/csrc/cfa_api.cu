@@ -378,10 +378,11 @@ int run_dkdv(const cfa_args* a, const Plan& p, const Maps& m, const BwdArgs& ba,
 }
 
 // SMs given to the dK/dV kernel when it runs beside the dQ kernel: its share
-// of the tensor work, estimated from window lengths averaged over the batch
-// (a dK/dV step -- query tile x chunk key tile -- is four 128x128xD products,
-// a dQ step -- query tile x key tile -- three), rounded up and one more, since
-// a dK/dV item cannot be split and a late dK/dV ends the backward.
+// of the work, estimated from window lengths averaged over the batch with the
+// per-step times measured on GB300 (a dQ step -- query tile x key tile -- about
+// 2100 cycles, a dK/dV step about 3000, plus about 4000 per dK/dV item for its
+// K/V load and epilogue), rounded up and one more, since a dK/dV item cannot
+// be split and a late dK/dV ends the backward.
 int dkdv_share(const cfa_args* a, const Tiling& tl, int sms, long long items, int horizon) {
   const double B = a->batch;
   const double lc = (double)a->total_lc / B, lp = (double)a->total_lp / B;
@@ -389,12 +390,13 @@ int dkdv_share(const cfa_args* a, const Tiling& tl, int sms, long long items, in
   const double nk = std::ceil(lc / kTileN);
   // chunk key tiles see the query tiles from their own on; horizon prefix
   // tiles see all of them
-  const double nh = std::ceil(std::min((double)horizon, lp) / kTileN);
+  const double nh = horizon > 0 ? std::ceil(std::min((double)horizon, lp) / kTileN) + 1 : 0;
   const double kv_steps = nk * qt - (double)kTileN / tl.tpt * nk * (nk - 1) / 2 + nh * qt;
-  const double dq_steps = qt * (std::ceil(lp / kTileN) + (nk + 1) / 2);
-  const double w_kv = 4 * kv_steps, w_dq = 3 * dq_steps;
+  const double dq_steps = qt * (std::ceil(lp / kTileN) + (nk + 1) / 2 + tl.setup);
+  const double w_kv = 3000 * kv_steps + 4000 * (nk + nh), w_dq = 2100 * dq_steps;
   long long k = (long long)std::ceil(sms * w_kv / (w_kv + w_dq)) + 1;
-  if (k > sms / 2) k = sms / 2;
+  if (k > sms / 2 && horizon == 0) k = sms / 2;
+  if (k > sms - 8) k = sms - 8;
   if (k > items) k = items;
   return k < 1 ? 1 : (int)k;
 }

@@ -726,7 +726,7 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          my_lse[u * 32 + lane] = lse_n[u];
+          my_lse[u * 32 + lane] = -lse_n[u];   // stored negated: p = 2^(s*scale_log2 + that)
           my_dl[u * 32 + lane] = dl_n[u];
         }
         __syncwarp();
@@ -749,11 +749,23 @@ __global__ void __launch_bounds__(320, 1)
           uint32_t r[64];
           tmem_ld_x64(t_lane + half * 64, r);
           uint32_t pk[32];
+          const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(my_lse);
+          if (__all_sync(0xffffffffu, r_lo <= 0 && r_hi >= 64)) {
+            // every column visible (all tiles but the diagonal and the ragged
+            // ends): packed scale-and-subtract, no mask
+            const uint64_t sl2x2 = f2(sl2, sl2);
 #pragma unroll
-          for (int jj = 0; jj < 64; ++jj)
-            p[jj] = (jj >= r_lo && jj < r_hi)
-                        ? ex2_approx(fmaf(__uint_as_float(r[jj]), sl2, -my_lse[jj]))
-                        : 0.f;
+            for (int jj = 0; jj < 32; ++jj)
+              f2_split(ex2_sfu_x2(f2_fma(f2(__uint_as_float(r[2 * jj]), __uint_as_float(r[2 * jj + 1])),
+                                         sl2x2, nlse2[jj])),
+                       p[2 * jj], p[2 * jj + 1]);
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 64; ++jj)
+              p[jj] = (jj >= r_lo && jj < r_hi)
+                          ? ex2_approx(fmaf(__uint_as_float(r[jj]), sl2, my_lse[jj]))
+                          : 0.f;
+          }
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) pk[jj] = pack_bf16x2(p[2 * jj], p[2 * jj + 1]);
           tmem_st_x32(t_lane + half * 64, pk);
@@ -770,10 +782,16 @@ __global__ void __launch_bounds__(320, 1)
           uint32_t r[64];
           tmem_ld_x64(t_lane + 128 + half * 64, r);
           uint32_t pk[32];
+          const uint64_t* dl2 = reinterpret_cast<const uint64_t*>(my_dl);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj)
-            pk[jj] = pack_bf16x2(p[2 * jj] * (__uint_as_float(r[2 * jj]) - my_dl[2 * jj]),
-                                 p[2 * jj + 1] * (__uint_as_float(r[2 * jj + 1]) - my_dl[2 * jj + 1]));
+          for (int jj = 0; jj < 32; ++jj) {
+            float d0, d1;
+            f2_split(f2_mul(f2(p[2 * jj], p[2 * jj + 1]),
+                            f2_sub(f2(__uint_as_float(r[2 * jj]), __uint_as_float(r[2 * jj + 1])),
+                                   dl2[jj])),
+                     d0, d1);
+            pk[jj] = pack_bf16x2(d0, d1);
+          }
           tmem_st_x32(t_lane + 128 + half * 64, pk);
         }
         tmem_st_wait();
