@@ -22,10 +22,12 @@ import torch
 from . import build as _build
 
 __all__ = ["CfaError", "Args", "lib", "workspace_size", "forward", "backward_preprocess",
-           "backward", "backward_dq", "backward_dkdv", "dequant_q8_0", "read_status", "PREFIX_BF16", "PREFIX_Q8_0"]
+           "backward", "backward_dq", "backward_dkdv", "dequant_q8_0", "read_status", "PREFIX_BF16", "PREFIX_Q8_0",
+           "PREFIX_F16", "backward_horizon"]
 
 PREFIX_BF16 = 0
 PREFIX_Q8_0 = 1
+PREFIX_F16 = 2
 WS_FORWARD = 0
 WS_BACKWARD = 1
 
@@ -112,7 +114,7 @@ def make_args(q, k_prefix, v_prefix, k_chunk, v_chunk, cu_seqlens_prefix, cu_seq
               total_lp=None) -> Args:
     """Fill cfa_args from tensors.  ``max_lp``/``max_lc`` are host ints (no
     device read).  For a q8_0 prefix, k/v_prefix are uint8
-    [total_lp, hkv, d/32*34]."""
+    [total_lp, hkv, d/32*34]; for an fp16 prefix, float16 [total_lp, hkv, d]."""
     total_lc, hq, d = q.shape
     if hkv is None:
         hkv = k_chunk.shape[1]

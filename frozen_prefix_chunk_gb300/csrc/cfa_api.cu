@@ -67,7 +67,8 @@ int validate(const cfa_args* a) {
   if (a->hq < 1 || a->hkv < 1 || a->hkv > 65535 || a->hq % a->hkv != 0) return CFA_ERR_INVALID_ARG;
   if (a->hq / a->hkv > 128 || a->hq > 65535) return CFA_ERR_UNSUPPORTED;
   if (a->head_dim != 64 && a->head_dim != 128) return CFA_ERR_UNSUPPORTED;
-  if (a->prefix_dtype != CFA_PREFIX_BF16 && a->prefix_dtype != CFA_PREFIX_Q8_0)
+  if (a->prefix_dtype != CFA_PREFIX_BF16 && a->prefix_dtype != CFA_PREFIX_Q8_0 &&
+      a->prefix_dtype != CFA_PREFIX_F16)
     return CFA_ERR_INVALID_ARG;
   if (a->max_lp < 0 || a->max_lc < 0 || a->total_lp < 0 || a->total_lc < 0)
     return CFA_ERR_INVALID_ARG;
@@ -134,7 +135,7 @@ int make_plan(const cfa_args* a, Plan* p) {
   p->n_kc_max = ceil_div(a->max_lc > 0 ? a->max_lc : 1, kTileN);
   const size_t G = (size_t)sms;
   const size_t wp = align256((size_t)(a->batch + 1) * 8);
-  const size_t kv16 = (a->prefix_dtype == CFA_PREFIX_Q8_0)
+  const size_t kv16 = (a->prefix_dtype != CFA_PREFIX_BF16)
                           ? align256((size_t)a->total_lp * a->hkv * a->head_dim * 2)
                           : 0;
   size_t off = kWsHeader;
@@ -192,8 +193,8 @@ int encode_kv_maps(const cfa_args* a, const void* kp16, const void* vp16, Maps* 
 }
 
 // The bf16 prefix rows the attention kernels read: the caller's tensors, or
-// for q8_0 the workspace copies, filled here (on the stream) by the dequant
-// kernel.
+// for a q8_0 / fp16 prefix the workspace copies, filled here (on the stream)
+// by the dequant / conversion kernel.
 int prefix_rows_bf16(const cfa_args* a, uint8_t* ws, size_t off_k, cudaStream_t s,
                      const void** kp16, const void** vp16) {
   if (a->total_lp == 0) {
@@ -208,11 +209,17 @@ int prefix_rows_bf16(const cfa_args* a, uint8_t* ws, size_t off_k, cudaStream_t 
   const size_t kv16 = align256((size_t)a->total_lp * a->hkv * a->head_dim * 2);
   __nv_bfloat16* k16 = reinterpret_cast<__nv_bfloat16*>(ws + off_k);
   __nv_bfloat16* v16 = reinterpret_cast<__nv_bfloat16*>(ws + off_k + kv16);
-  const long long nb = (long long)a->total_lp * a->hkv * (a->head_dim / 32);
-  if (launch_dequant_prefix(static_cast<const uint8_t*>(a->k_prefix),
-                            static_cast<const uint8_t*>(a->v_prefix), nb, k16, v16,
-                            s) != cudaSuccess)
-    return CFA_ERR_LAUNCH;
+  cudaError_t e;
+  if (a->prefix_dtype == CFA_PREFIX_F16) {
+    e = launch_f16_to_bf16(static_cast<const __half*>(a->k_prefix),
+                           static_cast<const __half*>(a->v_prefix),
+                           (long long)a->total_lp * a->hkv * a->head_dim, k16, v16, s);
+  } else {
+    const long long nb = (long long)a->total_lp * a->hkv * (a->head_dim / 32);
+    e = launch_dequant_prefix(static_cast<const uint8_t*>(a->k_prefix),
+                              static_cast<const uint8_t*>(a->v_prefix), nb, k16, v16, s);
+  }
+  if (e != cudaSuccess) return CFA_ERR_LAUNCH;
   *kp16 = k16;
   *vp16 = v16;
   return CFA_OK;

@@ -1028,6 +1028,29 @@ __global__ void __launch_bounds__(kDqWarps * 32)
   for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
 }
 
+// fp16 prefix -> bf16 rows for the attention kernels' TMA maps, K and V in one
+// launch (blockIdx.y): exact fp16 -> fp32, then round to nearest even.  Eight
+// values (16 bytes) per thread; n is a multiple of 64 (head_dim).
+__global__ void __launch_bounds__(256) f16_to_bf16_kernel(const __half* __restrict__ k,
+                                                          const __half* __restrict__ v,
+                                                          long long n8,
+                                                          __nv_bfloat16* __restrict__ k_out,
+                                                          __nv_bfloat16* __restrict__ v_out) {
+  pdl_start();
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const uint4 x = reinterpret_cast<const uint4*>(blockIdx.y ? v : k)[i];
+  const __half2* h = reinterpret_cast<const __half2*>(&x);
+  uint4 y;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&y);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(h[e]);
+    w[e] = pack_bf16x2(f.x, f.y);
+  }
+  reinterpret_cast<uint4*>(blockIdx.y ? v_out : k_out)[i] = y;
+}
+
 // Zero the horizon rows of the prefix gradients of every window (used when
 // no window has chunk rows, so nothing attends to the prefix).  One CTA per
 // window; the rows of a window are contiguous.
@@ -1120,6 +1143,15 @@ cudaError_t launch_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, floa
     delta_kernel<128><<<blocks, 256, 0, st>>>(o, dout, delta, total_lc, hq);
   else
     delta_kernel<64><<<blocks, 256, 0, st>>>(o, dout, delta, total_lc, hq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f16_to_bf16(const __half* k, const __half* v, long long n, __nv_bfloat16* k_out,
+                               __nv_bfloat16* v_out, cudaStream_t st) {
+  const long long n8 = n / 8;
+  if (n8 <= 0) return cudaSuccess;
+  const dim3 grid((unsigned)((n8 + 255) / 256), 2);
+  f16_to_bf16_kernel<<<grid, 256, 0, st>>>(k, v, n8, k_out, v_out);
   return cudaGetLastError();
 }
 

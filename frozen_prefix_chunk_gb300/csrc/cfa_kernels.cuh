@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "cfa_sched.cuh"
@@ -106,6 +107,9 @@ cudaError_t launch_delta(const __nv_bfloat16* o, const __nv_bfloat16* dout, floa
 cudaError_t launch_dequant_prefix(const uint8_t* k_blocks, const uint8_t* v_blocks,
                                   long long n_blocks, __nv_bfloat16* k_out,
                                   __nv_bfloat16* v_out, cudaStream_t st);
+// fp16 -> bf16 (round to nearest even) of two tensors of n values each.
+cudaError_t launch_f16_to_bf16(const __half* k, const __half* v, long long n, __nv_bfloat16* k_out,
+                               __nv_bfloat16* v_out, cudaStream_t st);
 cudaError_t launch_zero_horizon(const int32_t* cu_p, int batch, int hkv, int d, int horizon,
                                 __nv_bfloat16* dk_p, __nv_bfloat16* dv_p, cudaStream_t st);
 cudaError_t launch_dequant_q8_0(const uint8_t* blocks, long long n_blocks, float* out_f32,

@@ -29,7 +29,8 @@
  *   k_prefix, v_prefix        [total_lp, hkv, d]      bf16, or
  *                             [total_lp, hkv, d/32] q8_0 blocks of 34 bytes:
  *                             little-endian fp16 scale then 32 int8 codes
- *                             (the llama.cpp q8_0 cache type; V untransposed)
+ *                             (the llama.cpp q8_0 cache type; V untransposed),
+ *                             or [total_lp, hkv, d] fp16 (its F16 cache type)
  *   lse, delta                [hq, total_lc]          fp32 (natural log)
  *   cu_seqlens_prefix/chunk   [batch + 1]             int32, device memory,
  *                             non-decreasing, starting at 0
@@ -37,8 +38,10 @@
  * [cu_c[b], cu_c[b+1]).  Empty windows and Lp = 0 are allowed.
  *
  * Ownership: every pointer is caller-owned device memory (the prefix may be an
- * imported cache); the library allocates nothing and keeps no state between
- * calls.  `ws` is caller-provided scratch of at least cfa_workspace_size()
+ * imported cache); the library allocates no device memory.  The state it
+ * keeps across calls is a second stream and two events per device (made by
+ * the first cfa_backward call there) and the fixed scratch array of
+ * cfa_forward_noalloc.  `ws` is caller-provided scratch of at least cfa_workspace_size()
  * bytes, 256-byte aligned.
  *
  * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL = the
@@ -80,7 +83,7 @@ typedef enum cfa_status {
                                    cfa_forward_noalloc */
 } cfa_status;
 
-enum { CFA_PREFIX_BF16 = 0, CFA_PREFIX_Q8_0 = 1 };
+enum { CFA_PREFIX_BF16 = 0, CFA_PREFIX_Q8_0 = 1, CFA_PREFIX_F16 = 2 };
 enum { CFA_WS_FORWARD = 0, CFA_WS_BACKWARD = 1 };
 
 typedef struct cfa_args {
@@ -99,7 +102,7 @@ typedef struct cfa_args {
   int32_t hq;                        /* query heads */
   int32_t hkv;                       /* kv heads; hq % hkv == 0, hq / hkv <= 128 */
   int32_t head_dim;                  /* 64 or 128 */
-  int32_t prefix_dtype;              /* CFA_PREFIX_BF16 or CFA_PREFIX_Q8_0 */
+  int32_t prefix_dtype;              /* CFA_PREFIX_BF16, CFA_PREFIX_Q8_0 or CFA_PREFIX_F16 */
   float softmax_scale;               /* s > 0, applied to the fp32 logits */
 } cfa_args;
 
@@ -109,9 +112,12 @@ typedef struct cfa_args {
 size_t cfa_workspace_size(const cfa_args* a, int which);
 
 /* Forward: O (bf16, [total_lc, hq, d]) and LSE (fp32, [hq, total_lc]).
- * Attention over prefix + causal chunk keys with an online softmax (q8_0
- * prefixes are dequantised on the fly), split across CTAs along the keys
- * when there are few query tiles, then a combine of the split partials. */
+ * Attention over prefix + causal chunk keys with an online softmax, the
+ * (query block, key tile) iterations split evenly over a persistent grid,
+ * then a merge of the partials of query blocks that CTAs share.  The tensor
+ * cores multiply bf16: a q8_0 prefix is dequantised (fp32(d) * q rounded to
+ * bf16) and an fp16 prefix rounded to bf16 (nearest even) into the workspace
+ * first. */
 int cfa_forward(const cfa_args* a, void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /* Backward preprocess: delta[h, t] = sum_c dO[t, h, c] * O[t, h, c] (fp32

@@ -60,6 +60,9 @@ def lib():
                 ctypes.c_void_p, ctypes.c_long, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_int]
             _lib.cfa_oracle_threads.restype = ctypes.c_int
+            _lib.cfa_oracle_quantize_q8_0.restype = None
+            _lib.cfa_oracle_quantize_q8_0.argtypes = [ctypes.c_void_p, ctypes.c_long,
+                                                      ctypes.c_void_p, ctypes.c_int]
             _lib.cfa_oracle_group_prefix_grad.restype = None
             _lib.cfa_oracle_group_prefix_grad.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
@@ -89,6 +92,17 @@ def dequant_q8_0(blocks, mutation: int = 0):
     lib().cfa_oracle_dequant_q8_0(b.ctypes.data, nb, f64.ctypes.data, f32.ctypes.data,
                                   bf.ctypes.data, mutation)
     return f64, f32, bf
+
+
+def quantize_q8_0(x_bf16_bits, mutation: int = 0) -> np.ndarray:
+    """bf16 bit patterns (uint16, last dim a multiple of 32) -> q8_0 bytes with
+    the last dim replaced by 34 per block."""
+    x = np.ascontiguousarray(np.asarray(x_bf16_bits, dtype=np.uint16))
+    assert x.shape[-1] % 32 == 0
+    nb = x.size // 32
+    out = np.empty(x.shape[:-1] + (x.shape[-1] // 32 * 34,), dtype=np.uint8)
+    lib().cfa_oracle_quantize_q8_0(x.ctypes.data, nb, out.ctypes.data, mutation)
+    return out
 
 
 def _f64(x) -> np.ndarray:
@@ -140,7 +154,7 @@ def _prefix_rows(x: torch.Tensor, p0: int, p1: int, hk: int, d: int, q8: bool,
         blocks = x[p0:p1, hk].numpy()                        # [lp, d/32*34]
         f64, _, _ = dequant_q8_0(blocks, mutation if mutation in (11, 12) else 0)
         return f64.reshape(p1 - p0, d)
-    return _f64(x[p0:p1, hk])
+    return _f64(x[p0:p1, hk])                                # bf16 or fp16: exact in fp64
 
 
 def run(inputs: dict, groups=None, mutation: int = 0, head_map=None, backward=True,

@@ -112,6 +112,72 @@ void cfa_oracle_dequant_q8_0(const uint8_t *blocks, long n_blocks, double *out_f
     }
 }
 
+/* fp32 -> IEEE 754 binary16 bits, round to nearest, ties to even, from the
+ * format's definition: |x| = (1 + m/1024) * 2^(e-15) for biased exponent e in
+ * [1, 30], m/1024 * 2^-14 for e = 0; magnitudes from 65520 up (halfway past
+ * the largest finite value, 65504, whose fraction is odd) become infinity.
+ * The scaled magnitudes below are exact in double; rint rounds them to the
+ * nearest integer, ties to even (the default rounding mode). */
+static uint16_t float_to_half_rne(float x)
+{
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double v = fabs((double)x);
+    if (v == 0.0) return sign;
+    if (v >= 65520.0) return (uint16_t)(sign | 0x7c00u);
+    int k;
+    frexp(v, &k);                   /* v = f * 2^k, f in [0.5, 1): v in [2^(k-1), 2^k) */
+    int E = k - 1;                  /* unbiased exponent of v */
+    if (E < -14) {                  /* subnormal: a multiple of 2^-24 */
+        const double m = rint(ldexp(v, 24));
+        return (uint16_t)(sign | (uint16_t)m);       /* m = 1024 is the smallest normal */
+    }
+    double m = rint(ldexp(v, 10 - E));               /* in [1024, 2048] */
+    if (m == 2048.0) {
+        m = 1024.0;
+        ++E;
+    }
+    if (E > 15) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(m - 1024.0));
+}
+
+/*
+ * Quantise n_blocks blocks of 32 bf16 values (given as bit patterns) to q8_0,
+ * the cache write of the walk ("train: walk the window": the chunk's keys and
+ * values go into the q8_0 cache for the next chunk).  Per block, in fp32:
+ * d = absmax / 127 (an all-zero block gets d = 0 and zero codes), code
+ * q_i = x_i / d rounded half away from zero, clamped to [-127, 127]; the
+ * stored scale is fp16(d), nearest even, little-endian.
+ */
+void cfa_oracle_quantize_q8_0(const uint16_t *x_bf16, long n_blocks, uint8_t *out, int mutation)
+{
+    for (long b = 0; b < n_blocks; ++b) {
+        float v[32];
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t u = (uint32_t)x_bf16[32 * b + i] << 16;   /* bf16 -> fp32, exact */
+            memcpy(&v[i], &u, 4);
+            const float a = fabsf(v[i]);
+            amax = a > amax ? a : amax;
+        }
+        const float d = amax / 127.0f;
+        const uint16_t dh = float_to_half_rne(d);
+        uint8_t *blk = out + 34 * b;
+        blk[0] = (uint8_t)(dh & 0xff);
+        blk[1] = (uint8_t)(dh >> 8);
+        float dq = d;
+        if (mutation == 16) dq = (float)half_bits_to_double(dh, 0);   /* planted: fp16 scale */
+        for (int i = 0; i < 32; ++i) {
+            int q = 0;
+            if (d > 0.0f) {
+                const float r = v[i] / dq;
+                q = (mutation == 15) ? (int)rintf(r) : (int)roundf(r);   /* planted: ties to even */
+                q = q > 127 ? 127 : (q < -127 ? -127 : q);
+            }
+            blk[2 + i] = (uint8_t)(int8_t)q;
+        }
+    }
+}
+
 /* ---- attention ---------------------------------------------------------- */
 
 static double dot(const double *a, const double *b, int n)

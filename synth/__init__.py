@@ -42,6 +42,7 @@ Q8_0_BYTES = 34          # fp16 scale + 32 int8 codes
 
 PREFIX_BF16 = 0
 PREFIX_Q8_0 = 1
+PREFIX_F16 = 2
 
 
 @dataclass
@@ -113,7 +114,9 @@ def encode_q8_0(x: torch.Tensor) -> torch.Tensor:
     d32 = (absmax / np.float32(127.0)).astype(np.float32)
     safe = np.where(d32 == 0, np.float32(1.0), d32).astype(np.float32)
     r = (v / safe[:, None]).astype(np.float32)
-    q = np.sign(r) * np.floor(np.abs(r) + np.float32(0.5))
+    # round half away from zero, exactly (|r| + 0.5 in float64 cannot round)
+    ra = np.abs(r).astype(np.float64)
+    q = np.sign(r) * np.floor(ra + 0.5)
     q = np.clip(q, -127, 127)
     q = np.where(d32[:, None] == 0, 0, q).astype(np.int8)
     d16 = d32.astype(np.float16)                      # RNE
@@ -145,6 +148,9 @@ def make_inputs(w: Workload) -> dict:
     if w.prefix_dtype == PREFIX_Q8_0:
         kp = encode_q8_0(normal((tp, w.hkv, d)))
         vp = encode_q8_0(normal((tp, w.hkv, d)))
+    elif w.prefix_dtype == PREFIX_F16:
+        kp = normal((tp, w.hkv, d)).to(torch.float16)
+        vp = normal((tp, w.hkv, d)).to(torch.float16)
     else:
         kp = normal((tp, w.hkv, d)).to(torch.bfloat16)
         vp = normal((tp, w.hkv, d)).to(torch.bfloat16)

@@ -120,3 +120,30 @@ def test_q8_0_prefix_equals_bf16_of_its_dequant_bitwise():
     b = gu.run_cuda(inp16)
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+F16 = [
+    dict(hq=8, hkv=2, head_dim=128, lp=[700, 0, 300], lc=[100, 5, 256]),
+    dict(hq=6, hkv=3, head_dim=64, lp=[513], lc=[130]),
+]
+
+
+@pytest.mark.parametrize("cfg", F16, ids=[str(i) for i in range(len(F16))])
+def test_f16_prefix_shapes(cfg):
+    w = synth.custom(**cfg, prefix_dtype=synth.PREFIX_F16, seed=7, dout_std=1.0)
+    _check(synth.make_inputs(w))
+
+
+def test_f16_prefix_equals_bf16_of_its_values_bitwise():
+    # the fp16 path multiplies with bf16(RNE(x)); feeding those bf16 values as
+    # a bf16 prefix must give bitwise the same outputs
+    cfg = dict(hq=8, hkv=2, head_dim=128, lp=[700, 129], lc=[100, 256])
+    inp = synth.make_inputs(synth.custom(**cfg, prefix_dtype=synth.PREFIX_F16, seed=9))
+    a = gu.run_cuda(inp)
+    inp16 = dict(inp)
+    for k in ("k_prefix", "v_prefix"):
+        inp16[k] = inp[k].float().to(torch.bfloat16)
+    inp16["workload"] = synth.custom(**cfg, seed=9)
+    b = gu.run_cuda(inp16)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
