@@ -23,7 +23,7 @@ from . import build as _build
 
 __all__ = ["CfaError", "Args", "lib", "workspace_size", "forward", "backward_preprocess",
            "backward", "backward_dq", "backward_dkdv", "dequant_q8_0", "read_status", "PREFIX_BF16", "PREFIX_Q8_0",
-           "PREFIX_F16", "backward_horizon"]
+           "PREFIX_F16", "backward_horizon", "quantize_q8_0"]
 
 PREFIX_BF16 = 0
 PREFIX_Q8_0 = 1
@@ -76,6 +76,7 @@ def lib(build_if_missing: bool = False):
             L.cfa_backward_dq.argtypes = [ap, vp, vp, vp, vp, vp, sz, vp]
             L.cfa_backward_dkdv.argtypes = [ap, vp, vp, vp, vp, vp, vp, sz, vp]
             L.cfa_dequant_q8_0.argtypes = [vp, ctypes.c_longlong, vp, vp, vp]
+            L.cfa_quantize_q8_0.argtypes = [vp, ctypes.c_longlong, vp, vp]
             L.cfa_read_status.argtypes = [vp, vp]
             L.cfa_forward_noalloc.argtypes = [ap, vp, vp, vp]
             L.cfa_forward_noalloc.restype = ctypes.c_int
@@ -253,6 +254,20 @@ def dequant_q8_0(blocks: torch.Tensor, stream=None, out_bf16=None, want_f32=True
     _check(lib().cfa_dequant_q8_0(_ptr(blocks), nb, _ptr(f32) if f32 is not None else None,
                                   _ptr(bf), _stream(stream)), "cfa_dequant_q8_0")
     return f32, bf
+
+
+def quantize_q8_0(x: torch.Tensor, out=None, stream=None):
+    """cfa_quantize_q8_0 on bf16 values (last dim a multiple of 32).  Returns
+    uint8 blocks with the last dim replaced by 34 per block; ``out`` may be a
+    preallocated uint8 tensor (or a view into a cache) of that many bytes."""
+    assert x.dtype == torch.bfloat16 and x.shape[-1] % 32 == 0 and x.is_contiguous()
+    nb = x.numel() // 32
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-1]) + (x.shape[-1] // 32 * 34,), dtype=torch.uint8,
+                          device=x.device)
+    assert out.dtype == torch.uint8 and out.numel() == nb * 34
+    _check(lib().cfa_quantize_q8_0(_ptr(x), nb, _ptr(out), _stream(stream)), "cfa_quantize_q8_0")
+    return out
 
 
 def read_status(ws: torch.Tensor, stream=None) -> int:

@@ -556,6 +556,19 @@ int cfa_dequant_q8_0(const void* blocks, long long n_blocks, float* out_f32, voi
   return CFA_OK;
 }
 
+int cfa_quantize_q8_0(const void* x_bf16, long long n_blocks, void* out_blocks, void* stream) {
+  if (n_blocks < 0) return CFA_ERR_INVALID_ARG;
+  if (n_blocks == 0) return CFA_OK;
+  if (!x_bf16 || !out_blocks || !aligned16(x_bf16) ||
+      (reinterpret_cast<uintptr_t>(out_blocks) & 1u))
+    return CFA_ERR_INVALID_ARG;
+  if (launch_quantize_q8_0(static_cast<const __nv_bfloat16*>(x_bf16), n_blocks,
+                           static_cast<uint8_t*>(out_blocks),
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CFA_ERR_LAUNCH;
+  return CFA_OK;
+}
+
 int cfa_read_status(const void* ws, void* stream) {
   if (!ws) return CFA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

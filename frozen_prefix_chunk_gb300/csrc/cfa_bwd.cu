@@ -1028,6 +1028,70 @@ __global__ void __launch_bounds__(kDqWarps * 32)
   for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
 }
 
+// bf16 -> q8_0 (the cache write of the walk: the chunk's K/V appended to a
+// q8_0 cache).  A warp takes 32 consecutive blocks: each lane encodes one
+// block -- d = absmax / 127 in fp32, codes x / d rounded half away from zero
+// and clamped to +-127, scale fp16(d) nearest even -- into shared memory, then
+// the warp writes the 1088 bytes out with 16-byte stores when the
+// destination allows it (2-byte stores otherwise: an append may start at any
+// block).
+__global__ void __launch_bounds__(kDqWarps * 32)
+    quantize_q8_0_kernel(const __nv_bfloat16* __restrict__ x, long long n_blocks,
+                         uint8_t* __restrict__ out) {
+  pdl_start();
+  __shared__ uint4 stage[kDqWarps][68];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long b0 = ((long long)blockIdx.x * kDqWarps + warp) * 32;
+  if (b0 >= n_blocks) return;
+  const int nb = (n_blocks - b0 < 32) ? (int)(n_blocks - b0) : 32;
+  uint8_t* st = reinterpret_cast<uint8_t*>(stage[warp]);
+  if (lane < nb) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (b0 + lane) * 32);
+    float v[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 w = src[c];
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        v[8 * c + 2 * e] = f.x;
+        v[8 * c + 2 * e + 1] = f.y;
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const float d = __fdiv_rn(amax, 127.f);
+    const uint16_t dh = __half_as_ushort(__float2half_rn(d));
+    uint16_t* o16 = reinterpret_cast<uint16_t*>(st + lane * 34);
+    o16[0] = dh;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      int q[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        int c = 0;
+        if (d > 0.f) {
+          c = (int)roundf(__fdiv_rn(v[2 * i + u], d));
+          c = c > 127 ? 127 : (c < -127 ? -127 : c);
+        }
+        q[u] = c;
+      }
+      o16[1 + i] = (uint16_t)((q[0] & 0xff) | ((q[1] & 0xff) << 8));
+    }
+  }
+  __syncwarp();
+  uint8_t* dst = out + b0 * 34;
+  if (nb == 32 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (int i = lane; i < 68; i += 32) d4[i] = stage[warp][i];
+  } else {
+    uint16_t* d2 = reinterpret_cast<uint16_t*>(dst);
+    for (int i = lane; i < nb * 17; i += 32) d2[i] = reinterpret_cast<const uint16_t*>(st)[i];
+  }
+}
+
 // fp16 prefix -> bf16 rows for the attention kernels' TMA maps, K and V in one
 // launch (blockIdx.y): exact fp16 -> fp32, then round to nearest even.  Eight
 // values (16 bytes) per thread; n is a multiple of 64 (head_dim).
@@ -1152,6 +1216,15 @@ cudaError_t launch_f16_to_bf16(const __half* k, const __half* v, long long n, __
   if (n8 <= 0) return cudaSuccess;
   const dim3 grid((unsigned)((n8 + 255) / 256), 2);
   f16_to_bf16_kernel<<<grid, 256, 0, st>>>(k, v, n8, k_out, v_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_q8_0(const __nv_bfloat16* x, long long n_blocks, uint8_t* out,
+                                 cudaStream_t st) {
+  if (n_blocks <= 0) return cudaSuccess;
+  const long long per_cta = 32LL * kDqWarps;
+  const unsigned grid = (unsigned)((n_blocks + per_cta - 1) / per_cta);
+  quantize_q8_0_kernel<<<grid, kDqWarps * 32, 0, st>>>(x, n_blocks, out);
   return cudaGetLastError();
 }
 

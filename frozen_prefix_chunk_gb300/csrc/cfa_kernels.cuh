@@ -110,6 +110,8 @@ cudaError_t launch_dequant_prefix(const uint8_t* k_blocks, const uint8_t* v_bloc
 // fp16 -> bf16 (round to nearest even) of two tensors of n values each.
 cudaError_t launch_f16_to_bf16(const __half* k, const __half* v, long long n, __nv_bfloat16* k_out,
                                __nv_bfloat16* v_out, cudaStream_t st);
+cudaError_t launch_quantize_q8_0(const __nv_bfloat16* x, long long n_blocks, uint8_t* out,
+                                 cudaStream_t st);
 cudaError_t launch_zero_horizon(const int32_t* cu_p, int batch, int hkv, int d, int horizon,
                                 __nv_bfloat16* dk_p, __nv_bfloat16* dv_p, cudaStream_t st);
 cudaError_t launch_dequant_q8_0(const uint8_t* blocks, long long n_blocks, float* out_f32,

@@ -175,6 +175,17 @@ int cfa_backward_dkdv(const cfa_args* a, const void* dout, const float* lse, con
 int cfa_dequant_q8_0(const void* blocks, long long n_blocks, float* out_f32, void* out_bf16,
                      void* stream);
 
+/* q8_0 quantisation of n_blocks blocks of 32 contiguous bf16 values into
+ * 34-byte blocks: the cache write of the walk ("train: walk the window",
+ * "What it is": a chunk's keys and values go into the q8_0 cache so that the
+ * next chunk sees them).  Per block, in fp32: d = absmax / 127 (0 for an
+ * all-zero block), code q_i = x_i / d rounded half away from zero and clamped
+ * to [-127, 127]; the stored scale is fp16(d), nearest even (infinity when d
+ * exceeds the fp16 range).  `out_blocks` may point anywhere into an existing
+ * cache, e.g. at the first row after a window's prefix (an append).  Device
+ * pointers; x 16-byte aligned, out 2-byte aligned; else CFA_ERR_INVALID_ARG. */
+int cfa_quantize_q8_0(const void* x_bf16, long long n_blocks, void* out_blocks, void* stream);
+
 /* Forward without a caller workspace, for callers that cannot allocate device
  * memory: a trainer sharing the GPU with an inference server that reserved
  * the memory up front, or a C program whose device memory comes only from

@@ -147,3 +147,33 @@ def test_f16_prefix_equals_bf16_of_its_values_bitwise():
     b = gu.run_cuda(inp16)
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+def _bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_quantize_q8_0_bit_exact():
+    import frozen_prefix_chunk_gb300 as cfa
+    g = torch.Generator().manual_seed(21)
+    x = torch.randn(3000, 128, generator=g) * torch.rand(3000, 1, generator=g) * 20
+    x[:3] = 0                                        # zero blocks
+    x[3, :32] = 1e-38                                # tiny values
+    x[4, :32] = 8323072.0                            # fp16 scale overflow
+    x[5, :32] = torch.tensor([0.5, -0.5, 2.5, -2.5] * 8) * 2   # halves at d = 1/127 * 5
+    xb = x.to(torch.bfloat16)
+    got = cfa.quantize_q8_0(xb.cuda()).cpu().numpy()
+    want = oracle.quantize_q8_0(_bf16_bits(xb))
+    assert np.array_equal(got, want)
+
+
+def test_quantize_q8_0_appends_into_a_cache_at_any_block():
+    import frozen_prefix_chunk_gb300 as cfa
+    x = (torch.randn(37, 64, generator=torch.Generator().manual_seed(22)) * 3).to(torch.bfloat16)
+    cache = torch.full((100 * 34,), 0xAB, dtype=torch.uint8, device="cuda")
+    start = 5 * 34                                   # 2-byte aligned, not 16-byte
+    n = x.numel() // 32 * 34
+    cfa.quantize_q8_0(x.cuda(), out=cache[start:start + n])
+    c = cache.cpu().numpy()
+    assert np.array_equal(c[start:start + n], oracle.quantize_q8_0(_bf16_bits(x)).reshape(-1))
+    assert np.all(c[:start] == 0xAB) and np.all(c[start + n:] == 0xAB)
