@@ -247,6 +247,109 @@ def config_of(w, l2, horizon=0):
 
 # ---------------------------------------------------------------- GPU arm --
 
+def run_walk(args, w):
+    """--walk C: the workload's first window walked chunk by chunk (chunks of
+    C rows over its Lc chunk rows, each attending to the context plus the
+    chunks before it in a growing cache), against one call over all the chunk
+    rows and, up to 32k rows, one full-window call (no frozen context)."""
+    import frozen_prefix_chunk_gb300 as cfa
+    from frozen_prefix_chunk_gb300.walk import WindowWalk
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cfa.lib(build_if_missing=True)
+    lp0, lcw, C = w.lp[0], w.lc[0], args.walk
+    if not 0 < C <= lcw:
+        raise SystemExit(f"--walk: chunk rows must be in [1, {lcw}] (the window's chunk rows)")
+    n_chunks = lcw // C
+    lcw = n_chunks * C
+    g = torch.Generator().manual_seed(0)
+    def rnd(*shape, std=1.0):
+        return (torch.randn(*shape, generator=g) * std).to(torch.bfloat16).to(dev)
+    k, v = rnd(lp0 + lcw, w.hkv, w.head_dim), rnd(lp0 + lcw, w.hkv, w.head_dim)
+    q, do = rnd(lcw, w.hq, w.head_dim), rnd(lcw, w.hq, w.head_dim, std=w.dout_std)
+    cache = cfa.PREFIX_Q8_0 if w.prefix_dtype == synth.PREFIX_Q8_0 else cfa.PREFIX_BF16
+    walk = WindowWalk(k[:lp0], v[:lp0], lp0 + lcw, w.hq, w.softmax_scale, cache)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def walk_once():
+        walk.rewind(lp0)
+        for c in range(n_chunks):
+            r, t = lp0 + c * C, c * C
+            walk.step(q[t:t + C], k[r:r + C], v[r:r + C], do[t:t + C])
+
+    def one_call(lp, kk, vv, qq, dd, pref, kpv=None):
+        kp, vp = (kpv if kpv is not None else (kk[:lp], vv[:lp])) if lp else (None, None)
+        cu_p = torch.tensor([0, lp], dtype=torch.int32, device=dev)
+        cu_c = torch.tensor([0, qq.shape[0]], dtype=torch.int32, device=dev)
+        a = cfa.make_args(qq, kp, vp, kk[lp:], vv[lp:], cu_p, cu_c, lp, qq.shape[0],
+                          w.softmax_scale, pref, hkv=w.hkv, total_lp=lp)
+        o, lse, wsf = cfa.forward(a, qq)
+        delta = cfa.backward_preprocess(a, o, dd)
+        dq, dk, dv, wsb = cfa.backward(a, dd, lse, delta)
+        def run():
+            cfa.forward(a, qq, o, lse, wsf)
+            cfa.backward_preprocess(a, o, dd, delta)
+            cfa.backward(a, dd, lse, delta, dq, dk, dv, wsb)
+        return run
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+    steps = max(3, min(args.steps, 200))
+    sampler = ClockSampler(0)
+    walk_ms = timed(walk_once, steps)
+    # the same walk replayed from a CUDA graph: no host work between chunks
+    walk_once()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        walk_once()
+    graph_ms = timed(graph.replay, steps)
+    # one call over all chunk rows, the context frozen (in the cache's format)
+    kpv = None
+    if cache == cfa.PREFIX_Q8_0:
+        kpv = (walk.k_rows[:lp0], walk.v_rows[:lp0])
+    single_ms = timed(one_call(lp0, k, v, q, do, cfa.PREFIX_BF16, kpv), steps)
+    full_ms = None
+    if lp0 + lcw <= 32768:
+        qf = torch.cat([rnd(lp0, w.hq, w.head_dim), q])
+        dof = torch.cat([rnd(lp0, w.hq, w.head_dim, std=w.dout_std), do])
+        full_ms = timed(one_call(0, k, v, qf, dof, cfa.PREFIX_BF16), max(3, steps // 4))
+    clocks = sampler.stop()
+    d, h = w.head_dim, w.hq
+    fl = 0
+    for c in range(n_chunks):
+        lp_c = lp0 + c * C
+        np_, nc_ = C * lp_c, C * (C + 1) // 2
+        fl += (4 * d * (np_ + nc_) + 6 * d * np_ + 10 * d * nc_) * h
+    line = {"metric": "window walk: fwd+bwd of every chunk over a growing KV cache, useful TFLOP/s",
+            "value": fl / (walk_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+            "value_graph": fl / (graph_ms * 1e-3) / 1e12,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": walk_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) q/k/v)",
+            "config": {"workload": w.name, "context": lp0, "chunk": C, "n_chunks": n_chunks,
+                       "cache": "q8_0" if cache == cfa.PREFIX_Q8_0 else "bf16",
+                       "l2": "flushed before every timed walk (256 MiB write)"},
+            "walk_ms": walk_ms, "walk_graph_ms": graph_ms, "single_call_ms": single_ms,
+            "full_window_ms": full_ms, "full_window_rows": lp0 + lcw,
+            "gpu_launches": None, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -256,6 +359,8 @@ def main():
     ap.add_argument("--workload", default="qwen3_8b", choices=list(synth.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--walk", type=int, default=0,
+                    help="chunk rows: walk the workload's window chunk by chunk instead")
     ap.add_argument("--horizon", type=int, default=0,
                     help="prefix rows per window that get dK/dV (cfa_backward_horizon)")
     args = ap.parse_args()
@@ -268,6 +373,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, w, rank)
+        return
+    if args.walk:
+        run_walk(args, w)
         return
 
     import torch.distributed as dist

@@ -115,7 +115,9 @@ def make_args(q, k_prefix, v_prefix, k_chunk, v_chunk, cu_seqlens_prefix, cu_seq
               total_lp=None) -> Args:
     """Fill cfa_args from tensors.  ``max_lp``/``max_lc`` are host ints (no
     device read).  For a q8_0 prefix, k/v_prefix are uint8
-    [total_lp, hkv, d/32*34]; for an fp16 prefix, float16 [total_lp, hkv, d]."""
+    [total_lp, hkv, d/32*34]; for an fp16 prefix, float16 [total_lp, hkv, d].
+    The result holds raw device pointers, not the tensors: keep every tensor
+    passed here referenced for as long as calls made with it may run."""
     total_lc, hq, d = q.shape
     if hkv is None:
         hkv = k_chunk.shape[1]

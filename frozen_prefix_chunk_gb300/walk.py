@@ -9,17 +9,25 @@ is that loop around the library's calls: per chunk one forward, backward
 preprocess and backward with the cache as the frozen prefix, then the cache
 write (a copy for a bf16 cache, ``cfa_quantize_q8_0`` for a q8_0 one).
 
+A q8_0 cache also keeps its rows decoded to bf16 (``cfa_dequant_q8_0`` of
+each appended chunk, once): every call of a chunk would otherwise decode the
+whole cache into its workspace again, twice per chunk (forward and backward),
+and those workspace rows take the same memory as the decoded copy.  The
+decoding is the one the calls do themselves, so the results are bitwise the
+same.
+
 The chunk's Q/K/V and the incoming dO come from the model and its loss, so
 they are the caller's inputs; the walk owns the cache and the workspaces
-(allocated once, for the cache capacity).  Everything runs asynchronously on
-the current stream; nothing is read back to the host.
+(grown to the largest chunk seen).  Everything runs asynchronously on the
+current stream; nothing is read back to the host and nothing waits for it.
 """
 from __future__ import annotations
 
 import torch
 
 from . import (PREFIX_BF16, PREFIX_Q8_0, backward, backward_horizon, backward_preprocess,
-               forward, make_args, quantize_q8_0, workspace_size, WS_BACKWARD, WS_FORWARD)
+               dequant_q8_0, forward, make_args, quantize_q8_0, workspace_size, WS_BACKWARD,
+               WS_FORWARD)
 
 
 class WindowWalk:
@@ -39,24 +47,37 @@ class WindowWalk:
         self.cache_dtype = cache_dtype
         self.horizon = int(horizon)
         self.capacity = capacity
+        # the bf16 rows the calls read: the cache itself, or its decoded copy
+        self.k_rows = torch.zeros(capacity, hkv, d, dtype=torch.bfloat16, device=self.dev)
+        self.v_rows = torch.zeros_like(self.k_rows)
         if cache_dtype == PREFIX_Q8_0:
             shape = (capacity, hkv, d // 32 * 34)
             self.k_cache = torch.zeros(shape, dtype=torch.uint8, device=self.dev)
             self.v_cache = torch.zeros(shape, dtype=torch.uint8, device=self.dev)
         else:
-            self.k_cache = torch.zeros(capacity, hkv, d, dtype=torch.bfloat16, device=self.dev)
-            self.v_cache = torch.zeros_like(self.k_cache)
+            self.k_cache, self.v_cache = self.k_rows, self.v_rows
         self.lp = 0
         self._append(context_k, context_v)
         self._ws = {}
+        # cu_seqlens of the one window, rewritten on the device every step:
+        # a host tensor copied over would block the host on the stream
+        self._cu = torch.zeros(2, 2, dtype=torch.int32, device=self.dev)
+
+    def rewind(self, rows: int):
+        """Forget every cache row from ``rows`` on (e.g. to walk the window
+        again from its context)."""
+        assert 0 <= rows <= self.lp
+        self.lp = rows
 
     def _append(self, k: torch.Tensor, v: torch.Tensor):
         """Cache write: rows [lp, lp + n) get the chunk's keys and values."""
         n = k.shape[0]
         assert self.lp + n <= self.capacity, "cache capacity exceeded"
         if self.cache_dtype == PREFIX_Q8_0:
-            quantize_q8_0(k.contiguous(), out=self.k_cache[self.lp:self.lp + n])
-            quantize_q8_0(v.contiguous(), out=self.v_cache[self.lp:self.lp + n])
+            rows = slice(self.lp, self.lp + n)
+            for x, blocks, dec in ((k, self.k_cache, self.k_rows), (v, self.v_cache, self.v_rows)):
+                quantize_q8_0(x.contiguous(), out=blocks[rows])
+                dequant_q8_0(blocks[rows], out_bf16=dec[rows], want_f32=False)
         else:
             self.k_cache[self.lp:self.lp + n].copy_(k)
             self.v_cache[self.lp:self.lp + n].copy_(v)
@@ -78,11 +99,12 @@ class WindowWalk:
         chunk) only with a horizon -- then appends k, v to the cache."""
         lc = q.shape[0]
         lp = self.lp
-        cu_p = torch.tensor([0, lp], dtype=torch.int32, device=self.dev)
-        cu_c = torch.tensor([0, lc], dtype=torch.int32, device=self.dev)
-        kp = self.k_cache[:lp] if lp else None
-        vp = self.v_cache[:lp] if lp else None
-        a = make_args(q, kp, vp, k, v, cu_p, cu_c, lp, lc, self.scale, self.cache_dtype,
+        cu_p, cu_c = self._cu[0], self._cu[1]
+        cu_p[1].fill_(lp)
+        cu_c[1].fill_(lc)
+        kp = self.k_rows[:lp] if lp else None
+        vp = self.v_rows[:lp] if lp else None
+        a = make_args(q, kp, vp, k, v, cu_p, cu_c, lp, lc, self.scale, PREFIX_BF16,
                       hkv=self.hkv, total_lp=lp)
         o, lse, _ = forward(a, q, ws=self._workspace(a, WS_FORWARD))
         delta = backward_preprocess(a, o, dout)

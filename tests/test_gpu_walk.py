@@ -122,3 +122,27 @@ def test_walk_with_horizon_prefix_gradients():
             assert np.linalg.norm(g - r) / np.linalg.norm(r) <= gu.TOL_GRAD
             assert np.all(got[:rows.start] == 0)       # outside the horizon: untouched zeros
         c0 += lc
+
+
+def test_walk_q8_0_decoded_rows_equal_the_calls_own_decoding():
+    # the walk's bf16 copy of a q8_0 cache gives bitwise the results of
+    # passing the q8_0 cache to the calls, which decode it themselves
+    import frozen_prefix_chunk_gb300 as cfa
+    lp0, chunks = 300, [128, 70]
+    (k, v, q, do), outs, walk = _walk(synth.PREFIX_Q8_0, lp0, chunks, seed=8)
+    c0 = 0
+    for i, lc in enumerate(chunks):
+        n = lp0 + c0
+        # the args hold raw pointers: every tensor they name stays referenced
+        qq, dd = q[c0:c0 + lc].cuda(), do[c0:c0 + lc].cuda()
+        kc, vc = k[n:n + lc].cuda(), v[n:n + lc].cuda()
+        cu_p = torch.tensor([0, n], dtype=torch.int32, device="cuda")
+        cu_c = torch.tensor([0, lc], dtype=torch.int32, device="cuda")
+        a = cfa.make_args(qq, walk.k_cache[:n], walk.v_cache[:n], kc, vc, cu_p, cu_c, n, lc,
+                          SCALE, cfa.PREFIX_Q8_0, hkv=HKV)
+        o, lse, _ = cfa.forward(a, qq)
+        delta = cfa.backward_preprocess(a, o, dd)
+        dq, dk, dv, _ = cfa.backward(a, dd, lse, delta)
+        for got, want in zip(outs[i], (o, lse, dq, dk, dv)):
+            assert torch.equal(got, want.cpu())
+        c0 += lc
