@@ -86,10 +86,14 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# the sources the dQ kernel (the roofline object's kernel) is built from
+DQ_KERNEL_SOURCES = ("cfa_bwd.cu", "cfa_kernels.cuh", "cfa_ptx.cuh", "cfa_sched.cuh")
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "frozen_prefix_chunk_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in DQ_KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
