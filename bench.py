@@ -354,6 +354,140 @@ def run_walk(args, w):
     print(json.dumps(line), flush=True)
 
 
+# MLP width of the Qwen3 layer each workload stands in for (hidden = hq * d)
+INTERMEDIATE = {"tiny": 512, "qwen3_1p7b": 6144}
+DEFAULT_INTERMEDIATE = 12288   # Qwen3-8B
+
+
+def rowsparse_gemms(w):
+    """The row-sparse projections of the layer ("POC: stop-gradient through
+    context tokens", "Mechanism": q/o and the dense MLP): (name, in, out)."""
+    hidden = w.hq * w.head_dim
+    inter = INTERMEDIATE.get(w.name, DEFAULT_INTERMEDIATE)
+    return [("q", hidden, hidden), ("o", hidden, hidden), ("gate", hidden, inter),
+            ("up", hidden, inter), ("down", inter, hidden)]
+
+
+def run_rowsparse(args, w):
+    """--rowsparse: the layer's row-sparse projection backward over the
+    workload's kept rows (its chunk rows; the context rows get no gradient):
+    per projection dW = dY_keep^T X[keep] (fp32) and dX[keep] = dY_keep W
+    (bf16).  One step = the ten GEMMs on one stream."""
+    import frozen_prefix_chunk_gb300 as cfa
+    from frozen_prefix_chunk_gb300 import rowsparse as R
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cfa.lib(build_if_missing=True)
+    n_rows = sum(w.lp) + sum(w.lc)
+    n_keep = sum(w.lc)
+    cu_p = synth.cu_seqlens(w.lp).to(dev)
+    cu_c = synth.cu_seqlens(w.lc).to(dev)
+    keep = R.keep_index_chunks(cu_p, cu_c, n_keep)
+    g = torch.Generator(device=dev).manual_seed(0)
+    gemms = []
+    xs = {}
+    for name, d_in, d_out in rowsparse_gemms(w):
+        # q/gate/up read the normed hidden states, o the attention output,
+        # down the MLP activation: one [n_rows, in] input per distinct source
+        src = {"q": "attn_in", "o": "attn_out", "gate": "mlp_in", "up": "mlp_in",
+               "down": "mlp_act"}[name]
+        if src not in xs:
+            xs[src] = torch.randn(n_rows, d_in, device=dev, generator=g).to(torch.bfloat16)
+        wt = (torch.randn(d_out, d_in, device=dev, generator=g) * d_in ** -0.5).to(torch.bfloat16)
+        dy = torch.randn(n_keep, d_out, device=dev, generator=g).to(torch.bfloat16)
+        dw = torch.empty(d_out, d_in, dtype=torch.float32, device=dev)
+        dx = torch.zeros(n_rows, d_in, dtype=torch.bfloat16, device=dev)
+        gemms.append(dict(name=name, d_in=d_in, d_out=d_out, x=xs[src], w=wt, dy=dy, dw=dw,
+                          dx=dx, ws_w=None, ws_x=None))
+    for G in gemms:
+        _, G["ws_w"] = R.dw(G["dy"], G["x"], keep, out=G["dw"])
+        _, G["ws_x"] = R.dx(G["dy"], G["w"], keep, G["dx"])
+    for G in gemms:
+        assert cfa.read_status(G["ws_w"]) == 0 and cfa.read_status(G["ws_x"]) == 0
+
+    def step():
+        for G in gemms:
+            R.dw(G["dy"], G["x"], keep, out=G["dw"], ws=G["ws_w"])
+            R.dx(G["dy"], G["w"], keep, G["dx"], ws=G["ws_x"])
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peaks, peak_src = load_peaks()
+    pk_t, pk_b = peaks["bf16_tflops"], peaks["hbm_gbs"]
+
+    def timed(fn, steps):
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ev = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ev.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    steps = max(3, min(args.steps, 300))
+    sampler = ClockSampler(0)
+    ms = timed(step, steps)
+    per = []
+    t_roof = 0.0
+    fl_total = 0
+    for G in gemms:
+        for kind in ("dW", "dX"):
+            fl = 2 * n_keep * G["d_in"] * G["d_out"]
+            if kind == "dW":
+                by = 2 * n_keep * (G["d_out"] + G["d_in"]) + 4 * G["d_in"] * G["d_out"]
+                fn = lambda G=G: R.dw(G["dy"], G["x"], keep, out=G["dw"], ws=G["ws_w"])
+            else:
+                by = 2 * n_keep * (G["d_out"] + G["d_in"]) + 2 * G["d_in"] * G["d_out"]
+                fn = lambda G=G: R.dx(G["dy"], G["w"], keep, G["dx"], ws=G["ws_x"])
+            t_ms = timed(fn, max(3, steps // 4))
+            roof = max(fl / (pk_t * 1e12), by / (pk_b * 1e9)) * 1e3
+            t_roof += roof
+            fl_total += fl
+            per.append({"gemm": f"{G['name']}.{kind}", "ms": t_ms,
+                        "tflops": fl / (t_ms * 1e-3) / 1e12, "gbs": by / (t_ms * 1e-3) / 1e9,
+                        "bound": "tensor" if fl / (pk_t * 1e12) > by / (pk_b * 1e9) else "hbm",
+                        "frac": roof / t_ms})
+    # what the row-sparse backward replaces: the dense full-row backward
+    # (cuBLAS through torch), dW over all n_rows and dX for every row
+    dense = []
+    for G in gemms:
+        dyf = torch.zeros(n_rows, G["d_out"], dtype=torch.bfloat16, device=dev)
+        dyf[keep.long()] = G["dy"]
+        dense.append((dyf, G))
+
+    def dense_step():
+        for dyf, G in dense:
+            torch.mm(dyf.t(), G["x"])
+            torch.mm(dyf, G["w"])
+
+    dense_ms = timed(dense_step, max(3, steps // 10))
+    clocks = sampler.stop()
+    dom = max(per, key=lambda r: r["ms"])
+    line = {"metric": "row-sparse projection backward (q, o, gate, up, down: dW and dX over the kept rows), TFLOP/s",
+            "value": fl_total / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) X and dY, W scaled by in^-1/2)",
+            "config": {"workload": w.name, "n_rows": n_rows, "n_keep": n_keep,
+                       "hidden": w.hq * w.head_dim,
+                       "intermediate": INTERMEDIATE.get(w.name, DEFAULT_INTERMEDIATE),
+                       "dW": "fp32", "dX": "bf16",
+                       "l2": "flushed before every timed step (256 MiB write)"},
+            "roofline": {"bound": "sum over the ten GEMMs of max(flops/peak, bytes/bw)",
+                         "t_roof_ms": t_roof, "frac": t_roof / ms, "peak_tflops": pk_t,
+                         "peak_gbs": pk_b, "peak_source": peak_src},
+            "dominant": dom, "per_gemm": per,
+            "dense_full_rows_ms": dense_ms, "speedup_vs_dense": dense_ms / ms,
+            "gpu_launches": 10 * steps, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -363,6 +497,8 @@ def main():
     ap.add_argument("--workload", default="qwen3_8b", choices=list(synth.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rowsparse", action="store_true",
+                    help="time the layer's row-sparse projection backward instead")
     ap.add_argument("--walk", type=int, default=0,
                     help="chunk rows: walk the workload's window chunk by chunk instead")
     ap.add_argument("--horizon", type=int, default=0,
@@ -380,6 +516,9 @@ def main():
         return
     if args.walk:
         run_walk(args, w)
+        return
+    if args.rowsparse:
+        run_rowsparse(args, w)
         return
 
     import torch.distributed as dist

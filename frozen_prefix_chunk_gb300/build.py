@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libcfa.so")
-SOURCES = ["cfa_api.cu", "cfa_fwd.cu", "cfa_bwd.cu", "cfa_noalloc.cu"]
+SOURCES = ["cfa_api.cu", "cfa_fwd.cu", "cfa_bwd.cu", "cfa_noalloc.cu", "cfa_rowsparse.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

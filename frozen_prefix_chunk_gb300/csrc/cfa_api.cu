@@ -579,3 +579,177 @@ int cfa_read_status(const void* ws, void* stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------- row-sparse projection backward --
+
+#include "cfa_rowsparse.cuh"
+
+namespace {
+
+// bf16 matrix [outer, inner] (row-major) -> 2-D map, 128-byte swizzle, boxes
+// of box_inner x box_outer elements.  Out-of-range elements read as zero.
+int make_map_2d(CUtensorMap* m, const void* ptr, long long inner, long long outer, int box_inner,
+                int box_outer) {
+  std::memset(m, 0, sizeof(*m));
+  if (inner <= 0 || outer <= 0) return CFA_OK;  // never dereferenced
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return CFA_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t es[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CFA_OK : CFA_ERR_INVALID_ARG;
+}
+
+int rs_validate(const cfa_rowsparse_args* r) {
+  if (!r) return CFA_ERR_INVALID_ARG;
+  if (r->n_keep < 0 || r->n_rows < 0 || r->in_features < 1 || r->out_features < 1)
+    return CFA_ERR_INVALID_ARG;
+  // 16-byte rows for TMA strides and the 16-byte gathers and stores
+  if (r->in_features % 8 != 0 || r->out_features % 8 != 0) return CFA_ERR_INVALID_ARG;
+  if (r->n_keep > 0 && (!r->dy || !aligned16(r->dy) || !r->keep_idx ||
+                        (reinterpret_cast<uintptr_t>(r->keep_idx) & 3u)))
+    return CFA_ERR_INVALID_ARG;
+  if ((long long)r->n_rows * r->in_features >= (1ll << 40) ||
+      (long long)r->out_features * r->in_features >= (1ll << 40) ||
+      (long long)r->n_keep * r->out_features >= (1ll << 40))
+    return CFA_ERR_UNSUPPORTED;
+  return CFA_OK;
+}
+
+struct RsPlan {
+  RsArgs a;
+  int grid;
+  size_t off_cnt, off_part, ws;
+};
+
+// Tiles of 128 x 128 outputs; K in 64-row stages, split when there are fewer
+// tiles than SMs (each split keeps at least two stages).  The workspace holds
+// the status word, the per-tile counters and the fp32 partial tiles.
+int rs_plan(const cfa_rowsparse_args* r, int mode, RsPlan* p) {
+  int sms = 0;
+  int st = sm_count(&sms);
+  if (st) return st;
+  RsArgs& a = p->a;
+  std::memset(&a, 0, sizeof(a));
+  a.mode = mode;
+  a.M = mode == 0 ? r->out_features : r->n_keep;
+  a.N = r->in_features;
+  a.K = mode == 0 ? r->n_keep : r->out_features;
+  a.n_keep = r->n_keep;
+  a.n_rows = r->n_rows;
+  const int tiles_m = ceil_div(a.M, kRsTile);
+  a.tiles_n = ceil_div(a.N, kRsTile);
+  a.tiles = tiles_m * a.tiles_n;
+  a.k_stages = ceil_div(a.K, kRsBK);
+  int splits = 1;
+  if (a.tiles > 0 && a.tiles < sms) {
+    splits = sms / a.tiles;
+    const int by_k = a.k_stages / 2 > 1 ? a.k_stages / 2 : 1;
+    if (splits > by_k) splits = by_k;
+    if (splits > kRsMaxSplits) splits = kRsMaxSplits;
+    if (splits < 1) splits = 1;
+  }
+  a.splits = splits;
+  a.units = (long long)a.tiles * splits;
+  p->grid = (int)(a.units < sms ? a.units : sms);
+  p->off_cnt = 16;
+  const size_t hdr = align256(p->off_cnt + (size_t)a.tiles * 16);
+  p->off_part = hdr;
+  p->ws = hdr + (splits > 1 ? (size_t)a.tiles * splits * kRsTile * kRsTile * 4 : 0);
+  if (p->ws < kWsHeader) p->ws = kWsHeader;
+  a.limit_ns = wait_limit_ns();
+  return CFA_OK;
+}
+
+int rs_run(const cfa_rowsparse_args* r, int mode, void* out, int out_f32, int accumulate,
+           void* ws, size_t ws_bytes, cudaStream_t s) {
+  RsPlan p;
+  int st = rs_plan(r, mode, &p);
+  if (st) return st;
+  if ((st = check_ws(ws, ws_bytes, p.ws))) return st;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  // status word and the (tile, lane quadrant) counters start at zero
+  if (cudaMemsetAsync(ws, 0, p.off_cnt + (size_t)p.a.tiles * 16, s) != cudaSuccess)
+    return CFA_ERR_LAUNCH;
+  RsArgs& a = p.a;
+  a.keep = r->keep_idx;
+  a.x = static_cast<const __nv_bfloat16*>(r->x);
+  a.out = out;
+  a.out_f32 = out_f32;
+  a.accumulate = accumulate;
+  a.part = reinterpret_cast<float*>(w + p.off_part);
+  a.counters = reinterpret_cast<unsigned*>(w + p.off_cnt);
+  a.status = reinterpret_cast<int*>(w);
+  if (a.units == 0) return CFA_OK;
+  CUtensorMap ma, mb;
+  if (mode == 0) {
+    if ((st = make_map_2d(&ma, r->dy, r->out_features, r->n_keep, 64, kRsBK))) return st;
+    std::memset(&mb, 0, sizeof(mb));
+  } else {
+    if ((st = make_map_2d(&ma, r->dy, r->out_features, r->n_keep, kRsBK, kRsTile))) return st;
+    if ((st = make_map_2d(&mb, r->w, r->in_features, r->out_features, 64, kRsBK))) return st;
+  }
+  if (launch_rowsparse(ma, mb, a, p.grid, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  return CFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t cfa_rowsparse_workspace_size(const cfa_rowsparse_args* a, int which) {
+  if (rs_validate(a) != CFA_OK) return 0;
+  if (which != CFA_RS_DW && which != CFA_RS_DX) return 0;
+  RsPlan p;
+  if (rs_plan(a, which == CFA_RS_DW ? 0 : 1, &p) != CFA_OK) return 0;
+  return p.ws;
+}
+
+int cfa_rowsparse_dw(const cfa_rowsparse_args* a, void* dw, int dw_dtype, int accumulate,
+                     void* ws, size_t ws_bytes, void* stream) {
+  int st = rs_validate(a);
+  if (st) return st;
+  if (dw_dtype != CFA_GRAD_F32 && dw_dtype != CFA_GRAD_BF16) return CFA_ERR_INVALID_ARG;
+  if (!dw || !aligned16(dw)) return CFA_ERR_INVALID_ARG;
+  if (a->n_keep > 0 && (!a->x || !aligned16(a->x))) return CFA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a->n_keep == 0) {
+    // no kept rows: the gradient is zero (accumulating leaves dW as it is)
+    RsPlan p;
+    if ((st = rs_plan(a, 0, &p))) return st;
+    if ((st = check_ws(ws, ws_bytes, p.ws))) return st;
+    if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+    if (!accumulate &&
+        cudaMemsetAsync(dw, 0, (size_t)a->out_features * a->in_features *
+                                   (dw_dtype == CFA_GRAD_F32 ? 4 : 2), s) != cudaSuccess)
+      return CFA_ERR_LAUNCH;
+    return CFA_OK;
+  }
+  return rs_run(a, 0, dw, dw_dtype == CFA_GRAD_F32, accumulate ? 1 : 0, ws, ws_bytes, s);
+}
+
+int cfa_rowsparse_dx(const cfa_rowsparse_args* a, void* dx, void* ws, size_t ws_bytes,
+                     void* stream) {
+  int st = rs_validate(a);
+  if (st) return st;
+  if (a->n_keep > 0 && (!dx || !aligned16(dx) || !a->w || !aligned16(a->w)))
+    return CFA_ERR_INVALID_ARG;
+  return rs_run(a, 1, dx, 0, 0, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int cfa_keep_index_chunks(const int32_t* cu_seqlens_prefix, const int32_t* cu_seqlens_chunk,
+                          int batch, int total_lc, int32_t* keep_idx, void* stream) {
+  if (batch < 1 || total_lc < 0) return CFA_ERR_INVALID_ARG;
+  if (total_lc == 0) return CFA_OK;
+  if (!cu_seqlens_prefix || !cu_seqlens_chunk || !keep_idx) return CFA_ERR_INVALID_ARG;
+  if (launch_keep_index_chunks(cu_seqlens_prefix, cu_seqlens_chunk, batch, total_lc, keep_idx,
+                               static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CFA_ERR_LAUNCH;
+  return CFA_OK;
+}
+
+}  // extern "C"

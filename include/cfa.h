@@ -206,9 +206,74 @@ int cfa_forward_noalloc(const cfa_args* a, void* o, float* lse, void* stream);
 /* Size in bytes of the fixed scratch array used by cfa_forward_noalloc. */
 size_t cfa_noalloc_scratch_bytes(void);
 
+/* ---------------------------------------------------------------------------
+ * Row-sparse projection backward ("POC: stop-gradient through context tokens",
+ * prime-rl, "Mechanism": row_sparse_linear).  A linear layer Y = X W^T keeps
+ * its full-row forward; when the gradient reaching Y is zero on every row but
+ * the kept ones (the context rows of a frozen-prefix step), its backward is
+ *   dW          = dY_keep^T X[keep]          [out, in]
+ *   dX[keep[i]] = dY_keep[i] W                [in] per kept row
+ * and dX is zero on every other row.  dY_keep is compact: row i is the
+ * gradient of Y row keep_idx[i].  The query-split attention backward produces
+ * exactly this for the q projection (cfa_backward's dQ, [total_lc, hq * d],
+ * is dY_keep as it is, with keep_idx from cfa_keep_index_chunks).
+ *
+ * Layouts (row-major, contiguous, bf16 unless stated):
+ *   dy        [n_keep, out_features]
+ *   x         [n_rows, in_features]   (cfa_rowsparse_dw only)
+ *   w         [out_features, in_features] (the nn.Linear weight; dx only)
+ *   keep_idx  [n_keep] int32, device memory; distinct rows of x for dx
+ *   dW        [out_features, in_features] fp32 or bf16
+ *   dX        [n_rows, in_features]; only the kept rows are written
+ * in_features and out_features are multiples of 8; dy, x, w, dW, dX 16-byte
+ * aligned.  A keep index outside [0, n_rows) reads as a zero row of x (dw),
+ * or its dX row is skipped (dx), and the status word at the start of the
+ * workspace is set to CFA_ERR_INVALID_ARG (cfa_read_status).
+ * Determinism: each output element is one fixed-order fp32 sum (split
+ * contraction ranges are added in range order), so the same inputs give the
+ * same bits. */
+typedef struct cfa_rowsparse_args {
+  const void* dy;
+  const void* x;
+  const void* w;
+  const int32_t* keep_idx;
+  int n_keep;        /* kept rows (rows of dy) */
+  int n_rows;        /* rows of x and dX */
+  int in_features;
+  int out_features;
+} cfa_rowsparse_args;
+
+enum { CFA_RS_DW = 0, CFA_RS_DX = 1 };          /* workspace size selector */
+enum { CFA_GRAD_F32 = 0, CFA_GRAD_BF16 = 1 };   /* dW element type */
+
+/* Workspace bytes (256-byte aligned buffer) for cfa_rowsparse_dw (CFA_RS_DW)
+ * or cfa_rowsparse_dx (CFA_RS_DX); 0 for invalid arguments. */
+size_t cfa_rowsparse_workspace_size(const cfa_rowsparse_args* a, int which);
+
+/* dW = dY_keep^T X[keep] (accumulate = 0) or dW += dY_keep^T X[keep]
+ * (accumulate != 0, read and written in dw_dtype), fp32 accumulation on the
+ * tensor cores.  With n_keep = 0, dW is zeroed (or left as it is when
+ * accumulating).  x, dy, keep_idx, dw device pointers; w unused. */
+int cfa_rowsparse_dw(const cfa_rowsparse_args* a, void* dw, int dw_dtype, int accumulate,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* dX[keep_idx[i]] = dY_keep[i] W (bf16, fp32 accumulation); rows of dX that
+ * are not kept are not written (the caller zeroes them once).  dy, w,
+ * keep_idx, dx device pointers; x unused. */
+int cfa_rowsparse_dx(const cfa_rowsparse_args* a, void* dx, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/* The kept rows of a frozen-prefix batch: chunk row j of window b (packed
+ * windows of Lp_b prefix rows followed by Lc_b chunk rows, in window order)
+ * sits at row cu_seqlens_prefix[b + 1] + j of the packed full sequence.
+ * Writes keep_idx[0 .. total_lc) on the device; cu_seqlens as in cfa_args. */
+int cfa_keep_index_chunks(const int32_t* cu_seqlens_prefix, const int32_t* cu_seqlens_chunk,
+                          int batch, int total_lc, int32_t* keep_idx, void* stream);
+
 /* Waits for `stream`, then returns the status word that the kernels of the
- * last cfa_forward / cfa_backward on this workspace left (CFA_OK or
- * CFA_ERR_DEVICE_TIMEOUT), or a CUDA error. */
+ * last call on this workspace left (CFA_OK, CFA_ERR_DEVICE_TIMEOUT, or for the
+ * row-sparse calls CFA_ERR_INVALID_ARG for a keep index outside x), or a CUDA
+ * error. */
 int cfa_read_status(const void* ws, void* stream);
 
 /* Short description of a status code (static string). */

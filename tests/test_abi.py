@@ -113,3 +113,54 @@ def test_backward_horizon_rejects_bad_arguments_on_the_host(L):
              1 << 20, None) == -1
     assert f(ctypes.byref(a), 4, 4096, 4096, 4096, 4096, 4096, 4096, 4096, 4104, 4096,
              1 << 20, None) == -1
+
+
+def _rs_args(**kw):
+    from frozen_prefix_chunk_gb300.rowsparse import RowSparseArgs
+    a = RowSparseArgs()
+    a.dy, a.x, a.w, a.keep_idx = 4096, 8192, 12288, 16384
+    a.n_keep, a.n_rows, a.in_features, a.out_features = 16, 64, 128, 256
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+RS_BAD = [
+    dict(in_features=12),        # rows not a multiple of 16 bytes
+    dict(out_features=100),
+    dict(in_features=0),
+    dict(n_keep=-1),
+    dict(n_rows=-5),
+    dict(dy=None),               # kept rows without a gradient
+    dict(dy=4100),               # misaligned
+    dict(keep_idx=None),
+    dict(keep_idx=16386),        # int32 indices need 4-byte alignment
+]
+
+
+@pytest.mark.parametrize("kw", RS_BAD, ids=[str(i) for i in range(len(RS_BAD))])
+def test_rowsparse_rejects_bad_arguments_on_the_host(L, kw):
+    from frozen_prefix_chunk_gb300 import rowsparse as R
+    R._L()
+    a = _rs_args(**kw)
+    assert L.cfa_rowsparse_dw(ctypes.byref(a), 4096, 0, 0, 4096, 1 << 20, None) == -1
+    assert L.cfa_rowsparse_dx(ctypes.byref(a), 4096, 4096, 1 << 20, None) == -1
+    assert L.cfa_rowsparse_workspace_size(ctypes.byref(a), 0) == 0
+
+
+def test_rowsparse_output_checks_on_the_host(L):
+    from frozen_prefix_chunk_gb300 import rowsparse as R
+    R._L()
+    a = _rs_args()
+    f = L.cfa_rowsparse_dw
+    assert f(ctypes.byref(a), 4096, 2, 0, 4096, 1 << 20, None) == -1     # unknown dW type
+    assert f(ctypes.byref(a), None, 0, 0, 4096, 1 << 20, None) == -1     # no output
+    assert f(ctypes.byref(a), 4104, 0, 0, 4096, 1 << 20, None) == -1     # misaligned output
+    b = _rs_args(x=None)
+    assert f(ctypes.byref(b), 4096, 0, 0, 4096, 1 << 20, None) == -1     # dW needs x
+    c = _rs_args(w=None)
+    assert L.cfa_rowsparse_dx(ctypes.byref(c), 4096, 4096, 1 << 20, None) == -1  # dX needs w
+    assert L.cfa_rowsparse_workspace_size(ctypes.byref(a), 7) == 0       # unknown selector
+    assert L.cfa_keep_index_chunks(4096, 4096, 0, 4, 4096, None) == -1   # no windows
+    assert L.cfa_keep_index_chunks(None, 4096, 1, 4, 4096, None) == -1
+    assert L.cfa_keep_index_chunks(4096, 4096, 1, 0, 4096, None) == 0    # nothing to do
