@@ -354,6 +354,30 @@ def run_walk(args, w):
     print(json.dumps(line), flush=True)
 
 
+class L2Flush:
+    """Evicts L2 before a timed step.  "write": a 256 MiB write (the lines it
+    leaves are dirty, and their write-back to HBM then runs during the timed
+    step); "write+read": the same write followed by a 256 MiB read of another
+    buffer, which forces that write-back before the step and leaves only clean
+    lines behind."""
+
+    def __init__(self, dev, mode="write"):
+        self.mode = mode
+        self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.rbuf = (torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+                     if mode == "write+read" else None)
+
+    def __call__(self):
+        self.buf.zero_()
+        if self.rbuf is not None:
+            self.rbuf.sum()   # read every line; the scalar result is not needed
+
+    def describe(self):
+        return {"write": "flushed before every timed step (256 MiB write)",
+                "write+read": "flushed before every timed step (256 MiB write, then a 256 MiB "
+                              "read that writes the dirty lines back before the step)"}[self.mode]
+
+
 # MLP width of the Qwen3 layer each workload stands in for (hidden = hq * d)
 INTERMEDIATE = {"tiny": 512, "qwen3_1p7b": 6144}
 DEFAULT_INTERMEDIATE = 12288   # Qwen3-8B
@@ -410,18 +434,18 @@ def run_rowsparse(args, w):
             R.dw(G["dy"], G["x"], keep, out=G["dw"], ws=G["ws_w"])
             R.dx(G["dy"], G["w"], keep, G["dx"], ws=G["ws_x"])
 
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, args.flush)
     peaks, peak_src = load_peaks()
     pk_t, pk_b = peaks["bf16_tflops"], peaks["hbm_gbs"]
 
     def timed(fn, steps):
         for _ in range(max(3, args.warmup)):
-            flush.zero_()
+            flush()
             fn()
         torch.cuda.synchronize()
         ev = []
         for _ in range(steps):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
@@ -477,8 +501,7 @@ def run_rowsparse(args, w):
             "config": {"workload": w.name, "n_rows": n_rows, "n_keep": n_keep,
                        "hidden": w.hq * w.head_dim,
                        "intermediate": INTERMEDIATE.get(w.name, DEFAULT_INTERMEDIATE),
-                       "dW": "fp32", "dX": "bf16",
-                       "l2": "flushed before every timed step (256 MiB write)"},
+                       "dW": "fp32", "dX": "bf16", "l2": flush.describe()},
             "roofline": {"bound": "sum over the ten GEMMs of max(flops/peak, bytes/bw)",
                          "t_roof_ms": t_roof, "frac": t_roof / ms, "peak_tflops": pk_t,
                          "peak_gbs": pk_b, "peak_source": peak_src},
@@ -497,6 +520,8 @@ def main():
     ap.add_argument("--workload", default="qwen3_8b", choices=list(synth.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flush", default="write", choices=["write", "write+read"],
+                    help="how L2 is evicted before each timed step")
     ap.add_argument("--rowsparse", action="store_true",
                     help="time the layer's row-sparse projection backward instead")
     ap.add_argument("--walk", type=int, default=0,
@@ -559,7 +584,7 @@ def main():
     dv = torch.empty_like(dk)
     ws_f = torch.empty(cfa.workspace_size(a, cfa.WS_FORWARD), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(cfa.workspace_size(a, cfa.WS_BACKWARD), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, args.flush)
     dkp = dvp = None
     if args.horizon:
         dkp = torch.zeros(sum(w.lp), w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
@@ -592,7 +617,7 @@ def main():
             ev[3].record(stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     for ws in (ws_f, ws_b):
@@ -606,7 +631,7 @@ def main():
     sampler = ClockSampler(local)
     t_wall = time.perf_counter()
     for k in range(args.steps):
-        flush.zero_()
+        flush()
         step(evs[k])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
@@ -661,7 +686,7 @@ def main():
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
     e2e_ms = []
     for k in range(args.e2e_steps + 2):
-        flush.zero_()
+        flush()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -688,7 +713,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v, N(0,0.1) dO)",
-                "config": config_of(w, "flushed before every timed step (256 MiB write)",
+                "config": config_of(w, flush.describe(),
                                     args.horizon),
                 "roofline": roofline, "step_roofline": step_roof,
                 "cpu_baseline": cpu,

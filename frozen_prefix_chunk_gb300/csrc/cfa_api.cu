@@ -586,19 +586,21 @@ int cfa_read_status(const void* ws, void* stream) {
 
 namespace {
 
-// bf16 matrix [outer, inner] (row-major) -> 2-D map, 128-byte swizzle, boxes
-// of box_inner x box_outer elements.  Out-of-range elements read as zero.
+// Matrix [outer, inner] (row-major, bf16 or fp32) -> 2-D map, 128-byte
+// swizzle, boxes of box_inner x box_outer elements.  Out-of-range elements
+// read as zero; stores to them are dropped.
 int make_map_2d(CUtensorMap* m, const void* ptr, long long inner, long long outer, int box_inner,
-                int box_outer) {
+                int box_outer, bool f32 = false) {
   std::memset(m, 0, sizeof(*m));
   if (inner <= 0 || outer <= 0) return CFA_OK;  // never dereferenced
   EncodeTiledFn fn = encode_fn();
   if (!fn) return CFA_ERR_CUDA;
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * (f32 ? 4 : 2)};
   cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
   cuuint32_t es[2] = {1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(ptr), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CFA_OK : CFA_ERR_INVALID_ARG;
@@ -626,7 +628,7 @@ struct RsPlan {
   size_t off_cnt, off_part, ws;
 };
 
-// Tiles of 128 x 128 outputs; K in 64-row stages, split when there are fewer
+// Tiles of 128 x 256 outputs; K in 64-row stages, split when there are fewer
 // tiles than SMs (each split keeps at least two stages).  The workspace holds
 // the status word, the per-tile counters and the fp32 partial tiles.
 int rs_plan(const cfa_rowsparse_args* r, int mode, RsPlan* p) {
@@ -641,8 +643,8 @@ int rs_plan(const cfa_rowsparse_args* r, int mode, RsPlan* p) {
   a.K = mode == 0 ? r->n_keep : r->out_features;
   a.n_keep = r->n_keep;
   a.n_rows = r->n_rows;
-  const int tiles_m = ceil_div(a.M, kRsTile);
-  a.tiles_n = ceil_div(a.N, kRsTile);
+  const int tiles_m = ceil_div(a.M, kRsTileM);
+  a.tiles_n = ceil_div(a.N, kRsTileN);
   a.tiles = tiles_m * a.tiles_n;
   a.k_stages = ceil_div(a.K, kRsBK);
   int splits = 1;
@@ -659,7 +661,7 @@ int rs_plan(const cfa_rowsparse_args* r, int mode, RsPlan* p) {
   p->off_cnt = 16;
   const size_t hdr = align256(p->off_cnt + (size_t)a.tiles * 16);
   p->off_part = hdr;
-  p->ws = hdr + (splits > 1 ? (size_t)a.tiles * splits * kRsTile * kRsTile * 4 : 0);
+  p->ws = hdr + (splits > 1 ? (size_t)a.tiles * splits * kRsTileM * kRsTileN * 4 : 0);
   if (p->ws < kWsHeader) p->ws = kWsHeader;
   a.limit_ns = wait_limit_ns();
   return CFA_OK;
@@ -685,15 +687,29 @@ int rs_run(const cfa_rowsparse_args* r, int mode, void* out, int out_f32, int ac
   a.counters = reinterpret_cast<unsigned*>(w + p.off_cnt);
   a.status = reinterpret_cast<int*>(w);
   if (a.units == 0) return CFA_OK;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mo, mp, mxt;
+  std::memset(&mo, 0, sizeof(mo));
+  std::memset(&mp, 0, sizeof(mp));
+  std::memset(&mxt, 0, sizeof(mxt));
+  if (mode == 0 && !accumulate &&
+      (st = make_map_2d(&mo, out, r->in_features, r->out_features, out_f32 ? 32 : 64, 32,
+                        out_f32 != 0)))
+    return st;
+  if (a.splits > 1 &&
+      (st = make_map_2d(&mp, a.part, kRsTileN, (long long)a.tiles * a.splits * kRsTileM, 32, 32,
+                        true)))
+    return st;
   if (mode == 0) {
     if ((st = make_map_2d(&ma, r->dy, r->out_features, r->n_keep, 64, kRsBK))) return st;
-    std::memset(&mb, 0, sizeof(mb));
+    // X read by 4-row gathers (64-column x 1-row boxes), or by 64 x 64 tiles
+    // where a stage's kept rows are consecutive
+    if ((st = make_map_2d(&mb, r->x, r->in_features, r->n_rows, 64, 1))) return st;
+    if ((st = make_map_2d(&mxt, r->x, r->in_features, r->n_rows, 64, kRsBK))) return st;
   } else {
-    if ((st = make_map_2d(&ma, r->dy, r->out_features, r->n_keep, kRsBK, kRsTile))) return st;
+    if ((st = make_map_2d(&ma, r->dy, r->out_features, r->n_keep, kRsBK, kRsTileM))) return st;
     if ((st = make_map_2d(&mb, r->w, r->in_features, r->out_features, 64, kRsBK))) return st;
   }
-  if (launch_rowsparse(ma, mb, a, p.grid, s) != cudaSuccess) return CFA_ERR_LAUNCH;
+  if (launch_rowsparse(ma, mb, mo, mp, mxt, a, p.grid, s) != cudaSuccess) return CFA_ERR_LAUNCH;
   return CFA_OK;
 }
 

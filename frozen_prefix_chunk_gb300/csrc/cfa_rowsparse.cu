@@ -8,8 +8,8 @@
 // the query-split attention backward produces (dQ exists for the chunk rows
 // only), so the q projection's backward reads that dQ as it is.
 //
-// One persistent kernel, two modes, 128 x 128 output tiles, K in 64-row
-// stages:
+// One persistent kernel, two modes, 128 x 256 output tiles, K in 64-row
+// stages (48 KB each, four in flight):
 //   mode 0, dW [out, in] = dY_keep^T X[keep]: A = dY_keep read MN-major by
 //     TMA (64 x 64 boxes), B = the kept rows of X gathered with cp.async into
 //     the same 128-byte-swizzled MN-major layout (each row of a stage comes
@@ -17,12 +17,16 @@
 //   mode 1, dX[keep[i]] = dY_keep[i] W: A = dY_keep K-major (TMA, 64-column x
 //     128-row box), B = W [out, in] MN-major (TMA, 64 x 64 boxes); the
 //     epilogue scatters each output row to its row of dX.
-// Warp roles (256 threads): warps 0-1 load (mode 0: one 64-column slab of
-// the gathered rows each, warp 0 lane 0 also the TMA of A; mode 1: warp 0
-// lane 0 issues all TMA), warp 2 owns TMEM and issues tcgen05.mma
-// (converged warp, elect.sync), warp 3 idles, warps 4-7 are the epilogue
-// (TMEM lane quadrant = warp % 4).  Two 128-column fp32 accumulators in TMEM
-// let the epilogue of one tile overlap the MMAs of the next.
+// Warp roles (288 threads): warps 0-3 load (mode 0: one 64-column slab of
+// the gathered rows each, with the next stage's keep indices fetched a stage
+// ahead so their latency stays off the copy path, and warp 0 lane 0 also the
+// TMA of A; mode 1: warp 0 lane 0 issues all TMA), warps 4-7 are the epilogue
+// (TMEM lane quadrant = warp % 4), warp 8 owns TMEM and issues tcgen05.mma
+// (converged warp, elect.sync).  Two 256-column fp32 accumulators in TMEM let
+// the epilogue of one tile overlap the MMAs of the next.  The epilogue stages
+// each 32 x 32 block of its rows through shared memory, so that every global
+// store instruction writes four whole rows' 128-byte runs instead of 32
+// scattered pieces.
 //
 // Split K (when there are fewer tiles than SMs): every split writes an fp32
 // partial tile to the workspace.  Each epilogue warp owns 32 rows of the tile
@@ -37,26 +41,32 @@
 namespace cfa {
 namespace {
 
-constexpr int kStages = 6;
-constexpr int kStageBytes = 2 * kRsTile * kRsBK * 2;  // A 16 KB + B 16 KB
-constexpr int kABytes = kRsTile * kRsBK * 2;
-constexpr int kSlabBytes = kRsBK * 128;              // 64 rows x 64 bf16 (128 B)
-constexpr int kGatherDepth = 4;                      // cp.async stages in flight per lane
-constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kStages = 4;
+constexpr int kABytes = kRsTileM * kRsBK * 2;          // 16 KB
+constexpr int kBBytes = kRsTileN * kRsBK * 2;          // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSlabBytes = kRsBK * 128;                // 64 rows x 64 bf16 (128 B)
+constexpr int kStgStride = 36;                         // put4 staging row: 32 floats + 4 pad
+constexpr int kStgBufBytes = 32 * 128;                 // TMA-store staging: 32 rows x 128 B
+constexpr int kStgWarpBytes = 2 * kStgBufBytes;        // two buffers per epilogue warp
+constexpr int kStgOff = kStages * kStageBytes;
+constexpr int kBarOff = kStgOff + 4 * kStgWarpBytes;
+static_assert(32 * kStgStride * 4 <= kStgWarpBytes, "put4 staging fits a warp's buffers");
 constexpr int kSmemBytes = kBarOff + 256 + 1024;
-static_assert(kGatherDepth <= kStages, "gather depth within the ring");
+constexpr int kThreads = 288;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// Four rows of a 2-D tensor, given by their row coordinates, each one box of
+// 64 columns x 1 row, into 4 consecutive 128-byte rows of shared memory
+// (swizzled by the tensor map's 128-byte mode like any tile).  Rows outside
+// the tensor (a negative or too large coordinate) read as zero.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int col, int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -68,8 +78,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
-  return __ldcg(reinterpret_cast<const float4*>(p));
+// Tile store (or add) of a 128-byte-wide box from shared memory; completion
+// tracked per thread with bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1,
+                                             uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   map),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 struct Unit {
@@ -87,80 +117,90 @@ __device__ __forceinline__ Unit unit_of(const RsArgs& a, long long u) {
   return r;
 }
 
-// Final store of one output row (128 fp32 values, columns tn*128 ...).
-template <int MODE>
-__device__ __forceinline__ void store_row(const RsArgs& a, const Unit& t, int row, const float* v) {
-  const int n0 = t.tn * kRsTile;
-  if (MODE == 0) {
-    const int m = t.tm * kRsTile + row;
-    if (m >= a.M) return;
-    if (a.out_f32) {
-      float* dst = static_cast<float*>(a.out) + (size_t)m * a.N + n0;
-#pragma unroll
-      for (int g = 0; g < 32; ++g) {
-        if (n0 + 4 * g >= a.N) break;
-        float4 w = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-        if (a.accumulate) {
-          const float4 o = *reinterpret_cast<const float4*>(dst + 4 * g);
-          w.x += o.x;
-          w.y += o.y;
-          w.z += o.z;
-          w.w += o.w;
-        }
-        *reinterpret_cast<float4*>(dst + 4 * g) = w;
-      }
-    } else {
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (size_t)m * a.N + n0;
-#pragma unroll
-      for (int g = 0; g < 16; ++g) {
-        if (n0 + 8 * g >= a.N) break;
-        float f[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = v[8 * g + e];
-        if (a.accumulate) {
-          const uint4 o = *reinterpret_cast<const uint4*>(dst + 8 * g);
-          const __nv_bfloat162* ob = reinterpret_cast<const __nv_bfloat162*>(&o);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 p = __bfloat1622float2(ob[e]);
-            f[2 * e] += p.x;
-            f[2 * e + 1] += p.y;
-          }
-        }
-        uint4 w;
-        w.x = pack_bf16x2(f[0], f[1]);
-        w.y = pack_bf16x2(f[2], f[3]);
-        w.z = pack_bf16x2(f[4], f[5]);
-        w.w = pack_bf16x2(f[6], f[7]);
-        *reinterpret_cast<uint4*>(dst + 8 * g) = w;
-      }
+// Walks a CTA's (unit, k stage) sequence: units c, c + grid, ... and the k
+// stages of each.
+struct StageIter {
+  long long u;
+  Unit t;
+  int kk;
+  bool valid;
+  __device__ __forceinline__ void start(const RsArgs& a, long long u0) {
+    u = u0;
+    valid = u < a.units;
+    if (valid) {
+      t = unit_of(a, u);
+      kk = t.kb;
     }
+  }
+  __device__ __forceinline__ void next(const RsArgs& a, long long ustep) {
+    if (++kk < t.ke) return;
+    u += ustep;
+    valid = u < a.units;
+    if (valid) {
+      t = unit_of(a, u);
+      kk = t.kb;
+    }
+  }
+};
+
+// Output of 4 consecutive columns (n, n+1, n+2, n+3) of one row at `dst`:
+// fp32 or bf16, overwritten or accumulated.
+__device__ __forceinline__ void put4(const RsArgs& a, void* dst, float4 q, bool f32) {
+  if (f32) {
+    float4* p = static_cast<float4*>(dst);
+    if (a.accumulate) {
+      const float4 o = *p;
+      q.x += o.x;
+      q.y += o.y;
+      q.z += o.z;
+      q.w += o.w;
+    }
+    *p = q;
   } else {
-    const int i = t.tm * kRsTile + row;
-    if (i >= a.n_keep) return;
-    const int r = a.keep[i];
-    if (r < 0 || r >= a.n_rows) {
-      atomicExch(a.status, -1 /* CFA_ERR_INVALID_ARG: a kept row outside X */);
-      return;
+    uint2* p = static_cast<uint2*>(dst);
+    if (a.accumulate) {
+      const uint2 o = *p;
+      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.x));
+      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.y));
+      q.x += lo.x;
+      q.y += lo.y;
+      q.z += hi.x;
+      q.w += hi.y;
     }
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (size_t)r * a.N + n0;
-#pragma unroll
-    for (int g = 0; g < 16; ++g) {
-      if (n0 + 8 * g >= a.N) break;
-      uint4 w;
-      w.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
-      w.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
-      w.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
-      w.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
-      *reinterpret_cast<uint4*>(dst + 8 * g) = w;
-    }
+    *p = make_uint2(pack_bf16x2(q.x, q.y), pack_bf16x2(q.z, q.w));
   }
 }
 
+// Where tile row `r` (0..127) of unit t goes, or null when it has no output
+// row: mode 0 row tm*128 + r of dW; mode 1 row keep[tm*128 + r] of dX
+// (`keep_r` = that index, fetched by the caller).
 template <int MODE>
-__global__ void __launch_bounds__(256, 1)
+__device__ __forceinline__ uint8_t* out_row(const RsArgs& a, const Unit& t, int r, int keep_r) {
+  const size_t esz = (MODE == 0 && a.out_f32) ? 4 : 2;
+  if (MODE == 0) {
+    const int m = t.tm * kRsTileM + r;
+    if (m >= a.M) return nullptr;
+    return static_cast<uint8_t*>(a.out) + (size_t)m * a.N * esz;
+  }
+  const int i = t.tm * kRsTileM + r;
+  if (i >= a.n_keep || keep_r < 0 || keep_r >= a.n_rows) return nullptr;
+  return static_cast<uint8_t*>(a.out) + (size_t)keep_r * a.N * esz;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
     rowsparse_kernel(const __grid_constant__ CUtensorMap map_a,
-                     const __grid_constant__ CUtensorMap map_b, const RsArgs a) {
+                     const __grid_constant__ CUtensorMap map_b,
+                     const __grid_constant__ CUtensorMap map_o,
+                     const __grid_constant__ CUtensorMap map_p,
+                     const __grid_constant__ CUtensorMap map_xt, const RsArgs a) {
+  // map_b: mode 0 X [n_rows, in] in 64-column x 1-row boxes (gathered),
+  //        mode 1 W [out, in] in 64 x 64 boxes
+  // map_o: mode 0 dW in 128-byte x 32-row boxes (TMA stores); map_p: the
+  //        split partials [tiles * splits * 128, 256] fp32 in 32 x 32 boxes
+  // map_xt: mode 0 X in 64 x 64 boxes, for stages whose 64 kept rows are one
+  //        run of consecutive rows (the chunk rows of a window): one tile
+  //        copy per slab instead of 16 gathers, same shared-memory layout
   pdl_start();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_addr(smem_raw);
@@ -180,8 +220,8 @@ __global__ void __launch_bounds__(256, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // mode 0: the A copy's expect_tx arrive plus one arrive per gather warp
-      mbar_init(bar_full + 8 * s, MODE == 0 ? 3 : 1);
+      // mode 0: one expect_tx arrive per gather warp (warp 0's covers A too)
+      mbar_init(bar_full + 8 * s, MODE == 0 ? 4 : 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -192,8 +232,8 @@ __global__ void __launch_bounds__(256, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 2) {
-    tmem_alloc(smem_addr(tmem_slot), 256);
+  if (warp == 8) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -203,86 +243,102 @@ __global__ void __launch_bounds__(256, 1)
   const Waiter W{a.limit_ns, abort_flag, a.status};
   const long long u0 = blockIdx.x, ustep = gridDim.x;
 
-  if (warp < 2) {
+  if (warp < 4) {
     // ---------------------------------------------------------- producers --
-    if (MODE == 1 && warp == 1) {
+    if (MODE == 1 && warp > 0) {
       // mode 1 loads everything by TMA from warp 0
     } else {
-      const bool tma_lane = warp == 0 && lane == 0;
-      int it = 0, signalled = 0;
+      const bool leader = lane == 0;
+      int it = 0;
       bool ok = true;
-      // mode 0 gather: this warp's slab (64 columns) of the stage's 64 rows;
-      // lane l always moves 16-byte chunk c = l % 8 of rows l / 8 + 4 j
-      const int c = lane & 7;
-      auto signal = [&](int upto) {
-        // the stages before `upto` have landed: make them visible to the
-        // tensor core (async proxy) and report them
-        fence_proxy_async_smem();
-        __syncwarp();
-        for (; signalled < upto; ++signalled)
-          if (lane == 0) mbar_arrive(bar_full + 8 * (signalled % kStages));
-      };
-      for (long long u = u0; ok && u < a.units; u += ustep) {
-        const Unit t = unit_of(a, u);
-        for (int kk = t.kb; kk < t.ke; ++kk, ++it) {
-          const int s = it % kStages;
-          if (!(ok = warp_wait(W, bar_empty + 8 * s, ((uint32_t)(it / kStages) & 1u) ^ 1u))) break;
-          const uint32_t st_a = base + s * kStageBytes, st_b = st_a + kABytes;
-          if (MODE == 1) {
-            if (tma_lane) {
-              mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
-              tma_load_2d(st_a, &map_a, bar_full + 8 * s, kk * kRsBK, t.tm * kRsTile);
-              tma_load_2d(st_b, &map_b, bar_full + 8 * s, t.tn * kRsTile, kk * kRsBK);
-              tma_load_2d(st_b + kSlabBytes, &map_b, bar_full + 8 * s, t.tn * kRsTile + 64,
-                          kk * kRsBK);
-            }
-            __syncwarp();
-          } else {
-            if (tma_lane) {
-              mbar_arrive_expect_tx(bar_full + 8 * s, kABytes);
-              tma_load_2d(st_a, &map_a, bar_full + 8 * s, t.tm * kRsTile, kk * kRsBK);
-              tma_load_2d(st_a + kSlabBytes, &map_a, bar_full + 8 * s, t.tm * kRsTile + 64,
-                          kk * kRsBK);
-            }
-            const int k0 = kk * kRsBK;
-            const int col = t.tn * kRsTile + warp * 64 + c * 8;
-            const bool col_ok = col < a.N;
-            int idx0 = -1, idx1 = -1;
-            if (k0 + lane < a.n_keep) idx0 = a.keep[k0 + lane];
-            if (k0 + 32 + lane < a.n_keep) idx1 = a.keep[k0 + 32 + lane];
-            const uint32_t slab = st_b + warp * kSlabBytes;
+      // Lane l < 16 gathers rows 4l .. 4l + 3 of a stage and holds their keep
+      // indices.  Rows past n_keep gather row 0 (their dY rows are
+      // zero-filled, so they add nothing); a kept index outside X gathers row
+      // n_rows, past the end, which the copy fills with zeros.
+      auto fetch_idx = [&](const StageIter& st, int (&r)[4]) {
+        r[0] = r[1] = r[2] = r[3] = 0;
+        if (MODE != 0 || !st.valid || lane >= 16) return;
+        const int k0 = st.kk * kRsBK + 4 * lane;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int r = j * 4 + (lane >> 3);  // row of the stage
-              const int idx = __shfl_sync(0xffffffffu, j < 8 ? idx0 : idx1, r & 31);
-              const bool in_keep = k0 + r < a.n_keep;
-              const bool row_ok = idx >= 0 && idx < a.n_rows;
-              if (in_keep && !row_ok) atomicExch(a.status, -1 /* kept row outside X */);
-              const bool take = in_keep && row_ok && col_ok;
-              const __nv_bfloat16* src = take ? a.x + (size_t)idx * a.N + col : a.x;
-              cp_async_16(slab + r * 128 + ((c ^ (r & 7)) << 4), src, take ? 16u : 0u);
+        for (int q = 0; q < 4; ++q)
+          if (k0 + q < a.n_keep) r[q] = a.keep[k0 + q];
+      };
+      StageIter cur;
+      cur.start(a, u0);
+      int nidx[4];
+      fetch_idx(cur, nidx);
+      for (; ok && cur.valid; ++it) {
+        const Unit t = cur.t;
+        const int kk = cur.kk;
+        int g[4] = {nidx[0], nidx[1], nidx[2], nidx[3]};
+        StageIter nxt = cur;
+        nxt.next(a, ustep);
+        fetch_idx(nxt, nidx);  // a stage ahead: consumed next iteration
+        if (MODE == 0) {
+          // a kept row outside X reads as zero; report it
+          bool bad = false;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (g[q] < 0 || g[q] >= a.n_rows) {
+              g[q] = a.n_rows;
+              bad = true;
             }
-            cp_async_commit();
-            if (it + 1 - signalled >= kGatherDepth) {
-              cp_async_wait<kGatherDepth - 1>();
-              signal(it + 2 - kGatherDepth);
-            }
+          if (warp == 0 && bad) atomicExch(a.status, -1 /* a kept row outside X */);
+        }
+        const int s = it % kStages;
+        if (leader) CFA_TRACE(warp, it, 0);
+        if (!(ok = warp_wait(W, bar_empty + 8 * s, ((uint32_t)(it / kStages) & 1u) ^ 1u))) break;
+        if (leader) CFA_TRACE(warp, it, 1);
+        const uint32_t st_a = base + s * kStageBytes, st_b = st_a + kABytes;
+        if (MODE == 1) {
+          if (leader) {
+            mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+            tma_load_2d(st_a, &map_a, bar_full + 8 * s, kk * kRsBK, t.tm * kRsTileM);
+#pragma unroll
+            for (int h = 0; h < kRsTileN / 64; ++h)
+              tma_load_2d(st_b + h * kSlabBytes, &map_b, bar_full + 8 * s,
+                          t.tn * kRsTileN + h * 64, kk * kRsBK);
+          }
+        } else {
+          // warp w: its 64-column slab of the stage's 64 kept rows -- one tile
+          // copy when they are 64 consecutive rows of X, else one 4-row
+          // gather per lane 0..15; warp 0 also loads A.  The expected bytes
+          // are posted before any of the warp's copies is issued.
+          const int run0 = __shfl_sync(0xffffffffu, g[0], 0);
+          const bool mine = lane >= 16 || (g[0] == run0 + 4 * lane && g[1] == g[0] + 1 &&
+                                           g[2] == g[0] + 2 && g[3] == g[0] + 3);
+          const bool run = __all_sync(0xffffffffu, mine) && (kk + 1) * kRsBK <= a.n_keep &&
+                           run0 + kRsBK <= a.n_rows;
+          if (leader)
+            mbar_arrive_expect_tx(bar_full + 8 * s, (warp == 0 ? kABytes : 0) + kSlabBytes);
+          __syncwarp();
+          if (leader && warp == 0) {
+            tma_load_2d(st_a, &map_a, bar_full + 8 * s, t.tm * kRsTileM, kk * kRsBK);
+            tma_load_2d(st_a + kSlabBytes, &map_a, bar_full + 8 * s, t.tm * kRsTileM + 64,
+                        kk * kRsBK);
+          }
+          if (run) {
+            if (leader)
+              tma_load_2d(st_b + warp * kSlabBytes, &map_xt, bar_full + 8 * s,
+                          t.tn * kRsTileN + warp * 64, run0);
+          } else if (lane < 16) {
+            tma_gather4(st_b + warp * kSlabBytes + lane * 512, &map_b, bar_full + 8 * s,
+                        t.tn * kRsTileN + warp * 64, g[0], g[1], g[2], g[3]);
           }
         }
+        if (leader) CFA_TRACE(warp, it, 2);
+        __syncwarp();
+        cur = nxt;
       }
-      if (MODE == 0) {
-        cp_async_wait<0>();
-        signal(it);
-      }
-      // unwind: the TMA copies this lane issued have landed before exit
-      if (tma_lane)
+      // unwind: the copies this lane issued have landed before exit
+      if (leader)
         for (int i = (it > kStages ? it - kStages : 0); i < it; ++i)
           mbar_wait_bounded(bar_full + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u,
                             kDrainLimitNs);
     }
-  } else if (warp == 2) {
+  } else if (warp == 8) {
     // ---------------------------------------------------------------- MMA --
-    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, MODE == 0 ? 1 : 0, 1);
+    constexpr uint32_t idesc = idesc_bf16_f32(kRsTileM, kRsTileN, MODE == 0 ? 1 : 0, 1);
     constexpr uint32_t hi = sw128_desc_hi(1024);
     int it = 0, tc = 0;
     bool ok = true;
@@ -291,10 +347,12 @@ __global__ void __launch_bounds__(256, 1)
       const int buf = tc & 1;
       if (!(ok = warp_wait(W, bar_tempty + 8 * buf, ((uint32_t)(tc >> 1) & 1u) ^ 1u))) break;
       tc_fence_after_sync();
-      const uint32_t d = tmem + (uint32_t)buf * 128u;
+      const uint32_t d = tmem + (uint32_t)buf * kRsTileN;
       for (int kk = t.kb; kk < t.ke; ++kk, ++it) {
         const int s = it % kStages;
+        CFA_TRACE(4, it, 0);
         if (!(ok = warp_wait(W, bar_full + 8 * s, (uint32_t)(it / kStages) & 1u))) break;
+        CFA_TRACE(4, it, 1);
         tc_fence_after_sync();
         const uint32_t st_a = base + s * kStageBytes, st_b = st_a + kABytes;
         const uint32_t a_lo = sw128_desc_lo(st_a, MODE == 0 ? kSlabBytes : 16);
@@ -315,36 +373,127 @@ __global__ void __launch_bounds__(256, 1)
     mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
   } else if (warp >= 4) {
     // ----------------------------------------------------------- epilogue --
+    // Warp q owns tile rows 32q .. 32q + 31 (its TMEM lane quadrant).
+    //  * dW overwritten, and split partials: each 32-row x 128-byte block is
+    //    written (128-byte swizzled) into one of the warp's two staging
+    //    buffers and sent by a TMA tile store;
+    //  * dW accumulated and dX (rows scattered by the keep index): the block
+    //    goes through padded staging rows and lanes read back 4 rows x 8
+    //    column groups per instruction, so each global access covers whole
+    //    128-byte row runs.
     const int quad = warp & 3;
-    const int row = quad * 32 + lane;
+    uint8_t* stg_g = gbase + kStgOff + quad * kStgWarpBytes;
+    const uint32_t stg_s = base + kStgOff + quad * kStgWarpBytes;
+    float* stg = reinterpret_cast<float*>(stg_g);
+    const int rr0 = lane >> 3, cg = lane & 7;  // read-back: row rr0 + 4 i, columns 4 cg ..
+    const bool f32 = MODE == 0 && a.out_f32;
+    const bool tma_out = MODE == 0 && !a.accumulate;
+    const size_t esz = f32 ? 4 : 2;
+    int sb = 0;  // staging buffer for the next TMA store
+    // one 128-byte row segment per lane (w: 32 words) -> TMA store at (c0, r0)
+    auto stage_store = [&](const CUtensorMap* map, int c0, int r0, const uint32_t* w) {
+      if (lane == 0) bulk_wait_read<1>();  // buffer sb no longer read by its last store
+      __syncwarp();
+      uint8_t* b = stg_g + sb * kStgBufBytes;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(b + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map, c0, r0, stg_s + sb * kStgBufBytes);
+        bulk_commit();
+      }
+      sb ^= 1;
+    };
     int tc = 0;
     bool ok = true;
     for (long long u = u0; ok && u < a.units; u += ustep, ++tc) {
       const Unit t = unit_of(a, u);
       const int buf = tc & 1;
+      int my_keep = -1;
+      if (MODE == 1) {
+        const int i = t.tm * kRsTileM + quad * 32 + lane;
+        if (i < a.n_keep) {
+          my_keep = a.keep[i];
+          if (my_keep < 0 || my_keep >= a.n_rows) atomicExch(a.status, -1 /* kept row outside X */);
+        }
+      }
+      if (quad == 0 && lane == 0) CFA_TRACE(5, tc, 0);
       if (!(ok = warp_wait(W, bar_tfull + 8 * buf, (uint32_t)(tc >> 1) & 1u))) break;
+      if (quad == 0 && lane == 0) CFA_TRACE(5, tc, 1);
       tc_fence_after_sync();
-      float v[128];
-      {
+      // output rows of the 8 read-back rows of this lane (put4 path)
+      uint8_t* orow[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = rr0 + 4 * i;
+        orow[i] = out_row<MODE>(a, t, quad * 32 + rr, __shfl_sync(0xffffffffu, my_keep, rr));
+      }
+      const bool split = a.splits > 1;
+      const int prow0 = ((t.tile * a.splits + t.split) * kRsTileM) + quad * 32;
+      if (!split && !tma_out) {
+        if (lane == 0) bulk_wait_read<0>();  // the padded staging overlaps both buffers
+        __syncwarp();
+      }
+      for (int h = 0; h < kRsTileN / 128; ++h) {
         uint32_t r[128];
-        tmem_ld_x128(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)buf * 128u, r);
+        tmem_ld_x128(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)buf * kRsTileN + h * 128, r);
+        if (quad == 0 && lane == 0) CFA_TRACE(5, tc, 2 + h);
+        if (h == kRsTileN / 128 - 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);  // the accumulator may be reused
+        }
+        if (split) {
 #pragma unroll
-        for (int e = 0; e < 128; ++e) v[e] = __uint_as_float(r[e]);
-      }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);  // the accumulator may be reused
-      if (a.splits == 1) {
-        store_row<MODE>(a, t, row, v);
-        continue;
-      }
-      // split K: publish this split's partial rows; the warp that adds the
-      // last split of its 32 rows sums them
-      float* mine = a.part + (((size_t)t.tile * a.splits + t.split) * kRsTile + row) * kRsTile;
+          for (int ch = 0; ch < 4; ++ch) stage_store(&map_p, h * 128 + ch * 32, prow0, r + ch * 32);
+        } else if (tma_out) {
+          const int c0 = t.tn * kRsTileN + h * 128;
+          const int r0 = t.tm * kRsTileM + quad * 32;
+          if (f32) {
 #pragma unroll
-      for (int g = 0; g < 32; ++g)
-        __stcg(reinterpret_cast<float4*>(mine + 4 * g),
-               make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+            for (int ch = 0; ch < 4; ++ch) stage_store(&map_o, c0 + ch * 32, r0, r + ch * 32);
+          } else {
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+              uint32_t pk[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                pk[e] = pack_bf16x2(__uint_as_float(r[ch * 64 + 2 * e]),
+                                    __uint_as_float(r[ch * 64 + 2 * e + 1]));
+              stage_store(&map_o, c0 + ch * 64, r0, pk);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            __syncwarp();  // the previous block has been read back
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(stg + lane * kStgStride + 4 * j) =
+                  make_uint4(r[ch * 32 + 4 * j], r[ch * 32 + 4 * j + 1], r[ch * 32 + 4 * j + 2],
+                             r[ch * 32 + 4 * j + 3]);
+            __syncwarp();
+            const int n = t.tn * kRsTileN + h * 128 + ch * 32 + 4 * cg;  // output column
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = rr0 + 4 * i;
+              const float4 q = *reinterpret_cast<const float4*>(stg + rr * kStgStride + 4 * cg);
+              if (orow[i] && n < a.N) put4(a, orow[i] + (size_t)n * esz, q, f32);
+            }
+          }
+        }
+      }
+      if (quad == 0 && lane == 0) CFA_TRACE(5, tc, 4);
+      if (!split) continue;
+      // split K: the partial rows are in global memory (async proxy) before
+      // the count; the warp that adds the last split of its 32 rows sums them
+      if (lane == 0) {
+        bulk_wait<0>();
+        fence_proxy_async_global();
+      }
       __threadfence();
       __syncwarp();
       unsigned old = 0;
@@ -352,29 +501,53 @@ __global__ void __launch_bounds__(256, 1)
       old = __shfl_sync(0xffffffffu, old, 0);
       if (old != (unsigned)(a.splits - 1)) continue;
       __threadfence();
+      const float* p0 = a.part + (size_t)t.tile * a.splits * kRsTileM * kRsTileN +
+                        (size_t)quad * 32 * kRsTileN;
+      // 32 independent loads in flight per round (4 splits x 8 rows), added
+      // in split order
+      for (int nb = 0; nb < kRsTileN; nb += 32) {
+        const int nt = nb + 4 * cg;
+        const int n = t.tn * kRsTileN + nt;
+        float4 acc[8];
 #pragma unroll
-      for (int e = 0; e < 128; ++e) v[e] = 0.f;
-      for (int sp = 0; sp < a.splits; ++sp) {
-        const float* p = a.part + (((size_t)t.tile * a.splits + sp) * kRsTile + row) * kRsTile;
+        for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp0 = 0; sp0 < a.splits; sp0 += 4) {
+          float4 x[4][8];
 #pragma unroll
-        for (int g = 0; g < 32; ++g) {
-          const float4 q = ld_cg_f4(p + 4 * g);
-          v[4 * g] += q.x;
-          v[4 * g + 1] += q.y;
-          v[4 * g + 2] += q.z;
-          v[4 * g + 3] += q.w;
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              x[q][i] = sp0 + q < a.splits
+                            ? __ldcg(reinterpret_cast<const float4*>(
+                                  p0 + (size_t)(sp0 + q) * kRsTileM * kRsTileN +
+                                  (size_t)(rr0 + 4 * i) * kRsTileN + nt))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              acc[i].x += x[q][i].x;
+              acc[i].y += x[q][i].y;
+              acc[i].z += x[q][i].z;
+              acc[i].w += x[q][i].w;
+            }
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (orow[i] && n < a.N) put4(a, orow[i] + (size_t)n * esz, acc[i], f32);
       }
-      store_row<MODE>(a, t, row, v);
       if (lane == 0) a.counters[4 * t.tile + quad] = 0u;  // ready for the next call
     }
+    // every store this warp issued has completed (and left shared memory)
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 8) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -399,13 +572,17 @@ __global__ void keep_index_chunks_kernel(const int32_t* __restrict__ cu_p,
 
 int rowsparse_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_rowsparse(const CUtensorMap& map_a, const CUtensorMap& map_b, const RsArgs& a,
-                             int grid, cudaStream_t st) {
-  void (*k)(const CUtensorMap, const CUtensorMap, const RsArgs) =
+cudaError_t launch_rowsparse(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                             const CUtensorMap& map_o, const CUtensorMap& map_p,
+                             const CUtensorMap& map_xt, const RsArgs& a, int grid,
+                             cudaStream_t st) {
+  void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+            const CUtensorMap, const RsArgs) =
       a.mode == 0 ? rowsparse_kernel<0> : rowsparse_kernel<1>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(grid), dim3(256), kSmemBytes, st, map_a, map_b, a);
+  return launch_pdl(k, dim3(grid), dim3(kThreads), kSmemBytes, st, map_a, map_b, map_o, map_p,
+                    map_xt, a);
 }
 
 cudaError_t launch_keep_index_chunks(const int32_t* cu_p, const int32_t* cu_c, int batch,
@@ -419,3 +596,15 @@ cudaError_t launch_keep_index_chunks(const int32_t* cu_p, const int32_t* cu_c, i
 }
 
 }  // namespace cfa
+
+#ifdef CFA_TRACE_BUILD
+extern "C" int cfa_trace_read_rs(long long* dst, int clear) {
+  const size_t n = sizeof(long long) * cfa::kTraceRoles * cfa::kTraceIters * cfa::kTraceEvents;
+  if (dst && cudaMemcpyFromSymbol(dst, cfa::cfa_trace_buf, n) != cudaSuccess) return -1;
+  if (clear) {
+    static long long zero[cfa::kTraceRoles * cfa::kTraceIters * cfa::kTraceEvents];
+    if (cudaMemcpyToSymbol(cfa::cfa_trace_buf, zero, n) != cudaSuccess) return -1;
+  }
+  return 0;
+}
+#endif
