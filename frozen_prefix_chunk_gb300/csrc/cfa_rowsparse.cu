@@ -499,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned old = 0;
       if (lane == 0) old = atomicAdd(a.counters + 4 * t.tile + quad, 1u);
       old = __shfl_sync(0xffffffffu, old, 0);
+      if (quad == 0 && lane == 0) CFA_TRACE(5, tc, 5);
       if (old != (unsigned)(a.splits - 1)) continue;
       __threadfence();
       const float* p0 = a.part + (size_t)t.tile * a.splits * kRsTileM * kRsTileN +
@@ -537,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (orow[i] && n < a.N) put4(a, orow[i] + (size_t)n * esz, acc[i], f32);
       }
       if (lane == 0) a.counters[4 * t.tile + quad] = 0u;  // ready for the next call
+      if (quad == 0 && lane == 0) CFA_TRACE(5, tc, 6);
     }
     // every store this warp issued has completed (and left shared memory)
     if (lane == 0) bulk_wait<0>();
