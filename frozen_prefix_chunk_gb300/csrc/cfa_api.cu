@@ -262,8 +262,8 @@ int cfa_forward(const cfa_args* a, void* o, float* lse, void* ws, size_t ws_byte
   if ((st = make_plan(a, &p))) return st;
   if ((st = check_ws(ws, ws_bytes, p.ws_fwd))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return CFA_ERR_LAUNCH;
-  if (a->total_lc == 0 || a->max_lc == 0) return CFA_OK;
+  if (a->total_lc == 0 || a->max_lc == 0)  // no kernel to clear the status word
+    return cudaMemsetAsync(ws, 0, 4, s) == cudaSuccess ? CFA_OK : CFA_ERR_LAUNCH;
 
   Maps m;
   std::memset(&m, 0, sizeof(m));
@@ -290,6 +290,7 @@ int cfa_forward(const cfa_args* a, void* o, float* lse, void* ws, size_t ws_byte
   fa.o_part = reinterpret_cast<float*>(w + p.off_opart);
   fa.lse_part = reinterpret_cast<float*>(w + p.off_lsepart);
   fa.status = reinterpret_cast<int*>(w);
+  fa.clear_status = 1;
   fa.limit_ns = wait_limit_ns();
   fa.debug_wait_never = debug_wait_never();
 
@@ -327,8 +328,9 @@ int prepare_backward(const cfa_args* a, const void* dout, const float* lse, cons
   if (a->total_lc > 0 && (!dout || !lse || !delta || !aligned16(dout))) return CFA_ERR_INVALID_ARG;
   if ((st = make_plan(a, p))) return st;
   if ((st = check_ws(ws, ws_bytes, need_partials ? p->ws_bwd : kWsHeader))) return st;
-  if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return CFA_ERR_LAUNCH;
   if (a->total_lc == 0 || a->max_lc == 0) {
+    // no attention kernel runs to clear the status word
+    if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess) return CFA_ERR_LAUNCH;
     *skip = true;
     return CFA_OK;
   }
@@ -362,6 +364,7 @@ int prepare_backward(const cfa_args* a, const void* dout, const float* lse, cons
   ba->pre_tiles = 0;
   ba->dk_p = ba->dv_p = nullptr;
   ba->status = reinterpret_cast<int*>(w);
+  ba->clear_status = 1;  // the caller turns it off for a kernel that is not the first
   ba->limit_ns = wait_limit_ns();
   ba->debug_wait_never = debug_wait_never();
   return CFA_OK;
@@ -495,7 +498,10 @@ int cfa_backward_horizon(const cfa_args* a, int horizon, const void* dout, const
   if (cudaEventRecord(ss->fork, s) != cudaSuccess ||
       cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
     return CFA_ERR_LAUNCH;
-  const int st_kv = run_dkdv(a, p, m, ba, k, ss->stream);
+  // the dQ kernel clears the status word; the dK/dV kernel beside it must not
+  BwdArgs ba_kv = ba;
+  ba_kv.clear_status = 0;
+  const int st_kv = run_dkdv(a, p, m, ba_kv, k, ss->stream);
   const int st_dq = run_dq(a, p, m, ba, s);
   // join even after a failed launch, so `s` never runs ahead of the side stream
   if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess ||

@@ -93,6 +93,11 @@ __global__ void __launch_bounds__(320, 1)
                   const __grid_constant__ CUtensorMap map_kc,
                   const __grid_constant__ CUtensorMap map_vc, const BwdArgs a) {
   pdl_start();
+  // A call's first kernel clears the status word once the previous work in
+  // the stream is done (no separate memset: one dependent launch less).  A
+  // device wait gives up only after its wall-clock limit, long after CTA 0
+  // has started, so no error of this launch is cleared.
+  if (a.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0;
   CFA_TRACE_CTA(0);
   using C = DqCfg<D>;
   constexpr int SK = C::kKStages;
@@ -512,6 +517,8 @@ __global__ void __launch_bounds__(320, 1)
                     const __grid_constant__ CUtensorMap map_kp,
                     const __grid_constant__ CUtensorMap map_vp, const BwdArgs a) {
   pdl_start();
+  // clears the status word when this kernel is its call's first (see the dQ kernel)
+  if (a.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0;
   using C = DkvCfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];

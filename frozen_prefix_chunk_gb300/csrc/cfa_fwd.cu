@@ -98,6 +98,11 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* gbase = smem_raw + (base - raw_base);
 
   pdl_start();
+  // A call's first kernel clears the status word once the previous work in
+  // the stream is done (no separate memset: one dependent launch less).  A
+  // device wait gives up only after its wall-clock limit, long after CTA 0
+  // has started, so no error of this launch is cleared.
+  if (a.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   CFA_TRACE_CTA(0);
   const Tiling tl = a.tl;
@@ -580,6 +585,27 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
     for (int u = 0; u < kBatch; ++u) sum += (ls[u] == -INFINITY) ? 0.f : expf(ls[u] - mx);
     lse = mx + logf(sum);
     accumulate(0, ls, v);
+  } else if (np <= 2 * kBatch) {
+    // two rounds of loads: all LSEs with the first batch of O, then the rest
+    float ls[kBatch], ls2[kBatch];
+    float4 v[kBatch][CW / 4];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      ls2[u] = (kBatch + u < np) ? a.lse_part[slot_of(kBatch + u) * rows_blk + r] : -INFINITY;
+    load_batch(0, ls, v);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) mx = fmaxf(mx, fmaxf(ls[u], ls2[u]));
+    float sum = 0.f;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      sum += (ls[u] == -INFINITY) ? 0.f : expf(ls[u] - mx);
+      sum += (ls2[u] == -INFINITY) ? 0.f : expf(ls2[u] - mx);
+    }
+    lse = mx + logf(sum);
+    accumulate(0, ls, v);
+    load_batch(kBatch, ls, v);
+    accumulate(kBatch, ls, v);
   } else {
     float mx = -INFINITY, sum = 0.f;
     for (int j0 = 0; j0 < np; j0 += kBatch) {

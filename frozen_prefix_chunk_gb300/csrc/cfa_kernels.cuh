@@ -31,6 +31,7 @@ struct FwdArgs {
   float* o_part;         // [grid, 2, rows per block, D]  partials of cut blocks
   float* lse_part;       // [grid, 2, rows per block]
   int* status;           // workspace status word
+  int clear_status;      // CTA 0 zeroes *status as the kernel starts
   unsigned long long limit_ns;
   int debug_wait_never;  // test hook: the MMA thread waits on a barrier nobody sets
 };
@@ -55,6 +56,7 @@ struct BwdArgs {
   __nv_bfloat16* dk_p;   // [total_lp, hkv, D]  prefix gradients in the horizon
   __nv_bfloat16* dv_p;
   int* status;
+  int clear_status;      // CTA 0 zeroes *status as the kernel starts
   unsigned long long limit_ns;
   int debug_wait_never;  // test hook: the MMA thread waits on a barrier nobody sets
 };

@@ -55,7 +55,10 @@
  * enqueued.  A device-side wait that does not finish in time (default 2 s;
  * the environment variable CFA_WAIT_LIMIT_NS overrides it) ends its kernel
  * early and records CFA_ERR_DEVICE_TIMEOUT in the status word at the start of
- * the workspace, readable with cfa_read_status().
+ * the workspace, readable with cfa_read_status().  Every call clears that
+ * word before it computes: the call's first attention kernel does it as it
+ * starts (stream-ordered after the previous work), or a 4-byte memset when
+ * there is nothing to compute.
  *
  * Determinism: the same inputs give bitwise-identical outputs (fixed-order
  * reductions, no atomics on data); the forward does not depend on whether a
