@@ -13,8 +13,10 @@ Roofline of the step: t_roof = max(F / bf16 peak, algorithmic bytes / HBM
 bandwidth), fraction = t_roof / t_measured.
 
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
-launching stream; L2 is flushed (256 MiB write) before every timed step,
-outside the events.  Under torchrun every rank runs its own replica of the
+launching stream; L2 is flushed before every timed step, outside the events:
+a 256 MiB write, then a 256 MiB read that writes those dirty lines back, so
+the step starts with none of its inputs in L2 and no write-back of the flush
+buffer left to do (--flush write keeps only the write).  Under torchrun every rank runs its own replica of the
 workload (weak scaling, no collective on the data path); value = all ranks'
 FLOPs / max over ranks of the time.
 
@@ -273,7 +275,7 @@ def run_walk(args, w):
     q, do = rnd(lcw, w.hq, w.head_dim), rnd(lcw, w.hq, w.head_dim, std=w.dout_std)
     cache = cfa.PREFIX_Q8_0 if w.prefix_dtype == synth.PREFIX_Q8_0 else cfa.PREFIX_BF16
     walk = WindowWalk(k[:lp0], v[:lp0], lp0 + lcw, w.hq, w.softmax_scale, cache)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, args.flush)
 
     def walk_once():
         walk.rewind(lp0)
@@ -298,12 +300,12 @@ def run_walk(args, w):
 
     def timed(fn, steps):
         for _ in range(args.warmup):
-            flush.zero_()
+            flush()
             fn()
         torch.cuda.synchronize()
         ts = []
         for _ in range(steps):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
@@ -361,7 +363,7 @@ class L2Flush:
     buffer, which forces that write-back before the step and leaves only clean
     lines behind."""
 
-    def __init__(self, dev, mode="write"):
+    def __init__(self, dev, mode="write+read"):
         self.mode = mode
         self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
         self.rbuf = (torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -520,7 +522,7 @@ def main():
     ap.add_argument("--workload", default="qwen3_8b", choices=list(synth.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--flush", default="write", choices=["write", "write+read"],
+    ap.add_argument("--flush", default="write+read", choices=["write", "write+read"],
                     help="how L2 is evicted before each timed step")
     ap.add_argument("--rowsparse", action="store_true",
                     help="time the layer's row-sparse projection backward instead")

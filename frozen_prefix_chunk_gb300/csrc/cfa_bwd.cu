@@ -862,35 +862,32 @@ __global__ void __launch_bounds__(320, 1)
 
 // Sum the dQ partials of every query tile that CTA boundaries cut, in CTA
 // order (deterministic), and round to bf16.  One CTA per (query tile, 32
-// rows); thread 0 lists the tile's parts once; thread t takes row t % 32 of
-// the chunk and column slice t / 32, so a warp reads consecutive rows of the
-// feature-major partials (coalesced).
+// rows); every thread finds the tile's parts in closed form (part_count /
+// part_cta); thread t takes row t % 32 of the chunk and column slice t / 32,
+// so a warp reads consecutive rows of the feature-major partials (coalesced).
 constexpr int kReduceRows = 32;
-constexpr int kMaxParts = 1024;
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
   pdl_start();
   constexpr int CW = D / 8;
-  __shared__ int parts[kMaxParts];
-  __shared__ int n_parts;
   const Tiling tl = a.tl;
   const int chunks = kTileM / kReduceRows;
   const int b = blockIdx.z, hk = blockIdx.y;
   const int qb = blockIdx.x / chunks;
   const int row = (blockIdx.x % chunks) * kReduceRows + (threadIdx.x & 31);
   const int c0col = (threadIdx.x >> 5) * CW;
+  const long long w0 = a.win_prefix[b], total = a.win_prefix[a.batch];
   const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
   const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
   if (qb >= blocks_of_window(tl, lc)) return;
-  if (threadIdx.x == 0) {
-    long long bs, be;  // the block's key-tile iterations
-    block_span(tl, a.win_prefix[b], hk, qb, lp, lc, &bs, &be);
-    n_parts = block_parts(bs, be, a.win_prefix[a.batch], tl.grid, parts, kMaxParts);
-  }
-  __syncthreads();
-  const int np = n_parts;
+  // the tile's parts (every thread finds them; no shared list, no barrier)
+  long long bs, be;
+  block_span(tl, w0, hk, qb, lp, lc, &bs, &be);
+  const int np = part_count(bs, be, total, tl.grid);
   if (np == 0) return;
+  const int cf = cta_of(bs, total, tl.grid);
+  const bool dense = total >= tl.grid;  // then the parts are CTAs cf, cf + 1, ...
   const int token = qb * tl.tpt + row / tl.g;
   if (row >= tl.rows || token >= lc) return;
   const int head = hk * tl.g + row % tl.g;
@@ -905,7 +902,8 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int j = j0 + u;
-      const size_t slot = (size_t)parts[j < np ? j : 0] * 2 + (j == 0);
+      const int jj = j < np ? j : 0;
+      const size_t slot = (size_t)(dense ? cf + jj : part_cta(bs, total, tl.grid, jj)) * 2 + (j == 0);
       const float4* src = reinterpret_cast<const float4*>(a.dq_part) + slot * (D / 4) * kTileM;
 #pragma unroll
       for (int e = 0; e < CW; e += 4)

@@ -501,19 +501,31 @@ __global__ void __launch_bounds__(352, 1)
 }
 
 // Merge the partials of every query block that CTA boundaries cut.  One CTA
-// per (query block, 32 packed rows); thread 0 lists the block's parts once
-// (slot 1 of the first CTA, slot 0 of the others).  Thread t takes row
-// r0 + t % 32 and the column slice t / 32 (of 8), so the lanes of a warp read
-// consecutive rows of the feature-major partials (coalesced).
+// per (query block, 32 packed rows); every thread finds the block's parts in
+// closed form (part_count / part_cta: slot 1 of the first CTA, slot 0 of the
+// others).  Thread t takes row r0 + t % 32 and the column slice t / 32 (of
+// 8), so the lanes of a warp read consecutive rows of the feature-major
+// partials (coalesced).
 constexpr int kMergeRows = 32;
-constexpr int kMaxParts = 1024;
+
+#ifdef CFA_TRACE_BUILD
+static __device__ unsigned long long cfa_trace_merge[4 * 1024];
+#define CFA_TRACE_MERGE(ev)                                                                  \
+  do {                                                                                       \
+    const int lin = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;         \
+    if (threadIdx.x == 0 && lin < 1024) cfa_trace_merge[4 * lin + (ev)] = global_timer_ns_raw(); \
+  } while (0)
+#else
+#define CFA_TRACE_MERGE(ev) \
+  do {                      \
+  } while (0)
+#endif
 
 template <int D>
 __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
   pdl_start();
+  CFA_TRACE_MERGE(0);
   constexpr int CW = D / 8;  // columns per thread
-  __shared__ int parts[kMaxParts];
-  __shared__ int n_parts;
   const Tiling tl = a.tl;
   const int tok_blk = tl.q_per_cta * tl.tpt;
   const int rows_blk = tl.q_per_cta * kTileM;
@@ -522,16 +534,16 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
   const int qb = blockIdx.x / chunks;
   const int r = (blockIdx.x % chunks) * kMergeRows + (threadIdx.x & 31);
   const int c0col = (threadIdx.x >> 5) * CW;
+  const long long w0 = a.win_prefix[b], total = a.win_prefix[a.batch];
   const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
   const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
   if (qb >= blocks_of_window(tl, lc)) return;
-  if (threadIdx.x == 0) {
-    long long bs, be;  // the block's key-tile iterations
-    block_span(tl, a.win_prefix[b], hk, qb, lp, lc, &bs, &be);
-    n_parts = block_parts(bs, be, a.win_prefix[a.batch], tl.grid, parts, kMaxParts);
-  }
-  __syncthreads();
-  const int np = n_parts;
+  CFA_TRACE_MERGE(1);
+  // the block's parts (every thread finds them; no shared list, no barrier)
+  long long bs, be;
+  block_span(tl, w0, hk, qb, lp, lc, &bs, &be);
+  const int np = part_count(bs, be, total, tl.grid);
+  CFA_TRACE_MERGE(2);
   if (np == 0) return;
   const int qt = r / kTileM, row = r % kTileM;
   const int token = qb * tok_blk + qt * tl.tpt + row / tl.g;
@@ -542,7 +554,13 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
   // common case) the LSE and O loads go out together, one round trip; more
   // parts take an online max/sum pass over the LSEs, then the O pass.
   constexpr int kBatch = 4;
-  auto slot_of = [&](int j) { return (size_t)parts[j < np ? j : 0] * 2 + (j == 0); };
+  const int cf = cta_of(bs, total, tl.grid);
+  const bool dense = total >= tl.grid;  // then the parts are CTAs cf, cf + 1, ...
+  auto slot_of = [&](int j) {
+    const int jj = j < np ? j : 0;
+    const int c = dense ? cf + jj : part_cta(bs, total, tl.grid, jj);
+    return (size_t)c * 2 + (j == 0);
+  };
   const float4* o4 = reinterpret_cast<const float4*>(a.o_part);
   float acc[CW];
 #pragma unroll
@@ -637,6 +655,7 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
                             pack_bf16x2(acc[e + 4], acc[e + 5]),
                             pack_bf16x2(acc[e + 6], acc[e + 7]));
   if (threadIdx.x < 32) a.lse[(size_t)head * a.total_lc + grow] = lse;
+  CFA_TRACE_MERGE(3);
 }
 
 }  // namespace
@@ -682,6 +701,11 @@ cudaError_t launch_fwd_merge(const FwdArgs& a, int d, int max_lc, cudaStream_t s
 #ifdef CFA_TRACE_BUILD
 extern "C" int cfa_trace_read_cta_fwd(unsigned long long* dst) {
   return cudaMemcpyFromSymbol(dst, cfa::cfa_trace_cta, sizeof(unsigned long long) * 2048) ==
+                 cudaSuccess ? 0 : -1;
+}
+
+extern "C" int cfa_trace_read_merge(unsigned long long* dst) {
+  return cudaMemcpyFromSymbol(dst, cfa::cfa_trace_merge, sizeof(unsigned long long) * 4096) ==
                  cudaSuccess ? 0 : -1;
 }
 

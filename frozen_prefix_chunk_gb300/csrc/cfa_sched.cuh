@@ -203,6 +203,20 @@ __host__ __device__ inline int block_parts(long long bs, long long be, long long
   return n;
 }
 
+// The same part list in closed form, for a block with iterations [bs, be):
+// the number of parts (0 when one CTA holds the whole block) and the CTA
+// holding part j.  With total >= G every CTA holds an iteration, so the parts
+// are the consecutive CTAs from the one holding bs; with total < G every CTA
+// holds at most one, so part j is the CTA holding iteration bs + j.
+__host__ __device__ inline int part_count(long long bs, long long be, long long total, int G) {
+  const int cf = cta_of(bs, total, G), cl = cta_of(be - 1, total, G);
+  if (cf == cl) return 0;
+  return total >= G ? cl - cf + 1 : (int)(be - bs);
+}
+__host__ __device__ inline int part_cta(long long bs, long long total, int G, int j) {
+  return total >= G ? cta_of(bs, total, G) + j : cta_of(bs + j, total, G);
+}
+
 #ifdef __CUDACC__
 // Prologue of the persistent kernels, run by all `nthreads` threads of the
 // CTA: scans the per-window iteration counts (each thread sums a contiguous

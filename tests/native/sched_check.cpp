@@ -96,6 +96,10 @@ int main(int argc, char** argv) {
           for (int i = 0; i < np; ++i)
             if (parts[i] != v[i].cta) { printf("FAIL block %lld: part %d is CTA %d, holder %d\n", key, i, parts[i], v[i].cta); return 1; }
         }
+        // the closed form the split kernels use agrees with the list
+        if (part_count(first, end, W, G) != np) { printf("FAIL block %lld: part_count\n", key); return 1; }
+        for (int i = 0; i < np; ++i)
+          if (part_cta(first, W, G, i) != parts[i]) { printf("FAIL block %lld: part_cta %d\n", key, i); return 1; }
       }
   }
   // balance: iterations per CTA differ by at most one
