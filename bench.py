@@ -379,7 +379,7 @@ class L2Flush:
         if self.rbuf is not None:
             # read every line; the result goes to a kept buffer, so a flush
             # allocates nothing
-            torch.sum(self.rbuf, dtype=torch.int64, out=self.out)
+            torch.sum(self.rbuf, dim=0, dtype=torch.int64, out=self.out)
 
     def describe(self):
         return {"write": "flushed before every timed step (256 MiB write)",
