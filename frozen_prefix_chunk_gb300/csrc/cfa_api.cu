@@ -117,12 +117,30 @@ Tiling make_tiling(const cfa_args* a, int q_per_cta, int sms) {
   // taking up a query block costs a CTA about two key tiles' time (measured:
   // CTAs whose range crosses a block start finished 2-3.5 us later)
   t.setup = 2;
+  t.nrow = 1;
   return t;
+}
+
+// Row mode (Tiling::nrow, cfa_sched.cuh) pays when the heads' K/V is well
+// beyond L2 (129 MB): then the query blocks of one (window, KV head), which
+// read the same keys, must run in lockstep for a key tile to come from DRAM
+// once.  It needs every window to have the same chunk length (the rows then
+// have the same layout) and a grid that the rows divide.  Returns the number
+// of rows for a grid of `grid` CTAs, or 1.
+constexpr double kRowModeKvBytes = 96.0 * (1 << 20);
+
+int row_mode_rows(const cfa_args* a, const Tiling& t, int grid) {
+  const double kv_bytes = 4.0 * (double)a->total_lp * a->hkv * a->head_dim;  // bf16 K and V
+  if (kv_bytes < kRowModeKvBytes) return 1;
+  if ((long long)a->total_lc != (long long)a->batch * a->max_lc) return 1;  // lengths differ
+  const int nb = blocks_of_window(t, a->max_lc);
+  if (nb <= 1 || grid % nb != 0) return 1;
+  return nb;
 }
 
 // Workspace layout (every region 256-byte aligned):
 //   [0, 256)           status word
-//   win_prefix         int64 [batch + 1]  (stream-K plan)
+//   win_prefix         int64 [rows][batch + 1]  (stream-K plan, per schedule row)
 //   partials           fp32, two slots per CTA: forward O [G, 2, 256, d] and
 //                      LSE [G, 2, 256]; backward dQ [G, 2, 128, d]
 //   bf16 prefix        K then V [total_lp, hkv, d], only for a q8_0 prefix
@@ -132,9 +150,14 @@ int make_plan(const cfa_args* a, Plan* p) {
   if (st) return st;
   p->fwd = make_tiling(a, 2, sms);
   p->dq = make_tiling(a, 1, sms);
+  p->fwd.nrow = row_mode_rows(a, p->fwd, sms);
+  // the dQ grid is the GPU less the dK/dV kernel's SMs, fixed by the call;
+  // its row count is settled there (dq_rows), the prefix arrays sized here
+  const int dq_rows_max = blocks_of_window(p->dq, a->max_lc > 0 ? a->max_lc : 1);
   p->n_kc_max = ceil_div(a->max_lc > 0 ? a->max_lc : 1, kTileN);
   const size_t G = (size_t)sms;
-  const size_t wp = align256((size_t)(a->batch + 1) * 8);
+  const size_t wp_rows = (size_t)(p->fwd.nrow > dq_rows_max ? p->fwd.nrow : dq_rows_max);
+  const size_t wp = align256(wp_rows * (size_t)(a->batch + 1) * 8);
   const size_t kv16 = (a->prefix_dtype != CFA_PREFIX_BF16)
                           ? align256((size_t)a->total_lp * a->hkv * a->head_dim * 2)
                           : 0;
@@ -490,7 +513,17 @@ int cfa_backward_horizon(const cfa_args* a, int horizon, const void* dout, const
   // its own, on a second stream forked from and joined back into `s`, while
   // the dQ kernel's persistent grid takes the rest.
   const long long items = dkdv_items(a, ba);
-  const int k = dkdv_share(a, p.dq, p.dq.grid, items, ba.horizon);
+  int k = dkdv_share(a, p.dq, p.dq.grid, items, ba.horizon);
+  // row mode for the dQ kernel: give the dK/dV kernel a few SMs more, if that
+  // makes the rows divide the dQ grid
+  for (int k2 = k; k2 <= k + 16 && k2 <= p.dq.grid / 2; ++k2) {
+    const int rows = row_mode_rows(a, p.dq, p.dq.grid - k2);
+    if (rows > 1) {
+      k = k2;
+      ba.tl.nrow = rows;
+      break;
+    }
+  }
   ba.tl.grid = p.dq.grid - k;
   std::lock_guard<std::mutex> lock(g_side_mutex);
   SideStream* ss = nullptr;
@@ -521,6 +554,7 @@ int cfa_backward_dq(const cfa_args* a, const void* dout, const float* lse, const
   int st = prepare_backward(a, dout, lse, delta, ws, ws_bytes, true, s, &p, &m, &ba, &skip);
   if (st || skip) return st;
   ba.dq = static_cast<__nv_bfloat16*>(dq);
+  ba.tl.nrow = row_mode_rows(a, p.dq, ba.tl.grid);
   return run_dq(a, p, m, ba, s);
 }
 

@@ -84,7 +84,7 @@ struct DqCfg {
   static_assert(8 * (2 + 2 * kKStages + 2 * kVStages + 8) <= 240, "barrier area");
 };
 
-template <int D>
+template <int D, bool ROW>
 __global__ void __launch_bounds__(320, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q,
                   const __grid_constant__ CUtensorMap map_do,
@@ -112,10 +112,10 @@ __global__ void __launch_bounds__(320, 1)
   {
     // schedule prologue: shared scratch in the (not yet used) barrier area
     long long* sched = reinterpret_cast<long long*>(gbase + C::kBarOff);
-    plan_schedule(a.cu_p, a.cu_c, a.batch, a.hkv, tl, a.win_prefix, sched + 4, sched,
+    plan_schedule<ROW>(a.cu_p, a.cu_c, a.batch, a.hkv, tl, a.win_prefix, sched + 4, sched,
                   reinterpret_cast<int*>(sched + 1), sched + 2);
   }
-  SegmentWalker walk;
+  SegmentWalkerT<ROW> walk;
   {
     const long long* sched = reinterpret_cast<const long long*>(gbase + C::kBarOff);
     walk.init(a.cu_p, a.cu_c, a.batch, a.hkv, tl, blockIdx.x, sched[0],
@@ -877,17 +877,20 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
   const int qb = blockIdx.x / chunks;
   const int row = (blockIdx.x % chunks) * kReduceRows + (threadIdx.x & 31);
   const int c0col = (threadIdx.x >> 5) * CW;
-  const long long w0 = a.win_prefix[b], total = a.win_prefix[a.batch];
+  // the block's schedule row: its prefix array and its first CTA
+  const int srow = row_of_block(tl, qb), rg = row_grid(tl);
+  const long long* wp = a.win_prefix + (size_t)srow * (a.batch + 1);
+  const long long w0 = wp[b], total = wp[a.batch];
   const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
   const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
   if (qb >= blocks_of_window(tl, lc)) return;
   // the tile's parts (every thread finds them; no shared list, no barrier)
   long long bs, be;
   block_span(tl, w0, hk, qb, lp, lc, &bs, &be);
-  const int np = part_count(bs, be, total, tl.grid);
+  const int np = part_count(bs, be, total, rg);
   if (np == 0) return;
-  const int cf = cta_of(bs, total, tl.grid);
-  const bool dense = total >= tl.grid;  // then the parts are CTAs cf, cf + 1, ...
+  const int cf = srow * rg + cta_of(bs, total, rg);
+  const bool dense = total >= rg;  // then the parts are CTAs cf, cf + 1, ...
   const int token = qb * tl.tpt + row / tl.g;
   if (row >= tl.rows || token >= lc) return;
   const int head = hk * tl.g + row % tl.g;
@@ -903,7 +906,7 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
     for (int u = 0; u < kBatch; ++u) {
       const int j = j0 + u;
       const int jj = j < np ? j : 0;
-      const size_t slot = (size_t)(dense ? cf + jj : part_cta(bs, total, tl.grid, jj)) * 2 + (j == 0);
+      const size_t slot = (size_t)(dense ? cf + jj : srow * rg + part_cta(bs, total, rg, jj)) * 2 + (j == 0);
       const float4* src = reinterpret_cast<const float4*>(a.dq_part) + slot * (D / 4) * kTileM;
 #pragma unroll
       for (int e = 0; e < CW; e += 4)
@@ -1157,24 +1160,24 @@ int bwd_dkdv_smem_bytes(int d) {
   return d == 128 ? DkvCfg<128>::kSmemBytes : DkvCfg<64>::kSmemBytes;
 }
 
+namespace {
+template <int D, bool ROW>
+cudaError_t launch_bwd_dq_t(const Maps& m, const BwdArgs& a, cudaStream_t st) {
+  auto k = bwd_dq_kernel<D, ROW>;
+  cudaError_t e =
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k, dim3((unsigned)a.tl.grid), 320, DqCfg<D>::kSmemBytes, st, m.q, m.dout, m.kp,
+                    m.vp, m.kc, m.vc, a);
+}
+}  // namespace
+
 cudaError_t launch_bwd_dq(const Maps& m, const BwdArgs& a, int d, int q8, cudaStream_t st) {
   (void)q8;
-  const dim3 grid((unsigned)a.tl.grid);
-  if (d == 128) {
-    auto k = bwd_dq_kernel<128>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DqCfg<128>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k, grid, 320, DqCfg<128>::kSmemBytes, st, m.q, m.dout, m.kp, m.vp, m.kc, m.vc,
-                      a);
-  } else {
-    auto k = bwd_dq_kernel<64>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DqCfg<64>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k, grid, 320, DqCfg<64>::kSmemBytes, st, m.q, m.dout, m.kp, m.vp, m.kc, m.vc,
-                      a);
-  }
+  const bool row = a.tl.nrow > 1;
+  if (d == 128)
+    return row ? launch_bwd_dq_t<128, true>(m, a, st) : launch_bwd_dq_t<128, false>(m, a, st);
+  return row ? launch_bwd_dq_t<64, true>(m, a, st) : launch_bwd_dq_t<64, false>(m, a, st);
 }
 
 cudaError_t launch_bwd_dkdv(const Maps& m, const BwdArgs& a, int d, int ctas, cudaStream_t st) {

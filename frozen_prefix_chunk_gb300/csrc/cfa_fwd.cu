@@ -83,7 +83,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
                 (accumulate || k > 0) ? 1u : 0u);
 }
 
-template <int D>
+template <int D, bool ROW>
 __global__ void __launch_bounds__(352, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kp,
                const __grid_constant__ CUtensorMap map_vp,
@@ -111,10 +111,10 @@ __global__ void __launch_bounds__(352, 1)
   {
     // schedule prologue: shared scratch in the (not yet used) barrier area
     long long* sched = reinterpret_cast<long long*>(gbase + C::kBarOff);
-    plan_schedule(a.cu_p, a.cu_c, a.batch, a.hkv, tl, a.win_prefix, sched + 4, sched,
+    plan_schedule<ROW>(a.cu_p, a.cu_c, a.batch, a.hkv, tl, a.win_prefix, sched + 4, sched,
                   reinterpret_cast<int*>(sched + 1), sched + 2);
   }
-  SegmentWalker walk;
+  SegmentWalkerT<ROW> walk;
   {
     const long long* sched = reinterpret_cast<const long long*>(gbase + C::kBarOff);
     walk.init(a.cu_p, a.cu_c, a.batch, a.hkv, tl, blockIdx.x, sched[0],
@@ -534,7 +534,10 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
   const int qb = blockIdx.x / chunks;
   const int r = (blockIdx.x % chunks) * kMergeRows + (threadIdx.x & 31);
   const int c0col = (threadIdx.x >> 5) * CW;
-  const long long w0 = a.win_prefix[b], total = a.win_prefix[a.batch];
+  // the block's schedule row: its prefix array and its first CTA
+  const int srow = row_of_block(tl, qb), rg = row_grid(tl);
+  const long long* wp = a.win_prefix + (size_t)srow * (a.batch + 1);
+  const long long w0 = wp[b], total = wp[a.batch];
   const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
   const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
   if (qb >= blocks_of_window(tl, lc)) return;
@@ -542,7 +545,7 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
   // the block's parts (every thread finds them; no shared list, no barrier)
   long long bs, be;
   block_span(tl, w0, hk, qb, lp, lc, &bs, &be);
-  const int np = part_count(bs, be, total, tl.grid);
+  const int np = part_count(bs, be, total, rg);
   CFA_TRACE_MERGE(2);
   if (np == 0) return;
   const int qt = r / kTileM, row = r % kTileM;
@@ -554,11 +557,11 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
   // common case) the LSE and O loads go out together, one round trip; more
   // parts take an online max/sum pass over the LSEs, then the O pass.
   constexpr int kBatch = 4;
-  const int cf = cta_of(bs, total, tl.grid);
-  const bool dense = total >= tl.grid;  // then the parts are CTAs cf, cf + 1, ...
+  const int cf = srow * rg + cta_of(bs, total, rg);
+  const bool dense = total >= rg;  // then the parts are CTAs cf, cf + 1, ...
   auto slot_of = [&](int j) {
     const int jj = j < np ? j : 0;
-    const int c = dense ? cf + jj : part_cta(bs, total, tl.grid, jj);
+    const int c = dense ? cf + jj : srow * rg + part_cta(bs, total, rg, jj);
     return (size_t)c * 2 + (j == 0);
   };
   const float4* o4 = reinterpret_cast<const float4*>(a.o_part);
@@ -665,24 +668,23 @@ int fwd_smem_bytes(int d, int q8) {
   return d == 128 ? FwdCfg<128>::kSmemBytes : FwdCfg<64>::kSmemBytes;
 }
 
+namespace {
+template <int D, bool ROW>
+cudaError_t launch_fwd_t(const Maps& m, const FwdArgs& a, cudaStream_t st) {
+  auto k = fwd_kernel<D, ROW>;
+  cudaError_t e =
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k, dim3((unsigned)a.tl.grid), FwdCfg<D>::kThreads, FwdCfg<D>::kSmemBytes, st,
+                    m.q, m.kp, m.vp, m.kc, m.vc, a);
+}
+}  // namespace
+
 cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, int q8, cudaStream_t st) {
   (void)q8;
-  const dim3 grid((unsigned)a.tl.grid);
-  if (d == 128) {
-    auto k = fwd_kernel<128>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FwdCfg<128>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k, grid, FwdCfg<128>::kThreads, FwdCfg<128>::kSmemBytes, st, m.q, m.kp, m.vp,
-                      m.kc, m.vc, a);
-  } else {
-    auto k = fwd_kernel<64>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FwdCfg<64>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k, grid, FwdCfg<64>::kThreads, FwdCfg<64>::kSmemBytes, st, m.q, m.kp, m.vp,
-                      m.kc, m.vc, a);
-  }
+  const bool row = a.tl.nrow > 1;
+  if (d == 128) return row ? launch_fwd_t<128, true>(m, a, st) : launch_fwd_t<128, false>(m, a, st);
+  return row ? launch_fwd_t<64, true>(m, a, st) : launch_fwd_t<64, false>(m, a, st);
 }
 
 cudaError_t launch_fwd_merge(const FwdArgs& a, int d, int max_lc, cudaStream_t st) {

@@ -20,9 +20,12 @@
 // block writes the final outputs; a block cut by CTA boundaries leaves one
 // partial per CTA, in slot 1 of the CTA holding its start and slot 0 of the
 // others, and a merge kernel combines them in CTA order (deterministic).
+// With Tiling::nrow > 1 (row mode, below) the same scheme runs once per
+// schedule row, over that row's own CTAs.
 // Every CTA scans the per-window work itself in its prologue (plan_schedule
-// below); CTA 0 also stores the prefix array win_prefix[b] (int64, [batch +
-// 1]) for the merge kernels that run afterwards.
+// below); the first CTA of each schedule row also stores the row's prefix
+// array win_prefix[row][b] (int64, [nrow][batch + 1]) for the merge kernels
+// that run afterwards.
 #pragma once
 
 #include <stdint.h>
@@ -45,7 +48,19 @@ struct Tiling {
   int q_per_cta;  // query tiles per query block
   int grid;       // persistent CTAs (G)
   int setup;      // virtual iterations charged at the start of every query block
+  int nrow;       // schedule rows: 1, or (row mode) the query blocks of every window
 };
+
+// Row mode.  With nrow > 1 every window has nrow query blocks, and the
+// schedule is nrow independent stream-K schedules over grid / nrow CTAs each:
+// row r holds block r of every (window, KV head), CTAs r * grid / nrow on.
+// The rows have the same layout (the same windows and heads in the same
+// order, the same prefix key tiles), so CTA j of every row reads the same key
+// tiles of the same head at about the same time: the blocks that share K/V
+// run in lockstep and a tile is read from DRAM about once, even when the
+// heads' K/V is far larger than L2.  With nrow = 1 the iterations are one
+// schedule, window-major, then KV head, then query block.
+__host__ __device__ inline int row_grid(const Tiling& tl) { return tl.grid / tl.nrow; }
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -77,13 +92,26 @@ __host__ __device__ inline long long head_work(const Tiling& tl, int lp, int lc)
   return w;
 }
 
+// Iterations of one KV head's share of a window in schedule row `row`: all
+// its query blocks (nrow = 1), or block `row` alone (row mode).
+__host__ __device__ inline long long head_work_row(const Tiling& tl, int lp, int lc, int row) {
+  if (tl.nrow <= 1) return head_work(tl, lp, lc);
+  return row < blocks_of_window(tl, lc) ? block_iters(tl, lp, lc, row) : 0;
+}
+
+// The schedule row holding query block qb.
+__host__ __device__ inline int row_of_block(const Tiling& tl, int qb) {
+  return tl.nrow > 1 ? qb : 0;
+}
+
 // Iterations [*first, *end) holding the key tiles of query block (b, hk, qb),
-// given the window's first iteration w0 (its virtual iterations come before
-// *first).
+// given the window's first iteration w0 in the block's schedule row (its
+// virtual iterations come before *first).
 __host__ __device__ inline void block_span(const Tiling& tl, long long w0, int hk, int qb, int lp,
                                            int lc, long long* first, long long* end) {
-  long long bs = w0 + (long long)hk * head_work(tl, lp, lc);
-  for (int q = 0; q < qb; ++q) bs += block_iters(tl, lp, lc, q);
+  long long bs = w0 + (long long)hk * head_work_row(tl, lp, lc, row_of_block(tl, qb));
+  if (tl.nrow <= 1)
+    for (int q = 0; q < qb; ++q) bs += block_iters(tl, lp, lc, q);
   *first = bs + tl.setup;
   *end = bs + block_iters(tl, lp, lc, qb);
 }
@@ -108,17 +136,20 @@ struct Segment {
 };
 
 // Walks a CTA's iteration range segment by segment.  Every role of the CTA
-// runs its own copy and sees the same sequence.
-struct SegmentWalker {
+// runs its own copy and sees the same sequence.  ROW selects row mode at
+// compile time (Tiling::nrow > 1), so that the one-row kernels carry no row
+// logic (their walker state lives in registers through the inner loops).
+template <bool ROW>
+struct SegmentWalkerT {
   const int32_t* cu_p;
   const int32_t* cu_c;
   int batch, hkv;
   Tiling tl;
   long long cur, end;
-  int b, hk, qb, tile;
+  int b, hk, qb, tile;  // in row mode qb stays the CTA's schedule row
 
   // Start at CTA `cta`'s first iteration: window b0 (whose first iteration
-  // is pre_b0) of a schedule with `total` iterations.
+  // is pre_b0) of its row's schedule, which has `total` iterations.
   __host__ __device__ void init(const int32_t* cp, const int32_t* cc, int nb, int nkv,
                                 const Tiling& t, int cta, long long total, int b0,
                                 long long pre_b0) {
@@ -127,23 +158,38 @@ struct SegmentWalker {
     batch = nb;
     hkv = nkv;
     tl = t;
-    cur = cta_begin(cta, total, t.grid);
-    end = cta_begin(cta + 1, total, t.grid);
-    if (cur >= end) return;
-    b = b0;
-    const int lp = cu_p[b + 1] - cu_p[b], lc = cu_c[b + 1] - cu_c[b];
-    const long long hw = head_work(tl, lp, lc);
-    long long o = cur - pre_b0;
-    hk = (int)(o / hw);
-    o -= (long long)hk * hw;
-    qb = 0;
-    for (;;) {
-      const int nk = block_iters(tl, lp, lc, qb);
-      if (o < nk) break;
-      o -= nk;
-      ++qb;
+    if constexpr (ROW) {
+      const int rg = row_grid(t), row = cta / rg;
+      cur = cta_begin(cta % rg, total, rg);
+      end = cta_begin(cta % rg + 1, total, rg);
+      if (cur >= end) return;
+      b = b0;
+      const int lp = cu_p[b + 1] - cu_p[b], lc = cu_c[b + 1] - cu_c[b];
+      const long long hw = head_work_row(tl, lp, lc, row);
+      long long o = cur - pre_b0;
+      hk = (int)(o / hw);
+      o -= (long long)hk * hw;
+      qb = row;
+      tile = (int)o;
+    } else {
+      cur = cta_begin(cta, total, t.grid);
+      end = cta_begin(cta + 1, total, t.grid);
+      if (cur >= end) return;
+      b = b0;
+      const int lp = cu_p[b + 1] - cu_p[b], lc = cu_c[b + 1] - cu_c[b];
+      const long long hw = head_work(tl, lp, lc);
+      long long o = cur - pre_b0;
+      hk = (int)(o / hw);
+      o -= (long long)hk * hw;
+      qb = 0;
+      for (;;) {
+        const int nk = block_iters(tl, lp, lc, qb);
+        if (o < nk) break;
+        o -= nk;
+        ++qb;
+      }
+      tile = (int)o;  // iteration within the block, virtual ones first
     }
-    tile = (int)o;  // iteration within the block, virtual ones first
   }
 
   // The next segment with key tiles; blocks of which this CTA holds only
@@ -169,15 +215,26 @@ struct SegmentWalker {
       s.head = s.t_begin > 0;
       s.tail = s.t_end < s.n_kt;
       cur += v_end - tile;
-      // advance to the next query block
       tile = 0;
-      if (++qb >= blocks_of_window(tl, s.lc)) {
-        qb = 0;
+      if constexpr (ROW) {
+        // the same block of the next head or window
         if (++hk >= hkv) {
           hk = 0;
           do {
             ++b;
-          } while (b < batch && cu_c[b + 1] - cu_c[b] == 0);
+          } while (b < batch &&
+                   head_work_row(tl, cu_p[b + 1] - cu_p[b], cu_c[b + 1] - cu_c[b], qb) == 0);
+        }
+      } else {
+        // the next query block
+        if (++qb >= blocks_of_window(tl, s.lc)) {
+          qb = 0;
+          if (++hk >= hkv) {
+            hk = 0;
+            do {
+              ++b;
+            } while (b < batch && cu_c[b + 1] - cu_c[b] == 0);
+          }
         }
       }
       if (s.t_end > s.t_begin) return true;
@@ -185,6 +242,9 @@ struct SegmentWalker {
     return false;
   }
 };
+
+using SegmentWalker = SegmentWalkerT<false>;
+using RowSegmentWalker = SegmentWalkerT<true>;
 
 // The CTAs holding parts of the block whose iterations are [bs, be), in CTA
 // order: the one holding bs, then every later one up to the one holding
@@ -222,9 +282,11 @@ __host__ __device__ inline int part_cta(long long bs, long long total, int G, in
 // CTA: scans the per-window iteration counts (each thread sums a contiguous
 // run of windows; warp shuffles and a shared array of warp totals turn the
 // run sums into prefixes), finds the window holding this CTA's first
-// iteration, and lets CTA 0 store the prefix array for the merge kernels.
-// Results land in *total, *b0 and *pre_b0 (shared memory) after the closing
-// __syncthreads.  `warp_tot` needs one slot per warp.
+// iteration, and lets the first CTA of each schedule row store that row's
+// prefix array for the merge kernels (win_prefix_out[row * (batch + 1) + b]).
+// Results land in *total (the row's iterations), *b0 and *pre_b0 (shared
+// memory) after the closing __syncthreads.  `warp_tot` needs one slot per warp.
+template <bool ROW>
 __device__ inline void plan_schedule(const int32_t* cu_p, const int32_t* cu_c, int batch, int hkv,
                                      const Tiling& tl, long long* win_prefix_out,
                                      long long* warp_tot, long long* total, int* b0,
@@ -234,9 +296,14 @@ __device__ inline void plan_schedule(const int32_t* cu_p, const int32_t* cu_c, i
   const int per = ceil_div(batch, nt);
   const int w0 = t * per;
   const int w1 = (w0 + per < batch) ? w0 + per : batch;
+  const int rg = ROW ? row_grid(tl) : tl.grid;
+  const int row = ROW ? (int)blockIdx.x / rg : 0, j = ROW ? (int)blockIdx.x % rg : (int)blockIdx.x;
+  auto work = [&](int b) {
+    const int lp = cu_p[b + 1] - cu_p[b], lc = cu_c[b + 1] - cu_c[b];
+    return (long long)hkv * (ROW ? head_work_row(tl, lp, lc, row) : head_work(tl, lp, lc));
+  };
   long long sum = 0;
-  for (int b = w0; b < w1; ++b)
-    sum += (long long)hkv * head_work(tl, cu_p[b + 1] - cu_p[b], cu_c[b + 1] - cu_c[b]);
+  for (int b = w0; b < w1; ++b) sum += work(b);
   long long inc = sum;  // inclusive scan within the warp
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -252,11 +319,11 @@ __device__ inline void plan_schedule(const int32_t* cu_p, const int32_t* cu_c, i
     all += v;
   }
   long long run = base + inc - sum;  // exclusive prefix of window w0
-  const long long start = cta_begin(blockIdx.x, all, tl.grid);
+  const long long start = cta_begin(j, all, rg);
+  long long* wp_row = win_prefix_out + (size_t)row * (batch + 1);
   for (int b = w0; b < w1; ++b) {
-    const long long wb =
-        (long long)hkv * head_work(tl, cu_p[b + 1] - cu_p[b], cu_c[b + 1] - cu_c[b]);
-    if (blockIdx.x == 0) win_prefix_out[b] = run;
+    const long long wb = work(b);
+    if (j == 0) wp_row[b] = run;
     if (wb > 0 && run <= start && start < run + wb) {
       *b0 = b;
       *pre_b0 = run;
@@ -265,7 +332,7 @@ __device__ inline void plan_schedule(const int32_t* cu_p, const int32_t* cu_c, i
   }
   if (t == 0) {
     *total = all;
-    if (blockIdx.x == 0) win_prefix_out[batch] = all;
+    if (j == 0) wp_row[batch] = all;
   }
   __syncthreads();
 }

@@ -8,7 +8,10 @@
 //   * block_parts lists exactly the CTAs holding a segment of the block, in
 //     CTA order, the one without `head` first;
 //   * each CTA's iterations, virtual setup ones included, are within one of
-//     the mean.
+//     the mean of its schedule row.
+// With nrow > 1 (row mode) the grid is nrow independent schedules of G / nrow
+// CTAs, row r holding query block r of every (window, KV head); every check
+// then applies per row, with the row's own prefix array and iteration count.
 // Prints "OK <total iterations> <segments>" or the first violation.
 #include <cstdio>
 #include <cstdlib>
@@ -20,15 +23,16 @@
 using namespace cfa;
 
 int main(int argc, char** argv) {
-  // args: G hkv g q_per_cta setup batch lp_0 lc_0 lp_1 lc_1 ...
-  if (argc < 7) return 2;
+  // args: G hkv g q_per_cta setup nrow batch lp_0 lc_0 lp_1 lc_1 ...
+  if (argc < 8) return 2;
   const int G = atoi(argv[1]), hkv = atoi(argv[2]), g = atoi(argv[3]);
-  const int qpc = atoi(argv[4]), setup = atoi(argv[5]), batch = atoi(argv[6]);
-  if (argc != 7 + 2 * batch) return 2;
+  const int qpc = atoi(argv[4]), setup = atoi(argv[5]), nrow = atoi(argv[6]);
+  const int batch = atoi(argv[7]);
+  if (argc != 8 + 2 * batch || nrow < 1 || G % nrow != 0) return 2;
   std::vector<int32_t> cu_p(batch + 1, 0), cu_c(batch + 1, 0);
   for (int b = 0; b < batch; ++b) {
-    cu_p[b + 1] = cu_p[b] + atoi(argv[7 + 2 * b]);
-    cu_c[b + 1] = cu_c[b] + atoi(argv[8 + 2 * b]);
+    cu_p[b + 1] = cu_p[b] + atoi(argv[8 + 2 * b]);
+    cu_c[b + 1] = cu_c[b] + atoi(argv[9 + 2 * b]);
   }
   Tiling tl;
   tl.g = g;
@@ -37,27 +41,45 @@ int main(int argc, char** argv) {
   tl.q_per_cta = qpc;
   tl.grid = G;
   tl.setup = setup;
-  // window prefixes, as plan_schedule computes them on the device
-  std::vector<long long> wp(batch + 1, 0);
-  for (int b = 0; b < batch; ++b)
-    wp[b + 1] = wp[b] + (long long)hkv * head_work(tl, cu_p[b + 1] - cu_p[b], cu_c[b + 1] - cu_c[b]);
-  const long long W = wp[batch];
+  tl.nrow = nrow;
+  const int rg = row_grid(tl);
+  // row mode: every window with chunk rows has exactly nrow query blocks
+  for (int b = 0; b < batch && nrow > 1; ++b) {
+    const int lc = cu_c[b + 1] - cu_c[b];
+    if (lc > 0 && blocks_of_window(tl, lc) != nrow) return 2;
+  }
+  // window prefixes of every schedule row, as plan_schedule computes them
+  std::vector<std::vector<long long>> wps(nrow, std::vector<long long>(batch + 1, 0));
+  long long W = 0;
+  for (int r = 0; r < nrow; ++r) {
+    for (int b = 0; b < batch; ++b)
+      wps[r][b + 1] = wps[r][b] + (long long)hkv * head_work_row(tl, cu_p[b + 1] - cu_p[b],
+                                                                  cu_c[b + 1] - cu_c[b], r);
+    W += wps[r][batch];
+  }
   // (b, hk, qb) -> segments as (cta, t_begin, t_end, head, tail)
   struct Seg { int cta, tb, te; bool head, tail; };
   std::map<long long, std::vector<Seg>> by_block;
   long long n_seg = 0;
   for (int c = 0; c < G; ++c) {
-    const long long start = cta_begin(c, W, G);
-    if (start >= cta_begin(c + 1, W, G)) continue;
+    const int row = c / rg, j = c % rg;
+    const std::vector<long long>& wp = wps[row];
+    const long long Wr = wp[batch];
+    const long long start = cta_begin(j, Wr, rg);
+    if (start >= cta_begin(j + 1, Wr, rg)) continue;
     int b0 = -1;
     for (int b = 0; b < batch; ++b)
       if (wp[b + 1] > wp[b] && wp[b] <= start && start < wp[b + 1]) b0 = b;
     if (b0 < 0) { printf("FAIL cta %d: no window holds iteration %lld\n", c, start); return 1; }
-    SegmentWalker walk;
-    walk.init(cu_p.data(), cu_c.data(), batch, hkv, tl, c, W, b0, wp[b0]);
+    SegmentWalkerT<false> walk1;
+    SegmentWalkerT<true> walkr;
+    if (nrow > 1)
+      walkr.init(cu_p.data(), cu_c.data(), batch, hkv, tl, c, Wr, b0, wp[b0]);
+    else
+      walk1.init(cu_p.data(), cu_c.data(), batch, hkv, tl, c, Wr, b0, wp[b0]);
     Segment sg;
     long long last_key = -1;
-    while (walk.next(sg)) {
+    while (nrow > 1 ? walkr.next(sg) : walk1.next(sg)) {
       ++n_seg;
       if (sg.t_end <= sg.t_begin) { printf("FAIL cta %d: empty segment\n", c); return 1; }
       const long long key = ((long long)sg.b * hkv + sg.hk) * 1000000 + sg.qb;
@@ -85,10 +107,14 @@ int main(int argc, char** argv) {
           next = v[i].te;
         }
         if (next != nk) { printf("FAIL block %lld: covers %d of %d tiles\n", key, next, nk); return 1; }
+        if (nrow > 1 && qb >= nrow) { printf("FAIL block %lld: no schedule row\n", key); return 1; }
+        const int row = row_of_block(tl, qb);
+        const long long Wr = wps[row][batch];
         long long first, end;
-        block_span(tl, wp[b], hk, qb, lp, lc, &first, &end);
+        block_span(tl, wps[row][b], hk, qb, lp, lc, &first, &end);
         int parts[4096];
-        const int np = block_parts(first, end, W, G, parts, 4096);
+        const int np = block_parts(first, end, Wr, rg, parts, 4096);
+        for (int i = 0; i < np; ++i) parts[i] += row * rg;
         if (v.size() == 1) {
           if (np != 0) { printf("FAIL block %lld: one holder but %d parts\n", key, np); return 1; }
         } else {
@@ -97,19 +123,22 @@ int main(int argc, char** argv) {
             if (parts[i] != v[i].cta) { printf("FAIL block %lld: part %d is CTA %d, holder %d\n", key, i, parts[i], v[i].cta); return 1; }
         }
         // the closed form the split kernels use agrees with the list
-        if (part_count(first, end, W, G) != np) { printf("FAIL block %lld: part_count\n", key); return 1; }
+        if (part_count(first, end, Wr, rg) != np) { printf("FAIL block %lld: part_count\n", key); return 1; }
         for (int i = 0; i < np; ++i)
-          if (part_cta(first, W, G, i) != parts[i]) { printf("FAIL block %lld: part_cta %d\n", key, i); return 1; }
+          if (row * rg + part_cta(first, Wr, rg, i) != parts[i]) { printf("FAIL block %lld: part_cta %d\n", key, i); return 1; }
       }
   }
-  // balance: iterations per CTA differ by at most one
-  long long lo = W, hi = 0;
-  for (int c = 0; c < G; ++c) {
-    const long long n = cta_begin(c + 1, W, G) - cta_begin(c, W, G);
-    lo = n < lo ? n : lo;
-    hi = n > hi ? n : hi;
+  // balance: within a schedule row, iterations per CTA differ by at most one
+  for (int r = 0; r < nrow; ++r) {
+    const long long Wr = wps[r][batch];
+    long long lo = Wr, hi = 0;
+    for (int j = 0; j < rg; ++j) {
+      const long long n = cta_begin(j + 1, Wr, rg) - cta_begin(j, Wr, rg);
+      lo = n < lo ? n : lo;
+      hi = n > hi ? n : hi;
+    }
+    if (hi - lo > 1) { printf("FAIL balance row %d: %lld..%lld\n", r, lo, hi); return 1; }
   }
-  if (hi - lo > 1) { printf("FAIL balance %lld..%lld\n", lo, hi); return 1; }
   printf("OK %lld %lld %lld\n", W, n_seg, n_blocks);
   return 0;
 }

@@ -51,10 +51,37 @@ CASES = [
 ]
 
 
+# Row mode (every window with the same chunk length; the rows divide the
+# grid): G, hkv, g, q_per_cta, setup, nrow, windows
+ROW_CASES = [
+    (152, 8, 4, 2, 2, 8, [(62976, 512)]),               # 63k window, forward
+    (144, 8, 4, 1, 2, 16, [(62976, 512)]),              # 63k window, dQ beside dK/dV on 8 SMs
+    (152, 8, 4, 2, 2, 4, [(lp, 256) for lp in VARLEN8_LP]),
+    (144, 8, 4, 1, 2, 8, [(lp, 256) for lp in VARLEN8_LP]),
+    (152, 8, 4, 2, 2, 4, [(16128, 256)]),               # 8B layer (row mode is legal there too)
+    (12, 2, 4, 1, 3, 4, [(5, 128), (0, 128), (700, 128), (128, 128)]),  # short and empty prefixes
+    (16, 1, 8, 2, 2, 8, [(100, 256)]),                  # two CTAs per row, tiny rows
+    (48, 1, 8, 2, 2, 8, [(0, 256)]),                    # fewer iterations than CTAs in a row
+]
+
+
+def _run(checker, G, hkv, g, qpc, setup, nrow, wins):
+    args = [str(x) for x in (G, hkv, g, qpc, setup, nrow, len(wins))]
+    for lp, lc in wins:
+        args += [str(lp), str(lc)]
+    return subprocess.run([checker] + args, capture_output=True, text=True)
+
+
+@pytest.mark.parametrize("case", ROW_CASES, ids=[str(i) for i in range(len(ROW_CASES))])
+def test_row_mode_schedule_covers_every_tile_once(checker, case):
+    r = _run(checker, *case)
+    assert r.returncode == 0 and r.stdout.startswith("OK"), r.stdout + r.stderr
+
+
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
 def test_schedule_covers_every_tile_once(checker, case):
     G, hkv, g, qpc, setup, wins = case
-    args = [str(x) for x in (G, hkv, g, qpc, setup, len(wins))]
+    args = [str(x) for x in (G, hkv, g, qpc, setup, 1, len(wins))]
     for lp, lc in wins:
         args += [str(lp), str(lc)]
     r = subprocess.run([checker] + args, capture_output=True, text=True)
