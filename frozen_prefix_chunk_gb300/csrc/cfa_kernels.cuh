@@ -22,7 +22,7 @@ constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s
 struct FwdArgs {
   const int32_t* cu_p;
   const int32_t* cu_c;
-  long long* win_prefix;  // [batch + 1], written by CTA 0 for the merge kernel
+  long long* win_prefix;  // [rows][batch + 1], each row's by its first CTA, for the merge kernel
   int batch, hq, hkv, total_lc;
   Tiling tl;
   float scale_log2;      // softmax_scale * log2(e)
@@ -39,7 +39,7 @@ struct FwdArgs {
 struct BwdArgs {
   const int32_t* cu_p;
   const int32_t* cu_c;
-  long long* win_prefix;  // [batch + 1], written by CTA 0 for the reduce kernel
+  long long* win_prefix;  // [rows][batch + 1], each row's by its first CTA, for the reduce kernel
   int batch, hq, hkv, total_lc;
   Tiling tl;             // dQ tiling (one query tile per block)
   float scale_log2;
@@ -71,8 +71,9 @@ struct Maps {
 // Launch `k` so that it may overlap the tail of the previous kernel in the
 // stream (programmatic stream serialisation); the kernel itself waits for that
 // kernel's completion in pdl_start() before touching memory.  Used for the
-// persistent attention kernels only (one CTA per SM, placed as the previous
-// grid's CTAs leave): a small grid launched this way would pile onto the
+// persistent kernels only (attention and row-sparse GEMM: one CTA per SM,
+// placed as the previous grid's CTAs leave): a small grid launched this way
+// would pile onto the
 // first SMs to free up and run on a fraction of the GPU (measured: the split
 // merge after the forward slowed by ~4 us; triggering dependents only at the
 // end of each kernel instead did not help either).
