@@ -73,10 +73,9 @@ struct Maps {
 // kernel's completion in pdl_start() before touching memory.  Used for the
 // persistent kernels only (attention and row-sparse GEMM: one CTA per SM,
 // placed as the previous grid's CTAs leave): a small grid launched this way
-// would pile onto the
-// first SMs to free up and run on a fraction of the GPU (measured: the split
-// merge after the forward slowed by ~4 us; triggering dependents only at the
-// end of each kernel instead did not help either).
+// would pile onto the first SMs to free up and run on a fraction of the GPU
+// (measured: the split merge after the forward slowed by ~4 us; triggering
+// dependents only at the end of each kernel instead did not help either).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args&&... args) {
