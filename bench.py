@@ -80,6 +80,23 @@ def algorithmic_bytes(w, horizon=0) -> dict:
     return dict(fwd=fwd, pre=pre, bwd=bwd, dq_kernel=dq_kernel, total=fwd + pre + bwd)
 
 
+def slowest_rank_ms(tot_ms: float, world: int, device) -> float:
+    """The timed region's length on the slowest rank.  Every rank times its
+    own replica between barriers; the job takes as long as the slowest one
+    (a MAX all-reduce, the only collective, outside the data path)."""
+    if world <= 1:
+        return tot_ms
+    import torch.distributed as dist
+    t = torch.tensor([tot_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank: float, ms_per_step: float) -> float:
+    """Whole-job useful TFLOP/s: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -653,16 +670,12 @@ def main():
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    tot_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = slowest_rank_ms(sum(step_ms), world, dev)
     ms_per_step = tot_ms / args.steps
 
     flops = useful_flops(w, args.horizon)
     byts = algorithmic_bytes(w, args.horizon)
-    value = world * flops["total"] / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(world, flops["total"], ms_per_step)
 
     peaks, peak_src = load_peaks()
     bf16_peak = peaks["bf16_tflops"]
@@ -708,7 +721,7 @@ def main():
         e1.synchronize()
         if k >= 2:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_val = world * flops["total"] / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+    e2e_val = job_tflops(world, flops["total"], statistics.mean(e2e_ms))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
