@@ -16,9 +16,16 @@ Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
 launching stream; L2 is flushed before every timed step, outside the events:
 a 256 MiB write, then a 256 MiB read that writes those dirty lines back, so
 the step starts with none of its inputs in L2 and no write-back of the flush
-buffer left to do (--flush write keeps only the write).  Under torchrun every rank runs its own replica of the
-workload (weak scaling, no collective on the data path); value = all ranks'
-FLOPs / max over ranks of the time.
+buffer left to do (--flush write keeps only the write).  Under torchrun every
+rank runs its own replica of the workload, with the same shapes (weak scaling,
+no collective on the data path); value = all ranks' FLOPs (a SUM all-reduce)
+over the slowest rank's time (a MAX all-reduce).
+
+The headline workload is the 63k-token window with its q8_0 prefix handed to
+the library as it is; the other configurations the roofline target names
+(the Qwen3-8B layer and the varlen batch) are timed in the same run, each
+long enough for the clock sampler to see it under load, and reported under
+"extra" with their own step roofline and dominant-kernel roofline.
 
 --impl reference times the fp64 CPU oracle instead (the deliberately slow
 baseline arm), on a bounded sample of the same workload.
@@ -92,11 +99,6 @@ def slowest_rank_ms(tot_ms: float, world: int, device) -> float:
     return float(t.item())
 
 
-def job_tflops(world: int, flops_per_rank: float, ms_per_step: float) -> float:
-    """Whole-job useful TFLOP/s: every rank's FLOPs over the slowest rank's time."""
-    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
-
-
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -143,7 +145,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(device_index), "-lms", "100"], stdout=self.f,
+                 "-i", str(device_index), "-lms", "50"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -260,11 +262,15 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w, l2, horizon=0):
+def config_of(w, l2, horizon=0, q8="product"):
+    if w.prefix_dtype != synth.PREFIX_Q8_0:
+        prefix = "bf16"
+    elif q8 == "export":
+        prefix = "q8_0 (expanded to bf16 once per step by cfa_dequant_q8_0, read by both passes)"
+    else:
+        prefix = "q8_0 (handed to cfa_forward / cfa_backward as it is)"
     return {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "horizon": horizon,
-            "head_dim": w.head_dim, "lp": w.lp, "lc": w.lc,
-            "prefix": ("q8_0 (dequantised to bf16 once per step, read by both passes)"
-                       if w.prefix_dtype == synth.PREFIX_Q8_0 else "bf16"),
+            "head_dim": w.head_dim, "lp": w.lp, "lc": w.lc, "prefix": prefix,
             "softmax_scale": w.softmax_scale, "l2": l2, "parallelism": "replicas"}
 
 
@@ -537,15 +543,206 @@ def run_rowsparse(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- the attention step --
+
+# the configurations the >= 60 %-of-roofline target names
+TARGETS = ("qwen3_8b", "window_63k_q8", "varlen8")
+# launches of the library per step: forward, split merge, delta, dQ, dQ reduce, dK/dV
+LAUNCHES_ATTN = 6
+
+
+class AttnStep:
+    """One workload resident in HBM and its fwd+bwd step through the C ABI.
+
+    The step is cfa_forward, cfa_backward_preprocess and cfa_backward (dQ on
+    the caller's stream, dK/dV beside it on the library's second stream,
+    joined back), or cfa_backward_horizon with a horizon.  A q8_0 prefix is
+    handed to the library as it is ("product", the path a caller with a q8_0
+    cache takes); q8 = "export" instead expands it once per step through
+    cfa_dequant_q8_0 into bf16 buffers that both passes read."""
+
+    def __init__(self, w, dev, horizon=0, q8="product"):
+        import frozen_prefix_chunk_gb300 as cfa
+        self.cfa, self.w, self.dev, self.horizon = cfa, w, dev, horizon
+        self.host = synth.make_inputs(w)
+        names = ("q", "k_prefix", "v_prefix", "k_chunk", "v_chunk", "dout",
+                 "cu_seqlens_prefix", "cu_seqlens_chunk")
+        self.names = names
+        d = {k: self.host[k].to(dev) for k in names}
+        self.d = d
+        self.q8 = q8 if w.prefix_dtype == synth.PREFIX_Q8_0 else None
+        pref = w.prefix_dtype
+        kp, vp = d["k_prefix"], d["v_prefix"]
+        if self.q8 == "export":
+            self.kp16 = torch.empty(sum(w.lp), w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
+            self.vp16 = torch.empty_like(self.kp16)
+            kp, vp, pref = self.kp16, self.vp16, synth.PREFIX_BF16
+        self.a = cfa.make_args(d["q"], kp, vp, d["k_chunk"], d["v_chunk"],
+                               d["cu_seqlens_prefix"], d["cu_seqlens_chunk"], max(w.lp),
+                               max(w.lc), w.softmax_scale, pref, hkv=w.hkv, total_lp=sum(w.lp))
+        tc = sum(w.lc)
+        self.o = torch.empty_like(d["q"])
+        self.lse = torch.empty(w.hq, tc, dtype=torch.float32, device=dev)
+        self.delta = torch.empty_like(self.lse)
+        self.dq = torch.empty_like(d["q"])
+        self.dk = torch.empty(tc, w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
+        self.dv = torch.empty_like(self.dk)
+        self.ws_f = torch.empty(cfa.workspace_size(self.a, cfa.WS_FORWARD), dtype=torch.uint8,
+                                device=dev)
+        self.ws_b = torch.empty(cfa.workspace_size(self.a, cfa.WS_BACKWARD), dtype=torch.uint8,
+                                device=dev)
+        self.dkp = self.dvp = None
+        if horizon:
+            self.dkp = torch.zeros(sum(w.lp), w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
+            self.dvp = torch.zeros_like(self.dkp)
+        self.stream = torch.cuda.current_stream()
+        # library launches per step: the six attention kernels, plus the
+        # prefix expansion (q8_0 / fp16) inside each pass or the two exports
+        self.launches = LAUNCHES_ATTN + (2 if self.q8 else 0)
+        self.flops = useful_flops(w, horizon)
+        self.bytes = algorithmic_bytes(w, horizon)
+
+    def step(self, ev=None):
+        cfa, d, s = self.cfa, self.d, self.stream
+        if ev:
+            ev[0].record(s)
+        if self.q8 == "export":
+            cfa.dequant_q8_0(d["k_prefix"], out_bf16=self.kp16, want_f32=False)
+            cfa.dequant_q8_0(d["v_prefix"], out_bf16=self.vp16, want_f32=False)
+        cfa.forward(self.a, d["q"], self.o, self.lse, self.ws_f)
+        if ev:
+            ev[1].record(s)
+        cfa.backward_preprocess(self.a, self.o, d["dout"], self.delta)
+        if ev:
+            ev[2].record(s)
+        if self.horizon:
+            cfa.backward_horizon(self.a, self.horizon, d["dout"], self.lse, self.delta, self.dq,
+                                 self.dk, self.dv, self.dkp, self.dvp, self.ws_b)
+        else:
+            cfa.backward(self.a, d["dout"], self.lse, self.delta, self.dq, self.dk, self.dv,
+                         self.ws_b)
+        if ev:
+            ev[3].record(s)
+
+    def check_status(self):
+        for ws in (self.ws_f, self.ws_b):
+            st = self.cfa.read_status(ws)
+            assert st == 0, f"device status {st}"
+
+    def outputs(self):
+        outs = [self.o, self.lse, self.dq, self.dk, self.dv]
+        return outs + ([self.dkp, self.dvp] if self.horizon else [])
+
+
+def time_steps(case, steps, warmup, flush, world, dev, sampler_index=None):
+    """W untimed warm-up steps, then exactly `steps` steps, each bracketed by
+    CUDA events on the launching stream, L2 flushed before each outside the
+    events; barrier + synchronize on both sides.  Returns per-step lists of
+    the step, forward and backward times (ms), the slowest rank's total, the
+    clock record and the wall time of the timed loop."""
+    import torch.distributed as dist
+    for _ in range(warmup):
+        flush()
+        case.step()
+    torch.cuda.synchronize()
+    case.check_status()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(sampler_index) if sampler_index is not None else None
+    t_wall = time.perf_counter()
+    for k in range(steps):
+        flush()
+        case.step(evs[k])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop() if sampler else None
+    if world > 1:
+        dist.barrier()
+    case.check_status()
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    tot_ms = slowest_rank_ms(sum(step_ms), world, dev)
+    return dict(step_ms=step_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, tot_ms=tot_ms, clocks=clocks,
+                wall_s=t_wall)
+
+
+def summarise(case, t, steps, world, dev, peaks, peak_src):
+    """Value, step roofline and the dominant kernel's roofline of one timed run."""
+    w, flops, byts = case.w, case.flops, case.bytes
+    ms_per_step = t["tot_ms"] / steps
+    value = job_tflops_sum(flops["total"], ms_per_step, world, dev)
+    bf16_peak, hbm_peak = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    fwd_mean, bwd_mean = statistics.mean(t["fwd_ms"]), statistics.mean(t["bwd_ms"])
+    # The dQ kernel (+ its split reduce) is the step's largest kernel.  It is
+    # timed by the events around cfa_backward on its own stream: that span is
+    # the dQ launch, or longer if the dK/dV kernel beside it (on a second
+    # stream, its FLOPs not counted here) finished later, or if the call first
+    # expands a q8_0 prefix into its workspace.
+    achieved = flops["dq_kernel"] / (bwd_mean * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": achieved / bf16_peak, "traffic": recorded_traffic(w.name),
+                "kernel": "bwd_dq_kernel + split reduce (timed as the cfa_backward span, a lower "
+                          "bound: dK/dV runs beside it on a second stream"
+                          + (", and the span includes the call's q8_0 expansion" if case.q8 ==
+                             "product" else "") + ")",
+                "peak_source": f"bf16_tflops burst, {peak_src}",
+                "algorithmic_flops_per_launch": flops["dq_kernel"], "ms_per_launch": bwd_mean}
+    t_roof = max(flops["total"] / (bf16_peak * 1e12), byts["total"] / (hbm_peak * 1e9))
+    step_roof = {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_per_step * 1e-3),
+                 "fwd_ms": fwd_mean, "bwd_ms": bwd_mean,
+                 "bwd_tflops": (flops["dq_kernel"] + flops["dkdv_kernel"]) / (bwd_mean * 1e-3) / 1e12,
+                 "fwd_tflops": flops["fwd"] / (fwd_mean * 1e-3) / 1e12,
+                 "useful_gflop": flops["total"] / 1e9, "algorithmic_mb": byts["total"] / 1e6,
+                 "peaks": f"bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s ({peak_src})"}
+    return ms_per_step, value, roofline, step_roof
+
+
+def job_tflops_sum(flops_rank: float, ms_per_step: float, world: int, device) -> float:
+    """Whole-job useful TFLOP/s: the FLOPs of all ranks (a SUM all-reduce, so
+    replicas of different sizes are counted as they are) over the slowest
+    rank's time per step."""
+    total = flops_rank
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([float(flops_rank)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        total = float(t.item())
+    return total / (ms_per_step * 1e-3) / 1e12
+
+
+def extra_steps(case, flush, want_s=0.3, lo=20, hi=4000):
+    """Steps for an extra workload's timed region: about `want_s` seconds, so
+    the clock sampler sees it under load (estimated from three steps)."""
+    for _ in range(2):
+        flush()
+        case.step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(3):
+        flush()
+        case.step()
+    torch.cuda.synchronize()
+    per = (time.perf_counter() - t0) / 3
+    return max(lo, min(hi, int(want_s / max(per, 1e-6))))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="cfa", choices=["cfa", "reference"])
-    ap.add_argument("--workload", default="qwen3_8b", choices=list(synth.WORKLOADS))
+    ap.add_argument("--workload", default="window_63k_q8", choices=list(synth.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time the headline workload only (not the other target configs)")
+    ap.add_argument("--q8", default="product", choices=["product", "export"],
+                    help="q8_0 prefix: handed to the library as it is, or expanded once per "
+                         "step through cfa_dequant_q8_0 and read as bf16")
     ap.add_argument("--flush", default="write+read", choices=["write", "write+read"],
                     help="how L2 is evicted before each timed step")
     ap.add_argument("--rowsparse", action="store_true",
@@ -580,148 +777,65 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     cfa.lib(build_if_missing=True)
-
-    # every rank has its own replica of the workload
-    w = synth.workload(args.workload, seed=rank)
-    host = synth.make_inputs(w)
-    names = ("q", "k_prefix", "v_prefix", "k_chunk", "v_chunk", "dout",
-             "cu_seqlens_prefix", "cu_seqlens_chunk")
-    d = {k: host[k].to(dev) for k in names}
-    a = cfa.make_args(d["q"], d["k_prefix"], d["v_prefix"], d["k_chunk"], d["v_chunk"],
-                      d["cu_seqlens_prefix"], d["cu_seqlens_chunk"], max(w.lp), max(w.lc),
-                      w.softmax_scale, w.prefix_dtype, hkv=w.hkv, total_lp=sum(w.lp))
-    q8 = w.prefix_dtype == synth.PREFIX_Q8_0
-    if q8:
-        # The prefix is frozen, so one step dequantises it once (one
-        # cfa_dequant_q8_0 launch per tensor) and both passes read the bf16
-        # copy; handing the q8_0 prefix to cfa_forward and cfa_backward
-        # instead would dequantise it inside each of them.
-        kp16 = torch.empty(sum(w.lp), w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
-        vp16 = torch.empty_like(kp16)
-        a = cfa.make_args(d["q"], kp16, vp16, d["k_chunk"], d["v_chunk"],
-                          d["cu_seqlens_prefix"], d["cu_seqlens_chunk"], max(w.lp), max(w.lc),
-                          w.softmax_scale, synth.PREFIX_BF16, hkv=w.hkv, total_lp=sum(w.lp))
-    tc = sum(w.lc)
-    o = torch.empty_like(d["q"])
-    lse = torch.empty(w.hq, tc, dtype=torch.float32, device=dev)
-    delta = torch.empty_like(lse)
-    dq = torch.empty_like(d["q"])
-    dk = torch.empty(tc, w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
-    dv = torch.empty_like(dk)
-    ws_f = torch.empty(cfa.workspace_size(a, cfa.WS_FORWARD), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(cfa.workspace_size(a, cfa.WS_BACKWARD), dtype=torch.uint8, device=dev)
     flush = L2Flush(dev, args.flush)
-    dkp = dvp = None
-    if args.horizon:
-        dkp = torch.zeros(sum(w.lp), w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
-        dvp = torch.zeros_like(dkp)
-    stream = torch.cuda.current_stream()
-    # kernels launched per step: forward (+ split combine), delta, dQ (+ split
-    # reduce), dK/dV; a workspace beyond its 256-byte header holds partials
-    launches_per_step = (1 + (ws_f.numel() > 256)) + 1 + (1 + (ws_b.numel() > 256)) + 1 + 2 * q8
-
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        if q8:
-            cfa.dequant_q8_0(d["k_prefix"], out_bf16=kp16, want_f32=False)
-            cfa.dequant_q8_0(d["v_prefix"], out_bf16=vp16, want_f32=False)
-        cfa.forward(a, d["q"], o, lse, ws_f)
-        if ev:
-            ev[1].record(stream)
-        cfa.backward_preprocess(a, o, d["dout"], delta)
-        if ev:
-            ev[2].record(stream)
-        # dQ on this stream; the library runs dK/dV beside it on a few SMs of
-        # a second stream and joins it back before returning
-        if args.horizon:
-            cfa.backward_horizon(a, args.horizon, d["dout"], lse, delta, dq, dk, dv, dkp, dvp,
-                                 ws_b)
-        else:
-            cfa.backward(a, d["dout"], lse, delta, dq, dk, dv, ws_b)
-        if ev:
-            ev[3].record(stream)
-
-    for _ in range(args.warmup):
-        flush()
-        step()
-    torch.cuda.synchronize()
-    for ws in (ws_f, ws_b):
-        st = cfa.read_status(ws)
-        assert st == 0, f"device status {st}"
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sampler = ClockSampler(local)
-    t_wall = time.perf_counter()
-    for k in range(args.steps):
-        flush()
-        step(evs[k])
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    clocks = sampler.stop()
-    if world > 1:
-        dist.barrier()
-    for ws in (ws_f, ws_b):
-        assert cfa.read_status(ws) == 0
-
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    tot_ms = slowest_rank_ms(sum(step_ms), world, dev)
-    ms_per_step = tot_ms / args.steps
-
-    flops = useful_flops(w, args.horizon)
-    byts = algorithmic_bytes(w, args.horizon)
-    value = job_tflops(world, flops["total"], ms_per_step)
-
     peaks, peak_src = load_peaks()
-    bf16_peak = peaks["bf16_tflops"]
-    hbm_peak = peaks["hbm_gbs"]
-    # The dQ kernel (+ its split reduce) is the step's largest kernel.  It is
-    # timed by the events around cfa_backward on its own stream: that span is
-    # the dQ launch, or longer if the dK/dV kernel beside it (on a second
-    # stream, its FLOPs not counted here) finished later.
-    bwd_mean = statistics.mean(bwd_ms)
-    achieved = flops["dq_kernel"] / (bwd_mean * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
-                "frac": achieved / bf16_peak, "traffic": recorded_traffic(w.name),
-                "kernel": "bwd_dq_kernel + split reduce (timed as the cfa_backward span; "
-                          "dK/dV runs beside it on a second stream)",
-                "peak_source": f"bf16_tflops burst, {peak_src}",
-                "algorithmic_flops_per_launch": flops["dq_kernel"], "ms_per_launch": bwd_mean}
-    t_roof = max(flops["total"] / (bf16_peak * 1e12), byts["total"] / (hbm_peak * 1e9))
-    step_roof = {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms_per_step * 1e-3),
-                 "fwd_ms": statistics.mean(fwd_ms), "bwd_ms": bwd_mean,
-                 "bwd_tflops": (flops["dq_kernel"] + flops["dkdv_kernel"]) / (bwd_mean * 1e-3) / 1e12,
-                 "fwd_tflops": flops["fwd"] / (statistics.mean(fwd_ms) * 1e-3) / 1e12,
-                 "useful_gflop": flops["total"] / 1e9, "algorithmic_mb": byts["total"] / 1e6,
-                 "peaks": f"bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s ({peak_src})"}
+
+    # Every rank has its own replica of the workload: the same shapes (the
+    # varlen window lengths drawn with seed 0), values seeded by the rank.
+    def make_case(name, horizon=0):
+        return AttnStep(synth.workload(name, seed=rank, shape_seed=0), dev, horizon, args.q8)
+
+    # ---- the other target configurations, each timed on its own, long
+    # enough for the clock sampler to see it under load
+    extras = {}
+    if not args.no_extras and not args.horizon:
+        for name in TARGETS:
+            if name == args.workload:
+                continue
+            case = make_case(name)
+            n = extra_steps(case, flush)
+            if world > 1:
+                t = torch.tensor([n], dtype=torch.int64, device=dev)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                n = int(t.item())
+            t = time_steps(case, n, args.warmup, flush, world, dev, sampler_index=local)
+            ms, val, roof, sroof = summarise(case, t, n, world, dev, peaks, peak_src)
+            extras[name] = {"value": val, "unit": "TFLOP/s", "ms_per_step": ms, "steps": n,
+                            "step_roofline": sroof, "roofline": roof,
+                            "config": config_of(case.w, flush.describe(), 0, case.q8),
+                            "gpu_launches": case.launches * n, "clocks": t["clocks"]}
+            del case
+            torch.cuda.empty_cache()
+
+    # ---- the headline workload: exactly K timed steps
+    case = make_case(args.workload, args.horizon)
+    t = time_steps(case, args.steps, args.warmup, flush, world, dev, sampler_index=local)
+    ms_per_step, value, roofline, step_roof = summarise(case, t, args.steps, world, dev, peaks,
+                                                        peak_src)
 
     # ---- end to end through the public API, host buffers, copies timed
-    pin = {k: host[k].pin_memory() for k in names}
-    outs = [o, lse, dq, dk, dv] + ([dkp, dvp] if args.horizon else [])
-    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    h2d = sum(t.numel() * t.element_size() for t in pin.values())
-    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    host, d, stream = case.host, case.d, case.stream
+    pin = {k: host[k].pin_memory() for k in case.names}
+    outs = case.outputs()
+    outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs_h)
     e2e_ms = []
     for k in range(args.e2e_steps + 2):
         flush()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for n in names:
+        for n in case.names:
             d[n].copy_(pin[n], non_blocking=True)
-        step()
+        case.step()
         for src, dst in zip(outs, outs_h):
             dst.copy_(src, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         if k >= 2:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_val = job_tflops(world, flops["total"], statistics.mean(e2e_ms))
+    e2e_val = job_tflops_sum(case.flops["total"], statistics.mean(e2e_ms), world, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -731,18 +845,20 @@ def main():
                "kind": "oracle", "sample": desc, "seconds": dt}
 
     if rank == 0:
+        fracs = {args.workload: step_roof["frac"]}
+        fracs.update({k: v["step_roofline"]["frac"] for k, v in extras.items()})
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v, N(0,0.1) dO)",
-                "config": config_of(w, flush.describe(),
-                                    args.horizon),
+                "config": config_of(case.w, flush.describe(), args.horizon, case.q8),
                 "roofline": roofline, "step_roofline": step_roof,
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
-                "gpu_launches": launches_per_step * args.steps,
-                "clocks": clocks, "wall_s_timed": t_wall}
+                "gpu_launches": case.launches * args.steps,
+                "clocks": t["clocks"], "wall_s_timed": t["wall_s"],
+                "target_step_fracs": fracs, "extra": extras}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -82,6 +82,8 @@ def lib(build_if_missing: bool = False):
             L.cfa_forward_noalloc.restype = ctypes.c_int
             L.cfa_noalloc_scratch_bytes.argtypes = []
             L.cfa_noalloc_scratch_bytes.restype = sz
+            L.cfa_noalloc_read_status.argtypes = [vp]
+            L.cfa_noalloc_read_status.restype = ctypes.c_int
             L.cfa_status_string.argtypes = [ctypes.c_int]
             L.cfa_status_string.restype = ctypes.c_char_p
             for f in ("cfa_forward", "cfa_backward_preprocess", "cfa_backward",
@@ -168,6 +170,12 @@ def forward_noalloc(args: Args, o: torch.Tensor, lse: torch.Tensor, stream=None)
     _check(lib().cfa_forward_noalloc(ctypes.byref(args), _ptr(o), _ptr(lse), _stream(stream)),
            "cfa_forward_noalloc")
     return o, lse
+
+
+def noalloc_read_status(stream=None) -> int:
+    """cfa_noalloc_read_status: synchronises the stream and returns the device
+    status word of the last cfa_forward_noalloc call on this device."""
+    return int(lib().cfa_noalloc_read_status(_stream(stream)))
 
 
 def backward_preprocess(args: Args, o, dout, delta=None, stream=None):

@@ -197,6 +197,15 @@ int debug_wait_never() {
   return (e && e[0] == '1') ? 1 : 0;
 }
 
+SeqLimits seq_limits(const cfa_args* a) {
+  SeqLimits l;
+  l.total_lp = a->total_lp;
+  l.total_lc = a->total_lc;
+  l.max_lp = a->max_lp;
+  l.max_lc = a->max_lc;
+  return l;
+}
+
 int check_ws(void* ws, size_t ws_bytes, size_t need) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < need)
     return CFA_ERR_WORKSPACE;
@@ -306,6 +315,7 @@ int cfa_forward(const cfa_args* a, void* o, float* lse, void* ws, size_t ws_byte
   fa.hq = a->hq;
   fa.hkv = a->hkv;
   fa.total_lc = a->total_lc;
+  fa.lim = seq_limits(a);
   fa.tl = tl;
   fa.scale_log2 = a->softmax_scale * kLog2e;
   fa.o = static_cast<__nv_bfloat16*>(o);
@@ -374,6 +384,7 @@ int prepare_backward(const cfa_args* a, const void* dout, const float* lse, cons
   ba->hq = a->hq;
   ba->hkv = a->hkv;
   ba->total_lc = a->total_lc;
+  ba->lim = seq_limits(a);
   ba->tl = tl;
   ba->scale_log2 = a->softmax_scale * kLog2e;
   ba->scale = a->softmax_scale;
@@ -505,7 +516,8 @@ int cfa_backward_horizon(const cfa_args* a, int horizon, const void* dout, const
     // rows' gradients are zero
     if (want_prefix &&
         launch_zero_horizon(a->cu_seqlens_prefix, a->batch, a->hkv, a->head_dim, horizon,
-                            ba.dk_p, ba.dv_p, s) != cudaSuccess)
+                            seq_limits(a), ba.dk_p, ba.dv_p, static_cast<int*>(ws),
+                            s) != cudaSuccess)
       return CFA_ERR_LAUNCH;
     return CFA_OK;
   }

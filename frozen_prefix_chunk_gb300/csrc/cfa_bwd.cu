@@ -110,10 +110,15 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Tiling tl = a.tl;
   {
-    // schedule prologue: shared scratch in the (not yet used) barrier area
+    // schedule prologue: shared scratch in the (not yet used) barrier area;
+    // inconsistent cu_seqlens end the kernel before any load or store (see
+    // the forward kernel)
     long long* sched = reinterpret_cast<long long*>(gbase + C::kBarOff);
-    plan_schedule<ROW>(a.cu_p, a.cu_c, a.batch, a.hkv, tl, a.win_prefix, sched + 4, sched,
-                  reinterpret_cast<int*>(sched + 1), sched + 2);
+    if (!plan_schedule<ROW>(a.cu_p, a.cu_c, a.batch, a.hkv, tl, a.lim, a.win_prefix, sched + 4,
+                            sched, reinterpret_cast<int*>(sched + 1), sched + 2)) {
+      if (threadIdx.x == 0) atomicExch(a.status, kStatusInvalidArg);
+      return;
+    }
   }
   SegmentWalkerT<ROW> walk;
   {
@@ -531,6 +536,17 @@ __global__ void __launch_bounds__(320, 1)
   const long long n_items = (long long)(a.pre_tiles + a.dkv_tiles) * a.batch * a.hkv;
   if ((long long)blockIdx.x >= n_items) return;
   const long long j0 = blockIdx.x, jstep = gridDim.x;
+  {
+    // the items' rows come from the device cu_seqlens: check them against the
+    // host sizes first (every CTA, all windows; see the forward kernel)
+    bool bad = false;
+    for (int b = threadIdx.x; b < a.batch; b += blockDim.x)
+      bad |= !window_valid(a.cu_p, a.cu_c, b, a.batch, a.lim);
+    if (__syncthreads_or(bad)) {
+      if (threadIdx.x == 0) atomicExch(a.status, kStatusInvalidArg);
+      return;
+    }
+  }
 
   const uint32_t bars = base + C::kBarOff;
   const uint32_t bar_kv = bars;
@@ -870,6 +886,9 @@ constexpr int kReduceRows = 32;
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
   pdl_start();
+  // the dQ kernel found inconsistent cu_seqlens (or gave up on a wait): its
+  // partials and prefix arrays were not written
+  if (*reinterpret_cast<volatile int*>(a.status) != 0) return;
   constexpr int CW = D / 8;
   const Tiling tl = a.tl;
   const int chunks = kTileM / kReduceRows;
@@ -1125,13 +1144,23 @@ __global__ void __launch_bounds__(256) f16_to_bf16_kernel(const __half* __restri
 
 // Zero the horizon rows of the prefix gradients of every window (used when
 // no window has chunk rows, so nothing attends to the prefix).  One CTA per
-// window; the rows of a window are contiguous.
+// window; the rows of a window are contiguous.  A window whose prefix rows
+// fall outside [0, total_lp) or exceed max_lp records CFA_ERR_INVALID_ARG and
+// writes nothing.
 __global__ void __launch_bounds__(256) zero_horizon_kernel(const int32_t* __restrict__ cu_p,
-                                                           int hkv, int d, int horizon,
+                                                           int batch, int hkv, int d, int horizon,
+                                                           SeqLimits lim,
                                                            __nv_bfloat16* __restrict__ dk_p,
-                                                           __nv_bfloat16* __restrict__ dv_p) {
+                                                           __nv_bfloat16* __restrict__ dv_p,
+                                                           int* status) {
   const int b = blockIdx.x;
-  const int p0 = cu_p[b], lp = cu_p[b + 1] - p0;
+  const long long p0l = cu_p[b], p1l = cu_p[b + 1];
+  if (p0l < 0 || p1l < p0l || p1l > lim.total_lp || p1l - p0l > lim.max_lp ||
+      (b == 0 && p0l != 0) || (b == batch - 1 && p1l != lim.total_lp)) {
+    if (threadIdx.x == 0) atomicExch(status, kStatusInvalidArg);
+    return;
+  }
+  const int p0 = (int)p0l, lp = (int)(p1l - p0l);
   const int h = horizon < lp ? horizon : lp;
   const size_t first = (size_t)(p0 + lp - h) * hkv * d / 8, count = (size_t)h * hkv * d / 8;
   uint4* k = reinterpret_cast<uint4*>(dk_p) + first;
@@ -1237,8 +1266,10 @@ cudaError_t launch_quantize_q8_0(const __nv_bfloat16* x, long long n_blocks, uin
 }
 
 cudaError_t launch_zero_horizon(const int32_t* cu_p, int batch, int hkv, int d, int horizon,
-                                __nv_bfloat16* dk_p, __nv_bfloat16* dv_p, cudaStream_t st) {
-  zero_horizon_kernel<<<batch, 256, 0, st>>>(cu_p, hkv, d, horizon, dk_p, dv_p);
+                                const SeqLimits& lim, __nv_bfloat16* dk_p, __nv_bfloat16* dv_p,
+                                int* status, cudaStream_t st) {
+  zero_horizon_kernel<<<batch, 256, 0, st>>>(cu_p, batch, hkv, d, horizon, lim, dk_p, dv_p,
+                                             status);
   return cudaGetLastError();
 }
 

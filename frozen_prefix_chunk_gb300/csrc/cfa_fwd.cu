@@ -109,10 +109,16 @@ __global__ void __launch_bounds__(352, 1)
   const int tok_blk = tl.q_per_cta * tl.tpt;
   const int rows_blk = tl.q_per_cta * kTileM;
   {
-    // schedule prologue: shared scratch in the (not yet used) barrier area
+    // schedule prologue: shared scratch in the (not yet used) barrier area.
+    // Device cu_seqlens that disagree with the host sizes: record the error
+    // and leave before any load or store (every CTA reaches this verdict;
+    // CTA 0 records it after its clear above).
     long long* sched = reinterpret_cast<long long*>(gbase + C::kBarOff);
-    plan_schedule<ROW>(a.cu_p, a.cu_c, a.batch, a.hkv, tl, a.win_prefix, sched + 4, sched,
-                  reinterpret_cast<int*>(sched + 1), sched + 2);
+    if (!plan_schedule<ROW>(a.cu_p, a.cu_c, a.batch, a.hkv, tl, a.lim, a.win_prefix, sched + 4,
+                            sched, reinterpret_cast<int*>(sched + 1), sched + 2)) {
+      if (threadIdx.x == 0) atomicExch(a.status, kStatusInvalidArg);
+      return;
+    }
   }
   SegmentWalkerT<ROW> walk;
   {
@@ -524,6 +530,9 @@ static __device__ unsigned long long cfa_trace_merge[4 * 1024];
 template <int D>
 __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
   pdl_start();
+  // the forward kernel found inconsistent cu_seqlens (or gave up on a wait):
+  // its partials and prefix arrays were not written
+  if (*reinterpret_cast<volatile int*>(a.status) != 0) return;
   CFA_TRACE_MERGE(0);
   constexpr int CW = D / 8;  // columns per thread
   const Tiling tl = a.tl;

@@ -14,6 +14,7 @@ namespace cfa {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kStatusInvalidArg = -1;  // CFA_ERR_INVALID_ARG, as the kernels record it
 
 // Wall-clock limit of the bounded waits that unwind a CTA after it has
 // already given up (draining copies and MMAs still in flight).
@@ -24,6 +25,7 @@ struct FwdArgs {
   const int32_t* cu_c;
   long long* win_prefix;  // [rows][batch + 1], each row's by its first CTA, for the merge kernel
   int batch, hq, hkv, total_lc;
+  SeqLimits lim;         // host sizes the device cu_seqlens must agree with
   Tiling tl;
   float scale_log2;      // softmax_scale * log2(e)
   __nv_bfloat16* o;      // [total_lc, hq, D]
@@ -41,6 +43,7 @@ struct BwdArgs {
   const int32_t* cu_c;
   long long* win_prefix;  // [rows][batch + 1], each row's by its first CTA, for the reduce kernel
   int batch, hq, hkv, total_lc;
+  SeqLimits lim;         // host sizes the device cu_seqlens must agree with
   Tiling tl;             // dQ tiling (one query tile per block)
   float scale_log2;
   float scale;
@@ -115,7 +118,8 @@ cudaError_t launch_f16_to_bf16(const __half* k, const __half* v, long long n, __
 cudaError_t launch_quantize_q8_0(const __nv_bfloat16* x, long long n_blocks, uint8_t* out,
                                  cudaStream_t st);
 cudaError_t launch_zero_horizon(const int32_t* cu_p, int batch, int hkv, int d, int horizon,
-                                __nv_bfloat16* dk_p, __nv_bfloat16* dv_p, cudaStream_t st);
+                                const SeqLimits& lim, __nv_bfloat16* dk_p, __nv_bfloat16* dv_p,
+                                int* status, cudaStream_t st);
 cudaError_t launch_dequant_q8_0(const uint8_t* blocks, long long n_blocks, float* out_f32,
                                 __nv_bfloat16* out_bf16, cudaStream_t st);
 

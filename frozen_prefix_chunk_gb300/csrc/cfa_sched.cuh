@@ -64,6 +64,38 @@ __host__ __device__ inline int row_grid(const Tiling& tl) { return tl.grid / tl.
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// The host-side sizes of a call: they size the grids, the TMA maps, the
+// output strides and the workspace, so the device cu_seqlens must agree with
+// them before any kernel derives a row index from a window.
+struct SeqLimits {
+  int total_lp, total_lc;  // cu_seqlens_prefix[batch], cu_seqlens_chunk[batch]
+  int max_lp, max_lc;      // longest window
+};
+
+// Window b of the device cu_seqlens agrees with the host sizes: both arrays
+// start at 0 and end at total_lp / total_lc, and the window's prefix and
+// chunk lengths lie in [0, max_lp] and [0, max_lc].  When every window
+// passes, both arrays are non-decreasing from 0 to their totals, so every row
+// a window spans lies inside the tensors the host described, and every
+// window is covered by the grids sized from the maxima.
+__host__ __device__ inline bool window_valid(const int32_t* cu_p, const int32_t* cu_c, int b,
+                                             int batch, const SeqLimits& s) {
+  const long long p0 = cu_p[b], p1 = cu_p[b + 1], c0 = cu_c[b], c1 = cu_c[b + 1];
+  if (p1 < p0 || p1 - p0 > s.max_lp || c1 < c0 || c1 - c0 > s.max_lc) return false;
+  if (b == 0 && (p0 != 0 || c0 != 0)) return false;
+  if (b == batch - 1 && (p1 != s.total_lp || c1 != s.total_lc)) return false;
+  return true;
+}
+
+// All windows (the host-side test and a reference for the device scans).
+__host__ __device__ inline bool seqlens_valid(const int32_t* cu_p, const int32_t* cu_c, int batch,
+                                              const SeqLimits& s) {
+  if (batch < 1) return false;
+  for (int b = 0; b < batch; ++b)
+    if (!window_valid(cu_p, cu_c, b, batch, s)) return false;
+  return true;
+}
+
 // Key tiles seen by a query block whose first token is t0 and which spans
 // `tok_blk` tokens, in a window with lp prefix rows and lc chunk rows.
 __host__ __device__ inline int block_key_tiles(int lp, int lc, int t0, int tok_blk) {
@@ -279,18 +311,23 @@ __host__ __device__ inline int part_cta(long long bs, long long total, int G, in
 
 #ifdef __CUDACC__
 // Prologue of the persistent kernels, run by all `nthreads` threads of the
-// CTA: scans the per-window iteration counts (each thread sums a contiguous
-// run of windows; warp shuffles and a shared array of warp totals turn the
-// run sums into prefixes), finds the window holding this CTA's first
+// CTA: checks the device cu_seqlens against the host sizes `lim`
+// (window_valid, every window in every CTA, so all CTAs reach the same
+// verdict), scans the per-window iteration counts (each thread sums a
+// contiguous run of windows; warp shuffles and a shared array of warp totals
+// turn the run sums into prefixes), finds the window holding this CTA's first
 // iteration, and lets the first CTA of each schedule row store that row's
 // prefix array for the merge kernels (win_prefix_out[row * (batch + 1) + b]).
-// Results land in *total (the row's iterations), *b0 and *pre_b0 (shared
-// memory) after the closing __syncthreads.  `warp_tot` needs one slot per warp.
+// Returns false, the same in every thread, when some window is inconsistent;
+// then nothing has been written and the caller must return before it loads
+// or stores anything.  Otherwise the results land in *total (the row's
+// iterations), *b0 and *pre_b0 (shared memory) after the closing
+// __syncthreads.  `warp_tot` needs one slot per warp.
 template <bool ROW>
-__device__ inline void plan_schedule(const int32_t* cu_p, const int32_t* cu_c, int batch, int hkv,
-                                     const Tiling& tl, long long* win_prefix_out,
-                                     long long* warp_tot, long long* total, int* b0,
-                                     long long* pre_b0) {
+__device__ inline bool plan_schedule(const int32_t* cu_p, const int32_t* cu_c, int batch, int hkv,
+                                     const Tiling& tl, const SeqLimits& lim,
+                                     long long* win_prefix_out, long long* warp_tot,
+                                     long long* total, int* b0, long long* pre_b0) {
   const int t = threadIdx.x, nt = blockDim.x;
   const int lane = t & 31, warp = t >> 5, nwarps = nt >> 5;
   const int per = ceil_div(batch, nt);
@@ -302,6 +339,9 @@ __device__ inline void plan_schedule(const int32_t* cu_p, const int32_t* cu_c, i
     const int lp = cu_p[b + 1] - cu_p[b], lc = cu_c[b + 1] - cu_c[b];
     return (long long)hkv * (ROW ? head_work_row(tl, lp, lc, row) : head_work(tl, lp, lc));
   };
+  bool bad = false;
+  for (int b = w0; b < w1; ++b) bad |= !window_valid(cu_p, cu_c, b, batch, lim);
+  if (__syncthreads_or(bad)) return false;
   long long sum = 0;
   for (int b = w0; b < w1; ++b) sum += work(b);
   long long inc = sum;  // inclusive scan within the warp
@@ -335,6 +375,7 @@ __device__ inline void plan_schedule(const int32_t* cu_p, const int32_t* cu_c, i
     if (j == 0) wp_row[batch] = all;
   }
   __syncthreads();
+  return true;
 }
 
 #endif  // __CUDACC__

@@ -38,11 +38,12 @@
  * [cu_c[b], cu_c[b+1]).  Empty windows and Lp = 0 are allowed.
  *
  * Ownership: every pointer is caller-owned device memory (the prefix may be an
- * imported cache); the library allocates no device memory.  The state it
- * keeps across calls is a second stream and two events per device (made by
- * the first cfa_backward call there) and the fixed scratch array of
- * cfa_forward_noalloc.  `ws` is caller-provided scratch of at least cfa_workspace_size()
- * bytes, 256-byte aligned.
+ * imported cache); the library allocates no device memory at run time.  The
+ * state it keeps across calls is a second stream and two events per device
+ * (made by the first cfa_backward call there) and the fixed scratch array of
+ * cfa_forward_noalloc (48 MiB, reserved when the module loads on a device;
+ * see there).  `ws` is caller-provided scratch of at least
+ * cfa_workspace_size() bytes, 256-byte aligned.
  *
  * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL = the
  * legacy default stream).  Nothing synchronises the host or copies device
@@ -195,19 +196,29 @@ int cfa_quantize_q8_0(const void* x_bf16, long long n_blocks, void* out_blocks, 
  * someone else's pool.  The pages have no counterpart to this entry point.
  * Same inputs and outputs as cfa_forward; the split partials live in a
  * fixed array of cfa_noalloc_scratch_bytes() bytes (48 MiB) inside the
- * library, which every GPU that runs this call holds until the process
- * exits.  The first call on a device looks up that array's address (this
- * loads the module that holds it), so make it before any stream capture.
- * Calls whose forward workspace would exceed the array return
- * CFA_ERR_SCRATCH_LIMIT before anything is enqueued.  Nothing is allocated.
- * All calls share the array: calls that overlap on the GPU (other streams or
- * threads on the same device) race and must be serialised by the caller.
- * The device status word is the array's first word (not readable through
- * cfa_read_status, which takes a caller workspace). */
+ * library.  The array is reserved on a device when the library's module is
+ * loaded there -- with lazy loading (the CUDA default) on the first call of
+ * this entry point, with CUDA_MODULE_LOADING=EAGER on every device where the
+ * process uses the library at all -- and held until the process exits.  The
+ * first call on a device looks up that array's address (loading the module
+ * if needed), so make it before any stream capture; a cudaDeviceReset makes
+ * the looked-up address stale, so do not use this entry point across a
+ * device reset.  Calls whose forward workspace would exceed the array return
+ * CFA_ERR_SCRATCH_LIMIT, and invalid arguments the status cfa_forward gives
+ * them, before anything is enqueued.  Nothing is allocated.  All calls share
+ * the array: calls that overlap on the GPU (other streams or threads on the
+ * same device) race and must be serialised by the caller.  The device status
+ * word is the array's first word; read it with cfa_noalloc_read_status. */
 int cfa_forward_noalloc(const cfa_args* a, void* o, float* lse, void* stream);
 
 /* Size in bytes of the fixed scratch array used by cfa_forward_noalloc. */
 size_t cfa_noalloc_scratch_bytes(void);
+
+/* The device status word of the last cfa_forward_noalloc call on the current
+ * device (CFA_OK, or CFA_ERR_DEVICE_TIMEOUT when a device-side wait ran out
+ * and O / LSE were not computed), after waiting for `stream`; or a CUDA
+ * error.  Allocates nothing. */
+int cfa_noalloc_read_status(void* stream);
 
 /* ---------------------------------------------------------------------------
  * Row-sparse projection backward ("POC: stop-gradient through context tokens",

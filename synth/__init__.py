@@ -57,6 +57,7 @@ class Workload:
     dout_std: float = 0.1
     seed: int = 0
     softmax_scale: float = field(default=0.0)
+    shape_seed: int = None   # seed the varlen window lengths were drawn with (default: seed)
 
     def __post_init__(self):
         if not self.softmax_scale:
@@ -72,8 +73,11 @@ def _varlen_lp(seed: int, n: int = 8) -> list:
     return torch.randint(1024, 32769, (n,), generator=g).tolist()
 
 
-def workload(name: str, seed: int = 0) -> Workload:
-    """The named workload, with its shapes and input distributions."""
+def workload(name: str, seed: int = 0, shape_seed: int = None) -> Workload:
+    """The named workload, with its shapes and input distributions.  ``seed``
+    seeds the values; ``shape_seed`` (default ``seed``) the varlen window
+    lengths, so replicas with different values can share one shape."""
+    ss = seed if shape_seed is None else shape_seed
     if name == "tiny":
         return Workload(name, 2, 1, 64, [256], [64], dout_std=1.0, seed=seed)
     if name == "qwen3_1p7b":
@@ -83,7 +87,7 @@ def workload(name: str, seed: int = 0) -> Workload:
     if name == "window_63k_q8":
         return Workload(name, 32, 8, 128, [62976], [512], prefix_dtype=PREFIX_Q8_0, seed=seed)
     if name == "varlen8":
-        return Workload(name, 32, 8, 128, _varlen_lp(seed), [256] * 8, seed=seed)
+        return Workload(name, 32, 8, 128, _varlen_lp(ss), [256] * 8, seed=seed, shape_seed=ss)
     raise KeyError(name)
 
 
@@ -134,9 +138,12 @@ def make_inputs(w: Workload) -> dict:
     """
     g = torch.Generator().manual_seed(w.seed)
     if w.name == "varlen8":
-        # the eight prefix lengths are the first draw from the stream
+        # the eight prefix lengths are the first draw from the stream (drawn
+        # even when the lengths come from another seed, so the values of a
+        # seed are the same whatever the shape)
         lp = torch.randint(1024, 32769, (8,), generator=g).tolist()
-        assert lp == w.lp, (lp, w.lp)
+        if w.shape_seed is None or w.shape_seed == w.seed:
+            assert lp == w.lp, (lp, w.lp)
     tp, tc = sum(w.lp), sum(w.lc)
     d = w.head_dim
 

@@ -13,8 +13,15 @@
 // CTAs, row r holding query block r of every (window, KV head); every check
 // then applies per row, with the row's own prefix array and iteration count.
 // Prints "OK <total iterations> <segments>" or the first violation.
+//
+// Mode "seq" checks the kernels' cu_seqlens validation instead: given the
+// host sizes and two raw cu_seqlens arrays (which need not be consistent), it
+// prints VALID or INVALID as seqlens_valid decides, and checks that the
+// per-window test window_valid, which the kernels run one window per thread,
+// agrees with a direct statement of the rule.
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <map>
 #include <vector>
 
@@ -22,7 +29,49 @@
 
 using namespace cfa;
 
+// The rule, stated directly: both arrays start at 0, never decrease, end at
+// the host totals, and no window is longer than the host maxima.
+static bool rule(const std::vector<long long>& p, const std::vector<long long>& c,
+                 const SeqLimits& s) {
+  const size_t n = p.size();
+  if (n < 2 || p[0] != 0 || c[0] != 0) return false;
+  if (p[n - 1] != s.total_lp || c[n - 1] != s.total_lc) return false;
+  for (size_t i = 0; i + 1 < n; ++i) {
+    if (p[i + 1] < p[i] || c[i + 1] < c[i]) return false;
+    if (p[i + 1] - p[i] > s.max_lp || c[i + 1] - c[i] > s.max_lc) return false;
+  }
+  return true;
+}
+
+static int seq_mode(int argc, char** argv) {
+  // args: seq total_lp total_lc max_lp max_lc batch cp_0 .. cp_batch cc_0 .. cc_batch
+  if (argc < 7) return 2;
+  SeqLimits s;
+  s.total_lp = atoi(argv[2]);
+  s.total_lc = atoi(argv[3]);
+  s.max_lp = atoi(argv[4]);
+  s.max_lc = atoi(argv[5]);
+  const int batch = atoi(argv[6]);
+  if (batch < 1 || argc != 7 + 2 * (batch + 1)) return 2;
+  std::vector<int32_t> cp(batch + 1), cc(batch + 1);
+  std::vector<long long> lp(batch + 1), lc(batch + 1);
+  for (int i = 0; i <= batch; ++i) {
+    lp[i] = strtoll(argv[7 + i], nullptr, 10);
+    lc[i] = strtoll(argv[8 + batch + i], nullptr, 10);
+    cp[i] = (int32_t)lp[i];
+    cc[i] = (int32_t)lc[i];
+  }
+  const bool v = seqlens_valid(cp.data(), cc.data(), batch, s);
+  if (v != rule(lp, lc, s)) {
+    printf("FAIL seqlens_valid disagrees with the rule\n");
+    return 1;
+  }
+  printf(v ? "VALID\n" : "INVALID\n");
+  return 0;
+}
+
 int main(int argc, char** argv) {
+  if (argc > 1 && std::strcmp(argv[1], "seq") == 0) return seq_mode(argc, argv);
   // args: G hkv g q_per_cta setup nrow batch lp_0 lc_0 lp_1 lc_1 ...
   if (argc < 8) return 2;
   const int G = atoi(argv[1]), hkv = atoi(argv[2]), g = atoi(argv[3]);

@@ -84,6 +84,9 @@ def test_forward_rejects_bad_arguments_on_the_host(L, kw, status):
     assert L.cfa_backward(ctypes.byref(a), 4096, 4096, 4096, 4096, 4096, 4096, 4096, 1 << 20,
                           None) == status
     assert L.cfa_workspace_size(ctypes.byref(a), 0) == 0
+    # the entry point without a workspace reports the same status, before it
+    # looks up its fixed scratch (nothing touches the device)
+    assert L.cfa_forward_noalloc(ctypes.byref(a), 4096, 4096, None) == status
 
 
 def test_null_args_and_dequant_checks(L):

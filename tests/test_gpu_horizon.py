@@ -7,7 +7,8 @@ Rows in the horizon are compared with the oracle's prefix gradient
 caller gave them; dK_chunk and dV_chunk must be bitwise those of
 cfa_backward, and dQ equal up to the order of its split partial sums (the
 horizon's dK/dV work takes SMs from the dQ kernel's stream-K grid, which moves
-the split points).
+the split points).  The horizon call's own dQ, dK_chunk and dV_chunk are also
+compared with the oracle, with the chunk-gradient tolerances.
 """
 import numpy as np
 import pytest
@@ -40,13 +41,16 @@ def _run(inp, horizon):
     rel = (dq.double() - dq0.double()).norm() / dq0.double().norm().clamp_min(1e-30)
     assert rel <= 1e-3, float(rel)
     torch.cuda.synchronize()
-    return dkp.double().cpu().numpy(), dvp.double().cpu().numpy()
+    outs = {k: v.cpu() for k, v in dict(o=o, lse=lse, delta=delta, dq=dq, dk=dk, dv=dv).items()}
+    return dkp.double().cpu().numpy(), dvp.double().cpu().numpy(), outs
 
 
 def _check(inp, horizon, groups=None):
     w = inp["workload"]
-    dkp, dvp = _run(inp, horizon)
+    dkp, dvp, outs = _run(inp, horizon)
     ref = oracle.run(inp, groups=groups, prefix_grad_rows=True)
+    # the chunk gradients of the horizon call itself, against the oracle
+    gu.assert_within(gu.errors(outs, ref, inp, groups))
     cu_p = inp["cu_seqlens_prefix"].tolist()
     if groups is None:
         groups = [(b, hk) for b in range(w.batch) for hk in range(w.hkv)]
@@ -94,7 +98,7 @@ def test_horizon_with_q8_0_prefix():
 def test_horizon_without_chunk_rows_zeroes_the_rows():
     w = synth.custom(hq=4, hkv=2, head_dim=128, lp=[300, 50], lc=[0, 0], seed=4)
     inp = synth.make_inputs(w)
-    dkp, dvp = _run(inp, 100)
+    dkp, dvp, _ = _run(inp, 100)
     cu_p = inp["cu_seqlens_prefix"].tolist()
     for b in range(2):
         p0, p1 = cu_p[b], cu_p[b + 1]

@@ -177,3 +177,50 @@ def test_quantize_q8_0_appends_into_a_cache_at_any_block():
     c = cache.cpu().numpy()
     assert np.array_equal(c[start:start + n], oracle.quantize_q8_0(_bf16_bits(x)).reshape(-1))
     assert np.all(c[:start] == 0xAB) and np.all(c[start + n:] == 0xAB)
+
+
+def _guarded(shape, dtype, fill, guard):
+    """A tensor of `shape` with `guard` leading-dimension rows of `fill` on
+    either side: (whole buffer, the inner view the library writes into)."""
+    n = shape[0]
+    full = torch.full((guard + n + guard,) + tuple(shape[1:]), fill, dtype=dtype, device="cuda")
+    return full, full[guard:guard + n]
+
+
+def test_outputs_have_no_stray_writes():
+    # Every output and both workspaces sit between guard rows holding a
+    # sentinel: a valid call (ragged and empty windows, split query blocks)
+    # must leave every guard untouched and give the same bits as a call on
+    # plain buffers.
+    import frozen_prefix_chunk_gb300 as cfa
+    w = synth.custom(hq=8, hkv=2, head_dim=128, lp=[2000, 0, 300, 4096], lc=[200, 64, 0, 129],
+                     seed=12, dout_std=1.0)
+    inp = synth.make_inputs(w)
+    ref = gu.run_cuda(inp)
+    d = gu.to_device(inp)
+    args = gu.make_args(d)
+    tc, G = sum(w.lc), 64
+    bf, f32 = torch.bfloat16, torch.float32
+    o_full, o = _guarded((tc, w.hq, w.head_dim), bf, -7.0, G)
+    dq_full, dq = _guarded((tc, w.hq, w.head_dim), bf, -7.0, G)
+    dk_full, dk = _guarded((tc, w.hkv, w.head_dim), bf, -7.0, G)
+    dv_full, dv = _guarded((tc, w.hkv, w.head_dim), bf, -7.0, G)
+    lse_full, lse = _guarded((w.hq * tc,), f32, -7.0, 1024)
+    dl_full, dl = _guarded((w.hq * tc,), f32, -7.0, 1024)
+    nf = cfa.workspace_size(args, cfa.WS_FORWARD)
+    nb = cfa.workspace_size(args, cfa.WS_BACKWARD)
+    wsf_full, wsf = _guarded((nf,), torch.uint8, 0xA5, 4096)
+    wsb_full, wsb = _guarded((nb,), torch.uint8, 0xA5, 4096)
+    lse, dl = lse.view(w.hq, tc), dl.view(w.hq, tc)
+    cfa.forward(args, d["q"], o, lse, wsf)
+    cfa.backward_preprocess(args, o, d["dout"], dl)
+    cfa.backward(args, d["dout"], lse, dl, dq, dk, dv, wsb)
+    assert cfa.read_status(wsf) == 0 and cfa.read_status(wsb) == 0
+    torch.cuda.synchronize()
+    for full, g in ((o_full, G), (dq_full, G), (dk_full, G), (dv_full, G), (lse_full, 1024),
+                    (dl_full, 1024), (wsf_full, 4096), (wsb_full, 4096)):
+        fill = 0xA5 if full.dtype == torch.uint8 else -7.0
+        assert bool((full[:g] == fill).all()) and bool((full[-g:] == fill).all())
+    got = dict(o=o, lse=lse, delta=dl, dq=dq, dk=dk, dv=dv)
+    for k, v in got.items():
+        assert torch.equal(v.cpu(), ref[k]), k

@@ -6,6 +6,12 @@ compiles for the host, and tests/native/sched_check.cpp walks every CTA's
 range and checks coverage, ordering, the head/tail flags and the part lists
 the split merges use.  Configurations span the benchmark layers, GQA group
 sizes, ragged and empty windows and grids larger than the work.
+
+The same checker also runs the cu_seqlens validation every kernel performs
+before it derives a row index from a window (window_valid / seqlens_valid):
+well-formed arrays pass, and each malformed one -- a non-zero start, a
+decrease, a wrong total, a window longer than the host maximum -- is rejected,
+so inconsistent host sizes never reach a load or a store on the GPU.
 """
 import os
 import shutil
@@ -86,3 +92,33 @@ def test_schedule_covers_every_tile_once(checker, case):
         args += [str(lp), str(lc)]
     r = subprocess.run([checker] + args, capture_output=True, text=True)
     assert r.returncode == 0 and r.stdout.startswith("OK"), r.stdout + r.stderr
+
+
+# (total_lp, total_lc, max_lp, max_lc, cu_seqlens_prefix, cu_seqlens_chunk, valid)
+SEQ_CASES = [
+    (16128, 256, 16128, 256, [0, 16128], [0, 256], True),
+    (700, 393, 700, 256, [0, 5, 5, 705 - 5, 700], [0, 37, 137, 137, 393], True),  # empty windows
+    (0, 64, 0, 64, [0, 0], [0, 64], True),                           # no prefix
+    (300, 0, 300, 0, [0, 300], [0, 0], True),                        # no chunk rows
+    (16128, 256, 16128, 256, [1, 16128], [0, 256], False),           # prefix does not start at 0
+    (16128, 256, 16128, 256, [0, 16128], [4, 256], False),           # chunk does not start at 0
+    (16128, 256, 16128, 256, [0, 16000], [0, 256], False),           # prefix total differs
+    (16128, 256, 16128, 256, [0, 16128], [0, 255], False),           # chunk total differs
+    (1000, 200, 1000, 200, [0, 600, 500, 1000], [0, 50, 100, 200], False),  # prefix decreases
+    (1000, 200, 1000, 200, [0, 300, 600, 1000], [0, 150, 100, 200], False),  # chunk decreases
+    (1000, 200, 400, 200, [0, 300, 800, 1000], [0, 50, 100, 200], False),    # window over max_lp
+    (1000, 200, 1000, 64, [0, 300, 600, 1000], [0, 50, 120, 200], False),    # window over max_lc
+    (1000, 200, 1000, 200, [0, -5, 600, 1000], [0, 50, 100, 200], False),    # negative entry
+    (2147483647, 64, 2147483647, 64, [0, 2147483647], [0, 64], True),        # int32 extremes
+    (5, 64, 5, 64, [0, -2147483648 + 2, 5], [0, 32, 64], False),              # wrap-around
+]
+
+
+@pytest.mark.parametrize("case", SEQ_CASES, ids=[str(i) for i in range(len(SEQ_CASES))])
+def test_cu_seqlens_validation(checker, case):
+    tlp, tlc, mlp, mlc, cp, cc, valid = case
+    args = ["seq", str(tlp), str(tlc), str(mlp), str(mlc), str(len(cp) - 1)]
+    args += [str(x) for x in cp] + [str(x) for x in cc]
+    r = subprocess.run([checker] + args, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip() == ("VALID" if valid else "INVALID"), (case, r.stdout)

@@ -5,9 +5,12 @@ to an inference server that reserved the GPU's memory up front, or a C
 program whose device memory comes only from someone else's pool -- so they
 cannot provide cfa_forward's workspace.  cfa_forward_noalloc keeps the split
 partials in a fixed scratch array inside the library instead.  These tests
-call it through the C ABI and compare it with cfa_forward on the same inputs,
-twice in a row with different inputs (the shared scratch keeps the previous
-call's contents), and check that an oversized request is refused.
+call it through the C ABI and check, on two calls in a row with different
+inputs (the shared scratch keeps the previous call's contents), that its
+output is bitwise that of cfa_forward on the same inputs and matches the fp64
+oracle within the forward's tolerance; that its device status word reads 0,
+and reports a device-side wait that ran out; and that an oversized request is
+refused.
 
 The file is named so that pytest collects it last.
 """
@@ -16,6 +19,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import synth
 from tests import gpu_util as gu
 
@@ -28,7 +32,8 @@ def _forward_both(seed):
     # Lp=1536, Lc=512, Hq=16, Hkv=8: the forward is split along the keys, so
     # the scratch array really holds partials
     w = synth.workload("qwen3_1p7b", seed=seed)
-    d = gu.to_device(synth.make_inputs(w))
+    inp = synth.make_inputs(w)
+    d = gu.to_device(inp)
     args = gu.make_args(d)
     need = cfa.workspace_size(args, cfa.WS_FORWARD)
     assert 256 < need <= cfa.lib().cfa_noalloc_scratch_bytes()
@@ -36,18 +41,22 @@ def _forward_both(seed):
     o = torch.empty_like(o_ref)
     lse = torch.empty_like(lse_ref)
     cfa.forward_noalloc(args, o, lse)
+    assert cfa.noalloc_read_status() == 0
     torch.cuda.synchronize()
-    return o_ref, lse_ref, o, lse
+    return inp, o_ref, lse_ref, o, lse
 
 
-def _compare(o_ref, lse_ref, o, lse):
-    err_o = ((o.double() - o_ref.double()).abs().max() / o_ref.double().abs().max()).item()
-    err_lse = (lse.double() - lse_ref.double()).abs().max().item()
-    assert err_o <= gu.TOL_O, err_o
-    assert err_lse <= gu.TOL_LSE, err_lse
+def _compare(inp, o_ref, lse_ref, o, lse):
+    # the same kernels on the same inputs: the same bits as cfa_forward
+    assert torch.equal(o, o_ref)
+    assert torch.equal(lse, lse_ref)
+    # and the oracle's values, element by element, within the tolerance
+    ref = oracle.run(inp)
+    err = gu.errors({"o": o.cpu(), "lse": lse.cpu()}, ref, inp)
+    gu.assert_within(err)
 
 
-def test_noalloc_forward_matches_forward_twice():
+def test_noalloc_forward_matches_forward_and_oracle_twice():
     import frozen_prefix_chunk_gb300 as cfa
 
     cfa.lib(build_if_missing=True)
@@ -56,7 +65,32 @@ def test_noalloc_forward_matches_forward_twice():
     second = _forward_both(seed=1)
     _compare(*second)
     # the second call saw different inputs, so its output differs from the first
-    assert not torch.equal(first[2], second[2])
+    assert not torch.equal(first[3], second[3])
+
+
+def test_noalloc_forward_reports_a_device_timeout(monkeypatch):
+    import frozen_prefix_chunk_gb300 as cfa
+
+    cfa.lib(build_if_missing=True)
+    inp = synth.make_inputs(synth.custom(hq=8, hkv=2, head_dim=128, lp=[2000], lc=[256], seed=2))
+    d = gu.to_device(inp)
+    args = gu.make_args(d)
+    o = torch.empty_like(d["q"])
+    lse = torch.empty(8, 256, dtype=torch.float32, device="cuda")
+    # every forward kernel's MMA warp first waits on a barrier nothing
+    # arrives on; the 2 ms bounded wait runs out and the kernel unwinds
+    monkeypatch.setenv("CFA_WAIT_LIMIT_NS", "2000000")
+    monkeypatch.setenv("CFA_DEBUG_WAIT_NEVER", "1")
+    cfa.forward_noalloc(args, o, lse)
+    assert cfa.noalloc_read_status() == -5
+    monkeypatch.delenv("CFA_DEBUG_WAIT_NEVER")
+    monkeypatch.delenv("CFA_WAIT_LIMIT_NS")
+    # the next call clears the status word and computes the forward
+    cfa.forward_noalloc(args, o, lse)
+    assert cfa.noalloc_read_status() == 0
+    o_ref, lse_ref, _ = cfa.forward(args, d["q"])
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
 
 
 def test_noalloc_forward_refuses_requests_beyond_its_scratch():
