@@ -343,14 +343,20 @@ __global__ void __launch_bounds__(320, 1)
         lim -= half * 64;  // visible columns [0, lim) of this warp's 64
         float p[64];
         {
+          // two 32-column loads: the exponentials of the first half run while
+          // the second half loads
           uint32_t r[64];
-          tmem_ld_x64(t_lane + sb, r);
+          tmem_ld_x32_async(t_lane + sb, r);
+          tmem_wait_ld_x32(r);
+          tmem_ld_x32_async(t_lane + sb + 32, r + 32);
           const uint64_t sl2x2 = f2(sl2, sl2), nl2 = f2(-lse2, -lse2);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < 32; ++j) {
+            if (j == 16) tmem_wait_ld_x32(r + 32);
             f2_split(ex2_sfu_x2(f2_fma(f2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
                                        sl2x2, nl2)),
                      p[2 * j], p[2 * j + 1]);
+          }
           if (lim < 64) {  // edge tiles only: the prefix tail, the causal diagonal, padding rows
 #pragma unroll
             for (int j = 0; j < 64; ++j) p[j] = (j < lim) ? p[j] : 0.f;
@@ -369,11 +375,16 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after_sync();
         uint32_t pk[32];
         {
+          // dP in two 32-column loads: dS of the first half is computed while
+          // the second half loads
           uint32_t r[64];
-          tmem_ld_x64(t_lane + 256 + half * 64, r);
+          tmem_ld_x32_async(t_lane + 256 + half * 64, r);
+          tmem_wait_ld_x32(r);
+          tmem_ld_x32_async(t_lane + 256 + half * 64 + 32, r + 32);
           const uint64_t dl2 = f2(dl, dl);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
+            if (j == 16) tmem_wait_ld_x32(r + 32);
             float d0, d1;
             f2_split(f2_mul(f2(p[2 * j], p[2 * j + 1]),
                             f2_sub(f2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), dl2)),
