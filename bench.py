@@ -751,6 +751,9 @@ def main():
                     help="chunk rows: walk the workload's window chunk by chunk instead")
     ap.add_argument("--horizon", type=int, default=0,
                     help="prefix rows per window that get dK/dV (cfa_backward_horizon)")
+    ap.add_argument("--lp", type=int, default=0,
+                    help="override every window's prefix length (smaller cases of the same "
+                         "kernels, for profiler captures)")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -783,7 +786,11 @@ def main():
     # Every rank has its own replica of the workload: the same shapes (the
     # varlen window lengths drawn with seed 0), values seeded by the rank.
     def make_case(name, horizon=0):
-        return AttnStep(synth.workload(name, seed=rank, shape_seed=0), dev, horizon, args.q8)
+        wl = synth.workload(name, seed=rank, shape_seed=0)
+        if args.lp:
+            wl.lp = [args.lp] * wl.batch
+            wl.shape_seed = -1   # lengths no longer those the seed draws
+        return AttnStep(wl, dev, horizon, args.q8)
 
     # ---- the other target configurations, each timed on its own, long
     # enough for the clock sampler to see it under load
