@@ -1024,36 +1024,33 @@ __global__ void dequant_q8_0_kernel(const uint8_t* __restrict__ blocks, long lon
 }
 
 // q8_0 prefix -> bf16 rows for the attention kernels' TMA maps, K and V in
-// one launch (blockIdx.y).  A warp takes 32 consecutive 34-byte blocks
-// (1088 bytes): it stages them in shared memory with coalesced 16-byte loads
-// (2-byte loads for a ragged or unaligned chunk), then each lane expands one
-// block to 32 values, fp32(d) * q (exact) rounded to nearest-even bf16 -- the
-// same operand the export kernel above produces -- and writes its 64 bytes.
+// one launch (blockIdx.y).  A warp takes chunks of 32 consecutive 34-byte
+// blocks (1088 bytes in, 2048 bytes out), grid-stride.  A full chunk at a
+// 16-byte aligned address comes in with three 16-byte loads per lane, issued
+// one chunk ahead so that they are in flight while the previous chunk is
+// expanded; a ragged or unaligned chunk comes in with 2-byte loads.  Each
+// lane expands one block to 32 values, fp32(d) * q (exact) rounded to
+// nearest-even bf16 -- the same operand the export kernel above produces --
+// into shared memory, and the warp writes the chunk's 2048 bytes back with
+// 16-byte stores, 512 contiguous bytes per instruction.  The staged output is
+// 16 rows of eight 16-byte columns, column XOR (row & 7), so that both the
+// per-lane writes and the coalesced read-back take four wavefronts.
 constexpr int kDqWarps = 8;
-__global__ void __launch_bounds__(kDqWarps * 32)
-    dequant_prefix_kernel(const uint8_t* __restrict__ k_blocks, const uint8_t* __restrict__ v_blocks,
-                          long long n_blocks, __nv_bfloat16* __restrict__ k_out,
-                          __nv_bfloat16* __restrict__ v_out) {
-  pdl_start();
-  __shared__ uint4 stage[kDqWarps][68];
-  const uint8_t* src = blockIdx.y ? v_blocks : k_blocks;
-  __nv_bfloat16* out = blockIdx.y ? v_out : k_out;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long b0 = ((long long)blockIdx.x * kDqWarps + warp) * 32;
-  if (b0 >= n_blocks) return;
-  const int nb = (n_blocks - b0 < 32) ? (int)(n_blocks - b0) : 32;
-  const uint8_t* chunk = src + b0 * 34;
-  uint8_t* st = reinterpret_cast<uint8_t*>(stage[warp]);
-  if (nb == 32 && (reinterpret_cast<uintptr_t>(chunk) & 15u) == 0) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(chunk);
-    for (int i = lane; i < 68; i += 32) stage[warp][i] = s4[i];
-  } else {
-    const uint16_t* s2 = reinterpret_cast<const uint16_t*>(chunk);
-    for (int i = lane; i < nb * 17; i += 32) reinterpret_cast<uint16_t*>(st)[i] = s2[i];
-  }
-  __syncwarp();
+#ifndef CFA_DQ_CTAS_PER_SM
+#define CFA_DQ_CTAS_PER_SM 8
+#endif
+constexpr int kDqCtasPerSm = CFA_DQ_CTAS_PER_SM;  // resident CTAs per SM the grid aims for
+
+__device__ __forceinline__ uint32_t dq_stage_slot(int chunk16) {
+  const int row = chunk16 >> 3, col = chunk16 & 7;
+  return (uint32_t)(row * 8 + (col ^ (row & 7)));
+}
+
+// Expand the `nb` blocks staged at `in` into the swizzled output stage; lane
+// `lane` takes block `lane`.
+__device__ __forceinline__ void dq_expand_block(const uint8_t* in, uint4* out, int lane, int nb) {
   if (lane >= nb) return;
-  const uint16_t* p = reinterpret_cast<const uint16_t*>(st + lane * 34);
+  const uint16_t* p = reinterpret_cast<const uint16_t*>(in + lane * 34);
   const float d = __half2float(__ushort_as_half(p[0]));
   uint32_t w[16];
 #pragma unroll
@@ -1061,9 +1058,65 @@ __global__ void __launch_bounds__(kDqWarps * 32)
     const uint16_t two = p[1 + i];
     w[i] = pack_bf16x2(d * (float)(int8_t)(two & 0xff), d * (float)(int8_t)(two >> 8));
   }
-  uint4* dst = reinterpret_cast<uint4*>(out + (b0 + lane) * 32);
 #pragma unroll
-  for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+  for (int v = 0; v < 4; ++v)
+    out[dq_stage_slot(lane * 4 + v)] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+}
+
+__global__ void __launch_bounds__(kDqWarps * 32)
+    dequant_prefix_kernel(const uint8_t* __restrict__ k_blocks, const uint8_t* __restrict__ v_blocks,
+                          long long n_blocks, __nv_bfloat16* __restrict__ k_out,
+                          __nv_bfloat16* __restrict__ v_out) {
+  pdl_start();
+  __shared__ uint4 in_st[kDqWarps][68];
+  __shared__ uint4 out_st[kDqWarps][128];
+  const uint8_t* src = blockIdx.y ? v_blocks : k_blocks;
+  uint4* out = reinterpret_cast<uint4*>(blockIdx.y ? v_out : k_out);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long n_chunks = (n_blocks + 31) / 32;
+  const long long full = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) ? n_blocks / 32 : 0;
+  const long long stride = (long long)gridDim.x * kDqWarps;
+  uint8_t* in_b = reinterpret_cast<uint8_t*>(in_st[warp]);
+  long long c = (long long)blockIdx.x * kDqWarps + warp;
+  // full aligned chunks, loads one chunk ahead
+  uint4 r0 = make_uint4(0, 0, 0, 0), r1 = r0, r2 = r0;
+  if (c < full) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + c * 1088);
+    r0 = s4[lane];
+    r1 = s4[lane + 32];
+    if (lane < 4) r2 = s4[lane + 64];
+  }
+  for (; c < full; c += stride) {
+    in_st[warp][lane] = r0;
+    in_st[warp][lane + 32] = r1;
+    if (lane < 4) in_st[warp][lane + 64] = r2;
+    __syncwarp();
+    if (c + stride < full) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src + (c + stride) * 1088);
+      r0 = s4[lane];
+      r1 = s4[lane + 32];
+      if (lane < 4) r2 = s4[lane + 64];
+    }
+    dq_expand_block(in_b, out_st[warp], lane, 32);
+    __syncwarp();
+    uint4* dst = out + c * 128;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[k * 32 + lane] = out_st[warp][dq_stage_slot(k * 32 + lane)];
+    __syncwarp();
+  }
+  // the ragged last chunk, or every chunk of an unaligned source
+  for (; c < n_chunks; c += stride) {
+    const long long b0 = c * 32;
+    const int nb = (n_blocks - b0 < 32) ? (int)(n_blocks - b0) : 32;
+    const uint16_t* s2 = reinterpret_cast<const uint16_t*>(src + b0 * 34);
+    for (int i = lane; i < nb * 17; i += 32) reinterpret_cast<uint16_t*>(in_b)[i] = s2[i];
+    __syncwarp();
+    dq_expand_block(in_b, out_st[warp], lane, nb);
+    __syncwarp();
+    uint4* dst = out + c * 128;
+    for (int j = lane; j < nb * 4; j += 32) dst[j] = out_st[warp][dq_stage_slot(j)];
+    __syncwarp();
+  }
 }
 
 // bf16 -> q8_0 (the cache write of the walk: the chunk's K/V appended to a
@@ -1185,8 +1238,16 @@ cudaError_t launch_dequant_prefix(const uint8_t* k_blocks, const uint8_t* v_bloc
                                   long long n_blocks, __nv_bfloat16* k_out,
                                   __nv_bfloat16* v_out, cudaStream_t st) {
   if (n_blocks <= 0) return cudaSuccess;
-  const long long per_cta = 32LL * kDqWarps;
-  const dim3 grid((unsigned)((n_blocks + per_cta - 1) / per_cta), v_blocks ? 2 : 1);
+  // grid-stride: enough CTAs to fill every SM several times over, no more
+  // than the chunks need
+  const long long chunks = (n_blocks + 31) / 32;
+  const long long ctas_needed = (chunks + kDqWarps - 1) / kDqWarps;
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorUnknown;
+  const long long cap = (long long)sms * kDqCtasPerSm / (v_blocks ? 2 : 1);
+  const dim3 grid((unsigned)(ctas_needed < cap ? ctas_needed : cap), v_blocks ? 2 : 1);
   dequant_prefix_kernel<<<grid, kDqWarps * 32, 0, st>>>(k_blocks, v_blocks, n_blocks, k_out,
                                                         v_out);
   return cudaGetLastError();
