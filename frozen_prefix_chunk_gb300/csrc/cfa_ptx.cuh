@@ -385,6 +385,32 @@ __device__ __forceinline__ uint64_t ex2_sfu_x2(uint64_t x) {
   return f2(ex2_approx(a), ex2_approx(b));
 }
 
+// 2^x for a pair on the FMA and integer pipes, so that part of a row's
+// exponentials leaves the special-function unit.  Cody and Waite's argument
+// reduction: adding 1.5 * 2^23 rounds x to the nearest integer j, which then
+// sits in the sum's low mantissa bits, and f = x - j lies in [-1/2, 1/2].
+// 2^f comes from a degree-3 polynomial fitted here to 2^f on that interval
+// for least maximum relative error (about 7.5e-5, far below bf16's 2^-9), and
+// 2^j is added into the exponent field.  x is clamped at -126 first, which
+// keeps the exponent in range; the underflowed tail then reads as about
+// 2^-126 instead of 0, so the caller keeps masked keys away from it.
+__device__ __forceinline__ uint64_t ex2_poly_x2(uint64_t x) {
+  float a, b;
+  f2_split(x, a, b);
+  const uint64_t xc = f2(fmaxf(a, -126.f), fmaxf(b, -126.f));
+  const uint64_t rnd = f2(12582912.f, 12582912.f);
+  const uint64_t t = f2_add(xc, rnd);
+  const uint64_t fr = f2_sub(xc, f2_sub(t, rnd));
+  uint64_t p = f2_fma(fr, f2(0.0551716685f, 0.0551716685f), f2(0.242611140f, 0.242611140f));
+  p = f2_fma(p, fr, f2(0.693260968f, 0.693260968f));
+  p = f2_fma(p, fr, f2(0.999928057f, 0.999928057f));
+  float pa, pb, ta, tb;
+  f2_split(p, pa, pb);
+  f2_split(t, ta, tb);
+  return f2(__uint_as_float(__float_as_uint(pa) + (__float_as_uint(ta) << 23)),
+            __uint_as_float(__float_as_uint(pb) + (__float_as_uint(tb) << 23)));
+}
+
 // max(a, b, c) in one instruction (3-input max.f32).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
