@@ -710,10 +710,19 @@ int rs_plan(const cfa_rowsparse_args* r, int mode, RsPlan* p) {
   a.splits = splits;
   a.units = (long long)a.tiles * splits;
   p->grid = (int)(a.units < sms ? a.units : sms);
+  // dX split K: one cluster per tile when every tile's splits can be resident
+  // together (the partials then never leave shared memory)
+  // (CFA_RS_CLUSTER=0 keeps the global-memory path: the tests compare the two)
+  const char* env = std::getenv("CFA_RS_CLUSTER");
+  const bool allow = !(env && env[0] == '0');
+  a.cluster = (allow && mode == 1 && splits > 1 && a.units <= sms &&
+               rowsparse_clusters_fit(splits, a.tiles))
+                  ? 1
+                  : 0;
   p->off_cnt = 16;
   const size_t hdr = align256(p->off_cnt + (size_t)a.tiles * 16);
   p->off_part = hdr;
-  p->ws = hdr + (splits > 1 ? (size_t)a.tiles * splits * kRsTileM * kRsTileN * 4 : 0);
+  p->ws = hdr + (splits > 1 && !a.cluster ? (size_t)a.tiles * splits * kRsTileM * kRsTileN * 4 : 0);
   if (p->ws < kWsHeader) p->ws = kWsHeader;
   a.limit_ns = wait_limit_ns();
   return CFA_OK;
@@ -726,8 +735,9 @@ int rs_run(const cfa_rowsparse_args* r, int mode, void* out, int out_f32, int ac
   if (st) return st;
   if ((st = check_ws(ws, ws_bytes, p.ws))) return st;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  // status word and the (tile, lane quadrant) counters start at zero
-  if (cudaMemsetAsync(ws, 0, p.off_cnt + (size_t)p.a.tiles * 16, s) != cudaSuccess)
+  // status word and the (tile, lane quadrant) counters start at zero (the
+  // cluster path has no counters, and its first CTA clears the status)
+  if (!p.a.cluster && cudaMemsetAsync(ws, 0, p.off_cnt + (size_t)p.a.tiles * 16, s) != cudaSuccess)
     return CFA_ERR_LAUNCH;
   RsArgs& a = p.a;
   a.keep = r->keep_idx;
@@ -747,7 +757,7 @@ int rs_run(const cfa_rowsparse_args* r, int mode, void* out, int out_f32, int ac
       (st = make_map_2d(&mo, out, r->in_features, r->out_features, out_f32 ? 32 : 64, 32,
                         out_f32 != 0)))
     return st;
-  if (a.splits > 1 &&
+  if (a.splits > 1 && !a.cluster &&
       (st = make_map_2d(&mp, a.part, kRsTileN, (long long)a.tiles * a.splits * kRsTileM, 32, 32,
                         true)))
     return st;

@@ -28,7 +28,18 @@
 // store instruction writes four whole rows' 128-byte runs instead of 32
 // scattered pieces.
 //
-// Split K (when there are fewer tiles than SMs): every split writes an fp32
+// Split K, mode 1 (dX, whose kept rows make few tiles): the splits of a tile
+// run as one thread-block cluster.  After its K range each CTA copies its fp32
+// accumulator from TMEM into its own shared memory (the freed pipeline
+// stages), the CTAs signal one another through mbarriers (remote arrives),
+// and CTA rank r of the cluster sums rows [r * 128 / splits, (r + 1) * 128 /
+// splits) of the tile over distributed shared memory, in split order
+// (deterministic, the same sums as the global-memory path below), and writes
+// them out.  A second exchange keeps every CTA resident until its peers have
+// read its partial.  Every wait is bounded; a CTA whose wait for the partials
+// runs out reads nothing remote.
+//
+// Split K otherwise (when there are fewer tiles than SMs): every split writes an fp32
 // partial tile to the workspace.  Each epilogue warp owns 32 rows of the tile
 // and a counter of its own per (tile, lane quadrant); the warp that finishes
 // its rows last sums their partials in split order -- deterministic -- and
@@ -101,6 +112,145 @@ __device__ __forceinline__ void bulk_wait() {
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+
+// ------------------------------------------------------------ cluster --
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's
+// (and, cumulatively, what it has observed of its CTA's) earlier writes.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Bounded wait for an exchange among the cluster's CTAs (acquire at cluster
+// scope, so the peers' shared-memory writes released by their arrivals are
+// visible).  `drain`: ignore the CTA's abort flag (used while unwinding).
+__device__ __forceinline__ bool cluster_wait(const Waiter& w, uint32_t bar, uint32_t parity,
+                                             bool drain) {
+  bool ok = mbar_try_wait_acq_cluster(bar, parity);
+  if (!ok) {
+    const uint64_t t0 = global_timer_ns();
+    const uint64_t lim = drain ? kDrainLimitNs : w.limit_ns;
+    for (uint32_t it = 1;; ++it) {
+      if (mbar_try_wait_acq_cluster(bar, parity)) {
+        ok = true;
+        break;
+      }
+      if ((it & 15u) == 0u) {
+        if (!drain && *w.abort) break;
+        if (global_timer_ns() - t0 > lim) {
+          if (!drain) {
+            *w.abort = 1;
+            atomicExch(w.status, -5 /* CFA_ERR_DEVICE_TIMEOUT */);
+          }
+          break;
+        }
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+// (no memory clobber: a batch of these issues back to back and its sums
+// follow; the exchanges around them are volatile asm with clobbers, which
+// these do not move across)
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr));
+  return v;
+}
+
+// Cluster split K: this warp's rows of the tile summed over the SP splits'
+// staged partials (in split order) and written out as bf16.  Rows go in
+// batches of 8 / SP so that every lane has 16 remote loads in flight.
+template <int SP>
+__device__ __forceinline__ void cluster_reduce_rows(const RsArgs& a, int tm, int tn, uint32_t base,
+                                                    uint32_t rank, int quad, int lane, int my_keep,
+                                                    int kept_row_stride, int cl_row_bytes) {
+  constexpr int R = kRsTileM / SP, RPW = R / 4, RB = 8 / SP;
+  const int col = 8 * lane;
+  const int n = tn * kRsTileN + col;  // output column
+  const bool vec = n + 8 <= a.N && (a.N & 7) == 0 && (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
+  for (int rb = 0; rb < RPW; rb += RB) {
+    float4 v[RB][SP][2];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const int row = (int)rank * R + quad * RPW + rb + r;
+      const uint32_t src = base + (uint32_t)(row * cl_row_bytes + col * 4);
+#pragma unroll
+      for (int k = 0; k < SP; ++k) {
+        const uint32_t ra = mapa_shared(src, (uint32_t)k);
+        v[r][k][0] = ld_shared_cluster_v4(ra);
+        v[r][k][1] = ld_shared_cluster_v4(ra + 16u);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < SP; ++k) {
+        s[0] += v[r][k][0].x; s[1] += v[r][k][0].y; s[2] += v[r][k][0].z; s[3] += v[r][k][0].w;
+        s[4] += v[r][k][1].x; s[5] += v[r][k][1].y; s[6] += v[r][k][1].z; s[7] += v[r][k][1].w;
+      }
+      const int row = (int)rank * R + quad * RPW + rb + r;
+      const int i = tm * kRsTileM + row;  // kept-row index
+      const int keep_r = __shfl_sync(0xffffffffu, my_keep, rb + r);  // fetched by lane rb + r
+      if (i >= a.n_keep) continue;
+      if (keep_r < 0 || keep_r >= a.n_rows) {
+        if (lane == 0) atomicExch(a.status, -1 /* kept row outside X */);
+        continue;
+      }
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (size_t)keep_r * kept_row_stride;
+      if (vec) {
+        *reinterpret_cast<uint4*>(orow + n) =
+            make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
+                       pack_bf16x2(s[6], s[7]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (n + e < a.N) orow[n + e] = __float2bfloat16_rn(s[e]);
+      }
+    }
+  }
+}
+// Hardware barrier over every thread of the cluster: used once, right after
+// the mbarriers are initialised and before any remote arrive, by all threads
+// of all CTAs (no CTA can leave before it).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Barrier among the four epilogue warps (named barrier 1, 128 threads).
+__device__ __forceinline__ void epilogue_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+// Row stride of a CTA's staged fp32 partial (256 floats + 16 bytes, so that
+// the lanes' row-per-thread writes spread over the banks).
+constexpr int kClRowBytes = 1040;
+static_assert(128 * kClRowBytes <= kStages * kStageBytes, "staged partial fits the stages");
 
 struct Unit {
   int tm, tn, tile, split, kb, ke;  // k stages [kb, ke)
@@ -187,7 +337,7 @@ __device__ __forceinline__ uint8_t* out_row(const RsArgs& a, const Unit& t, int 
   return static_cast<uint8_t*>(a.out) + (size_t)keep_r * a.N * esz;
 }
 
-template <int MODE>
+template <int MODE, bool CL>
 __global__ void __launch_bounds__(kThreads, 1)
     rowsparse_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b,
@@ -202,11 +352,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   //        run of consecutive rows (the chunk rows of a window): one tile
   //        copy per slab instead of 16 gathers, same shared-memory layout
   pdl_start();
+  // cluster path: no memset before the launch; the first CTA clears the
+  // status word (a device wait gives up only after its wall-clock limit,
+  // long after this store, so no error of this launch is cleared)
+  if (CL && blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_addr(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // (the cluster path launches exactly one CTA per unit: no CTA returns here)
   if ((long long)blockIdx.x >= a.units) return;
 
   const uint32_t bars = base + kBarOff;
@@ -215,6 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_tfull = bars + 16 * kStages;    // [2]
   const uint32_t bar_tempty = bar_tfull + 16;        // [2]
   const uint32_t bar_drain = bar_tempty + 16;
+  const uint32_t bar_staged = bar_drain + 8;  // cluster path: every split's partial staged
+  const uint32_t bar_done = bar_drain + 16;   // cluster path: every split's reads done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kBarOff + 240);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kBarOff + 244);
 
@@ -229,6 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_tempty + 8 * b, 4);
     }
     mbar_init(bar_drain, 1);
+    if (CL) {
+      mbar_init(bar_staged, (uint32_t)a.splits);
+      mbar_init(bar_done, (uint32_t)a.splits);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -238,6 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
+  // every CTA of the cluster has initialised its barriers before any remote
+  // arrive
+  if (CL) cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const Waiter W{a.limit_ns, abort_flag, a.status};
@@ -371,6 +535,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_commit_warp(bar_drain);
     mbar_wait_bounded(bar_drain, 0, kDrainLimitNs);
+  } else if (CL) {
+    // ------------------------------------------- epilogue, cluster split K --
+    // One unit per CTA; its split is the CTA's rank in the cluster.
+    const int quad = warp & 3;
+    const Unit t = unit_of(a, u0);
+    const int splits = a.splits;
+    const uint32_t rank = cluster_ctarank();
+    // lane j < (128 / splits) / 4 fetches the keep index of this warp's row j
+    // of the reduction now, so that its latency is off the reduction
+    int my_keep = -1;
+    {
+      const int rpw = kRsTileM / splits / 4;
+      const int i = t.tm * kRsTileM + (int)rank * (kRsTileM / splits) + quad * rpw + lane;
+      if (lane < rpw && i < a.n_keep) my_keep = a.keep[i];
+    }
+    if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 0);
+    bool ok = warp_wait(W, bar_tfull, 0u);
+    if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 1);
+    if (ok) {
+      tc_fence_after_sync();
+      // this split's 128 x 256 fp32 accumulator into the freed pipeline
+      // stages: tile row r at base + r * kClRowBytes
+      const int row = quad * 32 + lane;
+#pragma unroll
+      for (int h = 0; h < kRsTileN / 128; ++h) {
+        uint32_t r[128];
+        tmem_ld_x128(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(h * 128), r);
+        const uint32_t dst = base + (uint32_t)(row * kClRowBytes + h * 512);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16u * j),
+                       "r"(r[4 * j]), "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
+                       : "memory");
+      }
+    }
+    epilogue_sync();
+    if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 2);
+    // one arrival per CTA on every CTA's `staged` barrier (this one's too)
+    if (warp == 4 && lane < splits) {
+      asm volatile("fence.acq_rel.cluster;" ::: "memory");
+      mbar_arrive_remote(mapa_shared(bar_staged, (uint32_t)lane));
+    }
+    if (ok) ok = cluster_wait(W, bar_staged, 0u, false);
+    if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 3);
+    if (ok) {
+      // rows [rank * R, rank * R + R) of the tile (R = 128 / splits), R / 4
+      // per warp; lane l sums columns 8l .. 8l + 7
+      if (splits == 2)
+        cluster_reduce_rows<2>(a, t.tm, t.tn, base, rank, quad, lane, my_keep, a.N,
+                                 kClRowBytes);
+      else if (splits == 4)
+        cluster_reduce_rows<4>(a, t.tm, t.tn, base, rank, quad, lane, my_keep, a.N,
+                                 kClRowBytes);
+      else
+        cluster_reduce_rows<8>(a, t.tm, t.tn, base, rank, quad, lane, my_keep, a.N,
+                                 kClRowBytes);
+    }
+    // this CTA's reads of its peers are done: tell every CTA, and stay until
+    // every peer has read this one's partial
+    epilogue_sync();
+    if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 4);
+    if (warp == 4 && lane < splits) mbar_arrive_remote(mapa_shared(bar_done, (uint32_t)lane));
+    cluster_wait(W, bar_done, 0u, true);
+    if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 5);
   } else if (warp >= 4) {
     // ----------------------------------------------------------- epilogue --
     // Warp q owns tile rows 32q .. 32q + 31 (its TMEM lane quadrant).
@@ -574,17 +802,58 @@ __global__ void keep_index_chunks_kernel(const int32_t* __restrict__ cu_p,
 
 int rowsparse_smem_bytes() { return kSmemBytes; }
 
+bool rowsparse_clusters_fit(int splits, int clusters) {
+  if (splits < 2 || splits > 8 || (splits & (splits - 1)) != 0) return false;
+  auto k = rowsparse_kernel<1, true>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
+    return false;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(splits * clusters));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return n >= clusters;
+}
+
 cudaError_t launch_rowsparse(const CUtensorMap& map_a, const CUtensorMap& map_b,
                              const CUtensorMap& map_o, const CUtensorMap& map_p,
                              const CUtensorMap& map_xt, const RsArgs& a, int grid,
                              cudaStream_t st) {
   void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
             const CUtensorMap, const RsArgs) =
-      a.mode == 0 ? rowsparse_kernel<0> : rowsparse_kernel<1>;
+      a.mode == 0 ? rowsparse_kernel<0, false>
+                  : (a.cluster ? rowsparse_kernel<1, true> : rowsparse_kernel<1, false>);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3(grid), dim3(kThreads), kSmemBytes, st, map_a, map_b, map_o, map_p,
-                    map_xt, a);
+  if (!a.cluster)
+    return launch_pdl(k, dim3(grid), dim3(kThreads), kSmemBytes, st, map_a, map_b, map_o, map_p,
+                      map_xt, a);
+  // one cluster per tile, its `splits` CTAs consecutive in x
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)a.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, map_a, map_b, map_o, map_p, map_xt, a);
 }
 
 cudaError_t launch_keep_index_chunks(const int32_t* cu_p, const int32_t* cu_c, int batch,

@@ -35,6 +35,10 @@ struct RsArgs {
   unsigned* counters;       // splits > 1: [tiles][4 lane quadrants], zero before the launch
   int* status;              // workspace status word
   unsigned long long limit_ns;
+  int cluster;              // mode 1, splits > 1: the splits of a tile are one cluster of
+                            // `splits` CTAs that sum their partials over distributed
+                            // shared memory (no partials in global memory, no counters);
+                            // CTA 0 then clears the status word itself
 };
 
 int rowsparse_smem_bytes();
@@ -47,6 +51,10 @@ int rowsparse_smem_bytes();
 // 256] fp32 in 32 x 32 boxes, used when splits > 1 (both 128-byte swizzled).
 // map_xt: mode 0 X [n_rows, in] in 64 x 64 boxes (stages whose kept rows are
 // one run of consecutive rows).
+// Whether `clusters` clusters of `splits` CTAs of the mode-1 kernel can be
+// resident at once on this device (the cluster path needs every split of
+// every tile running together).
+bool rowsparse_clusters_fit(int splits, int clusters);
 cudaError_t launch_rowsparse(const CUtensorMap& map_a, const CUtensorMap& map_b,
                              const CUtensorMap& map_o, const CUtensorMap& map_p,
                              const CUtensorMap& map_xt, const RsArgs& a, int grid,

@@ -8,6 +8,8 @@ most 2^-9 relative per element): checked at Frobenius-relative 4e-3 and
 normwise-max 8e-3.  Keep indices are integers: the rows written must be
 exactly the kept ones.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -241,3 +243,63 @@ def test_qwen3_8b_projection_shapes_at_full_size():
         ref = rs.rowsparse_dx(dy, w, keep.numpy(), n_rows)[n_rows - n_keep:]
         assert _rel(got, ref) <= TOL_BF16 and _maxrel(got, ref) <= TOL_BF16_MAX
         assert torch.count_nonzero(dx[: n_rows - n_keep]) == 0
+
+
+def _dx_with(env_cluster, dy, w, keep, n_rows, d_in):
+    from frozen_prefix_chunk_gb300 import rowsparse as R
+    import frozen_prefix_chunk_gb300 as cfa
+    old = os.environ.get("CFA_RS_CLUSTER")
+    os.environ["CFA_RS_CLUSTER"] = env_cluster
+    try:
+        dx = torch.full((n_rows, d_in), SENTINEL, dtype=torch.bfloat16, device="cuda")
+        dx, ws = R.dx(dy, w, keep, dx)
+        torch.cuda.synchronize()
+        return dx, cfa.read_status(ws), ws
+    finally:
+        if old is None:
+            del os.environ["CFA_RS_CLUSTER"]
+        else:
+            os.environ["CFA_RS_CLUSTER"] = old
+
+
+@pytest.mark.parametrize("shape", [(4096, 256, 4096, 512), (3000, 200, 8192, 1024)],
+                         ids=["m256", "m200"])
+def test_dx_split_k_cluster_path_equals_global_path(shape):
+    """dX split K runs as one cluster per tile (partials summed over
+    distributed shared memory) where the splits fit; the sums are the same, in
+    the same order, as the global-memory path's: bitwise equal outputs."""
+    x, w, dy, keep = _inputs(*shape, seed=sum(shape) + 7, sort=False)
+    n_rows, n_keep, d_in, d_out = shape
+    a, st_a, _ = _dx_with("1", dy.cuda(), w.cuda(), keep.cuda(), n_rows, d_in)
+    b, st_b, _ = _dx_with("0", dy.cuda(), w.cuda(), keep.cuda(), n_rows, d_in)
+    assert st_a == 0 and st_b == 0
+    assert torch.equal(a, b)
+    got = a.double().cpu().numpy()
+    ref = rs.rowsparse_dx(dy, w, keep.numpy(), n_rows)
+    kept = np.zeros(n_rows, dtype=bool)
+    kept[keep.numpy()] = True
+    assert np.all(got[~kept] == SENTINEL)
+    assert _rel(got[kept], ref[kept]) <= TOL_BF16 and _maxrel(got[kept], ref[kept]) <= TOL_BF16_MAX
+
+
+def test_dx_cluster_path_reports_a_bad_index_and_the_next_call_starts_clean():
+    x, w, dy, keep = _inputs(500, 40, 8192, 512, seed=11)
+    bad = keep.clone()
+    bad[5] = 500
+    bad[33] = -1
+    dx, st, ws = _dx_with("1", dy.cuda(), w.cuda(), bad.cuda(), 500, 8192)
+    assert st == -1
+    ok = np.ones(40, dtype=bool)
+    ok[[5, 33]] = False
+    good = keep.numpy()[ok]
+    got = dx.double().cpu().numpy()
+    ref = rs.rowsparse_dx(dy[ok], w, good, 500)
+    assert _rel(got[good], ref[good]) <= TOL_BF16
+    rest = np.ones(500, dtype=bool)
+    rest[good] = False
+    assert np.all(got[rest] == SENTINEL)
+    from frozen_prefix_chunk_gb300 import rowsparse as R
+    import frozen_prefix_chunk_gb300 as cfa
+    d2 = torch.zeros(500, 8192, dtype=torch.bfloat16, device="cuda")
+    R.dx(dy.cuda(), w.cuda(), keep.cuda(), d2, ws=ws)
+    assert cfa.read_status(ws) == 0
