@@ -624,6 +624,30 @@ class AttnStep:
         if ev:
             ev[3].record(s)
 
+    def capture(self):
+        """Capture one step (the same C-ABI calls, on a side stream) into a
+        CUDA graph; replay() then launches the whole step at once.  The
+        library's calls are capture-safe: no host synchronisation, no
+        allocation, its second stream forked and joined with events."""
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step()  # first call on this stream: outside the capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=s, capture_error_mode="relaxed"):
+            self.step()
+        torch.cuda.synchronize()
+
+    def replay(self, ev=None):
+        s = self.stream
+        if ev:
+            ev[0].record(s)
+        self.graph.replay()
+        if ev:
+            ev[3].record(s)
+
     def check_status(self):
         for ws in (self.ws_f, self.ws_b):
             st = self.cfa.read_status(ws)
@@ -634,18 +658,40 @@ class AttnStep:
         return outs + ([self.dkp, self.dvp] if self.horizon else [])
 
 
-def time_steps(case, steps, warmup, flush, world, dev, sampler_index=None):
+def time_steps(case, steps, warmup, flush, world, dev, sampler_index=None, launch="graph"):
     """W untimed warm-up steps, then exactly `steps` steps, each bracketed by
     CUDA events on the launching stream, L2 flushed before each outside the
-    events; barrier + synchronize on both sides.  Returns per-step lists of
-    the step, forward and backward times (ms), the slowest rank's total, the
-    clock record and the wall time of the timed loop."""
+    events; barrier + synchronize on both sides.  launch = "graph": the step
+    is captured once as a CUDA graph and each timed step is one replay (the
+    forward / backward split then comes from a short run of stream-launched
+    steps before the timed region, which is also reported); "stream": each
+    timed step launches the calls one by one.  Returns per-step lists of the
+    step, forward and backward times (ms), the slowest rank's total, the
+    clock record, the wall time of the timed loop and the stream-launched
+    step times."""
     import torch.distributed as dist
     for _ in range(warmup):
         flush()
         case.step()
     torch.cuda.synchronize()
     case.check_status()
+
+    def stream_run(n):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        for k in range(n):
+            flush()
+            case.step(evs[k])
+        torch.cuda.synchronize()
+        return evs
+
+    split = None
+    if launch == "graph":
+        split = stream_run(min(steps, 50))
+        case.capture()
+        for _ in range(3):
+            flush()
+            case.replay()
+        torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     if world > 1:
         dist.barrier()
@@ -654,7 +700,10 @@ def time_steps(case, steps, warmup, flush, world, dev, sampler_index=None):
     t_wall = time.perf_counter()
     for k in range(steps):
         flush()
-        case.step(evs[k])
+        if launch == "graph":
+            case.replay(evs[k])
+        else:
+            case.step(evs[k])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     clocks = sampler.stop() if sampler else None
@@ -662,11 +711,13 @@ def time_steps(case, steps, warmup, flush, world, dev, sampler_index=None):
         dist.barrier()
     case.check_status()
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    sp = split if split is not None else evs
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in sp]
+    bwd_ms = [e[2].elapsed_time(e[3]) for e in sp]
+    stream_ms = [e[0].elapsed_time(e[3]) for e in sp]
     tot_ms = slowest_rank_ms(sum(step_ms), world, dev)
     return dict(step_ms=step_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, tot_ms=tot_ms, clocks=clocks,
-                wall_s=t_wall)
+                wall_s=t_wall, stream_ms=stream_ms, launch=launch)
 
 
 def summarise(case, t, steps, world, dev, peaks, peak_src):
@@ -696,7 +747,13 @@ def summarise(case, t, steps, world, dev, peaks, peak_src):
                  "bwd_tflops": (flops["dq_kernel"] + flops["dkdv_kernel"]) / (bwd_mean * 1e-3) / 1e12,
                  "fwd_tflops": flops["fwd"] / (fwd_mean * 1e-3) / 1e12,
                  "useful_gflop": flops["total"] / 1e9, "algorithmic_mb": byts["total"] / 1e6,
-                 "peaks": f"bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s ({peak_src})"}
+                 "peaks": f"bf16 {bf16_peak} TFLOP/s, HBM {hbm_peak} GB/s ({peak_src})",
+                 "launch": t["launch"]}
+    if t["launch"] == "graph":
+        # the same step with the calls launched one by one on the stream
+        st_ms = statistics.mean(t["stream_ms"])
+        step_roof["stream_launch"] = {"ms_per_step": st_ms, "frac": t_roof / (st_ms * 1e-3),
+                                      "steps": len(t["stream_ms"])}
     return ms_per_step, value, roofline, step_roof
 
 
@@ -743,6 +800,9 @@ def main():
     ap.add_argument("--q8", default="product", choices=["product", "export"],
                     help="q8_0 prefix: handed to the library as it is, or expanded once per "
                          "step through cfa_dequant_q8_0 and read as bf16")
+    ap.add_argument("--launch", default="graph", choices=["graph", "stream"],
+                    help="each timed step: one replay of the step captured as a CUDA graph "
+                         "(through the same C-ABI calls), or the calls launched one by one")
     ap.add_argument("--flush", default="write+read", choices=["write", "write+read"],
                     help="how L2 is evicted before each timed step")
     ap.add_argument("--rowsparse", action="store_true",
@@ -805,7 +865,8 @@ def main():
                 t = torch.tensor([n], dtype=torch.int64, device=dev)
                 dist.all_reduce(t, op=dist.ReduceOp.MAX)
                 n = int(t.item())
-            t = time_steps(case, n, args.warmup, flush, world, dev, sampler_index=local)
+            t = time_steps(case, n, args.warmup, flush, world, dev, sampler_index=local,
+                           launch=args.launch)
             ms, val, roof, sroof = summarise(case, t, n, world, dev, peaks, peak_src)
             extras[name] = {"value": val, "unit": "TFLOP/s", "ms_per_step": ms, "steps": n,
                             "step_roofline": sroof, "roofline": roof,
@@ -816,7 +877,8 @@ def main():
 
     # ---- the headline workload: exactly K timed steps
     case = make_case(args.workload, args.horizon)
-    t = time_steps(case, args.steps, args.warmup, flush, world, dev, sampler_index=local)
+    t = time_steps(case, args.steps, args.warmup, flush, world, dev, sampler_index=local,
+                   launch=args.launch)
     ms_per_step, value, roofline, step_roof = summarise(case, t, args.steps, world, dev, peaks,
                                                         peak_src)
 
@@ -864,6 +926,9 @@ def main():
                 "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
                 "gpu_launches": case.launches * args.steps,
+                "launch": ("cuda_graph (one step captured through the C-ABI calls, one replay "
+                           "per timed step; step_roofline.stream_launch has the same step "
+                           "launched call by call)" if args.launch == "graph" else "stream"),
                 "clocks": t["clocks"], "wall_s_timed": t["wall_s"],
                 "target_step_fracs": fracs, "extra": extras}
         print(json.dumps(line), flush=True)

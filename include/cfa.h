@@ -51,6 +51,16 @@
  * max_*, total_*) must agree with the device cu_seqlens; they size the grids
  * and the TMA descriptors, so no device-to-host read is needed.
  *
+ * CUDA graphs: cfa_forward, cfa_backward_preprocess, cfa_backward(_horizon),
+ * and cfa_dequant_q8_0 can be captured into a CUDA graph
+ * (stream capture on a non-default stream; the side stream of the backward
+ * joins the capture through its fork / join events).  The TMA descriptors
+ * are built at call time and captured as kernel parameters, so a replay
+ * works on the buffers and sizes of the captured calls.  Make one call of
+ * each kind before the capture: the first cfa_backward on a device creates
+ * the library's second stream.  A replay gives bitwise the outputs of the
+ * same calls launched one by one, and its status word reads as after them.
+ *
  * Errors: every entry point returns CFA_OK (0) or a negative cfa_status and
  * never aborts.  Argument errors are found on the host before anything is
  * enqueued.  A device-side wait that does not finish in time (default 2 s;

@@ -1,0 +1,41 @@
+"""A whole fwd+bwd step captured as a CUDA graph and replayed.
+
+cfa_forward, cfa_backward_preprocess and cfa_backward do no host
+synchronisation and no allocation, and fork / join their second stream with
+events, so a caller can capture them into a CUDA graph (the benchmark times
+the step that way).  The replays must give bitwise the outputs of the same
+calls launched one by one, for the bf16 and the q8_0 prefix, and leave the
+device status clean.
+"""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["qwen3_1p7b", "tiny"])
+@pytest.mark.parametrize("mode", ["bf16", "q8_product", "q8_export"])
+def test_graph_replay_equals_stream_launches(name, mode):
+    import bench
+    import synth
+    dev = torch.device("cuda", 0)
+    w = synth.workload(name, seed=0)
+    if mode != "bf16":
+        w.prefix_dtype = synth.PREFIX_Q8_0
+    case = bench.AttnStep(w, dev, 0, "export" if mode == "q8_export" else "product")
+    for _ in range(2):
+        case.step()
+    torch.cuda.synchronize()
+    case.check_status()
+    ref = [t.clone() for t in case.outputs()]
+    for t in case.outputs():
+        t.fill_(0)
+    case.capture()
+    for t in case.outputs():
+        t.fill_(0)
+    for _ in range(3):
+        case.replay()
+    torch.cuda.synchronize()
+    case.check_status()
+    for a, b in zip(ref, case.outputs()):
+        assert torch.equal(a, b)
