@@ -74,11 +74,11 @@ struct Maps {
 // Launch `k` so that it may overlap the tail of the previous kernel in the
 // stream (programmatic stream serialisation); the kernel itself waits for that
 // kernel's completion in pdl_start() before touching memory.  Used for the
-// persistent kernels only (attention and row-sparse GEMM: one CTA per SM,
-// placed as the previous grid's CTAs leave): a small grid launched this way
-// would pile onto the first SMs to free up and run on a fraction of the GPU
-// (measured: the split merge after the forward slowed by ~4 us; triggering
-// dependents only at the end of each kernel instead did not help either).
+// persistent kernels (attention and row-sparse GEMM: one CTA per SM, placed
+// as the previous grid's CTAs leave) and the delta kernel.  The split merge
+// and the dQ reduce keep normal launches: launched this way the merge piled
+// onto the first SMs to free up (~4 us slower), and the reduce's waiting CTAs
+// held SMs that the dK/dV kernel beside the dQ kernel needed.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args&&... args) {
