@@ -92,7 +92,9 @@ __global__ void __launch_bounds__(320, 1)
                   const __grid_constant__ CUtensorMap map_vp,
                   const __grid_constant__ CUtensorMap map_kc,
                   const __grid_constant__ CUtensorMap map_vc, const BwdArgs a) {
+  CFA_TRACE_SPAN(2, 0);
   pdl_start();
+  CFA_TRACE_SPAN(2, 1);
   // A call's first kernel clears the status word once the previous work in
   // the stream is done (no separate memset: one dependent launch less).  A
   // device wait gives up only after its wall-clock limit, long after CTA 0
@@ -461,6 +463,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
+  CFA_TRACE_SPAN(2, 2);
 }
 
 template <int D>
@@ -532,7 +535,9 @@ __global__ void __launch_bounds__(320, 1)
                     const __grid_constant__ CUtensorMap map_vc,
                     const __grid_constant__ CUtensorMap map_kp,
                     const __grid_constant__ CUtensorMap map_vp, const BwdArgs a) {
+  CFA_TRACE_SPAN(5, 0);
   pdl_start();
+  CFA_TRACE_SPAN(5, 1);
   // clears the status word when this kernel is its call's first (see the dQ kernel)
   if (a.clear_status && blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0;
   using C = DkvCfg<D>;
@@ -885,6 +890,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
+  CFA_TRACE_SPAN(5, 2);
 }
 
 // Sum the dQ partials of every query tile that CTA boundaries cut, in CTA
@@ -896,7 +902,9 @@ constexpr int kReduceRows = 32;
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
+  CFA_TRACE_SPAN(3, 0);
   pdl_start();
+  CFA_TRACE_SPAN(3, 1);
   // the dQ kernel found inconsistent cu_seqlens (or gave up on a wait): its
   // partials and prefix arrays were not written
   if (*reinterpret_cast<volatile int*>(a.status) != 0) return;
@@ -961,6 +969,7 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
     dst[e / 8] = make_uint4(pack_bf16x2(acc[e], acc[e + 1]), pack_bf16x2(acc[e + 2], acc[e + 3]),
                             pack_bf16x2(acc[e + 4], acc[e + 5]),
                             pack_bf16x2(acc[e + 6], acc[e + 7]));
+  CFA_TRACE_SPAN(3, 2);
 }
 
 // delta[h, t] = sum_c dO[t, h, c] * O[t, h, c].  A CTA takes kDeltaRows
@@ -973,7 +982,9 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
                                                     const __nv_bfloat16* __restrict__ dout,
                                                     float* __restrict__ delta, int total_lc,
                                                     int hq) {
+  CFA_TRACE_SPAN(4, 0);
   pdl_start();
+  CFA_TRACE_SPAN(4, 1);
   constexpr int TPR = D / 8;              // threads per row
   constexpr int RPP = 256 / TPR;          // rows per pass of the CTA
   constexpr int NP = kDeltaRows / RPP;    // passes
@@ -1006,6 +1017,7 @@ __global__ void __launch_bounds__(256) delta_kernel(const __nv_bfloat16* __restr
     const long long t = (long long)blockIdx.x * kDeltaRows + p * RPP + sub;
     if (part == 0 && t < total_lc) delta[(size_t)h * total_lc + t] = sum;
   }
+  CFA_TRACE_SPAN(4, 2);
 }
 
 // q8_0 -> fp32 (exact) and bf16 (round to nearest even), one thread per value.
@@ -1067,7 +1079,9 @@ __global__ void __launch_bounds__(kDqWarps * 32)
     dequant_prefix_kernel(const uint8_t* __restrict__ k_blocks, const uint8_t* __restrict__ v_blocks,
                           long long n_blocks, __nv_bfloat16* __restrict__ k_out,
                           __nv_bfloat16* __restrict__ v_out) {
+  CFA_TRACE_SPAN(6, 0);
   pdl_start();
+  CFA_TRACE_SPAN(6, 1);
   __shared__ uint4 in_st[kDqWarps][68];
   __shared__ uint4 out_st[kDqWarps][128];
   const uint8_t* src = blockIdx.y ? v_blocks : k_blocks;
@@ -1117,6 +1131,7 @@ __global__ void __launch_bounds__(kDqWarps * 32)
     for (int j = lane; j < nb * 4; j += 32) dst[j] = out_st[warp][dq_stage_slot(j)];
     __syncwarp();
   }
+  CFA_TRACE_SPAN(6, 2);
 }
 
 // bf16 -> q8_0 (the cache write of the walk: the chunk's K/V appended to a
@@ -1373,6 +1388,18 @@ extern "C" int cfa_trace_read_bwd(long long* dst, int clear) {
   if (clear) {
     static long long zero[cfa::kTraceRoles * cfa::kTraceIters * cfa::kTraceEvents];
     if (cudaMemcpyToSymbol(cfa::cfa_trace_buf, zero, n) != cudaSuccess) return -1;
+  }
+  return 0;
+}
+// Kernel spans of this translation unit's kernels; reset = 1 re-arms them.
+extern "C" int cfa_trace_read_span_bwd(unsigned long long* dst, int reset) {
+  if (dst && cudaMemcpyFromSymbol(dst, cfa::cfa_trace_span, sizeof(unsigned long long) * 24) !=
+                 cudaSuccess)
+    return -1;
+  if (reset) {
+    unsigned long long init[24];
+    for (int i = 0; i < 24; ++i) init[i] = (i % 3 == 2) ? 0ull : ~0ull;
+    if (cudaMemcpyToSymbol(cfa::cfa_trace_span, init, sizeof(init)) != cudaSuccess) return -1;
   }
   return 0;
 }

@@ -98,7 +98,9 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_base);
 
+  CFA_TRACE_SPAN(0, 0);
   pdl_start();
+  CFA_TRACE_SPAN(0, 1);
   // A call's first kernel clears the status word once the previous work in
   // the stream is done (no separate memset: one dependent launch less).  A
   // device wait gives up only after its wall-clock limit, long after CTA 0
@@ -528,6 +530,7 @@ __global__ void __launch_bounds__(352, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
+  CFA_TRACE_SPAN(0, 2);
 }
 
 // Merge the partials of every query block that CTA boundaries cut.  One CTA
@@ -553,7 +556,9 @@ static __device__ unsigned long long cfa_trace_merge[4 * 1024];
 
 template <int D>
 __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
+  CFA_TRACE_SPAN(1, 0);
   pdl_start();
+  CFA_TRACE_SPAN(1, 1);
   // the forward kernel found inconsistent cu_seqlens (or gave up on a wait):
   // its partials and prefix arrays were not written
   if (*reinterpret_cast<volatile int*>(a.status) != 0) return;
@@ -692,6 +697,7 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const FwdArgs a) {
                             pack_bf16x2(acc[e + 6], acc[e + 7]));
   if (threadIdx.x < 32) a.lse[(size_t)head * a.total_lc + grow] = lse;
   CFA_TRACE_MERGE(3);
+  CFA_TRACE_SPAN(1, 2);
 }
 
 }  // namespace
@@ -750,6 +756,18 @@ extern "C" int cfa_trace_read_fwd(long long* dst, int clear) {
   if (clear) {
     static long long zero[cfa::kTraceRoles * cfa::kTraceIters * cfa::kTraceEvents];
     if (cudaMemcpyToSymbol(cfa::cfa_trace_buf, zero, n) != cudaSuccess) return -1;
+  }
+  return 0;
+}
+// Kernel spans of this translation unit's kernels; reset = 1 re-arms them.
+extern "C" int cfa_trace_read_span_fwd(unsigned long long* dst, int reset) {
+  if (dst && cudaMemcpyFromSymbol(dst, cfa::cfa_trace_span, sizeof(unsigned long long) * 24) !=
+                 cudaSuccess)
+    return -1;
+  if (reset) {
+    unsigned long long init[24];
+    for (int i = 0; i < 24; ++i) init[i] = (i % 3 == 2) ? 0ull : ~0ull;
+    if (cudaMemcpyToSymbol(cfa::cfa_trace_span, init, sizeof(init)) != cudaSuccess) return -1;
   }
   return 0;
 }

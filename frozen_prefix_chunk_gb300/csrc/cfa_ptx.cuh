@@ -40,7 +40,22 @@ static __device__ unsigned long long cfa_trace_cta[2 * 1024];  // per-CTA start 
       cfa::cfa_trace_buf[((role) * cfa::kTraceIters + (iter)) * cfa::kTraceEvents + (ev)] = \
           clock64();                                                                       \
   } while (0)
+// Kernel spans (ns): per kernel id, the first CTA's arrival (ev 0), the first
+// CTA past its wait for the previous kernel (ev 1), the last CTA's end (ev 2).
+static __device__ unsigned long long cfa_trace_span[8 * 3];
+#define CFA_TRACE_SPAN(kid, ev)                                                           \
+  do {                                                                                    \
+    if (threadIdx.x == 0) {                                                               \
+      if ((ev) < 2)                                                                       \
+        atomicMin(&cfa::cfa_trace_span[3 * (kid) + (ev)], cfa::global_timer_ns_raw());    \
+      else                                                                                \
+        atomicMax(&cfa::cfa_trace_span[3 * (kid) + (ev)], cfa::global_timer_ns_raw());    \
+    }                                                                                     \
+  } while (0)
 #else
+#define CFA_TRACE_SPAN(kid, ev) \
+  do {                          \
+  } while (0)
 #define CFA_TRACE(role, iter, ev) \
   do {                            \
   } while (0)
