@@ -905,9 +905,6 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
   CFA_TRACE_SPAN(3, 0);
   pdl_start();
   CFA_TRACE_SPAN(3, 1);
-  // the dQ kernel found inconsistent cu_seqlens (or gave up on a wait): its
-  // partials and prefix arrays were not written
-  if (*reinterpret_cast<volatile int*>(a.status) != 0) return;
   constexpr int CW = D / 8;
   const Tiling tl = a.tl;
   const int chunks = kTileM / kReduceRows;
@@ -915,12 +912,18 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const BwdArgs a) {
   const int qb = blockIdx.x / chunks;
   const int row = (blockIdx.x % chunks) * kReduceRows + (threadIdx.x & 31);
   const int c0col = (threadIdx.x >> 5) * CW;
-  // the block's schedule row: its prefix array and its first CTA
+  // the block's schedule row: its prefix array and its first CTA.  The status
+  // word and the index loads go out together (one round trip, not two); the
+  // indices are in bounds whatever the status says.
   const int srow = row_of_block(tl, qb), rg = row_grid(tl);
   const long long* wp = a.win_prefix + (size_t)srow * (a.batch + 1);
+  const int status = *reinterpret_cast<volatile int*>(a.status);
   const long long w0 = wp[b], total = wp[a.batch];
   const int p0 = a.cu_p[b], lp = a.cu_p[b + 1] - p0;
   const int c0 = a.cu_c[b], lc = a.cu_c[b + 1] - c0;
+  // the dQ kernel found inconsistent cu_seqlens (or gave up on a wait): its
+  // partials and prefix arrays were not written
+  if (status != 0) return;
   if (qb >= blocks_of_window(tl, lc)) return;
   // the tile's parts (every thread finds them; no shared list, no barrier)
   long long bs, be;

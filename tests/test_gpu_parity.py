@@ -71,6 +71,33 @@ def test_deterministic_and_forward_independent_of_backward():
     assert torch.equal(a["o"], c["o"]) and torch.equal(a["lse"], c["lse"])
 
 
+def test_backward_workspace_contents_do_not_matter():
+    """Everything the backward keeps in its workspace (the schedule's prefix
+    arrays, the fp32 partials of the query tiles that CTA boundaries cut, the
+    status word) is written in the call before it is read: a workspace full
+    of arbitrary bytes, one reused by earlier calls and a fresh one give
+    bitwise the same results."""
+    import frozen_prefix_chunk_gb300 as cfa
+    inp = synth.make_inputs(synth.custom(hq=8, hkv=2, head_dim=128, lp=[5000, 700, 0],
+                                         lc=[200, 129, 64], seed=4))
+    ref = gu.run_cuda(inp)
+    d = gu.to_device(inp)
+    args = gu.make_args(d)
+    o, lse, _ = cfa.forward(args, d["q"])
+    delta = cfa.backward_preprocess(args, o, d["dout"])
+    n = cfa.workspace_size(args, cfa.WS_BACKWARD)
+    g = torch.Generator(device="cuda").manual_seed(1)
+    for fill in ("random", "ones", "reused", "reused"):
+        if fill == "random":
+            ws = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda", generator=g)
+        elif fill == "ones":
+            ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")
+        dq, dk, dv, ws = cfa.backward(args, d["dout"], lse, delta, ws=ws)
+        assert cfa.read_status(ws) == 0
+        assert torch.equal(dq.cpu(), ref["dq"]), fill
+        assert torch.equal(dk.cpu(), ref["dk"]) and torch.equal(dv.cpu(), ref["dv"]), fill
+
+
 def test_dequant_q8_0_bit_exact():
     import frozen_prefix_chunk_gb300 as cfa
     x = torch.randn(4096, 128, generator=torch.Generator().manual_seed(9)) * 3
