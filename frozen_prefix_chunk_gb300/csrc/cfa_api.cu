@@ -445,6 +445,40 @@ int dkdv_share(const cfa_args* a, const Tiling& tl, int sms, long long items, in
   return k < 1 ? 1 : (int)k;
 }
 
+// With equal chunk lengths and no horizon the dK/dV items' costs are known
+// exactly (the same per-step costs as above; item j walks the query tiles from
+// its key tile's on), so the share can shrink to the fewest CTAs whose
+// busiest one (items c, c + k, ...) is no busier than with k: those SMs go to
+// the dQ grid at no cost to the dK/dV kernel (qwen3_8b: 16 items, 5 -> 4).
+int trim_dkdv_share(const cfa_args* a, const Tiling& tl, int k, long long items, int horizon) {
+  if (horizon != 0 || k <= 1 || items > 65536 ||
+      (long long)a->total_lc != (long long)a->batch * a->max_lc)
+    return k;
+  const long long per_slot = (long long)a->batch * a->hkv;
+  const int qt = ceil_div(a->max_lc, tl.tpt);
+  auto cost = [&](long long j) -> long long {
+    const int key0 = (int)(j / per_slot) * kTileN;
+    if (key0 >= a->max_lc) return 0;
+    return 3000LL * (qt - key0 / tl.tpt) + 4000;
+  };
+  auto busiest = [&](int kk) {
+    long long worst = 0;
+    for (int c = 0; c < kk; ++c) {
+      long long sum = 0;
+      for (long long j = c; j < items; j += kk) sum += cost(j);
+      worst = sum > worst ? sum : worst;
+    }
+    return worst;
+  };
+  const long long target = busiest(k);
+  int best = k;
+  for (int kk = k - 1; kk >= 1; --kk) {
+    if (busiest(kk) > target) break;
+    best = kk;
+  }
+  return best;
+}
+
 // The second stream and the fork / join events cfa_backward uses to run the
 // dK/dV kernel beside the dQ kernel, one set per device, made on first use.
 struct SideStream {
@@ -525,7 +559,8 @@ int cfa_backward_horizon(const cfa_args* a, int horizon, const void* dout, const
   // its own, on a second stream forked from and joined back into `s`, while
   // the dQ kernel's persistent grid takes the rest.
   const long long items = dkdv_items(a, ba);
-  int k = dkdv_share(a, p.dq, p.dq.grid, items, ba.horizon);
+  int k = trim_dkdv_share(a, p.dq, dkdv_share(a, p.dq, p.dq.grid, items, ba.horizon), items,
+                          ba.horizon);
   // row mode for the dQ kernel: give the dK/dV kernel a few SMs more, if that
   // makes the rows divide the dQ grid
   for (int k2 = k; k2 <= k + 16 && k2 <= p.dq.grid / 2; ++k2) {
