@@ -41,7 +41,24 @@ EDGE = [
     dict(hq=8, hkv=1, head_dim=128, lp=[1000], lc=[200]),     # g = 8
     dict(hq=4, hkv=2, head_dim=128, lp=[5, 0, 700, 128], lc=[37, 100, 0, 256]),  # varlen + empty
     dict(hq=2, hkv=2, head_dim=64, lp=[4096], lc=[3]),        # long prefix, many splits
+    dict(hq=16, hkv=1, head_dim=128, lp=[700], lc=[50]),      # g = 16: 8-token tiles
+    dict(hq=128, hkv=1, head_dim=64, lp=[200], lc=[5]),       # g = 128, the largest group
 ]
+
+
+def _many_windows(n=600, seed=3):
+    # more windows than the persistent kernels have threads, most of them
+    # tiny and many empty: the schedule scan takes several windows per thread
+    r = np.random.RandomState(seed)
+    lp = r.randint(0, 49, size=n)
+    lc = r.randint(0, 7, size=n)
+    lp[::5] = 0
+    lc[1::7] = 0
+    lc[0] = 3
+    return dict(hq=4, hkv=2, head_dim=64, lp=lp.tolist(), lc=lc.tolist())
+
+
+EDGE.append(_many_windows())
 
 
 @pytest.mark.parametrize("cfg", EDGE, ids=[str(i) for i in range(len(EDGE))])
