@@ -42,8 +42,9 @@
  * bits); the bf16 that a kernel multiplies with is that value rounded to
  * nearest, ties to even.  The attention itself uses the exact values.
  *
- * `mutation` plants one deliberate mistake (0 = none).  Only the tests that
- * check that the pins catch such mistakes pass a non-zero value.
+ * This file is the plain definition and nothing else.  The tests that check
+ * that the pins catch mistakes compile copies of it with a mistake planted by
+ * a textual edit (tests/oracle_mutants.py).
  */
 #include <math.h>
 #include <stdint.h>
@@ -56,14 +57,8 @@
 /* ---- number formats, from their definitions ---------------------------- */
 
 /* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
-static double half_bits_to_double(uint16_t h, int mutation)
+static double half_bits_to_double(uint16_t h)
 {
-    if (mutation == 11) {            /* planted: read the scale as bf16 bits */
-        uint32_t u = (uint32_t)h << 16;
-        float f;
-        memcpy(&f, &u, 4);
-        return (double)f;
-    }
     int sign = (h >> 15) & 1;
     int e = (h >> 10) & 0x1f;
     int m = h & 0x3ff;
@@ -95,14 +90,14 @@ static uint16_t float_to_bf16_rne(float x)
  * block in order.
  */
 void cfa_oracle_dequant_q8_0(const uint8_t *blocks, long n_blocks, double *out_f64,
-                             float *out_f32, uint16_t *out_bf16, int mutation)
+                             float *out_f32, uint16_t *out_bf16)
 {
     for (long b = 0; b < n_blocks; ++b) {
         const uint8_t *blk = blocks + 34 * b;
         uint16_t hbits = (uint16_t)(blk[0] | (blk[1] << 8));
-        double d = half_bits_to_double(hbits, mutation);
+        double d = half_bits_to_double(hbits);
         for (int i = 0; i < 32; ++i) {
-            int qi = (mutation == 12) ? (int)blk[2 + i] : (int)(int8_t)blk[2 + i];
+            int qi = (int)(int8_t)blk[2 + i];
             double v = d * (double)qi;                 /* exact in double */
             long k = 32 * b + i;
             if (out_f64) out_f64[k] = v;
@@ -148,7 +143,7 @@ static uint16_t float_to_half_rne(float x)
  * q_i = x_i / d rounded half away from zero, clamped to [-127, 127]; the
  * stored scale is fp16(d), nearest even, little-endian.
  */
-void cfa_oracle_quantize_q8_0(const uint16_t *x_bf16, long n_blocks, uint8_t *out, int mutation)
+void cfa_oracle_quantize_q8_0(const uint16_t *x_bf16, long n_blocks, uint8_t *out)
 {
     for (long b = 0; b < n_blocks; ++b) {
         float v[32];
@@ -164,13 +159,11 @@ void cfa_oracle_quantize_q8_0(const uint16_t *x_bf16, long n_blocks, uint8_t *ou
         uint8_t *blk = out + 34 * b;
         blk[0] = (uint8_t)(dh & 0xff);
         blk[1] = (uint8_t)(dh >> 8);
-        float dq = d;
-        if (mutation == 16) dq = (float)half_bits_to_double(dh, 0);   /* planted: fp16 scale */
         for (int i = 0; i < 32; ++i) {
             int q = 0;
             if (d > 0.0f) {
-                const float r = v[i] / dq;
-                q = (mutation == 15) ? (int)rintf(r) : (int)roundf(r);   /* planted: ties to even */
+                const float r = v[i] / d;
+                q = (int)roundf(r);
                 q = q > 127 ? 127 : (q < -127 ? -127 : q);
             }
             blk[2 + i] = (uint8_t)(int8_t)q;
@@ -199,7 +192,7 @@ int cfa_oracle_group(int lp, int lc, int g, int d, double scale,
                      const double *q, const double *kp, const double *vp,
                      const double *kc, const double *vc, const double *dout,
                      double *o, double *lse, double *delta,
-                     double *dq, double *dkc, double *dvc, int mutation)
+                     double *dq, double *dkc, double *dvc)
 {
     const int nrow = lc * g;
     double *o_own = NULL, *lse_own = NULL, *delta_own = NULL;
@@ -227,29 +220,24 @@ int cfa_oracle_group(int lp, int lc, int g, int d, double scale,
             const int t = r / g, hh = r % g;
             const double *qt = q + (size_t)r * d;
             const double *dot_ = dout + (size_t)r * d;
-            /* visible chunk keys: j <= t (planted mistake 1: one future key) */
-            int nc = t + 1;
-            if (mutation == 1 && nc < lc) nc = t + 2;
+            const int nc = t + 1;                 /* visible chunk keys: j <= t */
             const int n = lp + nc;
             for (int j = 0; j < lp; ++j) S[j] = scale * dot(qt, kp + (size_t)j * d, d);
             for (int j = 0; j < nc; ++j) S[lp + j] = scale * dot(qt, kc + (size_t)j * d, d);
             double m = -INFINITY;
             for (int j = 0; j < n; ++j) m = S[j] > m ? S[j] : m;
             double sum = 0.0;
-            int j0 = (mutation == 9) ? lp : 0;       /* planted: drop prefix from the sum */
-            for (int j = j0; j < n; ++j) sum += exp(S[j] - m);
-            double L = (mutation == 7) ? m + log2(sum) : m + log(sum);
+            for (int j = 0; j < n; ++j) sum += exp(S[j] - m);
+            const double L = m + log(sum);
             lse[(size_t)hh * lc + t] = L;
             for (int j = 0; j < n; ++j) P[j] = exp(S[j] - L);
             double *ot = o + (size_t)r * d;
             for (int c = 0; c < d; ++c) ot[c] = 0.0;
             for (int j = 0; j < n; ++j) {
-                const double *vj = (mutation == 8)
-                    ? (j < lp ? kp + (size_t)j * d : kc + (size_t)(j - lp) * d)
-                    : (j < lp ? vp + (size_t)j * d : vc + (size_t)(j - lp) * d);
+                const double *vj = j < lp ? vp + (size_t)j * d : vc + (size_t)(j - lp) * d;
                 for (int c = 0; c < d; ++c) ot[c] += P[j] * vj[c];
             }
-            double dl = dot(dot_, ot, d);
+            const double dl = dot(dot_, ot, d);
             delta[(size_t)hh * lc + t] = dl;
             if (dq) {
                 double *dqt = dq + (size_t)r * d;
@@ -257,10 +245,9 @@ int cfa_oracle_group(int lp, int lc, int g, int d, double scale,
                 for (int j = 0; j < n; ++j) {
                     const double *vj = j < lp ? vp + (size_t)j * d : vc + (size_t)(j - lp) * d;
                     const double *kj = j < lp ? kp + (size_t)j * d : kc + (size_t)(j - lp) * d;
-                    if (mutation == 6) kj = vj;               /* planted: transposed operand */
-                    double dpj = dot(dot_, vj, d);
-                    double dsj = (mutation == 3) ? P[j] * (dpj + dl) : P[j] * (dpj - dl);
-                    double f = (mutation == 2) ? dsj : scale * dsj;
+                    const double dpj = dot(dot_, vj, d);
+                    const double dsj = P[j] * (dpj - dl);
+                    const double f = scale * dsj;
                     for (int c = 0; c < d; ++c) dqt[c] += f * kj[c];
                 }
             }
@@ -279,20 +266,17 @@ int cfa_oracle_group(int lp, int lc, int g, int d, double scale,
             if (dk) for (int c = 0; c < d; ++c) dk[c] = 0.0;
             if (dv) for (int c = 0; c < d; ++c) dv[c] = 0.0;
             for (int t = j; t < lc; ++t) {
-                for (int hh = 0; hh < g; ++hh) {
-                    if (mutation == 10 && hh > 0) continue;   /* planted: drop the group sum */
+                for (int hh = 0; hh < g; ++hh) {      /* the group's query heads */
                     const int r = t * g + hh;
                     const double *qt = q + (size_t)r * d;
                     const double *dot_ = dout + (size_t)r * d;
-                    double s = scale * dot(qt, kj, d);
-                    double p = exp(s - lse[(size_t)hh * lc + t]);
-                    double dp = dot(dot_, vj, d);
-                    double ds = p * (dp - delta[(size_t)hh * lc + t]);
-                    if (mutation == 3) ds = p * (dp + delta[(size_t)hh * lc + t]);
-                    double fk = (mutation == 5) ? ds : scale * ds;
-                    double fv = (mutation == 4) ? ds : p;
+                    const double s = scale * dot(qt, kj, d);
+                    const double p = exp(s - lse[(size_t)hh * lc + t]);
+                    const double dp = dot(dot_, vj, d);
+                    const double ds = p * (dp - delta[(size_t)hh * lc + t]);
+                    const double fk = scale * ds;
                     if (dk) for (int c = 0; c < d; ++c) dk[c] += fk * qt[c];
-                    if (dv) for (int c = 0; c < d; ++c) dv[c] += fv * dot_[c];
+                    if (dv) for (int c = 0; c < d; ++c) dv[c] += p * dot_[c];
                 }
             }
         }
@@ -322,25 +306,23 @@ int cfa_oracle_group(int lp, int lc, int g, int d, double scale,
 void cfa_oracle_group_prefix_grad(int lp, int lc, int g, int d, double scale,
                                   const double *q, const double *kp, const double *vp,
                                   const double *dout, const double *lse,
-                                  const double *delta, double *dkp, double *dvp,
-                                  int mutation)
+                                  const double *delta, double *dkp, double *dvp)
 {
 #pragma omp parallel for schedule(dynamic, 4)
     for (int j = 0; j < lp; ++j) {
         const double *kj = kp + (size_t)j * d, *vj = vp + (size_t)j * d;
-        double *dk = dkp + (size_t)j * d, *dv = dvp + (size_t)j * d;
-        for (int c = 0; c < d; ++c) dk[c] = dv[c] = 0.0;
+        double *dkr = dkp + (size_t)j * d, *dvr = dvp + (size_t)j * d;
+        for (int c = 0; c < d; ++c) dkr[c] = dvr[c] = 0.0;
         for (int t = 0; t < lc; ++t) {
-            for (int hh = 0; hh < g; ++hh) {
-                if (mutation == 14 && hh > 0) continue;   /* planted: drop the group sum */
+            for (int hh = 0; hh < g; ++hh) {      /* every query head of the group */
                 const int r = t * g + hh;
                 const double *qt = q + (size_t)r * d;
                 const double *dot_ = dout + (size_t)r * d;
                 const double p = exp(scale * dot(qt, kj, d) - lse[(size_t)hh * lc + t]);
                 const double ds = p * (dot(dot_, vj, d) - delta[(size_t)hh * lc + t]);
-                const double fk = (mutation == 13) ? ds : scale * ds;  /* planted: scale dropped */
-                for (int c = 0; c < d; ++c) dk[c] += fk * qt[c];
-                for (int c = 0; c < d; ++c) dv[c] += p * dot_[c];
+                const double fkp = scale * ds;
+                for (int c = 0; c < d; ++c) dkr[c] += fkp * qt[c];
+                for (int c = 0; c < d; ++c) dvr[c] += p * dot_[c];
             }
         }
     }

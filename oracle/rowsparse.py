@@ -18,7 +18,8 @@ numpy matmul in fp64 (the library routine the definition names), with no
 blocking or reordering of our own.  Pinned in tests/test_oracle_rowsparse.py
 against torch fp64 autograd of the dense layer with the gradient masked to
 the kept rows, brute-force loops on tiny inputs, and invariants (row order,
-linearity in the kept set, all rows kept = the dense backward).
+linearity in the kept set, all rows kept = the dense backward).  The tests
+plant mistakes in edited copies of this file (tests/oracle_mutants.py).
 """
 from __future__ import annotations
 
@@ -31,35 +32,23 @@ def _f64(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float64)
 
 
-def rowsparse_dw(dy_keep, x, keep, mutation: int = 0) -> np.ndarray:
-    """dW = dY_keep^T X[keep] in fp64, shape [out, in].
-
-    ``mutation`` plants a mistake for the pin tests (0 = none): 1 reads the
-    first n_keep rows of X instead of the kept ones, 2 returns the transpose
-    of the gradient's transpose (X[keep]^T dY_keep)."""
+def rowsparse_dw(dy_keep, x, keep) -> np.ndarray:
+    """dW = dY_keep^T X[keep] in fp64, shape [out, in]."""
     dy = _f64(dy_keep)
     xs = _f64(x)
     idx = np.asarray(keep, dtype=np.int64)
-    rows = xs[: len(idx)] if mutation == 1 else xs[idx]
+    rows = xs[idx]
     dw = dy.T @ rows
-    if mutation == 2:
-        dw = rows.T @ dy
     return dw
 
 
-def rowsparse_dx(dy_keep, w, keep, n_rows: int, mutation: int = 0) -> np.ndarray:
+def rowsparse_dx(dy_keep, w, keep, n_rows: int) -> np.ndarray:
     """dX in fp64, shape [n_rows, in]: row keep[i] = dY_keep[i] W, zero
-    elsewhere.
-
-    ``mutation``: 1 writes row i instead of row keep[i], 2 multiplies by W^T's
-    leading block instead of W (a transposed operand, square W only)."""
+    elsewhere."""
     dy = _f64(dy_keep)
     ws = _f64(w)
     idx = np.asarray(keep, dtype=np.int64)
     out = np.zeros((n_rows, ws.shape[1]), dtype=np.float64)
-    vals = dy @ (ws.T if mutation == 2 else ws)
-    if mutation == 1:
-        out[: len(idx)] = vals
-    else:
-        out[idx] = vals
+    vals = dy @ ws
+    out[idx] = vals
     return out

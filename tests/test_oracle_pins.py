@@ -14,7 +14,8 @@
 * Prefix gradients for the horizon extension (the exact reverse pass):
   central finite differences wrt the prefix K/V, and full-window attention
   with the prefix NOT detached (torch fp64 autograd).
-* Planted mistakes in the oracle each fail at least one of the above.
+* Planted mistakes in the oracle (edited copies of its sources,
+  tests/oracle_mutants.py) each fail at least one of the above.
 """
 import math
 import os
@@ -26,6 +27,7 @@ import torch.nn.functional as F
 
 import oracle
 import synth
+from tests import oracle_mutants as mutants
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "q8_0_dequant.txt")
 
@@ -40,9 +42,9 @@ def _rand_group(lp, lc, g, d, seed, scale_q=1.0):
                 dout=rng.standard_normal((lc, g, d)))
 
 
-def _oracle(x, lp, lc, g, d, scale, mutation=0):
+def _oracle(x, lp, lc, g, d, scale):
     return oracle.group(lp, lc, g, d, scale, x["q"], x["kp"], x["vp"], x["kc"], x["vc"],
-                        x["dout"], mutation=mutation)
+                        x["dout"])
 
 
 def _detached_reference(x, lp, lc, g, d, scale):
@@ -90,19 +92,18 @@ def test_golden_file_is_nonempty():
     assert len(_golden_cases()) >= 10
 
 
-@pytest.mark.parametrize("mutation", [0])
-def test_dequant_q8_0_golden(mutation):
-    assert _dequant_golden_ok(mutation)
+def test_dequant_q8_0_golden():
+    assert _dequant_golden_ok()
 
 
-def _dequant_golden_ok(mutation):
+def _dequant_golden_ok():
     cases = _golden_cases()
     blocks = np.zeros((len(cases), 34), dtype=np.uint8)
     for i, (sbits, code, _, _) in enumerate(cases):
         blocks[i, 0] = sbits & 0xFF
         blocks[i, 1] = sbits >> 8
         blocks[i, 2 + (i % 32)] = np.int8(code).view(np.uint8)   # vary the position
-    f64, f32, bf = oracle.dequant_q8_0(blocks, mutation)
+    f64, f32, bf = oracle.dequant_q8_0(blocks)
     ok = True
     for i, (sbits, code, f32bits, bfbits) in enumerate(cases):
         pos = i % 32
@@ -130,16 +131,16 @@ def test_dequant_matches_encoder_roundtrip_bound():
 
 # ------------------------------------------------------ finite differences --
 
-def _loss(x, lp, lc, g, d, scale, mutation=0):
+def _loss(x, lp, lc, g, d, scale):
     r = oracle.group(lp, lc, g, d, scale, x["q"], x["kp"], x["vp"], x["kc"], x["vc"],
-                     x["dout"], mutation=mutation, backward=False)
+                     x["dout"], backward=False)
     return float(np.sum(r["o"] * x["dout"]))
 
 
-def _fd_ok(lp, lc, g, d, seed, mutation=0, tol=1e-7):
+def _fd_ok(lp, lc, g, d, seed, tol=1e-7):
     scale = 1.0 / math.sqrt(d)
     x = _rand_group(lp, lc, g, d, seed)
-    r = _oracle(x, lp, lc, g, d, scale, mutation)
+    r = _oracle(x, lp, lc, g, d, scale)
     h = 1e-6
     ok = True
     for name, grad in (("q", r["dq"]), ("kc", r["dk"]), ("vc", r["dv"])):
@@ -151,8 +152,7 @@ def _fd_ok(lp, lc, g, d, seed, mutation=0, tol=1e-7):
             xm = {k: v.copy() for k, v in x.items()}
             xp[name][idx] += h
             xm[name][idx] -= h
-            fd[idx] = (_loss(xp, lp, lc, g, d, scale, mutation)
-                       - _loss(xm, lp, lc, g, d, scale, mutation)) / (2 * h)
+            fd[idx] = (_loss(xp, lp, lc, g, d, scale) - _loss(xm, lp, lc, g, d, scale)) / (2 * h)
         ok &= _rel(grad, fd) <= tol
     return bool(ok)
 
@@ -185,10 +185,10 @@ def test_prefix_has_true_nonzero_gradient_that_is_truncated():
 SHAPES_I3 = [(37, 19, 2, 16), (0, 9, 2, 8), (130, 5, 1, 32), (6, 17, 4, 8)]
 
 
-def _detached_ok(lp, lc, g, d, seed, mutation=0, tol=1e-12):
+def _detached_ok(lp, lc, g, d, seed, tol=1e-12):
     scale = 1.0 / math.sqrt(d) * 1.3
     x = _rand_group(lp, lc, g, d, seed)
-    r = _oracle(x, lp, lc, g, d, scale, mutation)
+    r = _oracle(x, lp, lc, g, d, scale)
     ref = _detached_reference(x, lp, lc, g, d, scale)
     errs = dict(o=_rel(r["o"], ref["o"]), lse=_rel(r["lse"], ref["lse"]),
                 dq=_rel(r["dq"], ref["dq"]), dk=_rel(r["dk"], ref["dk"]),
@@ -202,12 +202,13 @@ def test_matches_full_window_with_detached_prefix(lp, lc, g, d):
     assert ok, errs
 
 
-def _packed_ok(head_map=None, mutation=0):
-    """Through the packed-batch glue: 2 windows, hkv=2, g=2, against the
-    detached reference written with repeat_interleave for GQA."""
+def _packed_ok(orc=oracle):
+    """Through the packed-batch glue (the oracle module `orc`): 2 windows,
+    hkv=2, g=2, against the detached reference written with repeat_interleave
+    for GQA."""
     w = synth.custom(hq=4, hkv=2, head_dim=16, lp=[11, 0], lc=[6, 5], dout_std=1.0, seed=5)
     inp = synth.make_inputs(w)
-    r = oracle.run(inp, head_map=head_map, mutation=mutation)
+    r = orc.run(inp)
     g = w.hq // w.hkv
     ok = True
     cu_p = inp["cu_seqlens_prefix"].tolist()
@@ -253,14 +254,14 @@ def test_no_prefix_is_plain_causal_attention():
 
 # ------------------------------------------------------------ closed forms --
 
-def _closed_forms_ok(mutation=0):
+def _closed_forms_ok():
     ok = True
     lp, lc, g, d = 9, 6, 2, 8
     scale = 0.3
     # Q = 0: uniform weights over the visible keys
     x = _rand_group(lp, lc, g, d, 4)
     x["q"][:] = 0.0
-    r = _oracle(x, lp, lc, g, d, scale, mutation)
+    r = _oracle(x, lp, lc, g, d, scale)
     for t in range(lc):
         vis = np.concatenate([x["vp"], x["vc"][: t + 1]], 0)
         for h in range(g):
@@ -270,19 +271,19 @@ def _closed_forms_ok(mutation=0):
     x = _rand_group(lp, lc, g, d, 5)
     x["kp"][:] = x["kc"][0]
     x["kc"][:] = x["kc"][0]
-    r = _oracle(x, lp, lc, g, d, scale, mutation)
+    r = _oracle(x, lp, lc, g, d, scale)
     ok &= np.abs(r["dq"]).max() < 1e-12
     # Lp = 0: column sums of P are the chunk dV; their total is sum of dO
     x = _rand_group(0, lc, g, d, 6)
-    r = _oracle(x, 0, lc, g, d, scale, mutation)
+    r = _oracle(x, 0, lc, g, d, scale)
     ok &= np.allclose(r["dv"].sum(0), x["dout"].sum((0, 1)), rtol=0, atol=1e-12)
     # identical query heads and dO within a group: dK, dV are g times one head's
     x = _rand_group(lp, lc, 1, d, 7)
-    r1 = _oracle(x, lp, lc, 1, d, scale, mutation)
+    r1 = _oracle(x, lp, lc, 1, d, scale)
     x3 = dict(x)
     x3["q"] = np.repeat(x["q"], 3, axis=1)
     x3["dout"] = np.repeat(x["dout"], 3, axis=1)
-    r3 = _oracle(x3, lp, lc, 3, d, scale, mutation)
+    r3 = _oracle(x3, lp, lc, 3, d, scale)
     ok &= np.allclose(r3["dk"], 3 * r1["dk"], rtol=1e-12, atol=1e-13)
     ok &= np.allclose(r3["dv"], 3 * r1["dv"], rtol=1e-12, atol=1e-13)
     return bool(ok)
@@ -294,62 +295,49 @@ def test_closed_forms():
 
 # ---------------------------------------------------------- planted mistakes --
 
-ATTN_MUTATIONS = {
-    1: "chunk mask lets a row see one future key",
-    2: "softmax scale dropped from dQ",
-    3: "wrong sign of delta in dS",
-    4: "dV accumulates dS instead of P",
-    5: "softmax scale dropped from dK",
-    6: "dQ multiplies dS by V instead of K",
-    7: "LSE taken in log2",
-    8: "O sums K rows instead of V rows",
-    9: "prefix dropped from the softmax denominator",
-    10: "dK/dV sum only the first head of the group",
-}
+ATTN_MUTANTS = list(range(1, 11))
 
 
-def _all_attention_pins_pass(mutation):
-    ok = _fd_ok(5, 4, 2, 8, seed=1, mutation=mutation)
+def _all_attention_pins_pass():
+    ok = _fd_ok(5, 4, 2, 8, seed=1)
     for lp, lc, g, d in SHAPES_I3[:2] + SHAPES_I3[3:]:
-        ok &= _detached_ok(lp, lc, g, d, seed=3, mutation=mutation)[0]
-    ok &= _closed_forms_ok(mutation)
+        ok &= _detached_ok(lp, lc, g, d, seed=3)[0]
+    ok &= _closed_forms_ok()
     return bool(ok)
 
 
-def test_pins_pass_without_mutation():
-    assert _all_attention_pins_pass(0)
+def test_pins_pass_on_the_oracle():
+    assert _all_attention_pins_pass()
 
 
-@pytest.mark.parametrize("mutation", sorted(ATTN_MUTATIONS))
-def test_pins_catch_planted_attention_mistake(mutation):
-    assert not _all_attention_pins_pass(mutation), ATTN_MUTATIONS[mutation]
+@pytest.mark.parametrize("n", ATTN_MUTANTS)
+def test_pins_catch_planted_attention_mistake(n):
+    with mutants.c_mutant(n):
+        assert not _all_attention_pins_pass(), mutants.C_MUTANTS[n][0]
 
 
-@pytest.mark.parametrize("mutation", [11, 12])
-def test_pins_catch_planted_dequant_mistake(mutation):
-    # 11: scale read as bf16 bits; 12: codes read unsigned
-    assert not _dequant_golden_ok(mutation)
+@pytest.mark.parametrize("n", [11, 12])
+def test_pins_catch_planted_dequant_mistake(n):
+    with mutants.c_mutant(n):
+        assert not _dequant_golden_ok(), mutants.C_MUTANTS[n][0]
 
 
 def test_pins_catch_transposed_head_map():
-    # query head h read from kv head h % hkv instead of h // g
-    def strided(hk, g, hkv):
-        return [h for h in range(g * hkv) if h % hkv == hk]
-    assert not _packed_ok(head_map=strided)
+    assert not _packed_ok(mutants.py_mutant("head_map")), mutants.PY_MUTANTS["head_map"][0]
 
 
 # ------------------------------------------- prefix gradients (horizon H) --
 
-def _prefix_grad(x, lp, lc, g, d, scale, mutation=0):
+def _prefix_grad(x, lp, lc, g, d, scale):
     r = _oracle(x, lp, lc, g, d, scale)
     return oracle.prefix_grad(lp, lc, g, d, scale, x["q"], x["kp"], x["vp"], x["dout"],
-                              r["lse"], r["delta"], mutation=mutation)
+                              r["lse"], r["delta"])
 
 
-def _prefix_fd_ok(lp, lc, g, d, seed, mutation=0, tol=1e-7):
+def _prefix_fd_ok(lp, lc, g, d, seed, tol=1e-7):
     scale = 1.0 / math.sqrt(d)
     x = _rand_group(lp, lc, g, d, seed)
-    dkp, dvp = _prefix_grad(x, lp, lc, g, d, scale, mutation)
+    dkp, dvp = _prefix_grad(x, lp, lc, g, d, scale)
     h = 1e-6
     ok = True
     for name, grad in (("kp", dkp), ("vp", dvp)):
@@ -385,10 +373,10 @@ def _full_window_prefix_grads(x, lp, lc, g, d, scale):
     return kp.grad.numpy(), vp.grad.numpy()
 
 
-def _prefix_full_window_ok(lp, lc, g, d, seed, mutation=0, tol=1e-12):
+def _prefix_full_window_ok(lp, lc, g, d, seed, tol=1e-12):
     scale = 1.0 / math.sqrt(d) * 1.3
     x = _rand_group(lp, lc, g, d, seed)
-    dkp, dvp = _prefix_grad(x, lp, lc, g, d, scale, mutation)
+    dkp, dvp = _prefix_grad(x, lp, lc, g, d, scale)
     rk, rv = _full_window_prefix_grads(x, lp, lc, g, d, scale)
     return _rel(dkp, rk) <= tol and _rel(dvp, rv) <= tol
 
@@ -413,12 +401,17 @@ def test_truncated_prefix_derivative_is_the_horizon_gradient():
     assert abs(dkp[1, 2] - fd) <= 1e-7 * max(1.0, abs(fd))
 
 
-PREFIX_MUTATIONS = {13: "softmax scale dropped from the prefix dK",
-                    14: "prefix dK/dV sum only the first head of the group"}
+@pytest.mark.parametrize("n", [13, 14])
+def test_pins_catch_planted_prefix_gradient_mistake(n):
+    with mutants.c_mutant(n):
+        ok = _prefix_fd_ok(5, 4, 2, 8, seed=2)
+        ok &= _prefix_full_window_ok(6, 17, 4, 8, seed=5)
+    assert not ok, mutants.C_MUTANTS[n][0]
 
 
-@pytest.mark.parametrize("mutation", sorted(PREFIX_MUTATIONS))
-def test_pins_catch_planted_prefix_gradient_mistake(mutation):
-    ok = _prefix_fd_ok(5, 4, 2, 8, seed=2, mutation=mutation)
-    ok &= _prefix_full_window_ok(6, 17, 4, 8, seed=5, mutation=mutation)
-    assert not ok, PREFIX_MUTATIONS[mutation]
+def test_every_planted_mistake_is_tested():
+    # each mutant of the oracle's sources has a pin test above or in the
+    # encoder / row-sparse pin files
+    assert sorted(mutants.C_MUTANTS) == list(range(1, 17))
+    assert set(mutants.PY_MUTANTS) == {"head_map", "dw_rows", "dw_transposed", "dx_rows",
+                                       "dx_transposed"}

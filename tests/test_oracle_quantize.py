@@ -10,7 +10,8 @@
   blocks, bit for bit.
 * Round trip: dequantised codes lie within half a step (plus the fp16
   rounding of the scale) of the inputs, and the absmax gets code +-127.
-* Planted mistakes (ties to even; dividing by the fp16-rounded scale) fail.
+* Planted mistakes (ties to even; dividing by the fp16-rounded scale) fail:
+  edited copies of the oracle's source (tests/oracle_mutants.py).
 """
 import os
 
@@ -20,6 +21,7 @@ import torch
 
 import oracle
 import synth
+from tests import oracle_mutants as mutants
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "q8_0_encode.txt")
 
@@ -52,13 +54,13 @@ def _golden():
     return cases
 
 
-def _golden_ok(mutation=0):
+def _golden_ok():
     cases = _golden()
     x = np.stack([c[2] for c in cases])
     bits = _bf16_bits(x)
     # every golden value is exact in bf16
     assert np.array_equal(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy(), x)
-    out = oracle.quantize_q8_0(bits, mutation)
+    out = oracle.quantize_q8_0(bits)
     ok = True
     for i, (name, scale, _, codes) in enumerate(cases):
         ok &= int(out[i, 0]) | (int(out[i, 1]) << 8) == scale
@@ -97,12 +99,12 @@ def _random_blocks(n, seed):
     return x
 
 
-def _matches_generator(mutation=0):
+def _matches_generator():
     x = _random_blocks(4096, 1)
     bits = _bf16_bits(x)
     xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float()
     want = synth.encode_q8_0(xb).numpy()
-    got = oracle.quantize_q8_0(bits, mutation)
+    got = oracle.quantize_q8_0(bits)
     return np.array_equal(got, want)
 
 
@@ -127,7 +129,8 @@ def test_round_trip_bound_and_absmax_code():
     assert np.all(np.abs(codes[nz]).max(1) == 127)
 
 
-@pytest.mark.parametrize("mutation", [15, 16])
-def test_pins_catch_planted_encoder_mistake(mutation):
-    # 15: halves rounded to even; 16: codes divided by the fp16-rounded scale
-    assert not (_golden_ok(mutation) and _matches_generator(mutation))
+@pytest.mark.parametrize("n", [15, 16])
+def test_pins_catch_planted_encoder_mistake(n):
+    with mutants.c_mutant(n):
+        caught = not (_golden_ok() and _matches_generator())
+    assert caught, mutants.C_MUTANTS[n][0]

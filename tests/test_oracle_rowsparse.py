@@ -8,13 +8,15 @@ same comparison against a masked dense reference).  Pinned here by
   * brute-force loops on tiny inputs and one hand-worked case,
   * invariants: the order of the kept rows does not matter, the result is
     linear in the kept set, and keeping every row gives the dense backward,
-and each planted mistake in the oracle fails at least one of them.
+and each planted mistake in the oracle (an edited copy of its source,
+tests/oracle_mutants.py) fails at least one of them.
 """
 import numpy as np
 import pytest
 import torch
 
 from oracle import rowsparse as rs
+from tests import oracle_mutants as mutants
 
 
 def _case(n_rows, n_keep, d_in, d_out, seed, sort=True):
@@ -52,11 +54,11 @@ SHAPES = [  # n_rows, n_keep, in, out
 ]
 
 
-def _pin_autograd(shape, seed, mutation=0):
+def _pin_autograd(shape, seed, m=rs):
     x, w, keep, dy = _case(*shape, seed, sort=seed % 2 == 0)
     rw, rx = _dense_autograd(x, w, keep, dy)
-    dw = rs.rowsparse_dw(dy, x, keep, mutation=mutation if mutation in (1, 2) else 0)
-    dx = rs.rowsparse_dx(dy, w, keep, x.shape[0], mutation=mutation - 2 if mutation in (3, 4) else 0)
+    dw = m.rowsparse_dw(dy, x, keep)
+    dx = m.rowsparse_dx(dy, w, keep, x.shape[0])
     return _rel(dw, rw) <= 1e-12 and _rel(dx, rx) <= 1e-12
 
 
@@ -88,11 +90,11 @@ def _brute(x, w, keep, dy):
     return np.array(dw), np.array(dx)
 
 
-def _pin_brute(seed, mutation=0):
+def _pin_brute(seed, m=rs):
     x, w, keep, dy = _case(7, 3, 4, 4, seed, sort=False)
     bw, bx = _brute(x, w, keep, dy)
-    dw = rs.rowsparse_dw(dy, x, keep, mutation=mutation if mutation in (1, 2) else 0)
-    dx = rs.rowsparse_dx(dy, w, keep, 7, mutation=mutation - 2 if mutation in (3, 4) else 0)
+    dw = m.rowsparse_dw(dy, x, keep)
+    dx = m.rowsparse_dx(dy, w, keep, 7)
     return _rel(dw, bw) <= 1e-13 and _rel(dx, bx) <= 1e-13
 
 
@@ -116,26 +118,24 @@ def test_hand_worked_case():
     assert np.array_equal(rs.rowsparse_dx(dy, w, keep, 3), [[3., 1.], [0., 0.], [1., 0.]])
 
 
-def _pin_invariants(seed, mutation=0):
+def _pin_invariants(seed, m=rs):
     x, w, keep, dy = _case(30, 12, 8, 8, seed)
-    m_w = mutation if mutation in (1, 2) else 0
-    m_x = mutation - 2 if mutation in (3, 4) else 0
-    dw = rs.rowsparse_dw(dy, x, keep, m_w)
-    dx = rs.rowsparse_dx(dy, w, keep, 30, m_x)
+    dw = m.rowsparse_dw(dy, x, keep)
+    dx = m.rowsparse_dx(dy, w, keep, 30)
     ok = True
     # any order of the kept rows (dY rows moved with them)
     p = np.random.default_rng(seed + 100).permutation(len(keep))
-    ok &= _rel(rs.rowsparse_dw(dy[p], x, keep[p], m_w), dw) <= 1e-13
-    ok &= _rel(rs.rowsparse_dx(dy[p], w, keep[p], 30, m_x), dx) <= 1e-13
+    ok &= _rel(m.rowsparse_dw(dy[p], x, keep[p]), dw) <= 1e-13
+    ok &= _rel(m.rowsparse_dx(dy[p], w, keep[p], 30), dx) <= 1e-13
     # linear in the kept set
     a, b = slice(0, 5), slice(5, None)
-    ok &= _rel(rs.rowsparse_dw(dy[a], x, keep[a], m_w) + rs.rowsparse_dw(dy[b], x, keep[b], m_w), dw) <= 1e-13
-    ok &= _rel(rs.rowsparse_dx(dy[a], w, keep[a], 30, m_x) + rs.rowsparse_dx(dy[b], w, keep[b], 30, m_x), dx) <= 1e-13
+    ok &= _rel(m.rowsparse_dw(dy[a], x, keep[a]) + m.rowsparse_dw(dy[b], x, keep[b]), dw) <= 1e-13
+    ok &= _rel(m.rowsparse_dx(dy[a], w, keep[a], 30) + m.rowsparse_dx(dy[b], w, keep[b], 30), dx) <= 1e-13
     # every row kept, in order: the dense backward of Y = X W^T
     full = np.arange(30)
     dyf = np.random.default_rng(seed + 7).standard_normal((30, 8))
-    ok &= _rel(rs.rowsparse_dw(dyf, x, full, m_w), np.einsum("ro,ri->oi", dyf, x)) <= 1e-13
-    ok &= _rel(rs.rowsparse_dx(dyf, w, full, 30, m_x), np.einsum("ro,oi->ri", dyf, w)) <= 1e-13
+    ok &= _rel(m.rowsparse_dw(dyf, x, full), np.einsum("ro,ri->oi", dyf, x)) <= 1e-13
+    ok &= _rel(m.rowsparse_dx(dyf, w, full, 30), np.einsum("ro,oi->ri", dyf, w)) <= 1e-13
     return bool(ok)
 
 
@@ -153,8 +153,11 @@ def test_input_dtypes_convert_exactly():
     assert np.array_equal(rs.rowsparse_dw(dy, x, keep), ref)
 
 
-@pytest.mark.parametrize("mutation", [1, 2, 3, 4])
-def test_pins_catch_planted_mistakes(mutation):
-    caught = (not all(_pin_autograd(s, 0, mutation) for s in SHAPES if s[2] == s[3] or mutation != 4)
-              or not _pin_brute(3, mutation) or not _pin_invariants(0, mutation))
-    assert caught, mutation
+@pytest.mark.parametrize("name", ["dw_rows", "dw_transposed", "dx_rows", "dx_transposed"])
+def test_pins_catch_planted_mistakes(name):
+    m = mutants.py_mutant(name)
+    # a transposed W only type-checks when W is square
+    shapes = [s for s in SHAPES if s[2] == s[3] or name != "dx_transposed"]
+    caught = (not all(_pin_autograd(s, 0, m) for s in shapes)
+              or not _pin_brute(3, m) or not _pin_invariants(0, m))
+    assert caught, mutants.PY_MUTANTS[name][0]
