@@ -746,7 +746,7 @@ int rs_plan(const cfa_rowsparse_args* r, int mode, RsPlan* p) {
   a.units = (long long)a.tiles * splits;
   p->grid = (int)(a.units < sms ? a.units : sms);
   // dX split K: one cluster per tile when every tile's splits can be resident
-  // together (the partials then never leave shared memory)
+  // together (they exchange their partials through L2 without counters)
   // (CFA_RS_CLUSTER=0 keeps the global-memory path: the tests compare the two)
   const char* env = std::getenv("CFA_RS_CLUSTER");
   const bool allow = !(env && env[0] == '0');
@@ -757,7 +757,7 @@ int rs_plan(const cfa_rowsparse_args* r, int mode, RsPlan* p) {
   p->off_cnt = 16;
   const size_t hdr = align256(p->off_cnt + (size_t)a.tiles * 16);
   p->off_part = hdr;
-  p->ws = hdr + (splits > 1 && !a.cluster ? (size_t)a.tiles * splits * kRsTileM * kRsTileN * 4 : 0);
+  p->ws = hdr + (splits > 1 ? (size_t)a.tiles * splits * kRsTileM * kRsTileN * 4 : 0);
   if (p->ws < kWsHeader) p->ws = kWsHeader;
   a.limit_ns = wait_limit_ns();
   return CFA_OK;
@@ -792,7 +792,7 @@ int rs_run(const cfa_rowsparse_args* r, int mode, void* out, int out_f32, int ac
       (st = make_map_2d(&mo, out, r->in_features, r->out_features, out_f32 ? 32 : 64, 32,
                         out_f32 != 0)))
     return st;
-  if (a.splits > 1 && !a.cluster &&
+  if (a.splits > 1 &&
       (st = make_map_2d(&mp, a.part, kRsTileN, (long long)a.tiles * a.splits * kRsTileM, 32, 32,
                         true)))
     return st;

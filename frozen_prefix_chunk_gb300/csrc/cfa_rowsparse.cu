@@ -29,15 +29,17 @@
 // scattered pieces.
 //
 // Split K, mode 1 (dX, whose kept rows make few tiles): the splits of a tile
-// run as one thread-block cluster.  After its K range each CTA copies its fp32
-// accumulator from TMEM into its own shared memory (the freed pipeline
-// stages), the CTAs signal one another through mbarriers (remote arrives),
-// and CTA rank r of the cluster sums rows [r * 128 / splits, (r + 1) * 128 /
-// splits) of the tile over distributed shared memory, in split order
-// (deterministic, the same sums as the global-memory path below), and writes
-// them out.  A second exchange keeps every CTA resident until its peers have
-// read its partial.  Every wait is bounded; a CTA whose wait for the partials
-// runs out reads nothing remote.
+// run as one thread-block cluster.  After its K range each CTA stores its fp32
+// partial tile to the workspace (TMA tile stores), the CTAs signal one
+// another through mbarriers (remote arrives, release / acquire at cluster
+// scope), and CTA rank r of the cluster copies rows [r * 128 / splits,
+// (r + 1) * 128 / splits) of every split's partial from L2 into its shared
+// memory (bulk copies, all in flight at once), sums them in split order
+// (deterministic, the same sums as the global-memory path below) and writes
+// them out.  No per-tile counter, no memset.  Summing over distributed shared
+// memory instead ran at about 12 bytes a cycle per SM, several times slower
+// than these copies.  Every wait is bounded; a CTA whose wait for its peers
+// runs out reads no partial.
 //
 // Split K otherwise (when there are fewer tiles than SMs): every split writes an fp32
 // partial tile to the workspace.  Each epilogue warp owns 32 rows of the tile
@@ -172,67 +174,59 @@ __device__ __forceinline__ bool cluster_wait(const Waiter& w, uint32_t bar, uint
   }
   return __all_sync(0xffffffffu, ok);
 }
-// (no memory clobber: a batch of these issues back to back and its sums
-// follow; the exchanges around them are volatile asm with clobbers, which
-// these do not move across)
-__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(cluster_addr));
-  return v;
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory, completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
-// Cluster split K: this warp's rows of the tile summed over the SP splits'
-// staged partials (in split order) and written out as bf16.  Rows go in
-// batches of 8 / SP so that every lane has 16 remote loads in flight.
-template <int SP>
-__device__ __forceinline__ void cluster_reduce_rows(const RsArgs& a, int tm, int tn, uint32_t base,
-                                                    uint32_t rank, int quad, int lane, int my_keep,
-                                                    int kept_row_stride, int cl_row_bytes) {
-  constexpr int R = kRsTileM / SP, RPW = R / 4, RB = 8 / SP;
+// Cluster split K: this warp's rows of the CTA's share of the tile, summed
+// over the `splits` partial rows staged at `base` (split k's row j at
+// base + (k * R + j) * 1024, R = 128 / splits) in split order, written out as
+// bf16; lane l takes columns 8l .. 8l + 7.
+__device__ __forceinline__ void cluster_sum_rows(const RsArgs& a, int tm, int tn, uint32_t base,
+                                                 uint32_t rank, int quad, int lane, int my_keep) {
+  const int splits = a.splits;
+  const int R = kRsTileM / splits, RPW = R / 4;
   const int col = 8 * lane;
   const int n = tn * kRsTileN + col;  // output column
   const bool vec = n + 8 <= a.N && (a.N & 7) == 0 && (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
-  for (int rb = 0; rb < RPW; rb += RB) {
-    float4 v[RB][SP][2];
-#pragma unroll
-    for (int r = 0; r < RB; ++r) {
-      const int row = (int)rank * R + quad * RPW + rb + r;
-      const uint32_t src = base + (uint32_t)(row * cl_row_bytes + col * 4);
-#pragma unroll
-      for (int k = 0; k < SP; ++k) {
-        const uint32_t ra = mapa_shared(src, (uint32_t)k);
-        v[r][k][0] = ld_shared_cluster_v4(ra);
-        v[r][k][1] = ld_shared_cluster_v4(ra + 16u);
-      }
+  for (int rw = 0; rw < RPW; ++rw) {
+    const int j = quad * RPW + rw;  // row within the CTA's share
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < splits; ++k) {
+      const uint32_t src = base + (uint32_t)((k * R + j) * (kRsTileN * 4) + col * 4);
+      float4 lo, hi;
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w)
+                   : "r"(src));
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(hi.w)
+                   : "r"(src + 16u));
+      s[0] += lo.x; s[1] += lo.y; s[2] += lo.z; s[3] += lo.w;
+      s[4] += hi.x; s[5] += hi.y; s[6] += hi.z; s[7] += hi.w;
     }
+    const int i = tm * kRsTileM + (int)rank * R + j;  // kept-row index
+    const int keep_r = __shfl_sync(0xffffffffu, my_keep, rw);  // fetched by lane rw
+    if (i >= a.n_keep) continue;
+    if (keep_r < 0 || keep_r >= a.n_rows) {
+      if (lane == 0) atomicExch(a.status, -1 /* kept row outside X */);
+      continue;
+    }
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (size_t)keep_r * a.N;
+    if (vec) {
+      *reinterpret_cast<uint4*>(orow + n) =
+          make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
+                     pack_bf16x2(s[6], s[7]));
+    } else {
 #pragma unroll
-    for (int r = 0; r < RB; ++r) {
-      float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int k = 0; k < SP; ++k) {
-        s[0] += v[r][k][0].x; s[1] += v[r][k][0].y; s[2] += v[r][k][0].z; s[3] += v[r][k][0].w;
-        s[4] += v[r][k][1].x; s[5] += v[r][k][1].y; s[6] += v[r][k][1].z; s[7] += v[r][k][1].w;
-      }
-      const int row = (int)rank * R + quad * RPW + rb + r;
-      const int i = tm * kRsTileM + row;  // kept-row index
-      const int keep_r = __shfl_sync(0xffffffffu, my_keep, rb + r);  // fetched by lane rb + r
-      if (i >= a.n_keep) continue;
-      if (keep_r < 0 || keep_r >= a.n_rows) {
-        if (lane == 0) atomicExch(a.status, -1 /* kept row outside X */);
-        continue;
-      }
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (size_t)keep_r * kept_row_stride;
-      if (vec) {
-        *reinterpret_cast<uint4*>(orow + n) =
-            make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
-                       pack_bf16x2(s[6], s[7]));
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (n + e < a.N) orow[n + e] = __float2bfloat16_rn(s[e]);
-      }
+      for (int e = 0; e < 8; ++e)
+        if (n + e < a.N) orow[n + e] = __float2bfloat16_rn(s[e]);
     }
   }
 }
@@ -247,10 +241,23 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void epilogue_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
-// Row stride of a CTA's staged fp32 partial (256 floats + 16 bytes, so that
-// the lanes' row-per-thread writes spread over the banks).
-constexpr int kClRowBytes = 1040;
-static_assert(128 * kClRowBytes <= kStages * kStageBytes, "staged partial fits the stages");
+// The same barrier, returning whether `p` holds in all four warps.
+__device__ __forceinline__ bool epilogue_all(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n"
+      ".reg .pred a, b;\n"
+      "setp.ne.u32 a, %1, 0;\n"
+      "bar.red.and.pred b, 1, 128, a;\n"
+      "selp.u32 %0, 1, 0, b;\n"
+      "}\n"
+      : "=r"(r)
+      : "r"((uint32_t)p)
+      : "memory");
+  return r != 0;
+}
+// The cluster path's partial rows copied in: 128 rows of 256 fp32.
+static_assert(kRsTileM * kRsTileN * 4 <= kStages * kStageBytes, "partial rows fit the stages");
 
 struct Unit {
   int tm, tn, tile, split, kb, ke;  // k stages [kb, ke)
@@ -370,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_tfull = bars + 16 * kStages;    // [2]
   const uint32_t bar_tempty = bar_tfull + 16;        // [2]
   const uint32_t bar_drain = bar_tempty + 16;
-  const uint32_t bar_staged = bar_drain + 8;  // cluster path: every split's partial staged
-  const uint32_t bar_done = bar_drain + 16;   // cluster path: every split's reads done
+  const uint32_t bar_staged = bar_drain + 8;  // cluster path: every split's partial stored
+  const uint32_t bar_rows = bar_drain + 16;   // cluster path: this CTA's partial rows copied in
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kBarOff + 240);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kBarOff + 244);
 
@@ -388,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_drain, 1);
     if (CL) {
       mbar_init(bar_staged, (uint32_t)a.splits);
-      mbar_init(bar_done, (uint32_t)a.splits);
+      mbar_init(bar_rows, 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -542,35 +549,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Unit t = unit_of(a, u0);
     const int splits = a.splits;
     const uint32_t rank = cluster_ctarank();
-    // lane j < (128 / splits) / 4 fetches the keep index of this warp's row j
-    // of the reduction now, so that its latency is off the reduction
+    const int R = kRsTileM / splits;  // rows of the tile this CTA sums
+    // lane j < R / 4 fetches the keep index of this warp's row j of the sum
+    // now, so that its latency is off the reduction
     int my_keep = -1;
     {
-      const int rpw = kRsTileM / splits / 4;
-      const int i = t.tm * kRsTileM + (int)rank * (kRsTileM / splits) + quad * rpw + lane;
-      if (lane < rpw && i < a.n_keep) my_keep = a.keep[i];
+      const int i = t.tm * kRsTileM + (int)rank * R + quad * (R / 4) + lane;
+      if (lane < R / 4 && i < a.n_keep) my_keep = a.keep[i];
     }
+    uint8_t* stg_g = gbase + kStgOff + quad * kStgWarpBytes;
+    const uint32_t stg_s = base + kStgOff + quad * kStgWarpBytes;
+    int sb = 0;
     if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 0);
     bool ok = warp_wait(W, bar_tfull, 0u);
     if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 1);
     if (ok) {
+      // this split's 128 x 256 fp32 partial to the workspace: each 32-row x
+      // 32-column block through a 128-byte swizzled staging buffer and a TMA
+      // tile store
       tc_fence_after_sync();
-      // this split's 128 x 256 fp32 accumulator into the freed pipeline
-      // stages: tile row r at base + r * kClRowBytes
-      const int row = quad * 32 + lane;
+      const int prow0 = (t.tile * splits + t.split) * kRsTileM + quad * 32;
 #pragma unroll
       for (int h = 0; h < kRsTileN / 128; ++h) {
         uint32_t r[128];
         tmem_ld_x128(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(h * 128), r);
-        const uint32_t dst = base + (uint32_t)(row * kClRowBytes + h * 512);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16u * j),
-                       "r"(r[4 * j]), "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
-                       : "memory");
+        for (int ch = 0; ch < 4; ++ch) {
+          if (lane == 0) bulk_wait_read<1>();  // buffer sb no longer read by its last store
+          __syncwarp();
+          uint8_t* b = stg_g + sb * kStgBufBytes;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(b + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                make_uint4(r[ch * 32 + 4 * q], r[ch * 32 + 4 * q + 1], r[ch * 32 + 4 * q + 2],
+                           r[ch * 32 + 4 * q + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&map_p, h * 128 + ch * 32, prow0, stg_s + sb * kStgBufBytes);
+            bulk_commit();
+          }
+          sb ^= 1;
+        }
       }
     }
-    epilogue_sync();
+    // the stores have completed, and are ordered before the release below
+    if (lane == 0) {
+      bulk_wait<0>();
+      fence_proxy_async_global();
+    }
+    __syncwarp();
+    ok = epilogue_all(ok);
     if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 2);
     // one arrival per CTA on every CTA's `staged` barrier (this one's too)
     if (warp == 4 && lane < splits) {
@@ -578,26 +607,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_remote(mapa_shared(bar_staged, (uint32_t)lane));
     }
     if (ok) ok = cluster_wait(W, bar_staged, 0u, false);
+    ok = epilogue_all(ok);  // the same branch in all four warps
     if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 3);
     if (ok) {
-      // rows [rank * R, rank * R + R) of the tile (R = 128 / splits), R / 4
-      // per warp; lane l sums columns 8l .. 8l + 7
-      if (splits == 2)
-        cluster_reduce_rows<2>(a, t.tm, t.tn, base, rank, quad, lane, my_keep, a.N,
-                                 kClRowBytes);
-      else if (splits == 4)
-        cluster_reduce_rows<4>(a, t.tm, t.tn, base, rank, quad, lane, my_keep, a.N,
-                                 kClRowBytes);
-      else
-        cluster_reduce_rows<8>(a, t.tm, t.tn, base, rank, quad, lane, my_keep, a.N,
-                                 kClRowBytes);
+      // rows [rank * R, rank * R + R) of every split's partial into the freed
+      // pipeline stages (split k's row j at base + (k * R + j) * 1 KB): one
+      // 1 KB bulk copy per thread, all on one mbarrier
+      fence_proxy_async_global();
+      if (warp == 4 && lane == 0) mbar_arrive_expect_tx(bar_rows, (uint32_t)(kRsTileM * kRsTileN * 4));
+      epilogue_sync();
+      const int e = (int)threadIdx.x - 128;  // 0 .. 127 = k * R + j
+      const int k = e / R, jr = e % R;
+      const float* src = a.part + ((size_t)(t.tile * splits + k) * kRsTileM + (size_t)rank * R + jr) *
+                                      kRsTileN;
+      bulk_load(base + (uint32_t)(e * kRsTileN * 4), src, (uint32_t)(kRsTileN * 4), bar_rows);
+      ok = warp_wait(W, bar_rows, 0u);
+      if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 4);
+      if (ok) cluster_sum_rows(a, t.tm, t.tn, base, rank, quad, lane, my_keep);
+      if (!ok) mbar_wait_bounded(bar_rows, 0u, kDrainLimitNs);  // no copy left in flight
     }
-    // this CTA's reads of its peers are done: tell every CTA, and stay until
-    // every peer has read this one's partial
-    epilogue_sync();
-    if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 4);
-    if (warp == 4 && lane < splits) mbar_arrive_remote(mapa_shared(bar_done, (uint32_t)lane));
-    cluster_wait(W, bar_done, 0u, true);
     if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 5);
   } else if (warp >= 4) {
     // ----------------------------------------------------------- epilogue --

@@ -36,9 +36,9 @@ struct RsArgs {
   int* status;              // workspace status word
   unsigned long long limit_ns;
   int cluster;              // mode 1, splits > 1: the splits of a tile are one cluster of
-                            // `splits` CTAs that sum their partials over distributed
-                            // shared memory (no partials in global memory, no counters);
-                            // CTA 0 then clears the status word itself
+                            // `splits` CTAs that exchange their partials through L2 and
+                            // each sum a share of the rows (no counters); CTA 0 then
+                            // clears the status word itself
 };
 
 int rowsparse_smem_bytes();

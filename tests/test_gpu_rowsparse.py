@@ -265,9 +265,10 @@ def _dx_with(env_cluster, dy, w, keep, n_rows, d_in):
 @pytest.mark.parametrize("shape", [(4096, 256, 4096, 512), (3000, 200, 8192, 1024)],
                          ids=["m256", "m200"])
 def test_dx_split_k_cluster_path_equals_global_path(shape):
-    """dX split K runs as one cluster per tile (partials summed over
-    distributed shared memory) where the splits fit; the sums are the same, in
-    the same order, as the global-memory path's: bitwise equal outputs."""
+    """dX split K runs as one cluster per tile (the splits exchange their
+    partials through L2 and each sums a share of the rows) where the splits
+    fit; the sums are the same, in the same order, as the global-memory path's:
+    bitwise equal outputs.  Four splits per tile (m256) and two (m200)."""
     x, w, dy, keep = _inputs(*shape, seed=sum(shape) + 7, sort=False)
     n_rows, n_keep, d_in, d_out = shape
     a, st_a, _ = _dx_with("1", dy.cuda(), w.cuda(), keep.cuda(), n_rows, d_in)
