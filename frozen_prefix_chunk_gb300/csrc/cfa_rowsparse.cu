@@ -185,29 +185,39 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory to global memory, tracked by the thread's bulk
+// groups.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+
 // Cluster split K: this warp's rows of the CTA's share of the tile, summed
 // over the `splits` partial rows staged at `base` (split k's row j at
 // base + (k * R + j) * 1024, R = 128 / splits) in split order, written out as
-// bf16; lane l takes columns 8l .. 8l + 7.
+// bf16.  Lane l takes columns 4l .. 4l + 3 and 128 + 4l .. 128 + 4l + 3, so
+// that each shared-memory load reads 512 contiguous bytes (no bank conflict)
+// and each store writes 256 contiguous bytes of the row.
 __device__ __forceinline__ void cluster_sum_rows(const RsArgs& a, int tm, int tn, uint32_t base,
                                                  uint32_t rank, int quad, int lane, int my_keep) {
   const int splits = a.splits;
   const int R = kRsTileM / splits, RPW = R / 4;
-  const int col = 8 * lane;
-  const int n = tn * kRsTileN + col;  // output column
-  const bool vec = n + 8 <= a.N && (a.N & 7) == 0 && (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
+  const int n0 = tn * kRsTileN + 4 * lane, n1 = n0 + 128;  // output columns
+  const bool vec = n1 + 4 <= a.N && (a.N & 3) == 0 && (reinterpret_cast<uintptr_t>(a.out) & 7u) == 0;
   for (int rw = 0; rw < RPW; ++rw) {
     const int j = quad * RPW + rw;  // row within the CTA's share
     float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int k = 0; k < splits; ++k) {
-      const uint32_t src = base + (uint32_t)((k * R + j) * (kRsTileN * 4) + col * 4);
+      const uint32_t src = base + (uint32_t)((k * R + j) * (kRsTileN * 4) + 16 * lane);
       float4 lo, hi;
       asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                    : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w)
                    : "r"(src));
       asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                    : "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(hi.w)
-                   : "r"(src + 16u));
+                   : "r"(src + 512u));
       s[0] += lo.x; s[1] += lo.y; s[2] += lo.z; s[3] += lo.w;
       s[4] += hi.x; s[5] += hi.y; s[6] += hi.z; s[7] += hi.w;
     }
@@ -220,13 +230,14 @@ __device__ __forceinline__ void cluster_sum_rows(const RsArgs& a, int tm, int tn
     }
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (size_t)keep_r * a.N;
     if (vec) {
-      *reinterpret_cast<uint4*>(orow + n) =
-          make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
-                     pack_bf16x2(s[6], s[7]));
+      *reinterpret_cast<uint2*>(orow + n0) = make_uint2(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]));
+      *reinterpret_cast<uint2*>(orow + n1) = make_uint2(pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (n + e < a.N) orow[n + e] = __float2bfloat16_rn(s[e]);
+      for (int e = 0; e < 4; ++e) {
+        if (n0 + e < a.N) orow[n0 + e] = __float2bfloat16_rn(s[e]);
+        if (n1 + e < a.N) orow[n1 + e] = __float2bfloat16_rn(s[4 + e]);
+      }
     }
   }
 }
@@ -256,7 +267,12 @@ __device__ __forceinline__ bool epilogue_all(bool p) {
       : "memory");
   return r != 0;
 }
-// The cluster path's partial rows copied in: 128 rows of 256 fp32.
+// The cluster path: a CTA's partial staged in the freed pipeline stages at
+// this row stride (256 floats + 16 bytes, so that the lanes' row-per-thread
+// writes spread over the banks), and later the 128 partial rows it sums
+// copied in at 1 KB each.
+constexpr int kClRowBytes = 1040;
+static_assert(kRsTileM * kClRowBytes <= kStages * kStageBytes, "staged partial fits the stages");
 static_assert(kRsTileM * kRsTileN * 4 <= kStages * kStageBytes, "partial rows fit the stages");
 
 struct Unit {
@@ -384,8 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // mode 0: one expect_tx arrive per gather warp (warp 0's covers A too)
-      mbar_init(bar_full + 8 * s, MODE == 0 ? 4 : 1);
+      // mode 0: one expect_tx arrive per gather warp (warp 0's covers A too);
+      // mode 1: one per loading warp (A; B's first half; B's second half)
+      mbar_init(bar_full + 8 * s, MODE == 0 ? 4 : 3);
       mbar_init(bar_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -416,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     // ---------------------------------------------------------- producers --
-    if (MODE == 1 && warp > 0) {
-      // mode 1 loads everything by TMA from warp 0
+    if (MODE == 1 && warp > 2) {
+      // mode 1 loads by TMA from warps 0-2
     } else {
       const bool leader = lane == 0;
       int it = 0;
@@ -462,11 +479,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) CFA_TRACE(warp, it, 1);
         const uint32_t st_a = base + s * kStageBytes, st_b = st_a + kABytes;
         if (MODE == 1) {
-          if (leader) {
-            mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+          // three warps issue a stage's copies side by side: warp 0 A, warps
+          // 1 and 2 a half of B each (a warp issuing all five took about 400
+          // cycles a stage, more than the stage's MMAs)
+          if (leader && warp == 0) {
+            mbar_arrive_expect_tx(bar_full + 8 * s, kABytes);
             tma_load_2d(st_a, &map_a, bar_full + 8 * s, kk * kRsBK, t.tm * kRsTileM);
+          } else if (leader) {
+            constexpr int kHalf = kRsTileN / 128;  // 64-column slabs per half of B
+            mbar_arrive_expect_tx(bar_full + 8 * s, kBBytes / 2);
 #pragma unroll
-            for (int h = 0; h < kRsTileN / 64; ++h)
+            for (int h = (warp - 1) * kHalf; h < warp * kHalf; ++h)
               tma_load_2d(st_b + h * kSlabBytes, &map_b, bar_full + 8 * s,
                           t.tn * kRsTileN + h * 64, kk * kRsBK);
           }
@@ -557,47 +580,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = t.tm * kRsTileM + (int)rank * R + quad * (R / 4) + lane;
       if (lane < R / 4 && i < a.n_keep) my_keep = a.keep[i];
     }
-    uint8_t* stg_g = gbase + kStgOff + quad * kStgWarpBytes;
-    const uint32_t stg_s = base + kStgOff + quad * kStgWarpBytes;
-    int sb = 0;
     if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 0);
     bool ok = warp_wait(W, bar_tfull, 0u);
     if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 1);
     if (ok) {
-      // this split's 128 x 256 fp32 partial to the workspace: each 32-row x
-      // 32-column block through a 128-byte swizzled staging buffer and a TMA
-      // tile store
+      // this split's 128 x 256 fp32 partial to the workspace: each lane
+      // stages its tile row in the freed pipeline stages and sends it with
+      // one 1 KB bulk copy
       tc_fence_after_sync();
-      const int prow0 = (t.tile * splits + t.split) * kRsTileM + quad * 32;
+      const int row = quad * 32 + lane;
+      const uint32_t srow = base + (uint32_t)(row * kClRowBytes);
 #pragma unroll
       for (int h = 0; h < kRsTileN / 128; ++h) {
         uint32_t r[128];
         tmem_ld_x128(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(h * 128), r);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          if (lane == 0) bulk_wait_read<1>();  // buffer sb no longer read by its last store
-          __syncwarp();
-          uint8_t* b = stg_g + sb * kStgBufBytes;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<uint4*>(b + lane * 128 + ((q ^ (lane & 7)) << 4)) =
-                make_uint4(r[ch * 32 + 4 * q], r[ch * 32 + 4 * q + 1], r[ch * 32 + 4 * q + 2],
-                           r[ch * 32 + 4 * q + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&map_p, h * 128 + ch * 32, prow0, stg_s + sb * kStgBufBytes);
-            bulk_commit();
-          }
-          sb ^= 1;
-        }
+        for (int j = 0; j < 32; ++j)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + (uint32_t)(h * 512 + 16 * j)),
+                       "r"(r[4 * j]), "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
+                       : "memory");
       }
+      fence_proxy_async_smem();
+      bulk_store(a.part + ((size_t)(t.tile * splits + t.split) * kRsTileM + row) * kRsTileN, srow,
+                 (uint32_t)(kRsTileN * 4));
+      bulk_commit();
     }
     // the stores have completed, and are ordered before the release below
-    if (lane == 0) {
-      bulk_wait<0>();
-      fence_proxy_async_global();
-    }
+    bulk_wait<0>();
+    fence_proxy_async_global();
     __syncwarp();
     ok = epilogue_all(ok);
     if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 2);
