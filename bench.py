@@ -568,33 +568,17 @@ class AttnStep:
         names = ("q", "k_prefix", "v_prefix", "k_chunk", "v_chunk", "dout",
                  "cu_seqlens_prefix", "cu_seqlens_chunk")
         self.names = names
-        d = {k: self.host[k].to(dev) for k in names}
-        self.d = d
         self.q8 = q8 if w.prefix_dtype == synth.PREFIX_Q8_0 else None
-        pref = w.prefix_dtype
-        kp, vp = d["k_prefix"], d["v_prefix"]
         if self.q8 == "export":
             self.kp16 = torch.empty(sum(w.lp), w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
             self.vp16 = torch.empty_like(self.kp16)
-            kp, vp, pref = self.kp16, self.vp16, synth.PREFIX_BF16
-        self.a = cfa.make_args(d["q"], kp, vp, d["k_chunk"], d["v_chunk"],
-                               d["cu_seqlens_prefix"], d["cu_seqlens_chunk"], max(w.lp),
-                               max(w.lc), w.softmax_scale, pref, hkv=w.hkv, total_lp=sum(w.lp))
-        tc = sum(w.lc)
-        self.o = torch.empty_like(d["q"])
-        self.lse = torch.empty(w.hq, tc, dtype=torch.float32, device=dev)
-        self.delta = torch.empty_like(self.lse)
-        self.dq = torch.empty_like(d["q"])
-        self.dk = torch.empty(tc, w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
-        self.dv = torch.empty_like(self.dk)
+        self.io = self.make_io({k: self.host[k].to(dev) for k in names})
+        self.d = self.io["d"]
+        self.a = self.io["a"]
         self.ws_f = torch.empty(cfa.workspace_size(self.a, cfa.WS_FORWARD), dtype=torch.uint8,
                                 device=dev)
         self.ws_b = torch.empty(cfa.workspace_size(self.a, cfa.WS_BACKWARD), dtype=torch.uint8,
                                 device=dev)
-        self.dkp = self.dvp = None
-        if horizon:
-            self.dkp = torch.zeros(sum(w.lp), w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
-            self.dvp = torch.zeros_like(self.dkp)
         self.stream = torch.cuda.current_stream()
         # library launches per step: the six attention kernels, plus the
         # prefix expansion (q8_0 / fp16) inside each pass or the two exports
@@ -602,24 +586,62 @@ class AttnStep:
         self.flops = useful_flops(w, horizon)
         self.bytes = algorithmic_bytes(w, horizon)
 
-    def step(self, ev=None):
-        cfa, d, s = self.cfa, self.d, self.stream
+    def make_io(self, d):
+        """The arguments and output buffers of a step over the device inputs
+        `d` (tensors shaped like the host inputs).  Steps over different
+        input sets share the workspaces (and, for q8 = "export", the bf16
+        prefix buffers), so they must run one after the other on one stream."""
+        cfa, w, dev = self.cfa, self.w, self.dev
+        pref = w.prefix_dtype
+        kp, vp = d["k_prefix"], d["v_prefix"]
+        if self.q8 == "export":
+            kp, vp, pref = self.kp16, self.vp16, synth.PREFIX_BF16
+        a = cfa.make_args(d["q"], kp, vp, d["k_chunk"], d["v_chunk"], d["cu_seqlens_prefix"],
+                          d["cu_seqlens_chunk"], max(w.lp), max(w.lc), w.softmax_scale, pref,
+                          hkv=w.hkv, total_lp=sum(w.lp))
+        tc = sum(w.lc)
+        io = dict(d=d, a=a, o=torch.empty_like(d["q"]),
+                  lse=torch.empty(w.hq, tc, dtype=torch.float32, device=dev),
+                  dq=torch.empty_like(d["q"]),
+                  dk=torch.empty(tc, w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev),
+                  dkp=None, dvp=None)
+        io["delta"] = torch.empty_like(io["lse"])
+        io["dv"] = torch.empty_like(io["dk"])
+        if self.horizon:
+            io["dkp"] = torch.zeros(sum(w.lp), w.hkv, w.head_dim, dtype=torch.bfloat16, device=dev)
+            io["dvp"] = torch.zeros_like(io["dkp"])
+        return io
+
+    # the first input set's outputs
+    o = property(lambda self: self.io["o"])
+    lse = property(lambda self: self.io["lse"])
+    delta = property(lambda self: self.io["delta"])
+    dq = property(lambda self: self.io["dq"])
+    dk = property(lambda self: self.io["dk"])
+    dv = property(lambda self: self.io["dv"])
+    dkp = property(lambda self: self.io["dkp"])
+    dvp = property(lambda self: self.io["dvp"])
+
+    def step(self, ev=None, io=None):
+        cfa, s = self.cfa, self.stream
+        io = io or self.io
+        d, a = io["d"], io["a"]
         if ev:
             ev[0].record(s)
         if self.q8 == "export":
             cfa.dequant_q8_0(d["k_prefix"], out_bf16=self.kp16, want_f32=False)
             cfa.dequant_q8_0(d["v_prefix"], out_bf16=self.vp16, want_f32=False)
-        cfa.forward(self.a, d["q"], self.o, self.lse, self.ws_f)
+        cfa.forward(a, d["q"], io["o"], io["lse"], self.ws_f)
         if ev:
             ev[1].record(s)
-        cfa.backward_preprocess(self.a, self.o, d["dout"], self.delta)
+        cfa.backward_preprocess(a, io["o"], d["dout"], io["delta"])
         if ev:
             ev[2].record(s)
         if self.horizon:
-            cfa.backward_horizon(self.a, self.horizon, d["dout"], self.lse, self.delta, self.dq,
-                                 self.dk, self.dv, self.dkp, self.dvp, self.ws_b)
+            cfa.backward_horizon(a, self.horizon, d["dout"], io["lse"], io["delta"], io["dq"],
+                                 io["dk"], io["dv"], io["dkp"], io["dvp"], self.ws_b)
         else:
-            cfa.backward(self.a, d["dout"], self.lse, self.delta, self.dq, self.dk, self.dv,
+            cfa.backward(a, d["dout"], io["lse"], io["delta"], io["dq"], io["dk"], io["dv"],
                          self.ws_b)
         if ev:
             ev[3].record(s)
@@ -653,9 +675,59 @@ class AttnStep:
             st = self.cfa.read_status(ws)
             assert st == 0, f"device status {st}"
 
-    def outputs(self):
-        outs = [self.o, self.lse, self.dq, self.dk, self.dv]
-        return outs + ([self.dkp, self.dvp] if self.horizon else [])
+    def outputs(self, io=None):
+        io = io or self.io
+        outs = [io["o"], io["lse"], io["dq"], io["dk"], io["dv"]]
+        return outs + ([io["dkp"], io["dvp"]] if self.horizon else [])
+
+
+def e2e_pipelined(case, pin, outs_h, steps, flush, dev):
+    """Milliseconds per step of `steps` steps through the public API with host
+    inputs and outputs, pipelined the way a training loop streams its data:
+    step k's inputs are copied in from pinned host memory on one copy stream
+    while step k-1 runs, and its outputs copied out to pinned host memory on
+    another while step k+1 runs.  Two sets of device inputs and outputs
+    alternate; a set is refilled only after the step that used it is done and
+    its outputs have been read.  L2 is flushed once before the first step.
+    One pair of events spans everything: the first input copy to the last
+    output copy."""
+    s = case.stream
+    ios = [case.io, case.make_io({k: torch.empty_like(v) for k, v in case.d.items()})]
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    out_read = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+    flush()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(h2d_s)
+    for k in range(steps):
+        b = k % 2
+        io = ios[b]
+        if used[b]:
+            h2d_s.wait_event(computed[b])
+        with torch.cuda.stream(h2d_s):
+            for n in case.names:
+                io["d"][n].copy_(pin[n], non_blocking=True)
+        in_ready[b].record(h2d_s)
+        s.wait_event(in_ready[b])
+        if used[b]:
+            s.wait_event(out_read[b])
+        case.step(io=io)
+        computed[b].record(s)
+        d2h_s.wait_event(computed[b])
+        with torch.cuda.stream(d2h_s):
+            for src, dst in zip(case.outputs(io), outs_h):
+                dst.copy_(src, non_blocking=True)
+        out_read[b].record(d2h_s)
+        used[b] = True
+    s.wait_stream(d2h_s)
+    s.wait_stream(h2d_s)
+    e1.record(s)
+    e1.synchronize()
+    case.check_status()
+    return e0.elapsed_time(e1) / steps
 
 
 def time_steps(case, steps, warmup, flush, world, dev, sampler_index=None, launch="graph"):
@@ -889,7 +961,8 @@ def main():
     outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = sum(v.numel() * v.element_size() for v in outs_h)
-    e2e_ms = []
+    # one step at a time (copy in, step, copy out; L2 flushed before each)
+    serial_ms = []
     for k in range(args.e2e_steps + 2):
         flush()
         torch.cuda.synchronize()
@@ -903,8 +976,11 @@ def main():
         e1.record(stream)
         e1.synchronize()
         if k >= 2:
-            e2e_ms.append(e0.elapsed_time(e1))
-    e2e_val = job_tflops_sum(case.flops["total"], statistics.mean(e2e_ms), world, dev)
+            serial_ms.append(e0.elapsed_time(e1))
+    # as a training loop streams its inputs: every step's copies, overlapped
+    e2e_pipe_ms = e2e_pipelined(case, pin, outs_h, 2, flush, dev)
+    e2e_pipe_ms = e2e_pipelined(case, pin, outs_h, args.e2e_steps, flush, dev)
+    e2e_val = job_tflops_sum(case.flops["total"], e2e_pipe_ms, world, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -924,7 +1000,16 @@ def main():
                 "roofline": roofline, "step_roofline": step_roof,
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                        "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_pipe_ms,
+                        "steps": args.e2e_steps,
+                        "overlap": "pipelined: each step's inputs copied in from pinned host "
+                                   "memory on a copy stream while the previous step runs, its "
+                                   "outputs copied out on another while the next one runs "
+                                   "(two input / output sets alternate); one event pair spans "
+                                   "all steps, every copy inside it",
+                        "serial_ms_per_step": statistics.mean(serial_ms),
+                        "serial_value": job_tflops_sum(case.flops["total"],
+                                                       statistics.mean(serial_ms), world, dev)},
                 "gpu_launches": case.launches * args.steps,
                 "launch": ("cuda_graph (one step captured through the C-ABI calls, one replay "
                            "per timed step; step_roofline.stream_launch has the same step "
