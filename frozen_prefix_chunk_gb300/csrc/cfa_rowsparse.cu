@@ -20,8 +20,9 @@
 // Warp roles (288 threads): warps 0-3 load (mode 0: one 64-column slab of
 // the gathered rows each, with the next stage's keep indices fetched a stage
 // ahead so their latency stays off the copy path, and warp 0 lane 0 also the
-// TMA of A; mode 1: warp 0 lane 0 issues all TMA), warps 4-7 are the epilogue
-// (TMEM lane quadrant = warp % 4), warp 8 owns TMEM and issues tcgen05.mma
+// TMA of A; mode 1: lane 0 of warps 0-2 issues A and the two halves of B),
+// warps 4-7 are the epilogue (TMEM lane quadrant = warp % 4), warp 8 owns
+// TMEM and issues tcgen05.mma
 // (converged warp, elect.sync).  Two 256-column fp32 accumulators in TMEM let
 // the epilogue of one tile overlap the MMAs of the next.  The epilogue stages
 // each 32 x 32 block of its rows through shared memory, so that every global
