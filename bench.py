@@ -186,51 +186,61 @@ class ClockSampler:
 
 # --------------------------------------------------------------- oracle arm --
 
-def _group_inputs(inp, b, hk, lc_sub):
-    """The first lc_sub chunk rows of window b, KV head hk, as a one-window
-    one-head-group workload (rows before lc_sub see exactly the same keys)."""
+def _group_inputs(inp, b, hk, lc_sub, nh=1):
+    """The first lc_sub chunk rows of window b, KV heads hk .. hk + nh - 1
+    (and their query heads), as a one-window workload (rows before lc_sub see
+    exactly the same keys)."""
     w = inp["workload"]
     g = w.hq // w.hkv
     cu_p = inp["cu_seqlens_prefix"].tolist()
     cu_c = inp["cu_seqlens_chunk"].tolist()
     c0, p0, p1 = cu_c[b], cu_p[b], cu_p[b + 1]
-    sub = synth.custom(hq=g, hkv=1, head_dim=w.head_dim, lp=[p1 - p0], lc=[lc_sub],
+    sub = synth.custom(hq=g * nh, hkv=nh, head_dim=w.head_dim, lp=[p1 - p0], lc=[lc_sub],
                        prefix_dtype=w.prefix_dtype, softmax_scale=w.softmax_scale,
                        name=w.name)
-    heads = slice(hk * g, (hk + 1) * g)
+    heads = slice(hk * g, (hk + nh) * g)
     rows = slice(c0, c0 + lc_sub)
     return dict(q=inp["q"][rows, heads].contiguous(),
-                k_prefix=inp["k_prefix"][p0:p1, hk:hk + 1].contiguous(),
-                v_prefix=inp["v_prefix"][p0:p1, hk:hk + 1].contiguous(),
-                k_chunk=inp["k_chunk"][rows, hk:hk + 1].contiguous(),
-                v_chunk=inp["v_chunk"][rows, hk:hk + 1].contiguous(),
+                k_prefix=inp["k_prefix"][p0:p1, hk:hk + nh].contiguous(),
+                v_prefix=inp["v_prefix"][p0:p1, hk:hk + nh].contiguous(),
+                k_chunk=inp["k_chunk"][rows, hk:hk + nh].contiguous(),
+                v_chunk=inp["v_chunk"][rows, hk:hk + nh].contiguous(),
                 dout=inp["dout"][rows, heads].contiguous(),
                 cu_seqlens_prefix=synth.cu_seqlens([p1 - p0]),
                 cu_seqlens_chunk=synth.cu_seqlens([lc_sub]), workload=sub)
 
 
 def oracle_sample(inp, budget_s, group=(0, 0)):
-    """Time the oracle, as it stands, on a bounded sample: the first rows of
-    one (window, KV head) group, as many as fit in about budget_s (calibrated
-    on two rows).  Returns (seconds, useful FLOPs of the sample, text)."""
+    """Time the oracle, as it stands, on a bounded sample of about budget_s:
+    the first rows of the (window, KV head) group, or, when the whole group
+    takes less, all chunk rows of that window's KV heads from hk on, as many
+    as fit (calibrated on the group's first 32 rows, enough to keep the
+    oracle's threads busy).  Returns (seconds, useful FLOPs of the sample,
+    text)."""
     import oracle
 
     oracle.build()
     w = inp["workload"]
     b, hk = group
     lc = w.lc[b]
-    probe = _group_inputs(inp, b, hk, min(lc, 2))
+    n_probe = min(lc, 32)
+    probe = _group_inputs(inp, b, hk, n_probe)
     t0 = time.perf_counter()
     oracle.run(probe)
-    per_row = (time.perf_counter() - t0) / min(lc, 2)
-    lc_sub = max(1, min(lc, int(budget_s / max(per_row, 1e-9))))
-    sub = _group_inputs(inp, b, hk, lc_sub)
+    per_row = (time.perf_counter() - t0) / n_probe
+    rows = budget_s / max(per_row, 1e-9)
+    if rows <= lc:
+        lc_sub, nh = max(1, int(rows)), 1
+    else:
+        lc_sub, nh = lc, max(1, min(w.hkv - hk, int(rows / lc)))
+    sub = _group_inputs(inp, b, hk, lc_sub, nh)
     t0 = time.perf_counter()
     oracle.run(sub)
     dt = time.perf_counter() - t0
     f = useful_flops(sub["workload"])["total"]
-    desc = (f"oracle fwd+bwd of chunk rows 0..{lc_sub - 1} of window {b}, kv head {hk} of "
-            f"{w.name} ({w.hq // w.hkv} query heads, Lp={w.lp[b]}, Lc={lc_sub} of {lc})")
+    heads = f"kv head {hk}" if nh == 1 else f"kv heads {hk}..{hk + nh - 1}"
+    desc = (f"oracle fwd+bwd of chunk rows 0..{lc_sub - 1} of window {b}, {heads} of "
+            f"{w.name} ({w.hq // w.hkv} query heads each, Lp={w.lp[b]}, Lc={lc_sub} of {lc})")
     return dt, f, desc
 
 
