@@ -39,3 +39,27 @@ def test_graph_replay_equals_stream_launches(name, mode):
     case.check_status()
     for a, b in zip(ref, case.outputs()):
         assert torch.equal(a, b)
+
+
+def test_pipelined_end_to_end_reads_back_each_steps_outputs():
+    """The benchmark's end-to-end loop: inputs copied in on one stream while
+    the previous step runs, outputs copied out on another while the next one
+    runs, two buffer sets alternating.  The outputs read back to the host are
+    bitwise those of a step launched on its own (the same inputs every step),
+    whichever buffer set the last step used."""
+    import bench
+    import synth
+    dev = torch.device("cuda", 0)
+    w = synth.workload("qwen3_1p7b", seed=0)
+    case = bench.AttnStep(w, dev, 0, "product")
+    case.step()
+    torch.cuda.synchronize()
+    ref = [t.cpu() for t in case.outputs()]
+    pin = {k: case.host[k].pin_memory() for k in case.names}
+    flush = bench.L2Flush(dev)
+    for steps in (4, 5):
+        outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ref]
+        ms = bench.e2e_pipelined(case, pin, outs_h, steps, flush, dev)
+        assert ms > 0
+        for a, b in zip(ref, outs_h):
+            assert torch.equal(a, b)
