@@ -196,49 +196,67 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t byt
 }
 
 // Cluster split K: this warp's rows of the CTA's share of the tile, summed
-// over the `splits` partial rows staged at `base` (split k's row j at
-// base + (k * R + j) * 1024, R = 128 / splits) in split order, written out as
+// over the SP partial rows staged at `base` (split k's row j at
+// base + (k * R + j) * 1024, R = 128 / SP) in split order, written out as
 // bf16.  Lane l takes columns 4l .. 4l + 3 and 128 + 4l .. 128 + 4l + 3, so
 // that each shared-memory load reads 512 contiguous bytes (no bank conflict)
-// and each store writes 256 contiguous bytes of the row.
+// and each store writes 256 contiguous bytes of the row.  Rows go in batches
+// of 8 / SP, every load of a batch issued before any is added (16 in flight
+// per lane; one row at a time, the loads' latency made a row about 600
+// cycles).
+template <int SP>
 __device__ __forceinline__ void cluster_sum_rows(const RsArgs& a, int tm, int tn, uint32_t base,
                                                  uint32_t rank, int quad, int lane, int my_keep) {
-  const int splits = a.splits;
-  const int R = kRsTileM / splits, RPW = R / 4;
+  constexpr int R = kRsTileM / SP, RPW = R / 4;
+  constexpr int RB = (8 / SP) < RPW ? 8 / SP : RPW;
+  static_assert(RPW % RB == 0, "whole batches of rows");
   const int n0 = tn * kRsTileN + 4 * lane, n1 = n0 + 128;  // output columns
   const bool vec = n1 + 4 <= a.N && (a.N & 3) == 0 && (reinterpret_cast<uintptr_t>(a.out) & 7u) == 0;
-  for (int rw = 0; rw < RPW; ++rw) {
-    const int j = quad * RPW + rw;  // row within the CTA's share
-    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int k = 0; k < splits; ++k) {
-      const uint32_t src = base + (uint32_t)((k * R + j) * (kRsTileN * 4) + 16 * lane);
-      float4 lo, hi;
-      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                   : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w)
-                   : "r"(src));
-      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                   : "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(hi.w)
-                   : "r"(src + 512u));
-      s[0] += lo.x; s[1] += lo.y; s[2] += lo.z; s[3] += lo.w;
-      s[4] += hi.x; s[5] += hi.y; s[6] += hi.z; s[7] += hi.w;
-    }
-    const int i = tm * kRsTileM + (int)rank * R + j;  // kept-row index
-    const int keep_r = __shfl_sync(0xffffffffu, my_keep, rw);  // fetched by lane rw
-    if (i >= a.n_keep) continue;
-    if (keep_r < 0 || keep_r >= a.n_rows) {
-      if (lane == 0) atomicExch(a.status, -1 /* kept row outside X */);
-      continue;
-    }
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (size_t)keep_r * a.N;
-    if (vec) {
-      *reinterpret_cast<uint2*>(orow + n0) = make_uint2(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]));
-      *reinterpret_cast<uint2*>(orow + n1) = make_uint2(pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
-    } else {
+  for (int rb = 0; rb < RPW; rb += RB) {
+    float4 v[RB][SP][2];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (n0 + e < a.N) orow[n0 + e] = __float2bfloat16_rn(s[e]);
-        if (n1 + e < a.N) orow[n1 + e] = __float2bfloat16_rn(s[4 + e]);
+    for (int r = 0; r < RB; ++r) {
+      const int j = quad * RPW + rb + r;  // row within the CTA's share
+#pragma unroll
+      for (int k = 0; k < SP; ++k) {
+        const uint32_t src = base + (uint32_t)((k * R + j) * (kRsTileN * 4) + 16 * lane);
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v[r][k][0].x), "=f"(v[r][k][0].y), "=f"(v[r][k][0].z), "=f"(v[r][k][0].w)
+                     : "r"(src));
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v[r][k][1].x), "=f"(v[r][k][1].y), "=f"(v[r][k][1].z), "=f"(v[r][k][1].w)
+                     : "r"(src + 512u));
       }
+    }
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < SP; ++k) {
+        s[0] += v[r][k][0].x; s[1] += v[r][k][0].y; s[2] += v[r][k][0].z; s[3] += v[r][k][0].w;
+        s[4] += v[r][k][1].x; s[5] += v[r][k][1].y; s[6] += v[r][k][1].z; s[7] += v[r][k][1].w;
+      }
+      const int j = quad * RPW + rb + r;
+      if (quad == 0 && lane == 0) CFA_TRACE(5, 1 + rb + r, 0);
+      const int i = tm * kRsTileM + (int)rank * R + j;  // kept-row index
+      const int keep_r = __shfl_sync(0xffffffffu, my_keep, rb + r);  // fetched by lane rb + r
+      if (i >= a.n_keep) continue;
+      if (keep_r < 0 || keep_r >= a.n_rows) {
+        if (lane == 0) atomicExch(a.status, -1 /* kept row outside X */);
+        continue;
+      }
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (size_t)keep_r * a.N;
+      if (vec) {
+        *reinterpret_cast<uint2*>(orow + n0) = make_uint2(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]));
+        *reinterpret_cast<uint2*>(orow + n1) = make_uint2(pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (n0 + e < a.N) orow[n0 + e] = __float2bfloat16_rn(s[e]);
+          if (n1 + e < a.N) orow[n1 + e] = __float2bfloat16_rn(s[4 + e]);
+        }
+      }
+      if (quad == 0 && lane == 0) CFA_TRACE(5, 1 + rb + r, 1);
     }
   }
 }
@@ -634,7 +652,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_load(base + (uint32_t)(e * kRsTileN * 4), src, (uint32_t)(kRsTileN * 4), bar_rows);
       ok = warp_wait(W, bar_rows, 0u);
       if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 4);
-      if (ok) cluster_sum_rows(a, t.tm, t.tn, base, rank, quad, lane, my_keep);
+      if (ok) {
+        if (splits == 2)
+          cluster_sum_rows<2>(a, t.tm, t.tn, base, rank, quad, lane, my_keep);
+        else if (splits == 4)
+          cluster_sum_rows<4>(a, t.tm, t.tn, base, rank, quad, lane, my_keep);
+        else
+          cluster_sum_rows<8>(a, t.tm, t.tn, base, rank, quad, lane, my_keep);
+      }
       if (!ok) mbar_wait_bounded(bar_rows, 0u, kDrainLimitNs);  // no copy left in flight
     }
     if (quad == 0 && lane == 0) CFA_TRACE(5, 0, 5);
