@@ -656,21 +656,26 @@ class AttnStep:
         if ev:
             ev[3].record(s)
 
-    def capture(self):
+    def capture(self, io=None):
         """Capture one step (the same C-ABI calls, on a side stream) into a
         CUDA graph; replay() then launches the whole step at once.  The
         library's calls are capture-safe: no host synchronisation, no
-        allocation, its second stream forked and joined with events."""
+        allocation, its second stream forked and joined with events.  With
+        `io` (an input / output set from make_io) the graph is returned for
+        that set instead."""
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            self.step()  # first call on this stream: outside the capture
+            self.step(io=io)  # first call on this stream: outside the capture
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph, stream=s, capture_error_mode="relaxed"):
-            self.step()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
+            self.step(io=io)
         torch.cuda.synchronize()
+        if io is not None:
+            return graph
+        self.graph = graph
 
     def replay(self, ev=None):
         s = self.stream
@@ -693,7 +698,9 @@ class AttnStep:
 
 def e2e_pipelined(case, pin, outs_h, steps, flush, dev):
     """Milliseconds per step of `steps` steps through the public API with host
-    inputs and outputs, pipelined the way a training loop streams its data:
+    inputs and outputs (each step one replay of its C-ABI calls captured as a
+    CUDA graph, as in the timed steps), pipelined the way a training loop
+    streams its data:
     step k's inputs are copied in from pinned host memory on one copy stream
     while step k-1 runs, and its outputs copied out to pinned host memory on
     another while step k+1 runs.  Two sets of device inputs and outputs
@@ -703,6 +710,11 @@ def e2e_pipelined(case, pin, outs_h, steps, flush, dev):
     output copy."""
     s = case.stream
     ios = [case.io, case.make_io({k: torch.empty_like(v) for k, v in case.d.items()})]
+    # each set's step captured once, as the timed steps are (the same C-ABI calls)
+    for io in ios:
+        for n in case.names:
+            io["d"][n].copy_(pin[n])
+    graphs = [case.capture(io) for io in ios]
     h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     in_ready = [torch.cuda.Event() for _ in range(2)]
     computed = [torch.cuda.Event() for _ in range(2)]
@@ -724,7 +736,7 @@ def e2e_pipelined(case, pin, outs_h, steps, flush, dev):
         s.wait_event(in_ready[b])
         if used[b]:
             s.wait_event(out_read[b])
-        case.step(io=io)
+        graphs[b].replay()
         computed[b].record(s)
         d2h_s.wait_event(computed[b])
         with torch.cuda.stream(d2h_s):
