@@ -266,7 +266,9 @@ def run_reference(args, w, rank):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w, "n/a (CPU)"),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
-                             "kind": "oracle", "sample": desc + " (one group per step)"},
+                             "kind": "oracle",
+                             "sample": desc + " (the last step's; each step samples from the "
+                                              "next (window, KV head) group on)"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
